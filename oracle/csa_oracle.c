@@ -1,0 +1,340 @@
+/*
+ * CPU oracle for the CSA2 decode step over an FP4 global KV cache.
+ *
+ * TEST INFRASTRUCTURE.  Only the test-suite, the smoke check and the timed CPU
+ * baseline of the benchmark may load this library.  It shares no code, table
+ * or header with the CUDA path; it is plain, slow C in double precision, written
+ * so that each function can be checked against its source passage by eye.
+ *
+ * Sources (web pages on DeepSeek-V4.1-Flash):
+ *  [G2C]  "G2C Brief - DeepSeek V4.1-Flash: a model designed around its KV cache",
+ *         sections "FP4 cache entries, and why they're safe",
+ *         "The global branch: compress, index, select",
+ *         "CSA2: most layers don't keep their own cache",
+ *         "The hierarchical indexer: making later indexers context-independent".
+ *  [FPR]  "DeepSeek V4.1 Flash: Pushing the Limits" (talk write-up), section
+ *         "The Paper" (Full / Reindex / Reuse modes).
+ *  [MET]  "DeepSeek Retires Its 1.6T Model for a 552B One" (the three modes).
+ * The indexer score formula sum_h w_h * ReLU(q_h . k) is not printed on any page;
+ * it is the workload statement's formula, used as given.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* bf16: the top 16 bits of an IEEE binary32. */
+double oracle_bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP FP8 E4M3 ("fn": no infinities, bias 7, S.1111.111 is NaN, max 448).
+ * [G2C] "FP4 cache entries": one 8-bit E4M3 scale per 16 channels. */
+double oracle_e4m3_value(uint8_t byte)
+{
+    int sign = byte >> 7;
+    int e = (byte >> 3) & 0xF;
+    int m = byte & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);                    /* subnormal: m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* OCP FP4 E2M1 (bias 1, no inf/NaN): sign bit 3, exponent bits 2..1, mantissa bit 0.
+ * [G2C] "FP4 cache entries": main cache entries are 4-bit floats (E2M1). */
+double oracle_e2m1_value(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 0x3;
+    int m = code & 0x1;
+    double v;
+    if (e == 0)
+        v = 0.5 * (double)m;                         /* subnormal: m/2 * 2^(1-1) */
+    else
+        v = ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Round a non-negative real v to the nearest finite non-negative E4M3 value,
+ * ties to the even code (= even mantissa), values beyond 448 clamp to 448.
+ * The target is num/den (callers pass amax and 6, so no division is made).
+ * Below the saturation point the 127 candidates are enumerated and their
+ * distances |num - den*value| compared; these are exact in double because num
+ * is a bf16 and den*value has at most 7 significant bits of similar size. */
+uint8_t oracle_e4m3_round_ratio(double num, double den)
+{
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    if (num >= den * 448.0)
+        return 0x7E;                                 /* saturate; keeps the distances below exact */
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(num - den * oracle_e4m3_value((uint8_t)c));
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = (uint8_t)c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* Nearest E2M1 magnitude code (0..7) to |x|/s for s > 0, ties to the even code,
+ * magnitudes at or beyond 6 clamp to 6.  Below that, the distances |x| - grid*s
+ * are exact in double (bf16 minus a product with at most 6 significant bits). */
+uint8_t oracle_e2m1_round_ratio(double ax, double s)
+{
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    if (ax >= 6.0 * s)
+        return 7;                                    /* saturate; keeps the distances below exact */
+    for (int c = 0; c <= 7; ++c) {
+        double d = fabs(ax - s * oracle_e2m1_value((uint8_t)c));
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = (uint8_t)c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------------- */
+/* a1: quantise latent rows ([G2C] "FP4 cache entries, and why they're safe") */
+/* ------------------------------------------------------------------------- */
+/*
+ * Each group of 16 consecutive channels gets one E4M3 scale s = RNE(amax / 6)
+ * (6 is the largest E2M1 magnitude, so the largest element lands on the top
+ * code), saturating at 448; each channel gets the E2M1 code nearest to x / s
+ * with its sign kept (so -0 and small negatives give 0x8).  A group whose scale
+ * rounds to zero stores all-zero codes.  Codes are packed two per byte, the
+ * even channel in the low nibble; scales are stored apart from codes.
+ *
+ * x      : [n_rows][D] bf16 bits
+ * codes  : [n_rows][D/2]
+ * scales : [n_rows][D/16]
+ */
+void oracle_quantize_rows(const uint16_t *x, int64_t n_rows, int D, uint8_t *codes, uint8_t *scales)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const uint16_t *xr = x + r * D;
+        for (int g = 0; g < D / 16; ++g) {
+            double amax = 0.0;
+            for (int i = 0; i < 16; ++i) {
+                double a = fabs(oracle_bf16_value(xr[g * 16 + i]));
+                if (a > amax)
+                    amax = a;
+            }
+            uint8_t sbyte = oracle_e4m3_round_ratio(amax, 6.0);
+            double s = oracle_e4m3_value(sbyte);
+            scales[r * (D / 16) + g] = sbyte;
+            for (int i = 0; i < 16; ++i) {
+                int ch = g * 16 + i;
+                uint16_t bits = xr[ch];
+                uint8_t code = 0;
+                if (s > 0.0) {
+                    double v = oracle_bf16_value(bits);
+                    code = oracle_e2m1_round_ratio(fabs(v), s);
+                    if (bits & 0x8000)
+                        code |= 0x8;
+                }
+                uint8_t *dst = codes + r * (D / 2) + ch / 2;
+                if ((ch & 1) == 0)
+                    *dst = (uint8_t)((*dst & 0xF0) | code);
+                else
+                    *dst = (uint8_t)((*dst & 0x0F) | (code << 4));
+            }
+        }
+    }
+}
+
+/* Dequantise rows back to doubles: v = E2M1(code) * E4M3(scale). */
+void oracle_dequantize_rows(const uint8_t *codes, const uint8_t *scales, int64_t n_rows, int D, double *out)
+{
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int ch = 0; ch < D; ++ch) {
+            uint8_t byte = codes[r * (D / 2) + ch / 2];
+            uint8_t code = (ch & 1) ? (byte >> 4) : (byte & 0xF);
+            out[r * D + ch] = oracle_e2m1_value(code) * oracle_e4m3_value(scales[r * (D / 16) + ch / 16]);
+        }
+}
+
+/* ------------------------------------------------------------------------- */
+/* a2/a4: indexer score ([G2C] "The global branch", item 3; [FPR] Full mode)  */
+/* ------------------------------------------------------------------------- */
+/*
+ * For one query (one sequence, one position) and each candidate row t:
+ *     score(t) = sum_h w[h] * ReLU( sum_d iq[h][d] * ik[t][d] )
+ * Products of two E4M3 values are exact in double, and so is every sum over
+ * d (at most 2^35 dynamic range plus 7 carry bits).  The weighted head sum is
+ * accumulated in double and rounded once to fp32.
+ *
+ * iq   : [HI][DI] E4M3 bytes        w : [HI] fp32
+ * ik   : key table, row t at ik + rows[j]*DI (E4M3 bytes)
+ * rows : candidate row ids, n of them
+ * out  : [n] fp32
+ */
+void oracle_index_score(const uint8_t *iq, const float *w, int HI, int DI,
+                        const uint8_t *ik, const int64_t *rows, int64_t n, float *out)
+{
+    double *q = (double *)malloc(sizeof(double) * (size_t)HI * DI);
+    for (int i = 0; i < HI * DI; ++i)
+        q[i] = oracle_e4m3_value(iq[i]);
+    double *k = (double *)malloc(sizeof(double) * (size_t)DI);
+    for (int64_t j = 0; j < n; ++j) {
+        const uint8_t *kr = ik + rows[j] * (int64_t)DI;
+        for (int d = 0; d < DI; ++d)
+            k[d] = oracle_e4m3_value(kr[d]);
+        double acc = 0.0;
+        for (int h = 0; h < HI; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < DI; ++d)
+                dot += q[h * DI + d] * k[d];
+            double relu = dot > 0.0 ? dot : 0.0;
+            acc += (double)w[h] * relu;
+        }
+        out[j] = (float)acc;
+    }
+    free(k);
+    free(q);
+}
+
+/* ------------------------------------------------------------------------- */
+/* a3: top-K selection ([FPR] "keep the best 512"; [G2C] "The global branch") */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    float score;
+    int64_t index;
+} scored;
+
+/* Larger score first; equal scores: lower index first.  -0 and +0 compare equal. */
+static int by_score_desc_index_asc(const void *pa, const void *pb)
+{
+    const scored *a = (const scored *)pa, *b = (const scored *)pb;
+    if (a->score > b->score)
+        return -1;
+    if (a->score < b->score)
+        return 1;
+    return (a->index < b->index) ? -1 : (a->index > b->index);
+}
+
+/*
+ * Indices (0..n-1) of the K largest scores, ties to the lower index, taken
+ * only among entries with valid[i] != 0 (valid == NULL: all).  Writes
+ * min(K, #valid) indices in rank order, then -1 up to K.
+ */
+void oracle_topk(const float *scores, const uint8_t *valid, int64_t n, int64_t K, int64_t *out)
+{
+    scored *s = (scored *)malloc(sizeof(scored) * (size_t)(n > 0 ? n : 1));
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i)
+        if (valid == NULL || valid[i]) {
+            s[m].score = scores[i];
+            s[m].index = i;
+            ++m;
+        }
+    qsort(s, (size_t)m, sizeof(scored), by_score_desc_index_asc);
+    for (int64_t j = 0; j < K; ++j)
+        out[j] = j < m ? s[j].index : -1;
+    free(s);
+}
+
+/*
+ * [G2C] "The hierarchical indexer": positions are grouped into blocks of
+ * `block` consecutive rows (block j = rows [j*block, (j+1)*block)), each block
+ * is scored by its best member, and the best n_keep blocks are kept.  Rows at
+ * or past n are not members (the last block may be partial).
+ * blockscore : [ceil(n/block)] out
+ */
+void oracle_block_max(const float *scores, int64_t n, int block, float *blockscore)
+{
+    int64_t nb = (n + block - 1) / block;
+    for (int64_t j = 0; j < nb; ++j) {
+        float best = -INFINITY;
+        for (int64_t t = j * block; t < (j + 1) * block && t < n; ++t)
+            if (scores[t] > best)
+                best = scores[t];
+        blockscore[j] = best;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* a5/a6: sparse attention over the selected FP4 rows                        */
+/* ([G2C] "The global branch", item 3; [FPR] Full mode: one W_KV so K = V)   */
+/* ------------------------------------------------------------------------- */
+/*
+ * For each head h: z_j = scale * q_h . v_{idx_j} over the selected entries j
+ * (idx_j < 0 is padding and is skipped), out_h = sum_j softmax(z)_j v_{idx_j},
+ * lse_h = log sum_j exp(z_j).  The cached latent serves as both key and value.
+ * Everything is accumulated in double and rounded once.  No valid entry:
+ * out_h = 0 and lse_h = -inf.
+ *
+ * q      : [H][D] bf16 bits
+ * codes  : row r at codes + r*(D/2);  scales: row r at scales + r*(D/16)
+ * idx    : [K] row ids
+ * out    : [H][D] fp32,  lse : [H] fp32 (may be NULL)
+ */
+void oracle_attend(const uint16_t *q, int H, int D, double scale,
+                   const uint8_t *codes, const uint8_t *scales,
+                   const int64_t *idx, int64_t K, float *out, float *lse)
+{
+    int64_t nv = 0;
+    for (int64_t j = 0; j < K; ++j)
+        if (idx[j] >= 0)
+            ++nv;
+    double *v = (double *)malloc(sizeof(double) * (size_t)(nv > 0 ? nv : 1) * D);
+    int64_t r = 0;
+    for (int64_t j = 0; j < K; ++j)
+        if (idx[j] >= 0) {
+            oracle_dequantize_rows(codes + idx[j] * (int64_t)(D / 2), scales + idx[j] * (int64_t)(D / 16),
+                                   1, D, v + r * D);
+            ++r;
+        }
+    double *z = (double *)malloc(sizeof(double) * (size_t)(nv > 0 ? nv : 1));
+    double *acc = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int h = 0; h < H; ++h) {
+        if (nv == 0) {
+            for (int d = 0; d < D; ++d)
+                out[h * D + d] = 0.0f;
+            if (lse)
+                lse[h] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nv; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += oracle_bf16_value(q[h * D + d]) * v[j * D + d];
+            z[j] = scale * dot;
+            if (z[j] > m)
+                m = z[j];
+        }
+        double l = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc[d] = 0.0;
+        for (int64_t j = 0; j < nv; ++j) {
+            double p = exp(z[j] - m);
+            l += p;
+            for (int d = 0; d < D; ++d)
+                acc[d] += p * v[j * D + d];
+        }
+        for (int d = 0; d < D; ++d)
+            out[h * D + d] = (float)(acc[d] / l);
+        if (lse)
+            lse[h] = (float)(m + log(l));
+    }
+    free(acc);
+    free(z);
+    free(v);
+}
