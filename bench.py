@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA2 decode step over an FP4 global KV cache.
+
+One step = one pass of the whole hot path over one batch: for the default
+workload (full_64k: 8 sequences x 65,536 cached FP4 rows, 64 query heads,
+D=512, a 64x128 FP8 indexer, top-2048) that is one Full-mode CSA2 layer:
+indexer scores over every cached row, top-K selection, sparse attention over
+the selected FP4 rows.  Chain workloads run every layer of the chain per step.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead (on a
+bounded sample of the same workload).  Under torchrun each rank runs its own
+copy of the workload (independent sequences: weak scaling, no collective on
+the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and achieved HBM GB/s (% of ~8 TB/s) per CSA2 layer step"
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="full_64k")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes (bytes that must move) per step
+# ---------------------------------------------------------------------------
+
+def step_bytes(wl):
+    """Indexer keys scanned + selected FP4 rows + queries (+ appended rows)."""
+    from fp4_compressed_sparse_append_b300 import workloads as W
+    units = wl.B * wl.P
+    row = wl.D // 2 + wl.D // 16
+    L = wl.length_after_append
+    total, index_bytes = 0, 0
+    pool_built = False
+    for mode in wl.layers:
+        q = units * wl.H * wl.D * 2
+        if mode != W.REUSE:
+            q += units * wl.HI * (wl.DI + 4)
+            if mode == W.REINDEX and wl.pool_blocks and pool_built:
+                keys = units * wl.pool_blocks * 8 * wl.DI
+            else:
+                # P positions of a sequence share one scan of the keys
+                keys = wl.B * L * wl.DI
+            total += keys
+            index_bytes = max(index_bytes, keys + units * wl.HI * (wl.DI + 4))
+            if mode == W.FULL and wl.pool_blocks:
+                pool_built = True
+        total += units * min(wl.K, L) * row + q
+    if wl.n_append:
+        total += wl.B * wl.n_append * (wl.D * 2 + wl.DI + row + wl.DI)
+    return total, index_bytes
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def build_state(wl, seed, device):
+    """Untimed setup: the cache (built through csa_quantize_append) and the
+    per-layer arguments with their workspaces."""
+    import torch
+    from fp4_compressed_sparse_append_b300 import binding as B
+    from fp4_compressed_sparse_append_b300 import workloads as W
+
+    cache = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=device)
+    lat = torch.empty((wl.B, wl.L, wl.D), dtype=torch.int16, device=device)
+    ik = torch.empty((wl.B, wl.L, wl.DI), dtype=torch.uint8, device=device)
+    for b in range(wl.B):
+        lat[b], ik[b] = W.cache_rows(wl, seed, b, device=device)
+    B.csa_quantize_append(cache, lat, ik)
+    del lat, ik
+    torch.cuda.synchronize()
+    app = W.append_rows(wl, seed, device=device) if wl.n_append else None
+    layers, prev, pool = [], None, None
+    for li, mode in enumerate(wl.layers):
+        inp = W.layer_inputs(wl, seed, li, device=device)
+        la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
+                         idx=prev if mode == W.REUSE else None,
+                         rows_new=app["rows"] if (app and li == 0) else None,
+                         ikeys_new=app["ikeys"] if (app and li == 0) else None,
+                         pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
+                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None))
+        if mode != W.REUSE:
+            prev = la.idx
+        if la.pool_out is not None:
+            pool = la.pool_out
+        layers.append(la)
+    base_len = cache.lengths.clone()
+    return cache, layers, base_len
+
+
+def run_step(cache, layers, base_len, wl):
+    from fp4_compressed_sparse_append_b300 import binding as B
+    for la in layers:
+        B.csa_layer_step(cache, la)
+
+
+def bench_ours(args, wl, rank, world, local_rank):
+    import torch
+    from fp4_compressed_sparse_append_b300 import binding as B
+    from fp4_compressed_sparse_append_b300 import build as BUILD
+
+    if rank == 0 or not os.path.exists(BUILD.LIB):
+        BUILD.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cache, layers, base_len = build_state(wl, args.seed, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def reset():
+        if wl.n_append:
+            cache.lengths.copy_(base_len)      # the step appends rows: start each step from the same cache
+        flush.fill_(1)                         # L2 flush between timed iterations
+
+    for _ in range(max(3, args.warmup)):
+        reset()
+        run_step(cache, layers, base_len, wl)
+    torch.cuda.synchronize()
+    if B.csa_device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    clocks = Clocks(local_rank)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = B.csa_kernel_launches()
+    for i in range(args.steps):
+        reset()
+        ev[i][0].record(stream)
+        run_step(cache, layers, base_len, wl)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    launches = B.csa_kernel_launches() - launches0
+    clock_info = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    units = wl.B * wl.P
+    value = world * units * args.steps / (total_ms / 1e3)
+    sbytes, ibytes = step_bytes(wl)
+    gbs = sbytes / (ms_per_step / 1e3) / 1e9
+
+    # Stage timings (the dominant kernel for the roofline): each stage alone.
+    stages = stage_times(cache, layers, wl, flush, args.steps, stream)
+    # e2e through the public API with host buffers
+    e2e = e2e_run(cache, layers, base_len, wl, args, stream, flush)
+    if B.csa_device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    return dict(value=value, ms_per_step=ms_per_step, gbs=gbs, step_bytes=sbytes, index_bytes=ibytes,
+                clocks=clock_info, launches=launches, stages=stages, e2e=e2e, step_ms=step_ms)
+
+
+def stage_times(cache, layers, wl, flush, steps, stream):
+    """Times the first layer's kernels one call at a time (same inputs, L2 flushed)."""
+    import torch
+    from fp4_compressed_sparse_append_b300 import binding as B
+    from fp4_compressed_sparse_append_b300 import workloads as W
+
+    la = layers[0]
+    q, iq, w = la.tensors["q"], la.tensors["iq"], la.tensors["w"]
+    out = {}
+    if la.struct.mode == W.REUSE:
+        return out
+    scores = B.csa_index_score(cache, iq, w)
+    ws = torch.empty(B.attend_workspace_size(cache, wl.P, wl.H, wl.K), dtype=torch.uint8, device=cache.device)
+
+    def timed(fn):
+        ts = []
+        for i in range(max(3, steps // 2) + 3):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return statistics.mean(ts)
+
+    out["index_score"] = timed(lambda: B.csa_index_score(cache, iq, w, scores=scores))
+    out["topk"] = timed(lambda: B.csa_topk(cache, scores, wl.K))
+    idx, _ = B.csa_topk(cache, scores, wl.K)
+    out["sparse_attend"] = timed(lambda: B.csa_sparse_attend(cache, q, idx, wl.scale, workspace=ws))
+    return out
+
+
+def e2e_run(cache, layers, base_len, wl, args, stream, flush):
+    """Same step through the public API with pinned host inputs and outputs:
+    per step, copy every layer's q/iq/w host->device, run the layers, copy every
+    layer's output device->host."""
+    import torch
+    hin, hout, h2d, d2h = [], [], 0, 0
+    for la in layers:
+        row = {}
+        for k in ("q", "iq", "w"):
+            t = la.tensors[k]
+            if t is not None:
+                row[k] = t.cpu().pin_memory()
+                h2d += t.numel() * t.element_size()
+        hin.append(row)
+        hout.append(torch.empty(la.out.shape, dtype=la.out.dtype).pin_memory())
+        d2h += la.out.numel() * la.out.element_size()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps + 2):
+        if wl.n_append:
+            cache.lengths.copy_(base_len)
+        flush.fill_(1)
+        if i >= 2:
+            ev[i - 2][0].record(stream)
+        for la, row in zip(layers, hin):
+            for k, h in row.items():
+                la.tensors[k].copy_(h, non_blocking=True)
+        run_step(cache, layers, base_len, wl)
+        for la, h in zip(layers, hout):
+            h.copy_(la.out, non_blocking=True)
+        if i >= 2:
+            ev[i - 2][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    return {"value": wl.B * wl.P / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the cpu_baseline leg and the --impl reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, seed, max_seconds):
+    """Times the oracle on whole query units of sequence 0 (every layer of the
+    chain for position 0, scoring split over the host's cores).  Returns
+    (units/s, cores, description, seconds)."""
+    import numpy as np
+    import oracle
+    from fp4_compressed_sparse_append_b300 import workloads as W
+
+    cores = os.cpu_count() or 1
+    lat, ik = W.cache_rows(wl, seed, 0, device="cpu")
+    oc = oracle.Cache(1, wl.capacity, wl.D, wl.DI)
+    oc.append(lat[None].numpy(), ik[None].numpy(), threads=cores)
+    if wl.n_append:
+        app = W.append_rows(wl, seed, device="cpu")
+        oc.append(app["rows"][:1].numpy(), app["ikeys"][:1].numpy())
+    inputs = [{k: v[:1].numpy() for k, v in W.layer_inputs(wl, seed, li, device="cpu").items()}
+              for li in range(len(wl.layers))]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run_chain(oc, wl.layers, inputs, wl.K, wl.scale, P=wl.P, pool_keep=wl.pool_blocks,
+                         units=[(0, 0)], score_threads=cores)
+        done += 1
+        el = time.perf_counter() - t0
+        if el > max_seconds or done >= 50:
+            break
+    sample = ("oracle (plain C, fp64) on %d query unit(s) of sequence 0, position 0, all %d layer(s); "
+              "indexer scoring split over %d threads; inputs drawn on the CPU" % (done, len(wl.layers), cores))
+    return done / el, cores, sample, el
+
+
+def bench_reference(args, wl, rank):
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    import oracle
+    oracle.build()
+    from fp4_compressed_sparse_append_b300 import workloads as W  # noqa: F401
+    # warm-up steps, then timed steps; each step = one query unit through the chain
+    per_step = []
+    cores = os.cpu_count() or 1
+    for i in range(args.warmup + args.steps):
+        rate, cores, sample, el = oracle_sample(wl, args.seed, 0.0)
+        if i >= args.warmup:
+            per_step.append(el)
+    ms = 1e3 * statistics.mean(per_step)
+    value = 1.0 / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: " + sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_of(wl):
+    from fp4_compressed_sparse_append_b300 import workloads as W
+    return {"workload": wl.name, "batch": wl.B, "context": wl.L, "query_positions": wl.P, "heads": wl.H,
+            "d_latent": wl.D, "indexer_heads": wl.HI, "indexer_dim": wl.DI, "top_k": wl.K,
+            "layers": "".join({W.FULL: "F", W.REINDEX: "X", W.REUSE: "R"}[m] for m in wl.layers),
+            "pool_blocks": wl.pool_blocks, "appended_rows": wl.n_append,
+            "kv_format": "E2M1 codes + E4M3 scale per 16 channels; FP8 E4M3 indexer keys",
+            "l2": "flushed between timed steps (256 MiB write outside the timed events)"}
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    from fp4_compressed_sparse_append_b300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        bench_reference(args, wl, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    r = bench_ours(args, wl, rank, world, local_rank)
+    if rank != 0:
+        return
+    import json as _json
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = _json.load(f)
+    except OSError:
+        pass
+    peak_hbm = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak_hbm else "fallback"
+    peak_hbm = peak_hbm or 6400.0
+    idx_ms = r["stages"].get("index_score")
+    dominant = max(r["stages"], key=r["stages"].get) if r["stages"] else None
+    roof = None
+    if idx_ms:
+        ach = r["index_bytes"] / (idx_ms / 1e3) / 1e9
+        roof = {"kernel": "index_score", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
+                "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
+                "algorithmic_bytes_per_launch": r["index_bytes"], "launch_ms": idx_ms, "traffic": None}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, cores, sample, el = oracle_sample(wl, args.seed, 20.0)
+        cpu = {"value": rate * wl.P, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": el}
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e2m1 operands, f32 accumulate",
+        "data": "synthetic (seeded draws shaped like the workload; no dataset)",
+        "config": config_of(wl),
+        "hbm_gbs": r["gbs"], "frac_of_8tbs": r["gbs"] / NOMINAL_HBM_GBS, "frac_of_measured_hbm": r["gbs"] / peak_hbm,
+        "step_algorithmic_bytes": r["step_bytes"],
+        "stages_ms": r["stages"], "dominant_stage": dominant,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

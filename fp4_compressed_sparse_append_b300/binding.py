@@ -1,0 +1,236 @@
+"""Thin ctypes binding of libcsa (the C ABI declared in include/csa.h).
+
+Every function here only marshals torch tensors (device memory owned by
+torch) and the current CUDA stream into the C calls of the same name; every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+path: if libcsa.so is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcsa.so")
+
+CSA_FULL, CSA_REINDEX, CSA_REUSE = 0, 1, 2
+CSA_POOL_BLOCK = 8
+CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+EXPORTS = (
+    "csa_quantize_append", "csa_index_score", "csa_topk", "csa_sparse_attend",
+    "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
+    "csa_device_status", "csa_kernel_launches", "csa_status_string",
+)
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+        self.status = status
+
+
+class csa_cache(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("capacity", ctypes.c_int32), ("d_latent", ctypes.c_int32),
+                ("d_index", ctypes.c_int32), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("ikeys", ctypes.c_void_p), ("lengths", ctypes.c_void_p)]
+
+
+class csa_layer_args(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("P", ctypes.c_int32), ("H", ctypes.c_int32), ("HI", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("scale", ctypes.c_float), ("q", ctypes.c_void_p),
+                ("iq", ctypes.c_void_p), ("w", ctypes.c_void_p), ("rows_new", ctypes.c_void_p),
+                ("ikeys_new", ctypes.c_void_p), ("n_new", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
+                ("pool_in", ctypes.c_void_p), ("pool_out", ctypes.c_void_p), ("idx", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libcsa.so (built by fp4_compressed_sparse_append_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libcsa.so is not built (run __graft_entry__.build()); "
+                               "there is no fallback path")
+        L = ctypes.CDLL(LIB_PATH)
+        V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        C = ctypes.POINTER(csa_cache)
+        L.csa_quantize_append.argtypes = [C, V, V, I32, V]
+        L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
+        L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V]
+        L.csa_sparse_attend.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V, SZ, V]
+        L.csa_attend_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
+        L.csa_layer_step.argtypes = [C, ctypes.POINTER(csa_layer_args), V]
+        L.csa_layer_workspace_size.argtypes = [C, ctypes.POINTER(csa_layer_args), ctypes.POINTER(SZ)]
+        L.csa_device_status.argtypes = [ctypes.POINTER(I32), I32, V]
+        L.csa_kernel_launches.argtypes = []
+        L.csa_kernel_launches.restype = ctypes.c_uint64
+        L.csa_status_string.argtypes = [ctypes.c_int]
+        L.csa_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name not in ("csa_status_string", "csa_kernel_launches"):
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().csa_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise CsaError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Cache:
+    """A global FP4 cache in device memory (torch tensors), laid out as csa_cache says.
+
+    codes [B, cap, D/2] u8, scales [B, cap, D/16] u8, ikeys [B, cap, DI] u8, lengths [B] i32.
+    """
+
+    def __init__(self, batch: int, capacity: int, d_latent: int, d_index: int, device="cuda"):
+        self.batch, self.capacity, self.d_latent, self.d_index = batch, capacity, d_latent, d_index
+        dev = torch.device(device)
+        self.codes = torch.zeros((batch, capacity, d_latent // 2), dtype=torch.uint8, device=dev)
+        self.scales = torch.zeros((batch, capacity, d_latent // 16), dtype=torch.uint8, device=dev)
+        self.ikeys = torch.zeros((batch, capacity, d_index), dtype=torch.uint8, device=dev)
+        self.lengths = torch.zeros((batch,), dtype=torch.int32, device=dev)
+        self._struct = csa_cache(batch, capacity, d_latent, d_index, self.codes.data_ptr(),
+                                 self.scales.data_ptr(), self.ikeys.data_ptr(), self.lengths.data_ptr())
+
+    @property
+    def ref(self):
+        return ctypes.byref(self._struct)
+
+    @property
+    def device(self):
+        return self.codes.device
+
+
+# ---------------------------------------------------------------------------
+# The calls of include/csa.h
+# ---------------------------------------------------------------------------
+
+def csa_quantize_append(cache: Cache, rows: torch.Tensor, ikeys_new: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """rows: [B, n, D] bf16 (or its int16 bits); ikeys_new: [B, n, DI] uint8 or None."""
+    n = rows.shape[1]
+    _check(lib().csa_quantize_append(cache.ref, _ptr(rows), _ptr(ikeys_new), n, _stream(stream)),
+           "csa_quantize_append")
+
+
+def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optional[torch.Tensor] = None,
+                    scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """iq [B, P, HI, DI] uint8, w [B, P, HI] fp32, pool [B, P, nblk] int32 or None
+    -> scores [B, P, ld] fp32 (ld = capacity rounded up to 4, or 8*nblk)."""
+    B, P, HI, _ = iq.shape
+    nblk = pool.shape[-1] if pool is not None else 0
+    n = nblk * CSA_POOL_BLOCK if pool is not None else cache.capacity
+    if scores is None:
+        scores = torch.empty((B, P, (n + 3) // 4 * 4), dtype=torch.float32, device=cache.device)
+    _check(lib().csa_index_score(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, _ptr(scores),
+                                 scores.shape[-1], _stream(stream)), "csa_index_score")
+    return scores
+
+
+def csa_topk(cache: Cache, scores: torch.Tensor, K: int, pool: Optional[torch.Tensor] = None,
+             pool_keep: int = 0, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """scores [B, P, ld] -> (idx [B, P, K] int32, pool_out [B, P, pool_keep] int32 or None)."""
+    B, P, ld = scores.shape
+    nblk = pool.shape[-1] if pool is not None else 0
+    idx = torch.empty((B, P, K), dtype=torch.int32, device=cache.device)
+    pool_out = torch.empty((B, P, pool_keep), dtype=torch.int32, device=cache.device) if pool_keep else None
+    _check(lib().csa_topk(cache.ref, P, _ptr(scores), ld, _ptr(pool), nblk, K, _ptr(idx), pool_keep,
+                          _ptr(pool_out), _stream(stream)), "csa_topk")
+    return idx, pool_out
+
+
+def attend_workspace_size(cache: Cache, P: int, H: int, K: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().csa_attend_workspace_size(cache.ref, P, H, K, ctypes.byref(n)), "csa_attend_workspace_size")
+    return n.value
+
+
+def csa_sparse_attend(cache: Cache, q: torch.Tensor, idx: torch.Tensor, scale: float,
+                      workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q [B, P, H, D] bf16 bits, idx [B, P, K] int32 -> (out [B, P, H, D] fp32, lse [B, P, H] fp32)."""
+    B, P, H, D = q.shape
+    K = idx.shape[-1]
+    if workspace is None:
+        workspace = torch.empty(attend_workspace_size(cache, P, H, K), dtype=torch.uint8, device=cache.device)
+    if out is None:
+        out = torch.empty((B, P, H, D), dtype=torch.float32, device=cache.device)
+    if lse is None:
+        lse = torch.empty((B, P, H), dtype=torch.float32, device=cache.device)
+    _check(lib().csa_sparse_attend(cache.ref, P, H, _ptr(q), scale, _ptr(idx), K, _ptr(out), _ptr(lse),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "csa_sparse_attend")
+    return out, lse
+
+
+class LayerArgs:
+    """Owns the tensors of one csa_layer_step call and its csa_layer_args struct."""
+
+    def __init__(self, cache: Cache, mode: int, q, K: int, scale: float, iq=None, w=None, idx=None,
+                 rows_new=None, ikeys_new=None, pool_in=None, pool_blocks: int = 0, make_pool: bool = False):
+        B, P, H, D = q.shape
+        dev = cache.device
+        self.tensors = dict(q=q, iq=iq, w=w, rows_new=rows_new, ikeys_new=ikeys_new, pool_in=pool_in)
+        self.idx = idx if idx is not None else torch.empty((B, P, K), dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, P, H, D), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, P, H), dtype=torch.float32, device=dev)
+        self.pool_out = (torch.empty((B, P, pool_blocks), dtype=torch.int32, device=dev)
+                         if make_pool else None)
+        HI = iq.shape[2] if iq is not None else 0
+        n_new = rows_new.shape[1] if rows_new is not None else 0
+        self.struct = csa_layer_args(mode, P, H, HI, K, scale, _ptr(q), _ptr(iq), _ptr(w), _ptr(rows_new),
+                                     _ptr(ikeys_new), n_new, pool_blocks, _ptr(pool_in), _ptr(self.pool_out),
+                                     _ptr(self.idx), _ptr(self.out), _ptr(self.lse), None, 0)
+        n = ctypes.c_size_t(0)
+        _check(lib().csa_layer_workspace_size(cache.ref, ctypes.byref(self.struct), ctypes.byref(n)),
+               "csa_layer_workspace_size")
+        self.workspace = torch.empty(max(n.value, 16), dtype=torch.uint8, device=dev)
+        self.struct.workspace = self.workspace.data_ptr()
+        self.struct.workspace_bytes = self.workspace.numel()
+
+
+def csa_layer_step(cache: Cache, args: LayerArgs, stream=None) -> LayerArgs:
+    _check(lib().csa_layer_step(cache.ref, ctypes.byref(args.struct), _stream(stream)), "csa_layer_step")
+    return args
+
+
+def csa_kernel_launches() -> int:
+    """Kernels launched by the library so far in this process (host counter)."""
+    return int(lib().csa_kernel_launches())
+
+
+def csa_device_status(clear: bool = True, stream=None) -> int:
+    """Waits for the stream and returns the device status bits (0 = no fault)."""
+    bits = ctypes.c_int32(0)
+    st = lib().csa_device_status(ctypes.byref(bits), 1 if clear else 0, _stream(stream))
+    if st not in (0, 4):
+        _check(st, "csa_device_status")
+    return bits.value

@@ -1,0 +1,300 @@
+// The C ABI (include/csa.h): argument checks, workspace layout, and the
+// per-layer composition of the kernels for the Full / Reindex / Reuse modes
+// ("G2C Brief - DeepSeek V4.1-Flash", section "CSA2: most layers don't keep
+// their own cache").  Every check here runs before any launch.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "csa_internal.h"
+
+namespace {
+
+// One status word per device (see csa_device_status).
+__device__ int g_csa_status;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+int *status_word()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_csa_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa_status check_cache(const csa_cache *c)
+{
+    if (!c || !c->codes || !c->scales || !c->ikeys || !c->lengths) return CSA_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->capacity < 1) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(c->codes) || !aligned16(c->scales) || !aligned16(c->ikeys) ||
+        (reinterpret_cast<uintptr_t>(c->lengths) & 3u))
+        return CSA_ERR_INVALID_ARG;
+    if (c->d_latent <= 0 || c->d_latent % 16) return CSA_ERR_INVALID_ARG;
+    if (c->d_index <= 0 || c->d_index % 16) return CSA_ERR_INVALID_ARG;
+    if (c->d_latent % 128 || c->d_latent > 512) return CSA_ERR_UNSUPPORTED;
+    if (c->d_index != 32 && c->d_index != 64 && c->d_index != 128) return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
+
+csa::CacheView view(const csa_cache *c)
+{
+    return csa::CacheView{c->batch, c->capacity, c->d_latent, c->d_index, c->codes, c->scales, c->ikeys, c->lengths};
+}
+
+csa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+csa_status check_index_args(const csa_cache *c, int P, int HI, const uint8_t *iq, const float *w,
+                            const int32_t *pool, int pool_blocks, const void *scores, int64_t ld)
+{
+    if (P < 1 || HI < 1 || !iq || !w || !scores) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(iq) || !aligned16(w) || !aligned16(scores)) return CSA_ERR_INVALID_ARG;
+    if (pool) {
+        if (pool_blocks < 1 || !aligned16(pool)) return CSA_ERR_INVALID_ARG;
+        if (ld < static_cast<int64_t>(pool_blocks) * CSA_POOL_BLOCK) return CSA_ERR_INVALID_ARG;
+    } else if (ld < c->capacity) {
+        return CSA_ERR_INVALID_ARG;
+    }
+    if (ld % 4) return CSA_ERR_INVALID_ARG;
+    if (HI * P > 512 || HI > 256) return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
+
+}  // namespace
+
+namespace csa {
+std::atomic<uint64_t> &launch_counter();
+}
+
+extern "C" {
+
+const char *csa_status_string(csa_status s)
+{
+    switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_DEVICE: return "device-side fault recorded in the status word";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+csa_status csa_quantize_append(const csa_cache *cache, const uint16_t *rows, const uint8_t *ikeys_new,
+                               int32_t n_new, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (n_new < 0) return CSA_ERR_INVALID_ARG;
+    if (n_new == 0) return CSA_OK;
+    if (!rows || !aligned16(rows) || (ikeys_new && !aligned16(ikeys_new))) return CSA_ERR_INVALID_ARG;
+    if (n_new > cache->capacity) return CSA_ERR_INVALID_ARG;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_quantize_append(view(cache), rows, ikeys_new, n_new, st, stream));
+}
+
+csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
+                           const int32_t *pool, int32_t pool_blocks, float *scores, int64_t ld, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    s = check_index_args(cache, P, HI, iq, w, pool, pool_blocks, scores, ld);
+    if (s != CSA_OK) return s;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_index_score(view(cache), P, HI, iq, w, pool, pool ? pool_blocks : 0, scores, ld, st,
+                                             stream));
+}
+
+csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld, const int32_t *pool,
+                    int32_t pool_blocks, int32_t K, int32_t *idx, int32_t pool_keep, int32_t *pool_out,
+                    csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (P < 1 || !scores || !idx || K < 1 || K > 16384) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(idx) || ld % 4) return CSA_ERR_INVALID_ARG;
+    if (pool) {
+        if (pool_blocks < 1 || !aligned16(pool) || ld < static_cast<int64_t>(pool_blocks) * CSA_POOL_BLOCK)
+            return CSA_ERR_INVALID_ARG;
+        if (pool_out) return CSA_ERR_INVALID_ARG;
+    } else if (ld < cache->capacity) {
+        return CSA_ERR_INVALID_ARG;
+    }
+    if (pool_out && (pool_keep < 1 || pool_keep > 16384 || !aligned16(pool_out))) return CSA_ERR_INVALID_ARG;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    const csa::CacheView v = view(cache);
+    cudaError_t e = csa::launch_select(v, P, scores, ld, pool, pool ? pool_blocks : 0, 1, K, idx, st, stream);
+    if (e == cudaSuccess && pool_out)
+        e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out, st, stream);
+    return from_cuda(e);
+}
+
+csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K, size_t *bytes)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (!bytes || P < 1 || H < 1 || K < 1) return CSA_ERR_INVALID_ARG;
+    if (H > 64) return CSA_ERR_UNSUPPORTED;
+    *bytes = csa::attend_workspace_bytes(view(cache), P, H, K);
+    return CSA_OK;
+}
+
+csa_status csa_sparse_attend(const csa_cache *cache, int32_t P, int32_t H, const uint16_t *q, float scale,
+                             const int32_t *idx, int32_t K, float *out, float *lse, void *workspace,
+                             size_t workspace_bytes, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (P < 1 || H < 1 || K < 1 || !q || !idx || !out) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse))) return CSA_ERR_INVALID_ARG;
+    if (H > 64) return CSA_ERR_UNSUPPORTED;
+    const csa::CacheView v = view(cache);
+    const size_t need = csa::attend_workspace_bytes(v, P, H, K);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_attend(v, P, H, q, scale, idx, K, out, lse, workspace, workspace_bytes, st, stream));
+}
+
+static size_t layer_scores_ld(const csa_cache *cache, const csa_layer_args *a)
+{
+    if (a->mode == CSA_REINDEX && a->pool_in) return round_up(static_cast<size_t>(a->pool_blocks) * CSA_POOL_BLOCK, 4);
+    return round_up(static_cast<size_t>(cache->capacity), 4);
+}
+
+static csa_status check_layer(const csa_cache *cache, const csa_layer_args *a)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (!a) return CSA_ERR_INVALID_ARG;
+    if (a->mode != CSA_FULL && a->mode != CSA_REINDEX && a->mode != CSA_REUSE) return CSA_ERR_INVALID_ARG;
+    if (a->P < 1 || a->H < 1 || a->K < 1 || a->K > 16384 || !a->q || !a->idx || !a->out) return CSA_ERR_INVALID_ARG;
+    if (a->H > 64) return CSA_ERR_UNSUPPORTED;
+    if (a->mode != CSA_REUSE) {
+        if (!a->iq || !a->w || a->HI < 1) return CSA_ERR_INVALID_ARG;
+        if (a->HI * a->P > 512 || a->HI > 256) return CSA_ERR_UNSUPPORTED;
+    }
+    if (a->n_new < 0 || (a->n_new > 0 && (a->mode != CSA_FULL || !a->rows_new))) return CSA_ERR_INVALID_ARG;
+    if ((a->pool_in || a->pool_out) && (a->pool_blocks < 1 || a->pool_blocks > 16384)) return CSA_ERR_INVALID_ARG;
+    if (a->pool_in && a->mode != CSA_REINDEX) return CSA_ERR_INVALID_ARG;
+    if (a->pool_out && a->mode != CSA_FULL) return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
+csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args *a, size_t *bytes)
+{
+    csa_status s = check_layer(cache, a);
+    if (s != CSA_OK) return s;
+    if (!bytes) return CSA_ERR_INVALID_ARG;
+    const csa::CacheView v = view(cache);
+    size_t total = 0;
+    if (a->mode != CSA_REUSE)
+        total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_scores_ld(cache, a) * sizeof(float), 256);
+    total += round_up(csa::attend_workspace_bytes(v, a->P, a->H, a->K), 256);
+    *bytes = total;
+    return CSA_OK;
+}
+
+csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_stream_t stream)
+{
+    csa_status s = check_layer(cache, a);
+    if (s != CSA_OK) return s;
+    size_t need = 0;
+    csa_layer_workspace_size(cache, a, &need);
+    if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return CSA_ERR_WORKSPACE;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    const csa::CacheView v = view(cache);
+    uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+    cudaError_t e = cudaSuccess;
+    if (a->mode != CSA_REUSE) {
+        const int64_t ld = static_cast<int64_t>(layer_scores_ld(cache, a));
+        float *scores = reinterpret_cast<float *>(ws);
+        ws += round_up(static_cast<size_t>(cache->batch) * a->P * ld * sizeof(float), 256);
+        if (a->n_new > 0) {
+            e = csa::launch_quantize_append(v, a->rows_new, a->ikeys_new, a->n_new, st, stream);
+            if (e != cudaSuccess) return CSA_ERR_CUDA;
+        }
+        const int32_t *pool = a->mode == CSA_REINDEX ? a->pool_in : nullptr;
+        const int pool_blocks = pool ? a->pool_blocks : 0;
+        e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);
+        if (e == cudaSuccess) e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, st, stream);
+        if (e == cudaSuccess && a->mode == CSA_FULL && a->pool_out)
+            e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out, st,
+                                   stream);
+        if (e != cudaSuccess) return CSA_ERR_CUDA;
+    }
+    const size_t att = csa::attend_workspace_bytes(v, a->P, a->H, a->K);
+    e = csa::launch_attend(v, a->P, a->H, a->q, a->scale, a->idx, a->K, a->out, a->lse, ws, att, st, stream);
+    return from_cuda(e);
+}
+
+uint64_t csa_kernel_launches(void) { return csa::launch_counter().load(); }
+
+csa_status csa_device_status(int32_t *bits, int32_t clear, csa_stream_t stream)
+{
+    if (!bits) return CSA_ERR_INVALID_ARG;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, st, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CSA_ERR_CUDA;
+    if (clear && cudaMemsetAsync(st, 0, sizeof(int), stream) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
+    *bits = v;
+    return v ? CSA_ERR_DEVICE : CSA_OK;
+}
+
+}  // extern "C"
+
+namespace csa {
+
+std::atomic<uint64_t> &launch_counter()
+{
+    static std::atomic<uint64_t> n{0};
+    return n;
+}
+
+void count_launch(int n) { launch_counter() += static_cast<uint64_t>(n); }
+
+CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                                 uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle)
+{
+    using Fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                            const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                            CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<Fn>(p);
+    });
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {inner_bytes, rows};
+    const cuuint64_t strides[1] = {inner_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace csa

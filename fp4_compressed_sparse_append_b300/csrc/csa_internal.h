@@ -1,0 +1,42 @@
+// Internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace csa {
+
+struct CacheView {
+    int B, cap, D, DI;
+    uint8_t *codes, *scales, *ikeys;
+    int32_t *lengths;
+};
+
+// a1
+cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, const uint8_t *ikeys_new, int n_new,
+                                   int *status, cudaStream_t st);
+
+// a2/a4
+cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
+                               const int32_t *pool, int pool_blocks, float *scores, int64_t ld, int *status,
+                               cudaStream_t st);
+
+// a3 (and the pool): `block` = 1 selects rows, 8 selects blocks of 8 rows by their best member.
+cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
+                          int pool_blocks, int block, int K, int32_t *out, int *status, cudaStream_t st);
+
+// a5/a6
+size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K);
+cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, float scale, const int32_t *idx,
+                          int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st);
+
+// Host-side count of kernel launches issued by the library (csa_kernel_launches).
+void count_launch(int n = 1);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                                 uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
+}  // namespace csa

@@ -1,0 +1,227 @@
+/*
+ * csa.h - C ABI of the CSA2 sparse-attention decode step over an FP4 global
+ * KV cache, for NVIDIA B300 (sm_103a).
+ *
+ * The step, as the pages on DeepSeek-V4.1-Flash describe it:
+ *  - "G2C Brief - DeepSeek V4.1-Flash: a model designed around its KV cache",
+ *    section "The global branch: compress, index, select": a learned indexer
+ *    scores every cached entry for the query with low-precision queries and
+ *    keys, the query keeps the best entries (top-k) and attends to only those.
+ *    One shared latent per cached position serves every query head.
+ *  - same page, section "FP4 cache entries, and why they're safe": main cache
+ *    entries are E2M1 4-bit floats with one E4M3 scale per 16 channels
+ *    (288 bytes for a 512-dim entry).
+ *  - same page, section "CSA2: most layers don't keep their own cache": each
+ *    layer is Full (own KV, own indexer keys, own selection), Reindex (borrows
+ *    the KV and indexer keys, re-scores with its own indexer query) or Reuse
+ *    (borrows the KV and the last selection); every layer has its own query.
+ *  - same page, section "The hierarchical indexer": the first Full layer also
+ *    groups positions into blocks of 8, scores each block by its best member
+ *    and keeps the top 2,048 blocks; later Reindex layers search only that pool.
+ * The indexer score is sum_h w_h * ReLU(q_h . k) with FP8 E4M3 indexer queries
+ * and keys (the pages give no formula; this is the workload statement's).
+ *
+ * Conventions for every call:
+ *  - Pointers named in the argument lists are DEVICE pointers, owned by the
+ *    caller; the library never allocates, frees or retains them.  Every
+ *    device pointer must be 16-byte aligned (cache lengths: 4-byte).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  No call synchronises the host, except csa_device_status.
+ *  - Argument errors return CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED before
+ *    anything is launched.  Launch failures return CSA_ERR_CUDA.
+ *  - Faults found on the device (a row index outside [0, length), an append
+ *    past capacity, a pipeline wait that ran out) do not trap: the kernel
+ *    skips the access, ORs a bit into a per-device status word and carries on.
+ *    csa_device_status reads (and optionally clears) that word.
+ *  - Sequence b holds valid rows [0, lengths[b]).  With P query positions per
+ *    sequence, the last P rows are the step's own positions and position p
+ *    (0 <= p < P) sees rows [0, lengths[b] - P + 1 + p).
+ *  - Index lists (top-K selections, pools) are written in ascending order
+ *    followed by -1 padding; an index of -1 is always skipped on read.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CSA_API __attribute__((visibility("default")))
+#else
+#define CSA_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *csa_stream_t;
+
+typedef enum csa_status {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, bad mode */
+    CSA_ERR_UNSUPPORTED = 2,  /* valid but outside the shapes this build handles */
+    CSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    CSA_ERR_DEVICE = 4,       /* csa_device_status: a device-side fault bit is set */
+    CSA_ERR_WORKSPACE = 5     /* workspace missing or smaller than the size query said */
+} csa_status;
+
+/* Bits of the device status word. */
+#define CSA_DEV_BAD_INDEX 0x1   /* a selected row id was >= lengths[b] (row skipped) */
+#define CSA_DEV_CAPACITY  0x2   /* an append would pass capacity (sequence left unchanged) */
+#define CSA_DEV_TIMEOUT   0x4   /* a pipeline wait ran past its limit (kernel returned early) */
+
+typedef enum csa_mode { CSA_FULL = 0, CSA_REINDEX = 1, CSA_REUSE = 2 } csa_mode;
+
+#define CSA_POOL_BLOCK 8        /* rows per hierarchical-pool block */
+
+/*
+ * The global cache shared by the layers of one chain (one "Full" owner).
+ *   codes   : [batch][capacity][d_latent/2]  two E2M1 codes per byte, the even
+ *             channel in the low nibble, sign in bit 3 of each nibble
+ *   scales  : [batch][capacity][d_latent/16] one E4M3 scale per 16 channels
+ *   ikeys   : [batch][capacity][d_index]     FP8 E4M3 indexer key per row
+ *   lengths : [batch] int32                  valid rows per sequence
+ * d_latent is 128, 256, 384 or 512; d_index is 32, 64 or 128; capacity >= 1.
+ */
+typedef struct csa_cache {
+    int32_t batch;
+    int32_t capacity;
+    int32_t d_latent;
+    int32_t d_index;
+    uint8_t *codes;
+    uint8_t *scales;
+    uint8_t *ikeys;
+    int32_t *lengths;
+} csa_cache;
+
+/*
+ * a1: quantise new latent rows to FP4 and append them.
+ * ("G2C Brief", section "FP4 cache entries, and why they're safe".)
+ *   rows      : [batch][n_new][d_latent] bf16 bits
+ *   ikeys_new : [batch][n_new][d_index] E4M3 bytes, or NULL to leave ikeys as is
+ * Per 16-channel group: scale = E4M3 round-to-nearest-even(amax / 6), saturating
+ * at 448; each channel's code is the E2M1 value nearest to x / scale (ties to
+ * the even code, beyond 6 clamped to 6) with the sign of x kept; a group whose
+ * scale rounds to 0 stores zero codes.  Rows go to positions lengths[b] ..
+ * lengths[b] + n_new - 1, then lengths[b] += n_new.  A sequence that would
+ * pass capacity is left unchanged and sets CSA_DEV_CAPACITY.
+ * Inputs must be finite (non-finite inputs give unspecified codes).
+ */
+CSA_API csa_status csa_quantize_append(const csa_cache *cache, const uint16_t *rows,
+                               const uint8_t *ikeys_new, int32_t n_new, csa_stream_t stream);
+
+/*
+ * a2/a4: indexer scores for B*P queries.
+ * ("G2C Brief", sections "The global branch" and "The hierarchical indexer".)
+ *   iq     : [batch][P][HI][d_index] E4M3 indexer queries
+ *   w      : [batch][P][HI] fp32 per-head weights
+ *   pool   : NULL   -> score rows t < L_p = lengths[b] - P + 1 + p;
+ *                      scores[(b*P+p)*ld + t]
+ *            [batch][P][pool_blocks] block ids (ascending, -1 padded)
+ *                   -> score candidate c = 8*j + m, row pool[j]*8 + m;
+ *                      scores[(b*P+p)*ld + c]
+ *   scores : fp32, row stride ld (>= capacity, or >= 8*pool_blocks with a pool)
+ * score = sum_h w[h] * ReLU(sum_d iq[h][d] * ik[row][d]), fp32.  Entries for
+ * rows past L_p or empty pool slots are left unspecified.
+ * Supported: HI*P <= 512, HI % 16 == 0 (or HI*P % 16 == 0).
+ */
+CSA_API csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI,
+                           const uint8_t *iq, const float *w,
+                           const int32_t *pool, int32_t pool_blocks,
+                           float *scores, int64_t ld, csa_stream_t stream);
+
+/*
+ * a3: top-K selection (and the hierarchical block pool) from scores.
+ * ("Pushing the Limits" talk write-up, "The Paper": keep the best indices;
+ *  "G2C Brief", "The hierarchical indexer": blocks of 8 scored by their best
+ *  member, keep the top blocks.)
+ *   scores, ld, pool, pool_blocks : as produced by csa_index_score
+ *   idx      : [batch][P][K] int32 row ids of the K largest scores among the
+ *              candidates (ties: lower row id), ascending, then -1 padding
+ *   pool_out : NULL, or (only with pool == NULL) [batch][P][pool_keep] ids of
+ *              the pool_keep blocks of 8 rows (block j = rows 8j..8j+7 < L_p)
+ *              with the largest best-member score (ties: lower id), ascending,
+ *              then -1 padding
+ * 1 <= K <= 16384; pool_keep <= 16384.
+ */
+CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld,
+                    const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx,
+                    int32_t pool_keep, int32_t *pool_out, csa_stream_t stream);
+
+/*
+ * a5/a6: sparse attention of each query over its selected FP4 rows.
+ * ("G2C Brief", "The global branch": the query attends to only the selected
+ *  entries; "Pushing the Limits", "The Paper": one W_KV, so K and V are equal.)
+ *   q     : [batch][P][H][d_latent] bf16 bits
+ *   idx   : [batch][P][K] row ids (-1 = skip; >= lengths[b] sets CSA_DEV_BAD_INDEX
+ *           and is skipped)
+ *   out   : [batch][P][H][d_latent] fp32 = sum_j softmax_j(scale * q.v_j) v_j
+ *   lse   : [batch][P][H] fp32 log-sum-exp of the logits, or NULL
+ *   workspace : device scratch of csa_attend_workspace_size bytes
+ * A query with no valid row gets out = 0, lse = -inf.  1 <= H <= 64.
+ */
+CSA_API csa_status csa_sparse_attend(const csa_cache *cache, int32_t P, int32_t H, const uint16_t *q,
+                             float scale, const int32_t *idx, int32_t K, float *out, float *lse,
+                             void *workspace, size_t workspace_bytes, csa_stream_t stream);
+
+CSA_API csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K,
+                                     size_t *bytes);
+
+/*
+ * a7: one CSA2 layer for B*P queries.
+ *   FULL    : [append rows_new/ikeys_new if n_new > 0] -> scores over every
+ *             visible row -> idx (top K) [-> pool_out] -> attention
+ *   REINDEX : scores over every visible row, or over pool_in's rows when
+ *             pool_in != NULL -> idx (fresh top K) -> attention
+ *   REUSE   : attention over the given idx
+ * idx is written by FULL/REINDEX and read by REUSE.  All arrays are laid out
+ * as in the calls above.  workspace: csa_layer_workspace_size bytes.
+ */
+typedef struct csa_layer_args {
+    csa_mode mode;
+    int32_t P;                   /* query positions per sequence */
+    int32_t H;                   /* main query heads */
+    int32_t HI;                  /* indexer heads (FULL/REINDEX) */
+    int32_t K;                   /* top-K */
+    float scale;                 /* softmax scale, e.g. 1/sqrt(d_latent) */
+    const uint16_t *q;           /* [batch][P][H][d_latent] bf16 bits */
+    const uint8_t *iq;           /* [batch][P][HI][d_index] (FULL/REINDEX) */
+    const float *w;              /* [batch][P][HI] (FULL/REINDEX) */
+    const uint16_t *rows_new;    /* FULL only: [batch][n_new][d_latent] bf16 bits, or NULL */
+    const uint8_t *ikeys_new;    /* FULL only: [batch][n_new][d_index], or NULL */
+    int32_t n_new;               /* rows appended before scoring (FULL), else 0 */
+    int32_t pool_blocks;         /* pool size in blocks (pool_in / pool_out) */
+    const int32_t *pool_in;      /* REINDEX: [batch][P][pool_blocks] or NULL */
+    int32_t *pool_out;           /* FULL: [batch][P][pool_blocks] or NULL */
+    int32_t *idx;                /* [batch][P][K] */
+    float *out;                  /* [batch][P][H][d_latent] fp32 */
+    float *lse;                  /* [batch][P][H] fp32 or NULL */
+    void *workspace;
+    size_t workspace_bytes;
+} csa_layer_args;
+
+CSA_API csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *args, csa_stream_t stream);
+
+CSA_API csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args *args, size_t *bytes);
+
+/*
+ * Waits for `stream`, then copies the device status word of the current
+ * device into *bits (0 = no fault) and, if clear != 0, resets it.
+ * Returns CSA_ERR_DEVICE when a bit is set, else CSA_OK.
+ */
+CSA_API csa_status csa_device_status(int32_t *bits, int32_t clear, csa_stream_t stream);
+
+/* Number of kernels this library has launched in the calling process (a host
+ * counter, for accounting in benchmarks; no device work). */
+CSA_API uint64_t csa_kernel_launches(void);
+
+/* Static description of a status code. */
+CSA_API const char *csa_status_string(csa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

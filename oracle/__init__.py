@@ -123,14 +123,30 @@ def bf16_value(bits: int) -> float:
 # a1: quantise (+ append)
 # --------------------------------------------------------------------------
 
-def quantize_rows(x_bits) -> tuple:
-    """bf16 bits [..., D] -> (codes uint8 [..., D/2], scales uint8 [..., D/16])."""
+def _chunks(n: int, threads: int):
+    step = max(1, -(-n // max(1, threads)))
+    return [(i, min(n, i + step)) for i in range(0, n, step)]
+
+
+def quantize_rows(x_bits, threads: int = 1) -> tuple:
+    """bf16 bits [..., D] -> (codes uint8 [..., D/2], scales uint8 [..., D/16]).
+    threads > 1 splits the rows over threads (the rows are independent)."""
     x = _np(x_bits, np.uint16)
     D = x.shape[-1]
     n = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
     codes = np.zeros(x.shape[:-1] + (D // 2,), np.uint8)
     scales = np.zeros(x.shape[:-1] + (D // 16,), np.uint8)
-    lib().oracle_quantize_rows(_ptr(x), n, D, _ptr(codes), _ptr(scales))
+    xf, cf, sf = x.reshape(n, D), codes.reshape(n, D // 2), scales.reshape(n, D // 16)
+
+    def part(r):
+        a, b = r
+        lib().oracle_quantize_rows(_ptr(xf[a:b]), b - a, D, _ptr(cf[a:b]), _ptr(sf[a:b]))
+
+    if threads > 1 and n > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(part, _chunks(n, threads)))
+    elif n:
+        part((0, n))
     return codes, scales
 
 
@@ -154,13 +170,13 @@ class Cache:
         self.ikeys = np.zeros((B, capacity, DI), np.uint8)
         self.lengths = np.zeros(B, np.int64)
 
-    def append(self, rows_bits, ikeys) -> None:
+    def append(self, rows_bits, ikeys, threads: int = 1) -> None:
         """Quantise rows [B, n, D] and write them, with their ikeys [B, n, DI],
         at positions lengths[b] .. lengths[b]+n-1; then lengths += n."""
         rows = _np(rows_bits, np.uint16)
         ik = _np(ikeys, np.uint8)
         n = rows.shape[1]
-        codes, scales = quantize_rows(rows)
+        codes, scales = quantize_rows(rows, threads)
         for b in range(self.B):
             l0 = int(self.lengths[b])
             assert l0 + n <= self.capacity
@@ -180,17 +196,26 @@ def visible_length(length: int, P: int, p: int) -> int:
 # a2 / a4: indexer scores
 # --------------------------------------------------------------------------
 
-def index_scores(iq, w, ikeys_b, rows) -> np.ndarray:
+def index_scores(iq, w, ikeys_b, rows, threads: int = 1) -> np.ndarray:
     """Scores of candidate rows for one query: iq [HI, DI] E4M3, w [HI] fp32,
-    ikeys_b [n_rows_total, DI], rows: int64 row ids -> fp32 [len(rows)]."""
+    ikeys_b [n_rows_total, DI], rows: int64 row ids -> fp32 [len(rows)].
+    threads > 1 splits the candidate rows over threads."""
     q = _np(iq, np.uint8)
     ww = _np(w, np.float32)
     ik = _np(ikeys_b, np.uint8)
     r = np.ascontiguousarray(np.asarray(rows, np.int64))
     HI, DI = q.shape
     out = np.zeros(r.shape[0], np.float32)
-    if r.shape[0]:
-        lib().oracle_index_score(_ptr(q), _ptr(ww), HI, DI, _ptr(ik), _ptr(r), r.shape[0], _ptr(out))
+
+    def part(c):
+        a, b = c
+        lib().oracle_index_score(_ptr(q), _ptr(ww), HI, DI, _ptr(ik), _ptr(r[a:b]), b - a, _ptr(out[a:b]))
+
+    if threads > 1 and r.shape[0] > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(part, _chunks(r.shape[0], threads)))
+    elif r.shape[0]:
+        part((0, r.shape[0]))
     return out
 
 
@@ -261,7 +286,7 @@ def attend(q_bits, codes_b, scales_b, idx, scale: float):
 # --------------------------------------------------------------------------
 
 def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int, scale: float,
-               prev_idx=None, pool_in=None, pool_keep: int = 0) -> Dict[str, np.ndarray]:
+               prev_idx=None, pool_in=None, pool_keep: int = 0, threads: int = 1) -> Dict[str, np.ndarray]:
     """One (sequence b, position p) through one CSA2 layer.
 
     Full    : score every visible row, keep the top K (and, with pool_keep > 0,
@@ -277,13 +302,13 @@ def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int
         idx = np.asarray(prev_idx, np.int64)
     elif mode == REINDEX and pool_in is not None:
         rows, valid = pool_rows(pool_in, L_p)
-        sc = index_scores(iq, w, cache.ikeys[b], rows)
+        sc = index_scores(iq, w, cache.ikeys[b], rows, threads)
         sel = topk(sc, K, valid)
         idx = np.where(sel >= 0, rows[np.maximum(sel, 0)], -1)
         res["scores"], res["rows"], res["valid"] = sc, rows, valid
     else:
         rows = np.arange(L_p, dtype=np.int64)
-        sc = index_scores(iq, w, cache.ikeys[b], rows)
+        sc = index_scores(iq, w, cache.ikeys[b], rows, threads)
         idx = topk(sc, K)
         res["scores"] = sc
         if mode == FULL and pool_keep:
@@ -295,7 +320,7 @@ def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int
 
 def run_layer(cache: Cache, mode: int, inputs: Dict, K: int, scale: float, P: int = 1,
               prev_idx=None, pool_in=None, pool_keep: int = 0,
-              units: Optional[Sequence] = None, threads: int = 1) -> Dict:
+              units: Optional[Sequence] = None, threads: int = 1, score_threads: int = 1) -> Dict:
     """One layer for every (b, p) unit (or the listed units).  inputs holds
     q [B,P,H,D] bf16 bits, iq [B,P,HI,DI], w [B,P,HI].  Returns per-unit dicts."""
     q = _np(inputs["q"], np.uint16)
@@ -308,7 +333,7 @@ def run_layer(cache: Cache, mode: int, inputs: Dict, K: int, scale: float, P: in
         b, p = u
         return u, unit_layer(cache, b, p, P, mode, q[b, p], iq[b, p], w[b, p], K, scale,
                              None if prev_idx is None else prev_idx[u],
-                             None if pool_in is None else pool_in[u], pool_keep)
+                             None if pool_in is None else pool_in[u], pool_keep, score_threads)
 
     if threads > 1:
         with ThreadPoolExecutor(threads) as ex:
@@ -317,7 +342,7 @@ def run_layer(cache: Cache, mode: int, inputs: Dict, K: int, scale: float, P: in
 
 
 def run_chain(cache: Cache, modes: Sequence[int], layer_inputs: Sequence[Dict], K: int, scale: float,
-              P: int = 1, pool_keep: int = 0, units=None, threads: int = 1):
+              P: int = 1, pool_keep: int = 0, units=None, threads: int = 1, score_threads: int = 1):
     """A chain of layers sharing one cache.  Reuse takes the nearest preceding
     Full/Reindex selection; Reindex uses the pool of the first Full layer when
     pool_keep > 0.  Returns a list of per-layer results."""
@@ -327,7 +352,7 @@ def run_chain(cache: Cache, modes: Sequence[int], layer_inputs: Sequence[Dict], 
                       prev_idx=prev if mode == REUSE else None,
                       pool_in=pool if mode == REINDEX else None,
                       pool_keep=pool_keep if (mode == FULL and pool is None) else 0,
-                      units=units, threads=threads)
+                      units=units, threads=threads, score_threads=score_threads)
         if mode != REUSE:
             prev = {u: v["idx"] for u, v in r.items()}
         if mode == FULL and pool is None and pool_keep:

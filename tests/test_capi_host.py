@@ -1,0 +1,102 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol the header declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from fp4_compressed_sparse_append_b300 import binding as B
+from fp4_compressed_sparse_append_b300 import build as BUILD
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BUILD.build()
+    return B.lib()
+
+
+def header_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"CSA_API\s+[\w\s\*]+?\b(csa_\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B.EXPORTS)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert B.status_string(s)
+    assert B.status_string(0) == "ok"
+
+
+def fake_cache(**kw):
+    # 16-byte aligned fake device addresses: only checked, never dereferenced.
+    d = dict(batch=2, capacity=64, d_latent=128, d_index=64, codes=0x10000, scales=0x20000, ikeys=0x30000,
+             lengths=0x40000)
+    d.update(kw)
+    return B.csa_cache(**d)
+
+
+def test_null_and_bad_cache_rejected_before_launch(lib):
+    assert lib.csa_quantize_append(None, None, None, 1, None) == 1
+    c = fake_cache(d_latent=100)
+    assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, 1, None) == 1
+    c = fake_cache(d_latent=1024)
+    assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, 1, None) == 2
+    c = fake_cache(codes=0x10008)                                     # misaligned
+    assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, 1, None) == 1
+    c = fake_cache()
+    assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, -1, None) == 1
+    assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, 0, None) == 0
+
+
+def test_argument_checks_of_each_call(lib):
+    c = ctypes.byref(fake_cache())
+    V = ctypes.c_void_p
+    # index score: ld below capacity, HI*P too large
+    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), None, 0, V(0x3000), 32, None) == 1
+    assert lib.csa_index_score(c, 8, 128, V(0x1000), V(0x2000), None, 0, V(0x3000), 64, None) == 2
+    # top-K: K out of range; pool_out together with a pool
+    assert lib.csa_topk(c, 1, V(0x1000), 64, None, 0, 0, V(0x2000), 0, None, None) == 1
+    assert lib.csa_topk(c, 1, V(0x1000), 64, V(0x4000), 8, 4, V(0x2000), 8, V(0x5000), None) == 1
+    # attention: too many heads, missing workspace
+    assert lib.csa_sparse_attend(c, 1, 65, V(0x1000), 1.0, V(0x2000), 8, V(0x3000), None, V(0x4000), 1 << 20,
+                                 None) == 2
+    assert lib.csa_sparse_attend(c, 1, 16, V(0x1000), 1.0, V(0x2000), 8, V(0x3000), None, None, 0, None) == 5
+    n = ctypes.c_size_t(0)
+    assert lib.csa_attend_workspace_size(c, 1, 16, 8, ctypes.byref(n)) == 0 and n.value > 0
+
+
+def test_layer_args_checks(lib):
+    c = ctypes.byref(fake_cache())
+    a = B.csa_layer_args(mode=7, P=1, H=16, HI=4, K=8, scale=1.0, q=0x1000, iq=0x2000, w=0x3000, idx=0x4000,
+                         out=0x5000)
+    n = ctypes.c_size_t(0)
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 1
+    a.mode = B.CSA_REUSE
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 0
+    reuse_bytes = n.value
+    a.mode = B.CSA_FULL
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value >= reuse_bytes + 2 * 64 * 4                      # + scores [B][P][capacity]
+    a.pool_in = 0x6000                                              # a pool is a Reindex input only
+    a.pool_blocks = 4
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 1
+    a.mode = B.CSA_REUSE
+    a.pool_in = None
+    a.n_new = 2                                                     # only Full appends
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 1
+    # workspace missing -> rejected before launch
+    a.mode, a.n_new = B.CSA_FULL, 0
+    assert lib.csa_layer_step(c, ctypes.byref(a), None) == 5

@@ -1,0 +1,137 @@
+"""a7 on the GPU: whole CSA2 layers and mode chains through csa_layer_step,
+against the oracle chain on the same seeded inputs.
+
+Small workloads are checked on every query; the full-size workloads (the
+launch configuration the benchmark times) are checked on sampled sequences,
+for which the oracle runs the whole chain on that sequence's rows.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_compressed_sparse_append_b300 import binding as B
+from fp4_compressed_sparse_append_b300 import workloads as W
+from gpu_common import ascending_then_padding, check_attention, check_topk, device_cache, need_gpu
+
+pytestmark = pytest.mark.gpu
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def run_gpu_chain(wl, seed, cache):
+    layers, prev, pool = [], None, None
+    for li, mode in enumerate(wl.layers):
+        inp = W.layer_inputs(wl, seed, li, device="cuda")
+        app = W.append_rows(wl, seed, device="cuda") if (li == 0 and wl.n_append) else None
+        la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
+                         idx=prev if mode == W.REUSE else None,
+                         rows_new=app["rows"] if app else None, ikeys_new=app["ikeys"] if app else None,
+                         pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
+                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None))
+        B.csa_layer_step(cache, la)
+        if mode != W.REUSE:
+            prev = la.idx
+        if la.pool_out is not None:
+            pool = la.pool_out
+        layers.append(la)
+    torch.cuda.synchronize()
+    assert B.csa_device_status() == 0
+    return layers
+
+
+def oracle_chain(wl, seed, lat, ik, seqs):
+    """Oracle chain for the listed sequences (host copies of the same draws)."""
+    cache = oracle.Cache(len(seqs), wl.capacity, wl.D, wl.DI)
+    cache.append(lat[seqs].cpu().numpy(), ik[seqs].cpu().numpy(), threads=THREADS)
+    if wl.n_append:
+        app = W.append_rows(wl, seed, device="cuda")
+        cache.append(app["rows"][seqs].cpu().numpy(), app["ikeys"][seqs].cpu().numpy())
+    inputs = []
+    for li in range(len(wl.layers)):
+        inp = W.layer_inputs(wl, seed, li, device="cuda")
+        inputs.append({k: v[seqs].cpu().numpy() for k, v in inp.items()})
+    return oracle.run_chain(cache, wl.layers, inputs, wl.K, wl.scale, P=wl.P, pool_keep=wl.pool_blocks,
+                            threads=min(THREADS, len(seqs) * wl.P), score_threads=THREADS)
+
+
+def compare_chain(wl, gpu_layers, ora_layers, seqs):
+    """Returns (#units compared for attention, #units with a near-tie swap)."""
+    compared, swapped = 0, 0
+    same_sel = {}
+    for li, mode in enumerate(wl.layers):
+        g = gpu_layers[li]
+        gi = g.idx.cpu().numpy()
+        go = g.out.cpu().numpy()
+        for j, b in enumerate(seqs):
+            for p in range(wl.P):
+                r = ora_layers[li][(j, p)]
+                what = (wl.name, li, b, p)
+                ascending_then_padding(gi[b, p])
+                if mode == W.REUSE:
+                    equal = same_sel[(b, p)]
+                else:
+                    if "rows" in r:
+                        by_row = dict(zip(r["rows"][r["valid"] > 0].tolist(), r["scores"][r["valid"] > 0].tolist()))
+                        scores_of = lambda rows, m=by_row: np.array([m[int(x)] for x in rows], np.float32)
+                    else:
+                        scores_of = lambda rows, s=r["scores"]: s[rows]
+                    equal = check_topk(gi[b, p], r["idx"], scores_of, wl.K, what)
+                    same_sel[(b, p)] = equal
+                if "pool" in r:
+                    gp = g.pool_out.cpu().numpy()[b, p]
+                    bm = oracle.block_max(r["scores"])
+                    check_topk(gp, r["pool"], lambda blocks, s=bm: s[blocks], wl.pool_blocks, what + ("pool",))
+                if equal:
+                    check_attention(go[b, p], r["out"], what)
+                    compared += 1
+                else:
+                    swapped += 1
+    return compared, swapped
+
+
+SMALL = [
+    W.WORKLOADS["tiny_full"],
+    W.Workload("chain_small", B=2, L=5003, H=16, D=256, HI=16, DI=128, K=300,
+               layers=(W.FULL, W.REINDEX, W.REINDEX, W.REUSE, W.REUSE)),
+    W.Workload("hier_small", B=1, L=40000, H=64, D=512, HI=64, DI=128, K=512,
+               layers=(W.FULL, W.REINDEX, W.REINDEX, W.REUSE), pool_blocks=128, planted=64),
+    W.Workload("verify_small", B=3, L=3000, H=8, D=128, HI=32, DI=64, K=700, P=6, n_append=6),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_small_workloads_every_query(wl):
+    need_gpu()
+    cache, lat, ik = device_cache(wl, seed=0)
+    gpu = run_gpu_chain(wl, 0, cache)
+    ora = oracle_chain(wl, 0, lat, ik, list(range(wl.B)))
+    compared, swapped = compare_chain(wl, gpu, ora, list(range(wl.B)))
+    assert compared >= 0.9 * (compared + swapped)
+    if wl.planted:
+        off = W.planted_offset(wl, 0)
+        for la in gpu:
+            sel = set(la.idx[0, 0].cpu().tolist())
+            assert set(range(off, off + wl.planted)) <= sel
+
+
+FULL_SIZE = [("full_64k", [0, 5]), ("chain_128k", [17]), ("hier_1m", [0]), ("verify_append_32k", [40])]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,seqs", FULL_SIZE, ids=[n for n, _ in FULL_SIZE])
+def test_full_size_sampled(name, seqs):
+    need_gpu()
+    wl = W.WORKLOADS[name]
+    cache, lat, ik = device_cache(wl, seed=0)
+    gpu = run_gpu_chain(wl, 0, cache)
+    ora = oracle_chain(wl, 0, lat, ik, seqs)
+    compared, swapped = compare_chain(wl, gpu, ora, seqs)
+    assert compared >= 0.75 * (compared + swapped)
+    # property at every query: selections are valid, sorted, unique, and in range
+    for la in gpu:
+        idx = la.idx.cpu().numpy()
+        assert idx.max() < wl.length_after_append
+        n = (idx >= 0).sum(axis=-1)
+        assert np.all(n == min(wl.K, wl.L))

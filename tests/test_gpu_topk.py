@@ -1,0 +1,84 @@
+"""a3 on the GPU: top-K and the block pool on identical fp32 scores must equal
+the oracle's selection exactly (same scores in, same sets out)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_compressed_sparse_append_b300 import binding as B
+from fp4_compressed_sparse_append_b300 import workloads as W
+from gpu_common import ascending_then_padding, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def lengths_cache(Bn, cap, lengths):
+    c = B.Cache(Bn, cap, 128, 64)
+    c.lengths.copy_(torch.tensor(lengths, dtype=torch.int32))
+    return c
+
+
+def scores_with_ties(shape, seed, kind):
+    s = W.random_scores(shape, seed).numpy()
+    if kind == "ties":
+        s = np.round(s * 4) / 4                 # many exact ties
+    elif kind == "zeros":
+        s = np.maximum(s, 0)                    # half exact zeros (the ReLU case)
+        s[..., ::7] = -0.0
+    elif kind == "negative":
+        s = -np.abs(s) - 1
+    return np.ascontiguousarray(s.astype(np.float32))
+
+
+@pytest.mark.parametrize("n,K,kind", [(100, 256, "plain"), (256, 256, "plain"), (4096, 256, "plain"),
+                                      (4096, 256, "ties"), (5000, 2048, "zeros"), (65536, 2048, "plain"),
+                                      (65536, 2048, "ties"), (131072, 2048, "zeros"), (3, 1, "negative"),
+                                      (1048576, 2048, "plain")])
+def test_topk_equals_oracle(n, K, kind):
+    need_gpu()
+    Bn = 2 if n < 200000 else 1
+    cap = (n + 3) // 4 * 4
+    s = scores_with_ties((Bn, 1, cap), n + K, kind)
+    cache = lengths_cache(Bn, cap, [n] * Bn)
+    idx, _ = B.csa_topk(cache, torch.from_numpy(s).cuda(), K)
+    got = idx.cpu().numpy()
+    for b in range(Bn):
+        ref = oracle.topk(s[b, 0, :n], K)
+        assert sorted(got[b, 0][got[b, 0] >= 0].tolist()) == sorted(ref[ref >= 0].tolist())
+        ascending_then_padding(got[b, 0])
+
+
+def test_causal_positions_and_pool():
+    need_gpu()
+    P, cap = 6, 4000
+    lengths = [3990, 17]
+    s = scores_with_ties((2, P, cap), 5, "ties")
+    cache = lengths_cache(2, cap, lengths)
+    idx, pool = B.csa_topk(cache, torch.from_numpy(s).cuda(), 64, pool_keep=100)
+    gi, gp = idx.cpu().numpy(), pool.cpu().numpy()
+    for b in range(2):
+        for p in range(P):
+            L = max(lengths[b] - P + 1 + p, 0)
+            ref = oracle.topk(s[b, p, :L], 64)
+            assert sorted(gi[b, p][gi[b, p] >= 0].tolist()) == sorted(ref[ref >= 0].tolist())
+            refp = oracle.build_pool(s[b, p, :L], 100) if L else -np.ones(100, np.int64)
+            assert gp[b, p].tolist() == refp.tolist()
+
+
+def test_select_over_pool_candidates():
+    need_gpu()
+    L, nblk = 5003, 300
+    nb = (L + 7) // 8
+    pool = np.full((1, 2, nblk), -1, np.int32)
+    pool[0, 0] = np.sort(W.random_ints((nb,), 0, 1 << 30, seed=3).numpy().argsort()[:nblk])
+    pool[0, 1, :50] = np.sort(W.random_ints((nb,), 0, 1 << 30, seed=4).numpy().argsort()[:49].tolist() + [nb - 1])
+    s = scores_with_ties((1, 2, nblk * 8), 9, "ties")
+    cache = lengths_cache(1, L + 1, [L + 1])           # P=2: position 0 sees L rows, position 1 sees L+1
+    idx, _ = B.csa_topk(cache, torch.from_numpy(s).cuda(), 128, pool=torch.from_numpy(pool).cuda())
+    gi = idx.cpu().numpy()
+    for p in range(2):
+        rows, valid = oracle.pool_rows(pool[0, p], L + p)
+        sel = oracle.topk(s[0, p], 128, valid)
+        ref = rows[sel[sel >= 0]]
+        assert sorted(gi[0, p][gi[0, p] >= 0].tolist()) == sorted(ref.tolist())
+        ascending_then_padding(gi[0, p])
