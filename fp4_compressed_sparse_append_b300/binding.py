@@ -21,7 +21,7 @@ CSA_POOL_BLOCK = 8
 CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
-    "csa_quantize_append", "csa_index_score", "csa_topk", "csa_sparse_attend",
+    "csa_quantize_append", "csa_index_score", "csa_topk", "csa_sparse_attend", "csa_sparse_attend_noalloc",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
 )
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
         L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V]
         L.csa_sparse_attend.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V, SZ, V]
+        L.csa_sparse_attend_noalloc.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V]
         L.csa_attend_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
         L.csa_layer_step.argtypes = [C, ctypes.POINTER(csa_layer_args), V]
         L.csa_layer_workspace_size.argtypes = [C, ctypes.POINTER(csa_layer_args), ctypes.POINTER(SZ)]
@@ -189,6 +190,16 @@ def csa_sparse_attend(cache: Cache, q: torch.Tensor, idx: torch.Tensor, scale: f
     _check(lib().csa_sparse_attend(cache.ref, P, H, _ptr(q), scale, _ptr(idx), K, _ptr(out), _ptr(lse),
                                    _ptr(workspace), workspace.numel(), _stream(stream)), "csa_sparse_attend")
     return out, lse
+
+
+def csa_sparse_attend_noalloc(cache: Cache, q: torch.Tensor, idx: torch.Tensor, scale: float,
+                              out: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Sparse attention into caller-provided out/lse, with the library's own
+    fixed device scratch (no workspace argument; the call allocates nothing)."""
+    B, P, H, D = q.shape
+    K = idx.shape[-1]
+    _check(lib().csa_sparse_attend_noalloc(cache.ref, P, H, _ptr(q), scale, _ptr(idx), K, _ptr(out), _ptr(lse),
+                                           _stream(stream)), "csa_sparse_attend_noalloc")
 
 
 class LayerArgs:

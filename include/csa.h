@@ -170,6 +170,36 @@ CSA_API csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, 
                                      size_t *bytes);
 
 /*
+ * csa_sparse_attend without a workspace argument and without any allocation.
+ * The pages describe no counterpart of this call; it exists for callers that
+ * cannot allocate device memory themselves: code running under a framework
+ * that owns the GPU's memory (its own caching allocator, or one arena sized at
+ * start-up, where a direct cudaMalloc would go around its accounting or fail
+ * once the arena is full), and serving loops that cannot afford an allocation,
+ * which may synchronise the device, in the middle of a step.
+ *
+ * Same arguments and results as csa_sparse_attend.  The split partials go to
+ * one array of CSA_NOALLOC_SCRATCH_BYTES bytes that the library places in
+ * device memory when it is loaded; every GPU that loads the library keeps that
+ * array until the process exits.
+ *  - Calls whose csa_attend_workspace_size exceeds CSA_NOALLOC_SCRATCH_BYTES
+ *    return CSA_ERR_WORKSPACE without launching anything.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and remembers it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array per device.  Calls that can run at the same
+ *    time on the GPU (different streams, no ordering between them) overwrite
+ *    each other's partials: order them on one stream or with events.
+ *  - The array keeps whatever the last call left in it; nothing in it has to
+ *    start at zero, because each call writes every partial it later reads.
+ */
+#define CSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+CSA_API csa_status csa_sparse_attend_noalloc(const csa_cache *cache, int32_t P, int32_t H, const uint16_t *q,
+                                             float scale, const int32_t *idx, int32_t K, float *out, float *lse,
+                                             csa_stream_t stream);
+
+/*
  * a7: one CSA2 layer for B*P queries.
  *   FULL    : [append rows_new/ikeys_new if n_new > 0] -> scores over every
  *             visible row -> idx (top K) [-> pool_out] -> attention

@@ -1,0 +1,56 @@
+"""csa_sparse_attend_noalloc: the attention entry point for callers that cannot
+allocate device memory (their memory belongs to a host framework's allocator or
+a fixed arena, or their serving loop cannot afford an allocation mid-step).
+
+It must give the same answer as csa_sparse_attend with a caller workspace, on
+two calls in a row (the fixed scratch array keeps the first call's partials),
+and must refuse a problem whose partials do not fit the fixed array.  This file
+is collected last so that a run stopping at its first failure has already run
+every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from fp4_compressed_sparse_append_b300 import binding as B
+from fp4_compressed_sparse_append_b300 import workloads as W
+from gpu_common import check_attention, device_cache, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 32 << 20      # CSA_NOALLOC_SCRATCH_BYTES in include/csa.h
+
+
+def test_noalloc_matches_workspace_call_twice():
+    need_gpu()
+    wl = W.Workload("noalloc", B=2, L=3000, H=16, D=256, HI=4, DI=64, K=300, P=2)
+    cache, _, _ = device_cache(wl, seed=31)
+    q = W.layer_inputs(wl, 31, 0, device="cuda")["q"]
+    idx = W.random_ints((wl.B, wl.P, wl.K), -1, wl.L - wl.P + 1, seed=32).to(torch.int32).cuda()
+    ref_out, ref_lse = B.csa_sparse_attend(cache, q, idx, wl.scale)
+    torch.cuda.synchronize()
+    assert B.attend_workspace_size(cache, wl.P, wl.H, wl.K) <= SCRATCH_BYTES
+    for call in range(2):
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        B.csa_sparse_attend_noalloc(cache, q, idx, wl.scale, out, lse)
+        torch.cuda.synchronize()
+        assert B.csa_device_status() == 0
+        check_attention(out.cpu().numpy(), ref_out.cpu().numpy(), ("call", call))
+        assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=1e-6, atol=1e-6)
+
+
+def test_noalloc_refuses_problems_larger_than_its_array():
+    need_gpu()
+    cache = B.Cache(64, 64, 512, 128)
+    P, H, K = 6, 64, 2048
+    assert B.attend_workspace_size(cache, P, H, K) > SCRATCH_BYTES
+    q = torch.zeros((64, P, H, 512), dtype=torch.int16, device="cuda")
+    idx = torch.full((64, P, K), -1, dtype=torch.int32, device="cuda")
+    out = torch.zeros((64, P, H, 512), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.CsaError) as e:
+        B.csa_sparse_attend_noalloc(cache, q, idx, 1.0, out)
+    assert e.value.status == 5                   # CSA_ERR_WORKSPACE
+    assert torch.all(out == 0)                   # nothing was launched
