@@ -79,42 +79,62 @@ def step_bytes(wl):
 # ---------------------------------------------------------------------------
 
 class Clocks:
-    """Samples SM clocks and clock-event reasons through NVML (read-only queries)
-    in a background thread while the timed region runs."""
+    """Samples the SM clock and the clock-event reasons while the timed region
+    runs (read-only queries: NVML when importable, else nvidia-smi one-shot
+    queries), in a background thread; one sample is always taken at start and
+    one at stop."""
 
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
-               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    QUERY = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index, period_s=0.02):
+    def __init__(self, gpu_index, period_s=0.05):
         self.gpu, self.period = gpu_index, period_s
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self._stop = None
-        self._thread = None
-        self.error = None
+        self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
+        self._stop, self._thread, self._nvml = None, None, None
+
+    def _sample(self):
+        if self._nvml is not None:
+            N, h = self._nvml
+            self.samples.append(N.nvmlDeviceGetClockInfo(h, N.NVML_CLOCK_SM))
+            self.max_mhz = N.nvmlDeviceGetMaxClockInfo(h, N.NVML_CLOCK_SM)
+            bits = N.nvmlDeviceGetCurrentClocksEventReasons(h)
+            consts = (N.nvmlClocksEventReasonHwSlowdown, N.nvmlClocksEventReasonHwThermalSlowdown,
+                      N.nvmlClocksEventReasonSwThermalSlowdown, N.nvmlClocksEventReasonSwPowerCap)
+            for name, c in zip(self.REASONS, consts):
+                if bits & c:
+                    self.reasons.add(name)
+            return
+        import subprocess
+        out = subprocess.run(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10).stdout
+        parts = [x.strip() for x in out.strip().split(",")]
+        self.samples.append(float(parts[0]))
+        self.max_mhz = float(parts[1])
+        for name, v in zip(self.REASONS, parts[2:6]):
+            if v.lower() == "active":
+                self.reasons.add(name)
 
     def _run(self):
-        import pynvml as N
         try:
-            N.nvmlInit()
-            h = N.nvmlDeviceGetHandleByIndex(self.gpu)
-            self.max_mhz = N.nvmlDeviceGetMaxClockInfo(h, N.NVML_CLOCK_SM)
-            while True:
-                self.samples.append(N.nvmlDeviceGetClockInfo(h, N.NVML_CLOCK_SM))
-                bits = N.nvmlDeviceGetCurrentClocksEventReasons(h)
-                for name, const in self.REASONS:
-                    if bits & getattr(N, const, 0):
-                        self.reasons.add(name)
-                if self._stop.wait(self.period):
-                    break
-            N.nvmlShutdown()
-        except Exception as e:  # NVML missing: report it instead of a number
+            while not self._stop.wait(self.period):
+                self._sample()
+        except Exception as e:
             self.error = repr(e)
 
     def start(self):
         import threading
+        try:
+            import pynvml as N
+            N.nvmlInit()
+            self._nvml = (N, N.nvmlDeviceGetHandleByIndex(self.gpu))
+        except Exception:
+            self._nvml = None
+        try:
+            self._sample()
+        except Exception as e:
+            self.error = repr(e)
         self._stop = threading.Event()
         self._thread = threading.Thread(target=self._run, daemon=True)
         self._thread.start()
@@ -122,10 +142,15 @@ class Clocks:
     def stop(self):
         self._stop.set()
         self._thread.join()
-        if self.error or not self.samples:
+        try:
+            self._sample()
+        except Exception as e:
+            self.error = self.error or repr(e)
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [self.error or "no samples"]}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------

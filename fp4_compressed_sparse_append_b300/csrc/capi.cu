@@ -165,7 +165,7 @@ csa_status csa_sparse_attend(const csa_cache *cache, int32_t P, int32_t H, const
     if (H > 64) return CSA_ERR_UNSUPPORTED;
     const csa::CacheView v = view(cache);
     const size_t need = csa::attend_workspace_bytes(v, P, H, K);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CSA_ERR_WORKSPACE;
     int *st = status_word();
     if (!st) return CSA_ERR_CUDA;
     return from_cuda(csa::launch_attend(v, P, H, q, scale, idx, K, out, lse, workspace, workspace_bytes, st, stream));
@@ -216,7 +216,7 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
     if (s != CSA_OK) return s;
     size_t need = 0;
     csa_layer_workspace_size(cache, a, &need);
-    if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return CSA_ERR_WORKSPACE;
+    if (need > 0 && (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace))) return CSA_ERR_WORKSPACE;
     int *st = status_word();
     if (!st) return CSA_ERR_CUDA;
     const csa::CacheView v = view(cache);

@@ -41,13 +41,23 @@ struct SelArgs {
     int32_t *out;
 };
 
+constexpr int kMaxCluster = 16;
+
+// Per-CTA shared state.  CTAs of a cluster only ever WRITE into each other's
+// shared memory (distributed shared-memory stores), and every such write is
+// followed by a cluster barrier before it is read; no CTA loads from another
+// CTA's shared memory.
 struct SelShared {
-    uint32_t hist[kBins];
-    uint32_t ghist[kBins];
+    uint32_t hist[kBins];                 // this CTA's histogram of the current digit
+    uint32_t stage[kBins];                // [src CTA][bins owned here]: pushed by every CTA
+    uint32_t slice[kBins];                // summed bins owned here
+    uint32_t totals[kMaxCluster];         // slice totals of every CTA (pushed)
+    uint32_t valid_all[kMaxCluster];      // candidate counts of every CTA (pushed)
+    uint32_t above_all[kMaxCluster];      // per-CTA count strictly above the threshold (pushed)
+    uint32_t eq_all[kMaxCluster];         // per-CTA count at the threshold (pushed)
+    uint32_t res_digit, res_gt, res_class;  // pushed by the CTA that owns the chosen digit
     uint32_t warp_tot[kSelWarps];
-    uint32_t local_valid, local_above, local_eq;
-    uint32_t found_digit, found_gt;
-    uint32_t red;
+    uint32_t bcast;
 };
 
 // Candidate i of a row: its key (0 = not a candidate) and its output id.
@@ -142,7 +152,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
     const bool cached = m <= kSelCache;
     const int tid = threadIdx.x;
 
-    // Pass 0: count candidates, cache keys.
+    const int lane = tid & 31;
+    const int bpc = kBins / C;  // histogram bins owned by each CTA
+
+    // Pass 0: count candidates, cache keys; every CTA learns every count.
     uint32_t cnt = 0;
     for (int i = tid; i < m; i += kSelThreads) {
         int32_t id;
@@ -151,10 +164,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
         cnt += k != 0;
     }
     cnt = block_sum(cnt, sh.warp_tot);
-    if (tid == 0) sh.local_valid = cnt;
+    if (tid < C) cluster.map_shared_rank(&sh, tid)->valid_all[rank] = cnt;
     cluster.sync();
     uint32_t total_valid = 0;
-    for (int q = 0; q < C; ++q) total_valid += cluster.map_shared_rank(&sh, q)->local_valid;
+    for (int q = 0; q < C; ++q) total_valid += sh.valid_all[q];
 
     const uint32_t K = static_cast<uint32_t>(a.K);
     uint32_t prefix = 0, above = 0, need = total_valid, local_above = 0, local_eq = cnt;
@@ -165,7 +178,101 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
             const int shift = 32 - pbits - width;
             const uint32_t mask = (1u << width) - 1u;
             for (int i = tid; i < kBins; i += kSelThreads) sh.hist[i] = 0;
+            if (tid == 0) {
+                sh.bcast = 0;
+                sh.res_gt = above;
+                sh.res_class = 0;
+            }
             __syncthreads();
+            // Local histogram; lanes with the same digit add once (warp-aggregated).
+            for (int base = 0; base < m; base += kSelThreads) {
+                const int i = base + tid;
+                uint32_t k = 0;
+                if (i < m) {
+                    if (cached) {
+                        k = cache[i];
+                    } else {
+                        int32_t id;
+                        k = rv.key(e0 + i, id);
+                    }
+                }
+                const bool in = k != 0 && (pbits == 0 || (k >> (32 - pbits)) == prefix);
+                const uint32_t digit = in ? ((k >> shift) & mask) : 0xFFFFFFFFu;
+                const unsigned peers = __match_any_sync(0xFFFFFFFFu, digit);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], static_cast<uint32_t>(__popc(peers)));
+            }
+            __syncthreads();
+            // Push each bin to the CTA that owns it.
+            for (int i = tid; i < kBins; i += kSelThreads) {
+                const int owner = i / bpc, j = i - owner * bpc;
+                cluster.map_shared_rank(sh.stage, owner)[rank * bpc + j] = sh.hist[i];
+            }
+            cluster.sync();
+            // Sum the owned bins over the sources; push the slice total everywhere.
+            uint32_t part = 0;
+            for (int j = tid; j < bpc; j += kSelThreads) {
+                uint32_t g = 0;
+                for (int q = 0; q < C; ++q) g += sh.stage[q * bpc + j];
+                sh.slice[j] = g;
+                part += g;
+            }
+            part = block_sum(part, sh.warp_tot);
+            if (tid < C) cluster.map_shared_rank(&sh, tid)->totals[rank] = part;
+            cluster.sync();
+            // The slice holding the K-th largest key, scanning from the top.
+            int owner = 0;
+            uint32_t cum = above;
+            for (int q = C - 1; q >= 0; --q) {
+                if (cum + sh.totals[q] >= K) {
+                    owner = q;
+                    break;
+                }
+                cum += sh.totals[q];
+            }
+            if (rank == owner) {
+                // Suffix sums over this slice's bins (each thread takes `per`
+                // consecutive bins; threads are scanned in reverse order).
+                const int per = (bpc + kSelThreads - 1) / kSelThreads;
+                uint32_t s_mine = 0;
+                for (int j = 0; j < per; ++j) {
+                    const int bin = tid * per + j;
+                    if (bin < bpc) s_mine += sh.slice[bin];
+                }
+                sh.hist[kSelThreads - 1 - tid] = s_mine;  // hist is free until the next pass
+                __syncthreads();
+                const uint32_t mirrored = sh.hist[tid];
+                __syncthreads();
+                uint32_t tot;
+                const uint32_t excl = block_exclusive_scan(mirrored, sh.warp_tot, &tot);
+                sh.hist[kSelThreads - 1 - tid] = excl;
+                __syncthreads();
+                uint32_t suf = cum + sh.hist[tid];  // keys in bins above my bins (whole cluster)
+                for (int j = per - 1; j >= 0; --j) {
+                    const int bin = tid * per + j;
+                    if (bin >= bpc) continue;
+                    const uint32_t gt = suf;
+                    suf += sh.slice[bin];
+                    if (gt < K && suf >= K) {
+                        sh.bcast = static_cast<uint32_t>(owner * bpc + bin);
+                        sh.res_gt = gt;
+                        sh.res_class = sh.slice[bin];
+                    }
+                }
+                __syncthreads();
+                if (tid < C) {
+                    SelShared *dst = cluster.map_shared_rank(&sh, tid);
+                    dst->res_digit = sh.bcast;
+                    dst->res_gt = sh.res_gt;
+                    dst->res_class = sh.res_class;
+                }
+            }
+            cluster.sync();
+            // The local histogram was reused as scratch by the owner: recount
+            // this CTA's share above and at the chosen digit from the keys.
+            const uint32_t d = sh.res_digit & mask;
+            const uint32_t gt = sh.res_gt;
+            const uint32_t class_total = sh.res_class;
+            uint32_t la = 0, le = 0;
             for (int i = tid; i < m; i += kSelThreads) {
                 uint32_t k;
                 if (cached) {
@@ -174,88 +281,39 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
                     int32_t id;
                     k = rv.key(e0 + i, id);
                 }
-                if (k != 0 && (pbits == 0 || (k >> (32 - pbits)) == prefix))
-                    atomicAdd(&sh.hist[(k >> shift) & mask], 1u);
-            }
-            __syncthreads();
-            cluster.sync();
-            // Combined histogram over the cluster; each thread owns 4 bins.
-            uint32_t g[4], s4 = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int bin = tid * 4 + j;
-                uint32_t acc = 0;
-                for (int q = 0; q < C; ++q) acc += cluster.map_shared_rank(sh.hist, q)[bin];
-                g[j] = acc;
-                s4 += acc;
-            }
-            // Suffix sums from the top bin down: scan over threads in reverse order.
-            uint32_t tot;
-            // Reverse order: thread t's rank in the scan is (kSelThreads-1-t).  Do
-            // the scan on the mirrored value by exchanging through shared memory.
-            if (tid == 0) {
-                sh.found_digit = 0;
-                sh.found_gt = 0;
-            }
-            sh.ghist[kSelThreads - 1 - tid] = s4;
-            __syncthreads();
-            const uint32_t mirrored = sh.ghist[tid];
-            __syncthreads();
-            const uint32_t excl_m = block_exclusive_scan(mirrored, sh.warp_tot, &tot);
-            sh.ghist[kSelThreads - 1 - tid] = excl_m;  // sum of bins above thread (kSelThreads-1-tid)'s bins
-            __syncthreads();
-            const uint32_t above_mine = sh.ghist[tid];  // sum of all bins above my 4 bins
-            __syncthreads();
-            uint32_t suf = above_mine;
-#pragma unroll
-            for (int j = 3; j >= 0; --j) {
-                const uint32_t gt = suf;  // bins strictly above bin tid*4+j
-                suf += g[j];
-                if (above + gt < K && above + suf >= K) {
-                    sh.found_digit = tid * 4 + j;
-                    sh.found_gt = gt;
+                if (k != 0 && (pbits == 0 || (k >> (32 - pbits)) == prefix)) {
+                    const uint32_t dg = (k >> shift) & mask;
+                    la += dg > d;
+                    le += dg == d;
                 }
             }
-            __syncthreads();
-            const uint32_t d = sh.found_digit & mask;
-            const uint32_t gt = sh.found_gt;
-            // Local counts above the digit and at it.
-            uint32_t la = 0;
-            for (int i = tid; i < kBins; i += kSelThreads)
-                if (static_cast<uint32_t>(i) > d) la += sh.hist[i];
             la = block_sum(la, sh.warp_tot);
+            le = block_sum(le, sh.warp_tot);
             local_above += la;
-            local_eq = sh.hist[d];
-            const uint32_t class_total = [&] {
-                uint32_t acc = 0;
-                for (int q = 0; q < C; ++q) acc += cluster.map_shared_rank(sh.hist, q)[d];
-                return acc;
-            }();
-            above += gt;
+            local_eq = le;
+            above = gt;
             prefix = (prefix << width) | d;
             pbits += width;
             need = K - above;
-            cluster.sync();  // every CTA is done reading remote histograms
             if (need == class_total) break;
         }
     }
 
     // Tied class: take the `need` candidates with the lowest ids.
-    if (tid == 0) {
-        sh.local_above = local_above;
-        sh.local_eq = local_eq;
+    if (tid < C) {
+        SelShared *dst = cluster.map_shared_rank(&sh, tid);
+        dst->above_all[rank] = local_above;
+        dst->eq_all[rank] = local_eq;
     }
-    cluster.sync();
+    cluster.sync();  // last remote write: after this, CTAs only touch their own memory
     uint32_t tie_before = 0, out_before = 0, take = 0;
     for (int q = 0; q < C; ++q) {
-        const SelShared *rs = cluster.map_shared_rank(&sh, q);
-        const uint32_t eq = rs->local_eq;
+        const uint32_t eq = sh.eq_all[q];
         const uint32_t tq = tie_before >= need ? 0u : min(eq, need - tie_before);
-        if (q < rank) out_before += rs->local_above + tq;
+        if (q < rank) out_before += sh.above_all[q] + tq;
         if (q == rank) take = tq;
         tie_before += eq;
     }
-    cluster.sync();  // no CTA leaves while another still reads its shared memory
 
     const uint32_t selected_total = total_valid > K ? K : total_valid;
     int32_t *orow = a.out + static_cast<int64_t>(r) * a.K;

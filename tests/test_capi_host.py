@@ -73,9 +73,10 @@ def test_argument_checks_of_each_call(lib):
     # attention: too many heads, missing workspace
     assert lib.csa_sparse_attend(c, 1, 65, V(0x1000), 1.0, V(0x2000), 8, V(0x3000), None, V(0x4000), 1 << 20,
                                  None) == 2
-    assert lib.csa_sparse_attend(c, 1, 16, V(0x1000), 1.0, V(0x2000), 8, V(0x3000), None, None, 0, None) == 5
+    # (K=2048 over 2 queries is split over several CTAs, so it needs a workspace)
+    assert lib.csa_sparse_attend(c, 1, 16, V(0x1000), 1.0, V(0x2000), 2048, V(0x3000), None, None, 0, None) == 5
     n = ctypes.c_size_t(0)
-    assert lib.csa_attend_workspace_size(c, 1, 16, 8, ctypes.byref(n)) == 0 and n.value > 0
+    assert lib.csa_attend_workspace_size(c, 1, 16, 2048, ctypes.byref(n)) == 0 and n.value > 0
 
 
 def test_layer_args_checks(lib):

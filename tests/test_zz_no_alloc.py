@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_call_twice():
 def test_noalloc_refuses_problems_larger_than_its_array():
     need_gpu()
     cache = B.Cache(64, 64, 512, 128)
-    P, H, K = 6, 64, 2048
+    P, H, K = 2, 64, 2048                        # 128 queries: partials of two splits each
     assert B.attend_workspace_size(cache, P, H, K) > SCRATCH_BYTES
     q = torch.zeros((64, P, H, 512), dtype=torch.int16, device="cuda")
     idx = torch.full((64, P, K), -1, dtype=torch.int32, device="cuda")
