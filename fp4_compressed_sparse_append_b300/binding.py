@@ -21,7 +21,8 @@ CSA_POOL_BLOCK = 8
 CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
-    "csa_quantize_append", "csa_index_score", "csa_topk", "csa_sparse_attend", "csa_sparse_attend_noalloc",
+    "csa_quantize_append", "csa_index_score", "csa_topk", "csa_topk_workspace_size", "csa_sparse_attend",
+    "csa_sparse_attend_noalloc",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
 )
@@ -64,7 +65,8 @@ def lib() -> ctypes.CDLL:
         C = ctypes.POINTER(csa_cache)
         L.csa_quantize_append.argtypes = [C, V, V, I32, V]
         L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
-        L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V]
+        L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, SZ, V]
+        L.csa_topk_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
         L.csa_sparse_attend.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V, SZ, V]
         L.csa_sparse_attend_noalloc.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V]
         L.csa_attend_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
@@ -157,15 +159,26 @@ def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optio
     return scores
 
 
+def topk_workspace_size(cache: Cache, P: int, K: int, pool_blocks: int = 0, pool_keep: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().csa_topk_workspace_size(cache.ref, P, pool_blocks, K, pool_keep, ctypes.byref(n)),
+           "csa_topk_workspace_size")
+    return n.value
+
+
 def csa_topk(cache: Cache, scores: torch.Tensor, K: int, pool: Optional[torch.Tensor] = None,
-             pool_keep: int = 0, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+             pool_keep: int = 0, workspace: Optional[torch.Tensor] = None,
+             stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """scores [B, P, ld] -> (idx [B, P, K] int32, pool_out [B, P, pool_keep] int32 or None)."""
     B, P, ld = scores.shape
     nblk = pool.shape[-1] if pool is not None else 0
     idx = torch.empty((B, P, K), dtype=torch.int32, device=cache.device)
     pool_out = torch.empty((B, P, pool_keep), dtype=torch.int32, device=cache.device) if pool_keep else None
+    if workspace is None:
+        n = topk_workspace_size(cache, P, K, nblk, pool_keep)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
     _check(lib().csa_topk(cache.ref, P, _ptr(scores), ld, _ptr(pool), nblk, K, _ptr(idx), pool_keep,
-                          _ptr(pool_out), _stream(stream)), "csa_topk")
+                          _ptr(pool_out), _ptr(workspace), workspace.numel(), _stream(stream)), "csa_topk")
     return idx, pool_out
 
 

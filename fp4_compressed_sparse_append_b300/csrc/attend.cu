@@ -139,10 +139,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         if (h < H) {
             const uint4 *qh = reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(unit) * H + h) * D) +
                               half * (D / 16);
-#pragma unroll 8
-            for (int i = 0; i < D / 16; ++i) {
-                const uint4 v = qh[i];
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint4 v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = i < D / 16 ? qh[i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     emax = max(emax, max((w4[k] >> 7) & 0xFFu, (w4[k] >> 23) & 0xFFu));
@@ -217,14 +219,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         for (int d0 = 0; d0 < D && ok; d0 += 256) {
             const int dn = min(256, D - d0);
             // stage Q[:, d0:d0+dn] as fp16 * 2^qexp (thread pairs per head)
-            for (int e = tid; e < NH * (dn / 8); e += kThreads) {
-                const int h = e / (dn / 8), c8 = e % (dn / 8);
-                uint4 o = make_uint4(0, 0, 0, 0);
-                if (h < H) {
-                    const uint4 raw8 = *reinterpret_cast<const uint4 *>(
-                        a.q + (static_cast<int64_t>(unit) * H + h) * D + d0 + c8 * 8);
-                    const float sc = exp2f(qexp[h]);
-                    const uint32_t w4[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
+            {
+                // NH*dn/8 16-byte pieces, at most 16 per thread: load them all, then convert.
+                constexpr int kPer = kMaxHeads * 256 / 8 / kThreads;
+                const int n_e = NH * (dn / 8);
+                uint4 raw8[kPer];
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int e = tid + i * kThreads;
+                    const int h = e / (dn / 8), c8 = e % (dn / 8);
+                    raw8[i] = (e < n_e && h < H) ? *reinterpret_cast<const uint4 *>(
+                                                       a.q + (static_cast<int64_t>(unit) * H + h) * D + d0 + c8 * 8)
+                                                 : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int e = tid + i * kThreads;
+                    if (e >= n_e) break;
+                    const int h = e / (dn / 8), c8 = e % (dn / 8);
+                    const float sc = h < H ? exp2f(qexp[h]) : 0.f;
+                    const uint32_t w4[4] = {raw8[i].x, raw8[i].y, raw8[i].z, raw8[i].w};
                     uint32_t r4[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -232,9 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                         const float hi = __uint_as_float(w4[k] & 0xFFFF0000u) * sc;
                         r4[k] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
                     }
-                    o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+                    *reinterpret_cast<uint4 *>(q_s + sw128_off(h, c8 * 8, NH)) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
                 }
-                *reinterpret_cast<uint4 *>(q_s + sw128_off(h, c8 * 8, NH)) = o;
             }
             fence_async_smem();
             tc_fence_before();
@@ -435,35 +448,40 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
 
 // Combines the split partials of one (query, head):
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, lse = ln 2 * (M + log2 sum).
-__global__ void attend_merge_kernel(int D, int H, int nsplit, const float *__restrict__ part_o,
-                                    const float2 *__restrict__ part_ml, float *__restrict__ out,
-                                    float *__restrict__ lse)
+__global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsplit, const float *__restrict__ part_o,
+                                                          const float2 *__restrict__ part_ml, float *__restrict__ out,
+                                                          float *__restrict__ lse)
 {
-    extern __shared__ float wsh[];  // [nsplit] weights
-    const int unit = blockIdx.y, h = blockIdx.x;
+    __shared__ float wsh[32];
     __shared__ float inv_l, lse_v;
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int s = 0; s < nsplit; ++s) {
-            const float2 ml = part_ml[(static_cast<int64_t>(unit) * nsplit + s) * H + h];
-            if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    const int unit = blockIdx.y, h = blockIdx.x;
+    if (threadIdx.x < 32) {
+        const int s = threadIdx.x;
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (s < nsplit) ml = part_ml[(static_cast<int64_t>(unit) * nsplit + s) * H + h];
+        float M = ml.y > 0.f ? ml.x : -INFINITY;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+        float L = wgt * ml.y;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        wsh[s] = wgt;
+        if (s == 0) {
+            inv_l = L > 0.f ? 1.f / L : 0.f;
+            lse_v = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-        float L = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-            const float2 ml = part_ml[(static_cast<int64_t>(unit) * nsplit + s) * H + h];
-            const float wgt = (ml.y > 0.f) ? exp2f(ml.x - M) : 0.f;
-            wsh[s] = wgt;
-            L += wgt * ml.y;
-        }
-        inv_l = L > 0.f ? 1.f / L : 0.f;
-        lse_v = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
     __syncthreads();
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float v[32];
+#pragma unroll
+        for (int s = 0; s < 32; ++s)
+            v[s] = (s < nsplit && wsh[s] != 0.f) ? part_o[((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d]
+                                                 : 0.f;
         float acc = 0.f;
-        for (int s = 0; s < nsplit; ++s)
-            if (wsh[s] != 0.f)
-                acc = fmaf(wsh[s], part_o[((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d], acc);
+#pragma unroll
+        for (int s = 0; s < 32; ++s) acc = fmaf(wsh[s], v[s], acc);
         out[(static_cast<int64_t>(unit) * H + h) * D + d] = acc * inv_l;
     }
     if (lse && threadIdx.x == 0) lse[static_cast<int64_t>(unit) * H + h] = lse_v;
@@ -484,6 +502,10 @@ Plan plan(const CacheView &c, int P, int K)
     p.tiles_total = tiles;
     p.tiles_per_split = (tiles + want - 1) / want;
     p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    while (p.nsplit > 32) {  // the merge combines at most 32 partials
+        ++p.tiles_per_split;
+        p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    }
     return p;
 }
 
@@ -547,8 +569,7 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     if (e != cudaSuccess) return e;
     count_launch();
     if (p.nsplit > 1) {
-        attend_merge_kernel<<<dim3(H, units), 128, p.nsplit * sizeof(float), st>>>(c.D, H, p.nsplit, a.part_o,
-                                                                                  a.part_ml, out, lse);
+        attend_merge_kernel<<<dim3(H, units), 128, 0, st>>>(c.D, H, p.nsplit, a.part_o, a.part_ml, out, lse);
         e = cudaGetLastError();
         if (e == cudaSuccess) count_launch();
     }

@@ -119,28 +119,67 @@ csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI, const 
                                              stream));
 }
 
-csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld, const int32_t *pool,
-                    int32_t pool_blocks, int32_t K, int32_t *idx, int32_t pool_keep, int32_t *pool_out,
-                    csa_stream_t stream)
+static csa_status check_topk(const csa_cache *cache, int32_t P, int32_t pool_blocks, int has_pool, int32_t K,
+                             int32_t pool_keep, int has_pool_out)
+{
+    if (P < 1 || K < 1 || K > 16384) return CSA_ERR_INVALID_ARG;
+    if (has_pool && pool_blocks < 1) return CSA_ERR_INVALID_ARG;
+    if (has_pool && has_pool_out) return CSA_ERR_INVALID_ARG;
+    if (has_pool_out && (pool_keep < 1 || pool_keep > 16384)) return CSA_ERR_INVALID_ARG;
+    const csa::CacheView v = view(cache);
+    const int32_t *fake_pool = has_pool ? reinterpret_cast<const int32_t *>(16) : nullptr;
+    if (!csa::select_supported(v, fake_pool, pool_blocks, 1, K)) return CSA_ERR_UNSUPPORTED;
+    if (has_pool_out && !csa::select_supported(v, nullptr, 0, CSA_POOL_BLOCK, pool_keep)) return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
+
+static size_t topk_ws(const csa_cache *cache, int32_t P, int32_t pool_blocks, int has_pool, int32_t K,
+                      int32_t pool_keep, int has_pool_out)
+{
+    const csa::CacheView v = view(cache);
+    const int32_t *fake_pool = has_pool ? reinterpret_cast<const int32_t *>(16) : nullptr;
+    size_t a = csa::select_workspace_bytes(v, P, fake_pool, pool_blocks, 1, K);
+    if (has_pool_out) {
+        const size_t b = csa::select_workspace_bytes(v, P, nullptr, 0, CSA_POOL_BLOCK, pool_keep);
+        if (b > a) a = b;
+    }
+    return a;
+}
+
+csa_status csa_topk_workspace_size(const csa_cache *cache, int32_t P, int32_t pool_blocks, int32_t K,
+                                   int32_t pool_keep, size_t *bytes)
 {
     csa_status s = check_cache(cache);
     if (s != CSA_OK) return s;
-    if (P < 1 || !scores || !idx || K < 1 || K > 16384) return CSA_ERR_INVALID_ARG;
+    if (!bytes) return CSA_ERR_INVALID_ARG;
+    s = check_topk(cache, P, pool_blocks, pool_blocks > 0, K, pool_keep, pool_keep > 0);
+    if (s != CSA_OK) return s;
+    *bytes = topk_ws(cache, P, pool_blocks, pool_blocks > 0, K, pool_keep, pool_keep > 0);
+    return CSA_OK;
+}
+
+csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld, const int32_t *pool,
+                    int32_t pool_blocks, int32_t K, int32_t *idx, int32_t pool_keep, int32_t *pool_out,
+                    void *workspace, size_t workspace_bytes, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (!scores || !idx) return CSA_ERR_INVALID_ARG;
     if (!aligned16(scores) || !aligned16(idx) || ld % 4) return CSA_ERR_INVALID_ARG;
-    if (pool) {
-        if (pool_blocks < 1 || !aligned16(pool) || ld < static_cast<int64_t>(pool_blocks) * CSA_POOL_BLOCK)
-            return CSA_ERR_INVALID_ARG;
-        if (pool_out) return CSA_ERR_INVALID_ARG;
-    } else if (ld < cache->capacity) {
+    if (pool && !aligned16(pool)) return CSA_ERR_INVALID_ARG;
+    if (pool_out && !aligned16(pool_out)) return CSA_ERR_INVALID_ARG;
+    s = check_topk(cache, P, pool_blocks, pool != nullptr, K, pool_keep, pool_out != nullptr);
+    if (s != CSA_OK) return s;
+    if (pool ? ld < static_cast<int64_t>(pool_blocks) * CSA_POOL_BLOCK : ld < cache->capacity)
         return CSA_ERR_INVALID_ARG;
-    }
-    if (pool_out && (pool_keep < 1 || pool_keep > 16384 || !aligned16(pool_out))) return CSA_ERR_INVALID_ARG;
-    int *st = status_word();
-    if (!st) return CSA_ERR_CUDA;
+    const size_t need = topk_ws(cache, P, pool_blocks, pool != nullptr, K, pool_keep, pool_out != nullptr);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CSA_ERR_WORKSPACE;
     const csa::CacheView v = view(cache);
-    cudaError_t e = csa::launch_select(v, P, scores, ld, pool, pool ? pool_blocks : 0, 1, K, idx, st, stream);
+    cudaError_t e =
+        csa::launch_select(v, P, scores, ld, pool, pool ? pool_blocks : 0, 1, K, idx, workspace, workspace_bytes, stream);
     if (e == cudaSuccess && pool_out)
-        e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out, st, stream);
+        e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out, workspace,
+                               workspace_bytes, stream);
     return from_cuda(e);
 }
 
@@ -193,7 +232,21 @@ static csa_status check_layer(const csa_cache *cache, const csa_layer_args *a)
     if ((a->pool_in || a->pool_out) && (a->pool_blocks < 1 || a->pool_blocks > 16384)) return CSA_ERR_INVALID_ARG;
     if (a->pool_in && a->mode != CSA_REINDEX) return CSA_ERR_INVALID_ARG;
     if (a->pool_out && a->mode != CSA_FULL) return CSA_ERR_INVALID_ARG;
+    if (a->mode != CSA_REUSE) {
+        const int has_pool = a->mode == CSA_REINDEX && a->pool_in != nullptr;
+        const int has_pool_out = a->mode == CSA_FULL && a->pool_out != nullptr;
+        s = check_topk(cache, a->P, a->pool_blocks, has_pool, a->K, a->pool_blocks, has_pool_out);
+        if (s != CSA_OK) return s;
+    }
     return CSA_OK;
+}
+
+static size_t layer_select_ws(const csa_cache *cache, const csa_layer_args *a)
+{
+    if (a->mode == CSA_REUSE) return 0;
+    const int has_pool = a->mode == CSA_REINDEX && a->pool_in != nullptr;
+    const int has_pool_out = a->mode == CSA_FULL && a->pool_out != nullptr;
+    return topk_ws(cache, a->P, a->pool_blocks, has_pool, a->K, a->pool_blocks, has_pool_out);
 }
 
 csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args *a, size_t *bytes)
@@ -203,8 +256,10 @@ csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args
     if (!bytes) return CSA_ERR_INVALID_ARG;
     const csa::CacheView v = view(cache);
     size_t total = 0;
-    if (a->mode != CSA_REUSE)
+    if (a->mode != CSA_REUSE) {
         total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_scores_ld(cache, a) * sizeof(float), 256);
+        total += round_up(layer_select_ws(cache, a), 256);
+    }
     total += round_up(csa::attend_workspace_bytes(v, a->P, a->H, a->K), 256);
     *bytes = total;
     return CSA_OK;
@@ -226,6 +281,9 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         const int64_t ld = static_cast<int64_t>(layer_scores_ld(cache, a));
         float *scores = reinterpret_cast<float *>(ws);
         ws += round_up(static_cast<size_t>(cache->batch) * a->P * ld * sizeof(float), 256);
+        void *sel_ws = ws;
+        const size_t sel_bytes = layer_select_ws(cache, a);
+        ws += round_up(sel_bytes, 256);
         if (a->n_new > 0) {
             e = csa::launch_quantize_append(v, a->rows_new, a->ikeys_new, a->n_new, st, stream);
             if (e != cudaSuccess) return CSA_ERR_CUDA;
@@ -233,10 +291,11 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         const int32_t *pool = a->mode == CSA_REINDEX ? a->pool_in : nullptr;
         const int pool_blocks = pool ? a->pool_blocks : 0;
         e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);
-        if (e == cudaSuccess) e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, st, stream);
+        if (e == cudaSuccess)
+            e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, sel_ws, sel_bytes, stream);
         if (e == cudaSuccess && a->mode == CSA_FULL && a->pool_out)
-            e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out, st,
-                                   stream);
+            e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out, sel_ws,
+                                   sel_bytes, stream);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
     }
     const size_t att = csa::attend_workspace_bytes(v, a->P, a->H, a->K);

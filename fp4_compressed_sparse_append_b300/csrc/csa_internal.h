@@ -24,8 +24,11 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
                                cudaStream_t st);
 
 // a3 (and the pool): `block` = 1 selects rows, 8 selects blocks of 8 rows by their best member.
+size_t select_workspace_bytes(const CacheView &c, int P, const int32_t *pool, int pool_blocks, int block, int K);
+int select_supported(const CacheView &c, const int32_t *pool, int pool_blocks, int block, int K);
 cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
-                          int pool_blocks, int block, int K, int32_t *out, int *status, cudaStream_t st);
+                          int pool_blocks, int block, int K, int32_t *out, void *ws, size_t ws_bytes,
+                          cudaStream_t st);
 
 // a5/a6
 size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K);

@@ -144,11 +144,19 @@ CSA_API csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI
  *              the pool_keep blocks of 8 rows (block j = rows 8j..8j+7 < L_p)
  *              with the largest best-member score (ties: lower id), ascending,
  *              then -1 padding
+ *   workspace: csa_topk_workspace_size bytes (zero for rows of at most 196,608
+ *              candidates; longer rows are selected in two stages through it)
  * 1 <= K <= 16384; pool_keep <= 16384.
  */
 CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld,
                     const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx,
-                    int32_t pool_keep, int32_t *pool_out, csa_stream_t stream);
+                    int32_t pool_keep, int32_t *pool_out, void *workspace, size_t workspace_bytes,
+                    csa_stream_t stream);
+
+/* pool_blocks > 0: the scores are over a pool of that many blocks; pool_keep > 0:
+ * a pool of that many blocks is also built. */
+CSA_API csa_status csa_topk_workspace_size(const csa_cache *cache, int32_t P, int32_t pool_blocks, int32_t K,
+                                           int32_t pool_keep, size_t *bytes);
 
 /*
  * a5/a6: sparse attention of each query over its selected FP4 rows.
