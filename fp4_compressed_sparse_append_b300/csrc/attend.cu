@@ -31,7 +31,7 @@ namespace csa {
 namespace {
 
 constexpr int kRows = 128;         // selected rows per tile (MMA M for S^T)
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;      // 8 warps: two per tensor-memory lane quarter
 constexpr int kMaxHeads = 64;
 constexpr float kRescaleLog2 = 8.f;  // rescale only when the running max grows by more than 2^8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -87,6 +87,31 @@ __device__ __forceinline__ uint32_t e4m3_to_h2(uint32_t byte)
     return v;
 }
 
+// 8 bf16 (one uint4) * 2^e -> 8 fp16 (exact unless below fp16's normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float sc)
+{
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    uint32_t r4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float lo = __uint_as_float(w4[k] << 16) * sc;
+        const float hi = __uint_as_float(w4[k] & 0xFFFF0000u) * sc;
+        r4[k] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
+    }
+    return make_uint4(r4[0], r4[1], r4[2], r4[3]);
+}
+
+// Every thread waits for the MMAs committed to `bar`; the verdict is read after a
+// CTA barrier so that all threads agree on it even if one wait ran out.
+__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, volatile int *abort_flag)
+{
+    mbar_wait(bar, phase, abort_flag);
+    phase ^= 1;
+    __syncthreads();
+    tc_fence_after();
+    return *abort_flag == 0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -106,20 +131,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
     float *m_run = st;                 // running max (log2 units)
     float *l_run = m_run + kMaxHeads;  // running sum
     float *fac = l_run + kMaxHeads;    // rescale factor this tile
-    float *qexp = fac + kMaxHeads;     // per-head log2 scale applied to Q
-    float *cfac = qexp + kMaxHeads;    // scale * log2(e) * 2^-qexp
-    int *valid = reinterpret_cast<int *>(cfac + kMaxHeads);  // [kRows]
-    uint64_t *mma_bar = reinterpret_cast<uint64_t *>(valid + kRows);
+    float *cfac = fac + kMaxHeads;     // scale * log2(e) * 2^-e (e: power of two applied to Q)
+    uint32_t *valid = reinterpret_cast<uint32_t *>(cfac + kMaxHeads);  // [kRows/32] bit masks
+    uint64_t *mma_bar = reinterpret_cast<uint64_t *>(valid + kRows / 32);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_bar + 1);
     int *flags = reinterpret_cast<int *>(tmem_slot + 1);  // [0] rescale needed, [1] abort
     volatile int *abort_flag = flags + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, whalf = warp >> 2;  // tensor-memory lane quarter; column half
     const int unit = blockIdx.y, split = blockIdx.x;
     const int b = unit / a.P;
     const int len = a.c.lengths[b];
     const int t_first = split * a.tiles_per_split;
     const int t_last = min(a.tiles_total, t_first + a.tiles_per_split);
+    const int32_t *irow = a.idx + static_cast<int64_t>(unit) * a.K;
 
     if (tid == 0) {
         mbar_init(mma_bar, 1);
@@ -131,32 +157,61 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         tmem_alloc(tmem_slot, a.tmem_cols);
         tmem_relinquish();
     }
-    // Per-head power-of-two scale for the fp16 copy of Q (max|q| * 2^e < 2^15),
-    // and the softmax factor; two threads per head, 16-byte loads.
+
+    // The selected rows of a tile are fetched one tile ahead: thread (row r,
+    // half rh) holds half of one FP4 row (D/4 code bytes, D/32 scale bytes).
+    const int gr = tid & (kRows - 1), grh = tid >> 7;
+    const int nc = D / 64;  // 16-byte code pieces per half row (32 channels each)
+    int32_t nrow = -1;
+    uint4 ncw[8];
+    uint32_t nsw[4];
+    auto prefetch = [&](int tile) {
+        const int j = tile * kRows + gr;
+        int32_t row = j < a.K ? irow[j] : -1;
+        if (row >= len) {
+            raise_status(a.status, CSA_DEV_BAD_INDEX);
+            row = -1;
+        }
+        nrow = row;
+        const int64_t g = static_cast<int64_t>(b) * a.c.cap + (row >= 0 ? row : 0);
+        const uint4 *cp = reinterpret_cast<const uint4 *>(a.c.codes + g * (D / 2)) + grh * nc;
+        const uint32_t *sp = reinterpret_cast<const uint32_t *>(a.c.scales + g * (D / 16)) + grh * (D / 128);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ncw[i] = (row >= 0 && i < nc) ? cp[i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nsw[i] = (row >= 0 && i < D / 128) ? sp[i] : 0u;
+    };
+    if (t_first < t_last) prefetch(t_first);
+
+    // Q lives in registers for the whole CTA, as fp16 scaled per head by a power
+    // of two: thread (head qh, quarter qq) holds dims [qq*D/4, (qq+1)*D/4).
+    const int qh = tid >> 2, qq = tid & 3;
+    const int qn = D / 32;  // 16-byte pieces per thread
+    uint4 qreg[16];
     {
-        const int h = tid >> 1, half = tid & 1;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(unit) * H + qh) * D) + qq * qn;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qreg[i] = (qh < H && i < qn) ? src[i] : make_uint4(0, 0, 0, 0);
+    }
+    // Per-head power of two e with max|q| * 2^e < 2^15 (fp16-safe, exact for bf16).
+    {
         uint32_t emax = 0;
-        if (h < H) {
-            const uint4 *qh = reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(unit) * H + h) * D) +
-                              half * (D / 16);
-            uint4 v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = i < D / 16 ? qh[i] : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t w4[4] = {qreg[i].x, qreg[i].y, qreg[i].z, qreg[i].w};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    emax = max(emax, max((w4[k] >> 7) & 0xFFu, (w4[k] >> 23) & 0xFFu));
-            }
+            for (int k = 0; k < 4; ++k) emax = max(emax, max((w4[k] >> 7) & 0xFFu, (w4[k] >> 23) & 0xFFu));
         }
         emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 1));
-        if (half == 0 && h < kMaxHeads) {
-            const float e = emax > 0 ? 14.f - (static_cast<float>(emax) - 127.f) : 0.f;
-            qexp[h] = e;
-            cfac[h] = a.scale * kLog2e * exp2f(-e);
-            m_run[h] = -INFINITY;
-            l_run[h] = 0.f;
+        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 2));
+        const float e = emax > 0 ? 14.f - (static_cast<float>(emax) - 127.f) : 0.f;
+        const float qscale = exp2f(e);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qreg[i] = bf16x8_to_f16x8(qreg[i], qscale);
+        if (qq == 0) {
+            cfac[qh] = a.scale * kLog2e * exp2f(-e);
+            m_run[qh] = -INFINITY;
+            l_run[qh] = 0.f;
         }
     }
     tc_fence_before();
@@ -165,45 +220,29 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
     const uint32_t tmem = *tmem_slot;
     const uint32_t t_s = tmem;             // S^T: NH columns
     const uint32_t t_o = tmem + NH;        // O^T: (D/128) blocks of NH columns
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t v_base = smem_u32(v_s), q_base = smem_u32(q_s);
     const uint32_t phi_base = smem_u32(p_hi), plo_base = smem_u32(p_lo);
     uint32_t mma_phase = 0;
     bool o_started = false;
     bool ok = true;
-    const int32_t *irow = a.idx + static_cast<int64_t>(unit) * a.K;
     const uint32_t idesc_s = instr_desc(128, NH, 0, 0, 0, 0);   // K-major V, K-major Q
     const uint32_t idesc_o = instr_desc(128, NH, 0, 0, 1, 0);   // MN-major V^T, K-major P
 
     for (int tile = t_first; tile < t_last && ok; ++tile) {
-        // ---- 1. gather + dequantise one selected row per thread
+        // ---- 1. dequantise the prefetched rows into the fp16 tile V
         {
-            const int j = tile * kRows + tid;
-            int32_t row = j < a.K ? irow[j] : -1;
-            if (row >= len) {
-                raise_status(a.status, CSA_DEV_BAD_INDEX);
-                row = -1;
-            }
-            valid[tid] = row >= 0;
-            const int64_t g = static_cast<int64_t>(b) * a.c.cap + (row >= 0 ? row : 0);
-            const uint4 *cp = reinterpret_cast<const uint4 *>(a.c.codes + g * (D / 2));
-            const uint2 *sp = reinterpret_cast<const uint2 *>(a.c.scales + g * (D / 16));
-            // Issue every load of the row before using any (up to 288 bytes in flight per thread).
-            uint4 cw[16];
-            uint2 s8[4];
+            const unsigned vb = __ballot_sync(0xFFFFFFFFu, nrow >= 0);
+            if (grh == 0 && lane == 0) valid[gr >> 5] = vb;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) cw[i] = (row >= 0 && i < D / 32) ? cp[i] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s8[i] = (row >= 0 && i < D / 128) ? sp[i] : make_uint2(0, 0);
-#pragma unroll
-            for (int c16 = 0; c16 < 16; ++c16) {             // 32 channels per 16 code bytes
-                if (c16 >= D / 32) break;
-                const uint32_t sw = (c16 >> 1) & 1 ? s8[c16 >> 2].y : s8[c16 >> 2].x;
-                const uint32_t sc = (sw >> (16 * (c16 & 1))) & 0xFFFF;  // the two scales of these 32 channels
+            for (int c16 = 0; c16 < 8; ++c16) {
+                if (c16 >= nc) break;
+                const uint32_t sc = (nsw[c16 >> 1] >> (16 * (c16 & 1))) & 0xFFFF;  // the 2 scales of 32 channels
                 const uint32_t s0 = e4m3_to_h2(sc & 0xFF), s1 = e4m3_to_h2(sc >> 8);
-                const uint32_t words[4] = {cw[c16].x, cw[c16].y, cw[c16].z, cw[c16].w};
+                const uint32_t words[4] = {ncw[c16].x, ncw[c16].y, ncw[c16].z, ncw[c16].w};
+                const int ch0 = grh * (D / 2) + c16 * 32;
 #pragma unroll
-                for (int h8 = 0; h8 < 4; ++h8) {             // 8 channels = 4 code bytes -> one 16-B chunk
+                for (int h8 = 0; h8 < 4; ++h8) {  // 8 channels = 4 code bytes -> one 16-byte chunk
                     const uint32_t sv = h8 < 2 ? s0 : s1;
                     const uint32_t wd = words[h8];
                     uint4 o;
@@ -211,43 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                     o.y = dequant_pair((wd >> 8) & 0xFF, sv);
                     o.z = dequant_pair((wd >> 16) & 0xFF, sv);
                     o.w = dequant_pair(wd >> 24, sv);
-                    *reinterpret_cast<uint4 *>(v_s + sw128_off(tid, c16 * 32 + h8 * 8, kRows)) = o;
+                    *reinterpret_cast<uint4 *>(v_s + sw128_off(gr, ch0 + h8 * 8, kRows)) = o;
                 }
             }
         }
-        // ---- 2. S^T = V . Q^T, Q staged in 256-dim chunks
+        // ---- 2. S^T = V . Q^T, Q staged in 256-dim chunks from registers
         for (int d0 = 0; d0 < D && ok; d0 += 256) {
             const int dn = min(256, D - d0);
-            // stage Q[:, d0:d0+dn] as fp16 * 2^qexp (thread pairs per head)
-            {
-                // NH*dn/8 16-byte pieces, at most 16 per thread: load them all, then convert.
-                constexpr int kPer = kMaxHeads * 256 / 8 / kThreads;
-                const int n_e = NH * (dn / 8);
-                uint4 raw8[kPer];
 #pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    const int e = tid + i * kThreads;
-                    const int h = e / (dn / 8), c8 = e % (dn / 8);
-                    raw8[i] = (e < n_e && h < H) ? *reinterpret_cast<const uint4 *>(
-                                                       a.q + (static_cast<int64_t>(unit) * H + h) * D + d0 + c8 * 8)
-                                                 : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    const int e = tid + i * kThreads;
-                    if (e >= n_e) break;
-                    const int h = e / (dn / 8), c8 = e % (dn / 8);
-                    const float sc = h < H ? exp2f(qexp[h]) : 0.f;
-                    const uint32_t w4[4] = {raw8[i].x, raw8[i].y, raw8[i].z, raw8[i].w};
-                    uint32_t r4[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float lo = __uint_as_float(w4[k] << 16) * sc;
-                        const float hi = __uint_as_float(w4[k] & 0xFFFF0000u) * sc;
-                        r4[k] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
-                    }
-                    *reinterpret_cast<uint4 *>(q_s + sw128_off(h, c8 * 8, NH)) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
-                }
+            for (int i = 0; i < 16; ++i) {
+                const int dim = qq * (D / 4) + i * 8;
+                if (i < qn && qh < NH && dim >= d0 && dim < d0 + dn)
+                    *reinterpret_cast<uint4 *>(q_s + sw128_off(qh, dim - d0, NH)) = qreg[i];
             }
             fence_async_smem();
             tc_fence_before();
@@ -264,36 +278,36 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                 mma_commit(mma_bar);
             }
             __syncwarp();
-            ok = mbar_wait(mma_bar, mma_phase, abort_flag);
-            mma_phase ^= 1;
-            tc_fence_after();
+            ok = wait_mma(mma_bar, mma_phase, abort_flag);
         }
         if (!ok) break;
-        // ---- 3. logits through shared memory: thread = row -> thread pair = head
+        if (tile + 1 < t_last) prefetch(tile + 1);  // in flight during softmax and PV
+        // ---- 3. logits via shared memory (thread = row, then thread quad = head)
         float *sst = reinterpret_cast<float *>(q_s);  // [kRows][NH+1]
-        for (int c0 = 0; c0 < NH; c0 += 16) {
-            uint32_t r[16];
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                  "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                  "=r"(r[14]), "=r"(r[15])
-                : "r"(t_s + lane_off + c0));
-            tmem_ld_wait();
+        {
+            const int row = quarter * 32 + lane;
+            for (int c0 = whalf * 16; c0 < NH; c0 += 32) {  // 16-column groups alternate between the warp halves
+                uint32_t r16[16];
+                tmem_ld16(t_s + lane_off + c0, r16);
+                tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) sst[tid * (NH + 1) + c0 + k] = __uint_as_float(r[k]);
+                for (int k = 0; k < 16; ++k) sst[row * (NH + 1) + c0 + k] = __uint_as_float(r16[k]);
+            }
         }
         __syncthreads();
         {
-            const int h = tid >> 1, half = tid & 1;  // 64 heads x 2 halves of 64 rows
+            const int h = tid >> 2, part = tid & 3;  // 64 heads x 4 parts of 32 rows
+            const float cf = h < H ? cfac[h] : 0.f;
+            const uint32_t vbits = valid[part];
+            float z[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                z[k] = (h < H && (vbits >> k & 1)) ? sst[(part * 32 + k) * (NH + 1) + h] * cf : -INFINITY;
             float tmax = -INFINITY;
-            if (h < H)
-                for (int k = 0; k < 64; ++k) {
-                    const int rr = half * 64 + k;
-                    if (valid[rr]) tmax = fmaxf(tmax, sst[rr * (NH + 1) + h] * cfac[h]);
-                }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) tmax = fmaxf(tmax, z[k]);
             tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 2));
             float mu = h < kMaxHeads ? m_run[h] : -INFINITY;
             float f = 1.f;
             if (h < H && tmax > -INFINITY && (mu == -INFINITY || tmax > mu + kRescaleLog2)) {
@@ -302,18 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
             }
             float lsum = 0.f;
             if (h < NH) {
-#pragma unroll 4
-                for (int k8 = 0; k8 < 8; ++k8) {
+#pragma unroll
+                for (int k8 = 0; k8 < 4; ++k8) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int k2 = 0; k2 < 4; ++k2) {
                         __half ph[2], pl[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int rr = half * 64 + k8 * 8 + k2 * 2 + e;
-                            float p = 0.f;
-                            if (h < H && valid[rr] && mu > -INFINITY)
-                                p = fast_exp2(sst[rr * (NH + 1) + h] * cfac[h] - mu);
+                            const float zz = z[k8 * 8 + k2 * 2 + e];
+                            const float p = (zz > -INFINITY && mu > -INFINITY) ? fast_exp2(zz - mu) : 0.f;
                             lsum += p;
                             ph[e] = __float2half_rn(p);
                             pl[e] = __float2half_rn(p - __half2float(ph[e]));
@@ -321,14 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                         hw[k2] = pack_half2(ph[0], ph[1]);
                         lw[k2] = pack_half2(pl[0], pl[1]);
                     }
-                    const uint32_t off = sw128_off(h, half * 64 + k8 * 8, NH);
+                    const uint32_t off = sw128_off(h, part * 32 + k8 * 8, NH);
                     *reinterpret_cast<uint4 *>(p_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4 *>(p_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
             lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
-            __syncwarp();
-            if (half == 0 && h < kMaxHeads) {
+            lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
+            if (part == 0 && h < kMaxHeads) {
                 fac[h] = f;
                 if (f != 1.f) flags[0] = 1;
                 m_run[h] = mu;
@@ -336,39 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
             }
         }
         __syncthreads();
-        // ---- rescale O^T when some head's running max moved (rare)
+        // ---- rescale O^T when some head's running max moved by more than 2^8 (rare)
         if (flags[0] && o_started) {
-            for (int mt = 0; mt < D / 128; ++mt)
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    uint32_t r[32];
+            for (int mt = whalf; mt < D / 128; mt += 2)
+                for (int c0 = 0; c0 < NH; c0 += 16) {
+                    uint32_t r16[16];
                     const uint32_t ta = t_o + mt * NH + lane_off + c0;
-                    if (c0 + 32 <= NH) {
-                        tmem_ld32(ta, r);
-                        tmem_ld_wait();
+                    tmem_ld16(ta, r16);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * fac[c0 + k]);
-                        tmem_st32(ta, r);
-                    } else {
-                        uint32_t r16[16];
-                        asm volatile(
-                            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                            : "=r"(r16[0]), "=r"(r16[1]), "=r"(r16[2]), "=r"(r16[3]), "=r"(r16[4]), "=r"(r16[5]),
-                              "=r"(r16[6]), "=r"(r16[7]), "=r"(r16[8]), "=r"(r16[9]), "=r"(r16[10]), "=r"(r16[11]),
-                              "=r"(r16[12]), "=r"(r16[13]), "=r"(r16[14]), "=r"(r16[15])
-                            : "r"(ta));
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            r16[k] = __float_as_uint(__uint_as_float(r16[k]) * fac[c0 + k]);
-                        asm volatile(
-                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-                            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
-                            "r"(r16[0]), "r"(r16[1]), "r"(r16[2]), "r"(r16[3]), "r"(r16[4]), "r"(r16[5]),
-                            "r"(r16[6]), "r"(r16[7]), "r"(r16[8]), "r"(r16[9]), "r"(r16[10]), "r"(r16[11]),
-                            "r"(r16[12]), "r"(r16[13]), "r"(r16[14]), "r"(r16[15])
-                            : "memory");
-                    }
+                    for (int k = 0; k < 16; ++k) r16[k] = __float_as_uint(__uint_as_float(r16[k]) * fac[c0 + k]);
+                    tmem_st16(ta, r16);
                 }
             tmem_st_wait();
         }
@@ -380,50 +370,41 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         if (tid == 0) {
             tc_fence_after();
             for (int mt = 0; mt < D / 128; ++mt)
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t pb = part ? plo_base : phi_base;
+                for (int hl = 0; hl < 2; ++hl) {
+                    const uint32_t pb = hl ? plo_base : phi_base;
                     for (int ks = 0; ks < kRows / 16; ++ks) {
                         const uint64_t da = smem_desc(v_base + (2 * mt) * kRows * 128 + ks * 2048,
                                                       kRows * 128 /*next 64 dims*/, 1024 /*next 8 rows*/, 2);
                         const uint64_t db = smem_desc(pb + (ks >> 2) * NH * 128 + (ks & 3) * 32, 16, 1024, 2);
-                        mma_f16(t_o + mt * NH, da, db, idesc_o, (o_started || part > 0 || ks > 0) ? 1u : 0u);
+                        mma_f16(t_o + mt * NH, da, db, idesc_o, (o_started || hl > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
             mma_commit(mma_bar);
         }
         __syncwarp();
-        ok = mbar_wait(mma_bar, mma_phase, abort_flag);
-        mma_phase ^= 1;
-        tc_fence_after();
+        ok = wait_mma(mma_bar, mma_phase, abort_flag);
         o_started = true;
     }
 
-    // ---- write the result (or the split partial): thread = one dim of each 128-dim block
+    // ---- the result (one split) or this split's partial (merged by the next kernel)
     if (ok) {
         __syncthreads();
         const bool final_out = a.nsplit == 1;
         float *obase = final_out ? a.out + static_cast<int64_t>(unit) * H * D
                                  : a.part_o + (static_cast<int64_t>(unit) * a.nsplit + split) * H * D;
-        for (int mt = 0; mt < D / 128; ++mt) {
-            const int d = mt * 128 + warp * 32 + lane;
-            for (int c0 = 0; c0 < NH; c0 += 16) {
-                uint32_t r[16];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                    "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                      "=r"(r[14]), "=r"(r[15])
-                    : "r"(t_o + mt * NH + lane_off + c0));
-                tmem_ld_wait();
+        for (int mt = whalf; mt < D / 128; mt += 2) {  // thread = one dim of a 128-dim block
+            const int d = mt * 128 + quarter * 32 + lane;
+            uint32_t r[kMaxHeads];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int h = c0 + k;
-                    if (h >= H) continue;
-                    float v = o_started ? __uint_as_float(r[k]) : 0.f;
-                    if (final_out) v = l_run[h] > 0.f ? v / l_run[h] : 0.f;
-                    obase[static_cast<int64_t>(h) * D + d] = v;
-                }
+            for (int c0 = 0; c0 < kMaxHeads; c0 += 16)
+                if (c0 < NH) tmem_ld16(t_o + mt * NH + lane_off + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < kMaxHeads; ++h) {
+                if (h >= H) break;
+                float v = o_started ? __uint_as_float(r[h]) : 0.f;
+                if (final_out) v = l_run[h] > 0.f ? v * __frcp_rn(l_run[h]) : 0.f;
+                obase[static_cast<int64_t>(h) * D + d] = v;
             }
         }
         if (tid < H) {
@@ -446,15 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
     }
 }
 
-// Combines the split partials of one (query, head):
-// out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, lse = ln 2 * (M + log2 sum).
+// Combines the split partials: block = (128 dims, head, query); each thread
+// loads its dim from every split at once.  out = sum_s 2^(m_s - M) O_s / L,
+// L = sum_s 2^(m_s - M) l_s, lse = ln 2 * (M + log2 L).
+constexpr int kMaxSplit = 16;
+
 __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsplit, const float *__restrict__ part_o,
                                                           const float2 *__restrict__ part_ml, float *__restrict__ out,
                                                           float *__restrict__ lse)
 {
-    __shared__ float wsh[32];
-    __shared__ float inv_l, lse_v;
-    const int unit = blockIdx.y, h = blockIdx.x;
+    __shared__ float wsh[kMaxSplit];
+    __shared__ float inv_l;
+    const int d = blockIdx.x * 128 + threadIdx.x, h = blockIdx.y, unit = blockIdx.z;
+    float pv[kMaxSplit];
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s)
+        pv[s] = (s < nsplit && d < D) ? part_o[((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d] : 0.f;
     if (threadIdx.x < 32) {
         const int s = threadIdx.x;
         float2 ml = make_float2(-INFINITY, 0.f);
@@ -462,50 +450,40 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
         float M = ml.y > 0.f ? ml.x : -INFINITY;
 #pragma unroll
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
-        float L = wgt * ml.y;
+        const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+        float L = w * ml.y;
 #pragma unroll
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
-        wsh[s] = wgt;
+        if (s < kMaxSplit) wsh[s] = w;
         if (s == 0) {
             inv_l = L > 0.f ? 1.f / L : 0.f;
-            lse_v = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+            if (lse && blockIdx.x == 0) lse[static_cast<int64_t>(unit) * H + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float v[32];
+    float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < 32; ++s)
-            v[s] = (s < nsplit && wsh[s] != 0.f) ? part_o[((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d]
-                                                 : 0.f;
-        float acc = 0.f;
-#pragma unroll
-        for (int s = 0; s < 32; ++s) acc = fmaf(wsh[s], v[s], acc);
-        out[(static_cast<int64_t>(unit) * H + h) * D + d] = acc * inv_l;
-    }
-    if (lse && threadIdx.x == 0) lse[static_cast<int64_t>(unit) * H + h] = lse_v;
+    for (int s = 0; s < kMaxSplit; ++s) acc = fmaf(wsh[s], pv[s], acc);
+    if (d < D) out[(static_cast<int64_t>(unit) * H + h) * D + d] = acc * inv_l;
 }
 
 struct Plan {
     int nsplit, tiles_per_split, tiles_total;
 };
 
+// Splits of one query's selection: about one wave of CTAs, at most kMaxSplit.
 Plan plan(const CacheView &c, int P, int K)
 {
     const int units = c.B * P;
     const int tiles = (K + kRows - 1) / kRows;
-    int want = (148 + units - 1) / units;  // about one wave of CTAs
+    int want = (148 + units - 1) / units;
     if (want > tiles) want = tiles;
+    if (want > kMaxSplit) want = kMaxSplit;
     if (want < 1) want = 1;
     Plan p;
     p.tiles_total = tiles;
     p.tiles_per_split = (tiles + want - 1) / want;
     p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    while (p.nsplit > 32) {  // the merge combines at most 32 partials
-        ++p.tiles_per_split;
-        p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    }
     return p;
 }
 
@@ -515,7 +493,7 @@ size_t smem_bytes(int D, int NH)
     const size_t qh = static_cast<size_t>(NH) * 256 * 2, sst = static_cast<size_t>(kRows) * (NH + 1) * 4;
     const size_t qs = ((qh > sst ? qh : sst) + 1023) & ~size_t(1023);
     const size_t p = 2 * static_cast<size_t>(NH) * kRows * 2;
-    return 1024 + v + qs + p + 5 * kMaxHeads * 4 + kRows * 4 + 64;
+    return 1024 + v + qs + p + 4 * kMaxHeads * 4 + kRows * 4 + 64;
 }
 
 }  // namespace
@@ -569,7 +547,8 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     if (e != cudaSuccess) return e;
     count_launch();
     if (p.nsplit > 1) {
-        attend_merge_kernel<<<dim3(H, units), 128, 0, st>>>(c.D, H, p.nsplit, a.part_o, a.part_ml, out, lse);
+        attend_merge_kernel<<<dim3((c.D + 127) / 128, H, units), 128, 0, st>>>(c.D, H, p.nsplit, a.part_o, a.part_ml,
+                                                                               out, lse);
         e = cudaGetLastError();
         if (e == cudaSuccess) count_launch();
     }

@@ -98,17 +98,6 @@ __device__ __forceinline__ uint32_t swizzle_mode(int di)
     return di == 128 ? 2u : (di == 64 ? 4u : 6u);  // 128B, 64B, 32B
 }
 
-// tcgen05.ld 32 lanes x 16 columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 // sum_h w[h] * ReLU(acc[h]) over one query position's HI columns (HI a multiple
 // of 32), which start at tensor-memory address `taddr` of this warp's lane
 // quarter; w is this warp's copy in shared memory.  Four partial sums keep the
