@@ -7,20 +7,25 @@
 // same vector.
 //
 // One CTA = one (sequence, position) query and a contiguous share of its
-// selection, in tiles of 128 selected rows.  Per tile:
-//   1. each thread gathers one selected FP4 row (D/2 code bytes + D/16 scale
-//      bytes) and dequantises it to fp16 in registers (E2M1 x E4M3 is exact in
-//      fp16) into a K-major 128B-swizzled tile V[128 rows][D];
-//   2. S^T = V . Q^T on the tensor cores (M = 128 rows, N = heads, K = D), with
-//      Q staged 256 dims at a time as fp16 scaled per head by a power of two
-//      (exact for bf16 queries, and safe from fp16 overflow);
-//   3. S^T goes through shared memory so that each thread owns one head's
-//      logits; softmax statistics with a lazily rescaled running maximum;
-//   4. O^T += V^T . P^T with P split into fp16 high and low parts (two MMAs
-//      into the same fp32 accumulator), which keeps P's precision near fp32.
-//      V^T is read from the same tile through an MN-major descriptor.
+// selection, in tiles of 64 selected rows, as a warp-specialised pipeline:
+//   gather warps   fetch one tile ahead: each thread holds half of one FP4 row
+//                  (D/4 code bytes + D/32 scale bytes) in registers, then
+//                  dequantises it to fp16 (E2M1 x E4M3 is exact in fp16) into a
+//                  K-major 128B-swizzled tile V[64 rows][D] (two buffers);
+//   MMA thread     S = Q . V^T (M = 64 heads, N = 64 rows, K = D; Q staged once
+//                  per CTA as fp16 scaled per head by a power of two, exact for
+//                  bf16 and safe from fp16 overflow), and O^T += V^T . P^T with
+//                  P split into fp16 high and low parts (two MMAs into one fp32
+//                  accumulator keep P's precision near fp32); V^T is read from
+//                  the same tile through an MN-major descriptor.  S of tile t+1
+//                  is issued before O^T of tile t, so the tensor core works
+//                  while the softmax runs;
+//   softmax warps  one thread per head: the head's 64 logits come out of tensor
+//                  memory as one row, so max, exp2 and sums need no cross-thread
+//                  traffic; the running maximum is rescaled lazily (only when
+//                  it grows by more than 2^8).
 // The accumulator O^T [D x heads] stays in tensor memory across the CTA's tiles;
-// at the end the CTA writes either the final output (one split) or a partial
+// at the end the softmax warps write the final output (one split) or a partial
 // (O, m, l) that the merge kernel combines.
 #include <cuda_fp16.h>
 
@@ -30,17 +35,19 @@
 namespace csa {
 namespace {
 
-constexpr int kRows = 128;         // selected rows per tile (MMA M for S^T)
-constexpr int kThreads = 256;      // 8 warps: two per tensor-memory lane quarter
-constexpr int kMaxHeads = 64;
-constexpr float kRescaleLog2 = 8.f;  // rescale only when the running max grows by more than 2^8
+constexpr int kRows = 64;           // selected rows per tile (MMA N of S, K of O^T)
+constexpr int kSoftWarps = 4;       // one per tensor-memory lane quarter
+constexpr int kGatherWarps = 4;     // two threads per selected row
+constexpr int kThreads = 32 * (kSoftWarps + kGatherWarps + 1);  // + the MMA warp
+constexpr int kMaxHeads = 64;       // S uses M = 64 (heads, zero-padded)
+constexpr float kRescaleLog2 = 8.f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct AttArgs {
     CacheView c;
     int P, H, K;
-    int NH;           // heads rounded up to 16 (MMA N)
+    int NH;           // heads rounded up to 16 (MMA N of O^T)
     const uint16_t *q;
     float scale;
     const int32_t *idx;
@@ -101,16 +108,17 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float sc)
     return make_uint4(r4[0], r4[1], r4[2], r4[3]);
 }
 
-// Every thread waits for the MMAs committed to `bar`; the verdict is read after a
-// CTA barrier so that all threads agree on it even if one wait ran out.
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, volatile int *abort_flag)
-{
-    mbar_wait(bar, phase, abort_flag);
-    phase ^= 1;
-    __syncthreads();
-    tc_fence_after();
-    return *abort_flag == 0;
-}
+struct AttSmem {
+    uint64_t vfull[2], vempty[2], sfull[2], sempty[2], pfull[2], pempty[2], xbar, done;
+    uint32_t valid[2][2];     // row-valid bits of each V buffer
+    float fac[2][kMaxHeads];  // rescale factor per head, by tile parity
+    float cfac[kMaxHeads];    // scale * log2(e) * 2^-e per head (e: power of two applied to Q)
+    float l_fin[kMaxHeads];   // final softmax sums (for the epilogue)
+    float m_fin[kMaxHeads];
+    int flag[2];              // == tile + 1 when some head rescales at that tile (by parity)
+    uint32_t tmem_slot;
+    int abort;
+};
 
 __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
 {
@@ -118,50 +126,51 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *base = smem_raw + ((1024 - (raw & 1023)) & 1023);
     const int D = a.c.D, NH = a.NH, H = a.H;
-    const int v_bytes = kRows * D * 2;
-    const int qh_bytes = NH * 256 * 2;        // one 256-dim chunk of Q
-    const int sst_bytes = kRows * (NH + 1) * 4;
-    const int qs_bytes = qh_bytes > sst_bytes ? qh_bytes : sst_bytes;
-    const int p_bytes = NH * kRows * 2;
-    uint8_t *v_s = base;
-    uint8_t *q_s = v_s + v_bytes;                               // Q chunk, then S^T staging
-    uint8_t *p_hi = q_s + ((qs_bytes + 1023) & ~1023);
-    uint8_t *p_lo = p_hi + p_bytes;
-    float *st = reinterpret_cast<float *>(p_lo + p_bytes);     // per-head state
-    float *m_run = st;                 // running max (log2 units)
-    float *l_run = m_run + kMaxHeads;  // running sum
-    float *fac = l_run + kMaxHeads;    // rescale factor this tile
-    float *cfac = fac + kMaxHeads;     // scale * log2(e) * 2^-e (e: power of two applied to Q)
-    uint32_t *valid = reinterpret_cast<uint32_t *>(cfac + kMaxHeads);  // [kRows/32] bit masks
-    uint64_t *mma_bar = reinterpret_cast<uint64_t *>(valid + kRows / 32);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_bar + 1);
-    int *flags = reinterpret_cast<int *>(tmem_slot + 1);  // [0] rescale needed, [1] abort
-    volatile int *abort_flag = flags + 1;
+    uint8_t *q_s = base;                                    // [64 heads][D] fp16, K-major SW128
+    uint8_t *v_s = q_s + kMaxHeads * D * 2;                 // 2 x [64 rows][D]
+    uint8_t *p_s = v_s + 2 * kRows * D * 2;                 // 2 x {hi, lo} x [NH heads][64 rows]
+    const int p_bytes = NH * kRows * 2;                     // one P tile
+    AttSmem &sm = *reinterpret_cast<AttSmem *>(p_s + 4 * p_bytes);
+    volatile int *abort_flag = &sm.abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, whalf = warp >> 2;  // tensor-memory lane quarter; column half
     const int unit = blockIdx.y, split = blockIdx.x;
     const int b = unit / a.P;
     const int len = a.c.lengths[b];
     const int t_first = split * a.tiles_per_split;
     const int t_last = min(a.tiles_total, t_first + a.tiles_per_split);
+    const int n_tiles = max(0, t_last - t_first);
     const int32_t *irow = a.idx + static_cast<int64_t>(unit) * a.K;
+    const int mma_warp = kSoftWarps + kGatherWarps;
 
     if (tid == 0) {
-        mbar_init(mma_bar, 1);
-        flags[0] = 0;
-        flags[1] = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.vfull[i], 32 * kGatherWarps);
+            mbar_init(&sm.vempty[i], 1);
+            mbar_init(&sm.sfull[i], 1);
+            mbar_init(&sm.sempty[i], 32 * kSoftWarps);
+            sm.flag[i] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.pfull[i], 32 * kSoftWarps);
+            mbar_init(&sm.pempty[i], 1);
+        }
+        mbar_init(&sm.xbar, 32 * kSoftWarps);
+        mbar_init(&sm.done, 1);
+        sm.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, a.tmem_cols);
+    if (warp == mma_warp) {
+        tmem_alloc(&sm.tmem_slot, a.tmem_cols);
         tmem_relinquish();
     }
 
-    // The selected rows of a tile are fetched one tile ahead: thread (row r,
-    // half rh) holds half of one FP4 row (D/4 code bytes, D/32 scale bytes).
-    const int gr = tid & (kRows - 1), grh = tid >> 7;
-    const int nc = D / 64;  // 16-byte code pieces per half row (32 channels each)
+    // Gather-warp state: the rows of tile i+1 are loaded while tile i is used;
+    // thread (row gr, half grh) holds half of one FP4 row.
+    const bool is_gather = warp >= kSoftWarps && warp < mma_warp;
+    const int gt = tid - 32 * kSoftWarps;
+    const int gr = gt & (kRows - 1), grh = (gt >> 6) & 1;
+    const int nc = D / 64;  // 16-byte code pieces per half row
     int32_t nrow = -1;
     uint4 ncw[8];
     uint32_t nsw[4];
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         const int j = tile * kRows + gr;
         int32_t row = j < a.K ? irow[j] : -1;
         if (row >= len) {
-            raise_status(a.status, CSA_DEV_BAD_INDEX);
+            if (grh == 0) raise_status(a.status, CSA_DEV_BAD_INDEX);
             row = -1;
         }
         nrow = row;
@@ -181,20 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
 #pragma unroll
         for (int i = 0; i < 4; ++i) nsw[i] = (row >= 0 && i < D / 128) ? sp[i] : 0u;
     };
-    if (t_first < t_last) prefetch(t_first);
+    if (is_gather && n_tiles > 0) prefetch(t_first);  // in flight while Q is staged
 
-    // Q lives in registers for the whole CTA, as fp16 scaled per head by a power
-    // of two: thread (head qh, quarter qq) holds dims [qq*D/4, (qq+1)*D/4).
-    const int qh = tid >> 2, qq = tid & 3;
-    const int qn = D / 32;  // 16-byte pieces per thread
-    uint4 qreg[16];
-    {
+    // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15: thread (head
+    // qh, quarter qq) of the first 256 threads converts dims [qq*D/4, (qq+1)*D/4).
+    if (tid < 4 * kMaxHeads) {
+        const int qh = tid >> 2, qq = tid & 3, qn = D / 32;
+        uint4 qreg[16];
         const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(unit) * H + qh) * D) + qq * qn;
 #pragma unroll
         for (int i = 0; i < 16; ++i) qreg[i] = (qh < H && i < qn) ? src[i] : make_uint4(0, 0, 0, 0);
-    }
-    // Per-head power of two e with max|q| * 2^e < 2^15 (fp16-safe, exact for bf16).
-    {
         uint32_t emax = 0;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -207,42 +212,85 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         const float e = emax > 0 ? 14.f - (static_cast<float>(emax) - 127.f) : 0.f;
         const float qscale = exp2f(e);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) qreg[i] = bf16x8_to_f16x8(qreg[i], qscale);
-        if (qq == 0) {
-            cfac[qh] = a.scale * kLog2e * exp2f(-e);
-            m_run[qh] = -INFINITY;
-            l_run[qh] = 0.f;
-        }
+        for (int i = 0; i < 16; ++i)
+            if (i < qn) *reinterpret_cast<uint4 *>(q_s + sw128_off(qh, qq * (D / 4) + i * 8, kMaxHeads)) =
+                            bf16x8_to_f16x8(qreg[i], qscale);
+        if (qq == 0) sm.cfac[qh] = a.scale * kLog2e * exp2f(-e);
     }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s = tmem;             // S^T: NH columns
-    const uint32_t t_o = tmem + NH;        // O^T: (D/128) blocks of NH columns
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t v_base = smem_u32(v_s), q_base = smem_u32(q_s);
-    const uint32_t phi_base = smem_u32(p_hi), plo_base = smem_u32(p_lo);
-    uint32_t mma_phase = 0;
-    bool o_started = false;
-    bool ok = true;
-    const uint32_t idesc_s = instr_desc(128, NH, 0, 0, 0, 0);   // K-major V, K-major Q
-    const uint32_t idesc_o = instr_desc(128, NH, 0, 0, 1, 0);   // MN-major V^T, K-major P
+    const uint32_t tmem = sm.tmem_slot;
+    const uint32_t t_s = tmem;                 // S: 2 buffers x 64 columns (rows of the tile)
+    const uint32_t t_o = tmem + 2 * kRows;     // O^T: (D/128) blocks of NH columns
 
-    for (int tile = t_first; tile < t_last && ok; ++tile) {
-        // ---- 1. dequantise the prefetched rows into the fp16 tile V
-        {
-            const unsigned vb = __ballot_sync(0xFFFFFFFFu, nrow >= 0);
-            if (grh == 0 && lane == 0) valid[gr >> 5] = vb;
+    if (warp == mma_warp) {
+        // ------------------------------------------------------------ MMA thread
+        if (lane == 0 && n_tiles > 0) {
+            const uint32_t v_bytes = kRows * D * 2;
+            const uint32_t idesc_s = instr_desc(64, kRows, 0, 0, 0, 0);  // K-major Q, K-major V
+            const uint32_t idesc_o = instr_desc(128, NH, 0, 0, 1, 0);    // MN-major V^T, K-major P
+            // Descriptors are built once; an MMA's operand is the base plus a
+            // byte offset added to the start-address field (>> 4).
+            const uint64_t dq = smem_desc(smem_u32(q_s), 16, 1024, 2);
+            const uint64_t dv = smem_desc(smem_u32(v_s), 16, 1024, 2);
+            const uint64_t dvt = smem_desc(smem_u32(v_s), kRows * 128 /*next 64 dims*/, 1024 /*next 8 rows*/, 2);
+            const uint64_t dp = smem_desc(smem_u32(p_s), 16, 1024, 2);
+            auto issue_pv = [&](int i) -> bool {
+                if (!mbar_wait(&sm.pfull[i & 1], (i >> 1) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint64_t vb = dvt + (((i & 1) * v_bytes) >> 4);
+                for (int mt = 0; mt < D / 128; ++mt)
+                    for (int hl = 0; hl < 2; ++hl) {
+                        const uint64_t pb = dp + ((((i & 1) * 2 + hl) * p_bytes) >> 4);
+#pragma unroll
+                        for (int ks = 0; ks < kRows / 16; ++ks)
+                            mma_f16(t_o + mt * NH, vb + ((2 * mt * kRows * 128 + ks * 2048) >> 4), pb + ((ks * 32) >> 4),
+                                    idesc_o, (i > 0 || hl > 0 || ks > 0) ? 1u : 0u);
+                    }
+                mma_commit(&sm.pempty[i & 1]);
+                mma_commit(&sm.vempty[i & 1]);
+                return true;
+            };
+            bool ok = true;
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const uint32_t par = (i >> 1) & 1;
+                if (!mbar_wait(&sm.vfull[i & 1], par, abort_flag)) break;
+                if (!mbar_wait(&sm.sempty[i & 1], par ^ 1, abort_flag)) break;
+                tc_fence_after();
+                const uint64_t vb = dv + (((i & 1) * v_bytes) >> 4);
+                for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(t_s + (i & 1) * kRows, dq + ((kb * kMaxHeads * 128 + ks * 32) >> 4),
+                                vb + ((kb * kRows * 128 + ks * 32) >> 4), idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&sm.sfull[i & 1]);
+                if (i > 0) ok = issue_pv(i - 1);
+            }
+            if (ok && !*abort_flag) issue_pv(n_tiles - 1);
+            mma_commit(&sm.done);
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(&sm.done, 0) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else if (is_gather) {
+        // ------------------------------------------------------------ gather warps
+        for (int i = 0; i < n_tiles; ++i) {
+            if (!mbar_wait(&sm.vempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+            uint8_t *vb = v_s + (i & 1) * kRows * D * 2;
+            const unsigned vbits = __ballot_sync(0xFFFFFFFFu, nrow >= 0);
+            if (grh == 0 && lane == 0) sm.valid[i & 1][gr >> 5] = vbits;
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) {
                 if (c16 >= nc) break;
-                const uint32_t sc = (nsw[c16 >> 1] >> (16 * (c16 & 1))) & 0xFFFF;  // the 2 scales of 32 channels
+                const uint32_t sc = (nsw[c16 >> 1] >> (16 * (c16 & 1))) & 0xFFFF;  // 2 scales of 32 channels
                 const uint32_t s0 = e4m3_to_h2(sc & 0xFF), s1 = e4m3_to_h2(sc >> 8);
                 const uint32_t words[4] = {ncw[c16].x, ncw[c16].y, ncw[c16].z, ncw[c16].w};
                 const int ch0 = grh * (D / 2) + c16 * 32;
 #pragma unroll
-                for (int h8 = 0; h8 < 4; ++h8) {  // 8 channels = 4 code bytes -> one 16-byte chunk
+                for (int h8 = 0; h8 < 4; ++h8) {
                     const uint32_t sv = h8 < 2 ? s0 : s1;
                     const uint32_t wd = words[h8];
                     uint4 o;
@@ -250,72 +298,91 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                     o.y = dequant_pair((wd >> 8) & 0xFF, sv);
                     o.z = dequant_pair((wd >> 16) & 0xFF, sv);
                     o.w = dequant_pair(wd >> 24, sv);
-                    *reinterpret_cast<uint4 *>(v_s + sw128_off(gr, ch0 + h8 * 8, kRows)) = o;
+                    *reinterpret_cast<uint4 *>(vb + sw128_off(gr, ch0 + h8 * 8, kRows)) = o;
                 }
             }
-        }
-        // ---- 2. S^T = V . Q^T, Q staged in 256-dim chunks from registers
-        for (int d0 = 0; d0 < D && ok; d0 += 256) {
-            const int dn = min(256, D - d0);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int dim = qq * (D / 4) + i * 8;
-                if (i < qn && qh < NH && dim >= d0 && dim < d0 + dn)
-                    *reinterpret_cast<uint4 *>(q_s + sw128_off(qh, dim - d0, NH)) = qreg[i];
-            }
             fence_async_smem();
+            mbar_arrive(&sm.vfull[i & 1]);
+            if (i + 1 < n_tiles) prefetch(t_first + i + 1);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        // Head h = 16*warp + (lane & 15) is tensor-memory lane 32*warp + (lane & 15)
+        // of S; lane < 16 takes the tile's rows 0..31, lane + 16 rows 32..63.
+        const int h = warp * 16 + (lane & 15), ch = lane >> 4;
+        const bool active = h < H;
+        const float cf = sm.cfac[h];
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int i = 0; i < n_tiles && ok; ++i) {
+            const uint32_t par = (i >> 1) & 1;
+            ok = mbar_wait(&sm.sfull[i & 1], par, abort_flag) && mbar_wait(&sm.vfull[i & 1], par, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t z[32];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+                "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;"
+                : "=r"(z[0]), "=r"(z[1]), "=r"(z[2]), "=r"(z[3]), "=r"(z[4]), "=r"(z[5]), "=r"(z[6]), "=r"(z[7]),
+                  "=r"(z[8]), "=r"(z[9]), "=r"(z[10]), "=r"(z[11]), "=r"(z[12]), "=r"(z[13]), "=r"(z[14]),
+                  "=r"(z[15]), "=r"(z[16]), "=r"(z[17]), "=r"(z[18]), "=r"(z[19]), "=r"(z[20]), "=r"(z[21]),
+                  "=r"(z[22]), "=r"(z[23]), "=r"(z[24]), "=r"(z[25]), "=r"(z[26]), "=r"(z[27]), "=r"(z[28]),
+                  "=r"(z[29]), "=r"(z[30]), "=r"(z[31])
+                : "r"(t_s + (i & 1) * kRows + lane_off));
+            tmem_ld_wait();
             tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                for (int kb = 0; kb < dn / 64; ++kb)
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t da =
-                            smem_desc(v_base + ((d0 / 64) + kb) * kRows * 128 + ks * 32, 16, 1024, 2);
-                        const uint64_t db = smem_desc(q_base + kb * NH * 128 + ks * 32, 16, 1024, 2);
-                        mma_f16(t_s, da, db, idesc_s, (d0 > 0 || kb > 0 || ks > 0) ? 1u : 0u);
-                    }
-                mma_commit(mma_bar);
-            }
-            __syncwarp();
-            ok = wait_mma(mma_bar, mma_phase, abort_flag);
-        }
-        if (!ok) break;
-        if (tile + 1 < t_last) prefetch(tile + 1);  // in flight during softmax and PV
-        // ---- 3. logits via shared memory (thread = row, then thread quad = head)
-        float *sst = reinterpret_cast<float *>(q_s);  // [kRows][NH+1]
-        {
-            const int row = quarter * 32 + lane;
-            for (int c0 = whalf * 16; c0 < NH; c0 += 32) {  // 16-column groups alternate between the warp halves
-                uint32_t r16[16];
-                tmem_ld16(t_s + lane_off + c0, r16);
-                tmem_ld_wait();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) sst[row * (NH + 1) + c0 + k] = __uint_as_float(r16[k]);
-            }
-        }
-        __syncthreads();
-        {
-            const int h = tid >> 2, part = tid & 3;  // 64 heads x 4 parts of 32 rows
-            const float cf = h < H ? cfac[h] : 0.f;
-            const uint32_t vbits = valid[part];
-            float z[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                z[k] = (h < H && (vbits >> k & 1)) ? sst[(part * 32 + k) * (NH + 1) + h] * cf : -INFINITY;
+            mbar_arrive(&sm.sempty[i & 1]);
+            const uint32_t vbits = sm.valid[i & 1][ch];
             float tmax = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) tmax = fmaxf(tmax, z[k]);
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 2));
-            float mu = h < kMaxHeads ? m_run[h] : -INFINITY;
-            float f = 1.f;
-            if (h < H && tmax > -INFINITY && (mu == -INFINITY || tmax > mu + kRescaleLog2)) {
-                f = mu == -INFINITY ? 0.f : fast_exp2(mu - tmax);
-                mu = tmax;
+            for (int k = 0; k < 32; ++k) {
+                const float zz = (vbits >> k & 1) ? __uint_as_float(z[k]) * cf : -INFINITY;
+                z[k] = __float_as_uint(zz);
+                tmax = fmaxf(tmax, zz);
             }
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 16));
+            float f = 1.f;
+            if (active && tmax > -INFINITY && (m_run == -INFINITY || tmax > m_run + kRescaleLog2)) {
+                f = m_run == -INFINITY ? 0.f : fast_exp2(m_run - tmax);
+                m_run = tmax;
+            }
+            if (lane < 16) sm.fac[i & 1][h] = f;
+            const bool mine = i > 0 && f != 1.f;
+            if (__any_sync(0xFFFFFFFFu, mine) && lane == 0) sm.flag[i & 1] = i + 1;
+            // Every softmax thread sees every head's factor and the flag; the P
+            // buffer of this tile is free once O^T of tile i-2 is done.
+            mbar_arrive(&sm.xbar);
+            ok = mbar_wait(&sm.xbar, i & 1, abort_flag) &&
+                 mbar_wait(&sm.pempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            if (sm.flag[i & 1] == i + 1) {
+                // Rescale O^T: wait for O^T of tile i-1, then this warp's quarter of
+                // the lanes (dims) of every 128-dim block, all head columns.
+                if (!mbar_wait(&sm.pempty[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int mt = 0; mt < D / 128; ++mt)
+                    for (int c0 = 0; c0 < NH; c0 += 16) {
+                        uint32_t r16[16];
+                        const uint32_t ta = t_o + mt * NH + lane_off + c0;
+                        tmem_ld16(ta, r16);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            r16[k] = __float_as_uint(__uint_as_float(r16[k]) * sm.fac[i & 1][c0 + k]);
+                        tmem_st16(ta, r16);
+                    }
+                tmem_st_wait();
+            }
+            l_run *= f;
             float lsum = 0.f;
             if (h < NH) {
+                uint8_t *ph_s = p_s + (i & 1) * 2 * p_bytes, *pl_s = ph_s + p_bytes;
 #pragma unroll
                 for (int k8 = 0; k8 < 4; ++k8) {
                     uint32_t hw[4], lw[4];
@@ -324,104 +391,71 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                         __half ph[2], pl[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const float zz = z[k8 * 8 + k2 * 2 + e];
-                            const float p = (zz > -INFINITY && mu > -INFINITY) ? fast_exp2(zz - mu) : 0.f;
-                            lsum += p;
-                            ph[e] = __float2half_rn(p);
-                            pl[e] = __float2half_rn(p - __half2float(ph[e]));
+                            const float zz = __uint_as_float(z[k8 * 8 + k2 * 2 + e]);
+                            const float pv = (active && zz > -INFINITY) ? fast_exp2(zz - m_run) : 0.f;
+                            lsum += pv;
+                            ph[e] = __float2half_rn(pv);
+                            pl[e] = __float2half_rn(pv - __half2float(ph[e]));
                         }
                         hw[k2] = pack_half2(ph[0], ph[1]);
                         lw[k2] = pack_half2(pl[0], pl[1]);
                     }
-                    const uint32_t off = sw128_off(h, part * 32 + k8 * 8, NH);
-                    *reinterpret_cast<uint4 *>(p_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4 *>(p_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    const uint32_t off = sw128_off(h, ch * 32 + k8 * 8, NH);
+                    *reinterpret_cast<uint4 *>(ph_s + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(pl_s + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
-            lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
-            lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
-            if (part == 0 && h < kMaxHeads) {
-                fac[h] = f;
-                if (f != 1.f) flags[0] = 1;
-                m_run[h] = mu;
-                l_run[h] = l_run[h] * f + lsum;
-            }
+            lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+            l_run += lsum;
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.pfull[i & 1]);
         }
-        __syncthreads();
-        // ---- rescale O^T when some head's running max moved by more than 2^8 (rare)
-        if (flags[0] && o_started) {
-            for (int mt = whalf; mt < D / 128; mt += 2)
-                for (int c0 = 0; c0 < NH; c0 += 16) {
-                    uint32_t r16[16];
-                    const uint32_t ta = t_o + mt * NH + lane_off + c0;
-                    tmem_ld16(ta, r16);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) r16[k] = __float_as_uint(__uint_as_float(r16[k]) * fac[c0 + k]);
-                    tmem_st16(ta, r16);
-                }
-            tmem_st_wait();
+        // ---- epilogue: the last O^T update done -> result or partial
+        if (ok && n_tiles > 0) ok = mbar_wait(&sm.pempty[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag);
+        if (lane < 16) {
+            sm.l_fin[h] = l_run;
+            sm.m_fin[h] = m_run;
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) flags[0] = 0;
-        // ---- 4. O^T += V^T . P_hi^T + V^T . P_lo^T
-        if (tid == 0) {
+        mbar_arrive(&sm.xbar);
+        if (ok) ok = mbar_wait(&sm.xbar, n_tiles & 1, abort_flag);
+        if (ok) {
             tc_fence_after();
-            for (int mt = 0; mt < D / 128; ++mt)
-                for (int hl = 0; hl < 2; ++hl) {
-                    const uint32_t pb = hl ? plo_base : phi_base;
-                    for (int ks = 0; ks < kRows / 16; ++ks) {
-                        const uint64_t da = smem_desc(v_base + (2 * mt) * kRows * 128 + ks * 2048,
-                                                      kRows * 128 /*next 64 dims*/, 1024 /*next 8 rows*/, 2);
-                        const uint64_t db = smem_desc(pb + (ks >> 2) * NH * 128 + (ks & 3) * 32, 16, 1024, 2);
-                        mma_f16(t_o + mt * NH, da, db, idesc_o, (o_started || hl > 0 || ks > 0) ? 1u : 0u);
-                    }
+            const bool final_out = a.nsplit == 1;
+            float *obase = final_out ? a.out + static_cast<int64_t>(unit) * H * D
+                                     : a.part_o + (static_cast<int64_t>(unit) * a.nsplit + split) * H * D;
+            for (int mt = 0; mt < D / 128; ++mt) {
+                const int d = mt * 128 + warp * 32 + lane;
+                uint32_t r[kMaxHeads];
+#pragma unroll
+                for (int c0 = 0; c0 < kMaxHeads; c0 += 16)
+                    if (c0 < NH) tmem_ld16(t_o + mt * NH + lane_off + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+                tmem_ld_wait();
+#pragma unroll
+                for (int hh = 0; hh < kMaxHeads; ++hh) {
+                    if (hh >= H) break;
+                    float v = n_tiles > 0 ? __uint_as_float(r[hh]) : 0.f;
+                    const float lh = sm.l_fin[hh];
+                    if (final_out) v = lh > 0.f ? v * __frcp_rn(lh) : 0.f;
+                    obase[static_cast<int64_t>(hh) * D + d] = v;
                 }
-            mma_commit(mma_bar);
+            }
+            if (lane < 16 && active) {
+                if (final_out) {
+                    if (a.lse)
+                        a.lse[static_cast<int64_t>(unit) * H + h] =
+                            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                } else {
+                    a.part_ml[(static_cast<int64_t>(unit) * a.nsplit + split) * H + h] = make_float2(m_run, l_run);
+                }
+            }
         }
-        __syncwarp();
-        ok = wait_mma(mma_bar, mma_phase, abort_flag);
-        o_started = true;
     }
 
-    // ---- the result (one split) or this split's partial (merged by the next kernel)
-    if (ok) {
-        __syncthreads();
-        const bool final_out = a.nsplit == 1;
-        float *obase = final_out ? a.out + static_cast<int64_t>(unit) * H * D
-                                 : a.part_o + (static_cast<int64_t>(unit) * a.nsplit + split) * H * D;
-        for (int mt = whalf; mt < D / 128; mt += 2) {  // thread = one dim of a 128-dim block
-            const int d = mt * 128 + quarter * 32 + lane;
-            uint32_t r[kMaxHeads];
-#pragma unroll
-            for (int c0 = 0; c0 < kMaxHeads; c0 += 16)
-                if (c0 < NH) tmem_ld16(t_o + mt * NH + lane_off + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < kMaxHeads; ++h) {
-                if (h >= H) break;
-                float v = o_started ? __uint_as_float(r[h]) : 0.f;
-                if (final_out) v = l_run[h] > 0.f ? v * __frcp_rn(l_run[h]) : 0.f;
-                obase[static_cast<int64_t>(h) * D + d] = v;
-            }
-        }
-        if (tid < H) {
-            if (final_out) {
-                if (a.lse)
-                    a.lse[static_cast<int64_t>(unit) * H + tid] =
-                        l_run[tid] > 0.f ? (m_run[tid] + log2f(l_run[tid])) * kLn2 : -INFINITY;
-            } else {
-                a.part_ml[(static_cast<int64_t>(unit) * a.nsplit + split) * H + tid] =
-                    make_float2(m_run[tid], l_run[tid]);
-            }
-        }
-    }
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && tid == 0) raise_status(a.status, CSA_DEV_TIMEOUT);
-    if (warp == 0) {
+    if (warp == mma_warp) {
         tc_fence_after();
         tmem_dealloc(tmem, a.tmem_cols);
     }
@@ -489,11 +523,8 @@ Plan plan(const CacheView &c, int P, int K)
 
 size_t smem_bytes(int D, int NH)
 {
-    const size_t v = static_cast<size_t>(kRows) * D * 2;
-    const size_t qh = static_cast<size_t>(NH) * 256 * 2, sst = static_cast<size_t>(kRows) * (NH + 1) * 4;
-    const size_t qs = ((qh > sst ? qh : sst) + 1023) & ~size_t(1023);
-    const size_t p = 2 * static_cast<size_t>(NH) * kRows * 2;
-    return 1024 + v + qs + p + 4 * kMaxHeads * 4 + kRows * 4 + 64;
+    return 1024 + static_cast<size_t>(kMaxHeads) * D * 2 + 2 * static_cast<size_t>(kRows) * D * 2 +
+           4 * static_cast<size_t>(NH) * kRows * 2 + sizeof(AttSmem);
 }
 
 }  // namespace
@@ -535,7 +566,7 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     a.out = out;
     a.lse = lse;
     uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(a.NH + (c.D / 128) * a.NH)) cols *= 2;
+    while (cols < static_cast<uint32_t>(2 * kRows + (c.D / 128) * a.NH)) cols *= 2;
     a.tmem_cols = cols;
     a.status = status;
     const size_t smem = smem_bytes(c.D, a.NH);
