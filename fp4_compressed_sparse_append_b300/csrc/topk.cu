@@ -6,20 +6,22 @@
 //
 // One thread-block cluster per query row (or per segment of a very long row).
 // The candidates are split into contiguous chunks, one per CTA, held in shared
-// memory as order-preserving 32-bit keys.  The K-th largest key is found by a
-// bucket select that adapts to the data: pass 0 finds the key range [lo, hi];
-// each pass histograms the live range into at most 2048 buckets of 2^shift
-// keys, so no pass wastes bins on bit patterns no score has.  The CTAs push
-// their histograms to the CTA that owns each bucket range (distributed shared
-// memory stores, then a cluster barrier); the owner of the bucket holding the
-// K-th key broadcasts it.  At most three passes resolve a 32-bit key.  Ties at
-// the threshold go to the lower row id: each CTA knows how many tied
-// candidates precede its chunk.  Output ids are written in ascending order.
+// memory as order-preserving 32-bit keys (0 = no candidate).  The K-th largest
+// key is found by a most-significant-digit radix select with fixed digits of
+// 12, 12 and 8 bits: each pass histograms, in shared memory, the keys whose
+// higher digits equal the threshold found so far, then every CTA adds its
+// non-zero bins into every CTA's cluster-wide histogram (distributed shared
+// memory reductions) and one cluster barrier later all CTAs hold the same
+// histogram and find the same threshold bin.  A pass stops early when the
+// threshold bin is taken whole, so typical data needs one or two passes.  Ties
+// at the final key go to the lower row id.  Output ids are written in ascending
+// order: per (iteration, warp) counts from warp ballots, one block scan, and
+// one exchange of per-CTA counts give every selected key its position.
 //
-// Rows longer than 16 x 12288 candidates are split into segments: stage 1
-// keeps each segment's own top K (with scores) in the workspace; stage 2
-// selects the row's top K among those, which is exact because every member of
-// the row's top K is in its segment's top K (the same order decides both).
+// Rows longer than one cluster holds are split into segments: stage 1 keeps
+// each segment's own top K (with scores) in the workspace; stage 2 selects the
+// row's top K among those, which is exact because every member of the row's
+// top K is in its segment's top K (the same order decides both).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -32,14 +34,18 @@ namespace {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kBins = 2048;
-constexpr int kSelCache = 12288;  // keys held per CTA (48 KB)
+constexpr int kDigit0Bins = 4096;    // key bits 31..20
+constexpr int kDigit1Bins = 4096;    // key bits 19..8
+constexpr int kDigit2Bins = 256;     // key bits 7..0
+constexpr int kSelCacheMax = 11264;  // keys held per CTA at most (44 KB): two CTAs fit one SM
+constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
+constexpr int kMinChunk = 4096;      // a row is not spread thinner than this per CTA
+constexpr int64_t kSegmentLen = static_cast<int64_t>(kMaxCluster) * 8192;
 
 enum SelSource { kRows = 0, kBlocks = 1, kPoolRows = 2, kPairs = 3 };
 
 struct SelArgs {
-    int source;
     const float *scores;       // kRows/kBlocks/kPoolRows: [rows][ld];  kPairs: [rows][n_pairs]
     int64_t ld;
     const int32_t *lengths;
@@ -55,56 +61,53 @@ struct SelArgs {
     float *out_scores;         // segments > 1: [rows*segments][K]
 };
 
-// Per-CTA shared state.  CTAs of a cluster only ever WRITE into each other's
-// shared memory, and every such write is followed by a cluster barrier before
-// it is read; no CTA loads from another CTA's shared memory.
+// Per-CTA shared state.  Other CTAs of the cluster only ever add into g0/g1/g2
+// and store into cnt_above/cnt_eq, and every such write is followed by a
+// cluster barrier before it is read; no CTA loads another CTA's shared memory.
 struct SelShared {
-    uint32_t hist[kBins];                 // this CTA's histogram of the current pass
-    uint32_t stage[kBins];                // [source CTA][buckets owned here], pushed by every CTA
-    uint32_t slice[kBins];                // owned buckets summed over the cluster
-    uint32_t scratch[kSelThreads];
-    uint32_t cnt_all[kMaxCluster];        // pass 0 counts (pushed)
-    uint32_t min_all[kMaxCluster];
-    uint32_t max_all[kMaxCluster];
-    uint32_t totals[kMaxCluster];         // owned-slice totals (pushed)
-    uint32_t sel_all[kMaxCluster];        // selected counts per CTA (pushed)
-    uint32_t eq_all[kMaxCluster];         // counts at the threshold per CTA (pushed)
-    uint32_t res_bucket, res_gt, res_class;
+    uint32_t l0[kDigit0Bins];  // this CTA's histogram, digit 0
+    uint32_t g0[kDigit0Bins];  // cluster-wide histogram, digit 0
+    uint32_t l1[kDigit1Bins];
+    uint32_t g1[kDigit1Bins];
+    uint32_t l2[kDigit2Bins];
+    uint32_t g2[kDigit2Bins];
+    uint32_t cnt_above[kMaxCluster];     // per-CTA count of keys above the threshold
+    uint32_t cnt_eq[kMaxCluster];        // per-CTA count of keys at the threshold
+    uint32_t jw[kMaxIters * kSelWarps];  // per (iteration, warp): above << 16 | equal
     uint32_t warp_tot[kSelWarps];
+    uint32_t res_bin, res_above;
 };
+constexpr int kZeroWords = 2 * (kDigit0Bins + kDigit1Bins + kDigit2Bins);
 
+template <int S>
 struct RowView {
-    int source;
     const float *s;
     const int32_t *prow;
     const int32_t *ids;
     int L;
     __device__ __forceinline__ uint32_t key(int64_t i) const
     {
-        switch (source) {
-        case kRows: return score_key(s[i]);
-        case kBlocks: {
+        if (S == kRows) return score_key(__ldg(s + i));
+        if (S == kBlocks) {
             const int64_t r0 = i * kPoolBlock;
-            float best = s[r0];
+            float best = __ldg(s + r0);
+#pragma unroll
             for (int m = 1; m < kPoolBlock; ++m)
-                if (r0 + m < L) best = fmaxf(best, s[r0 + m]);
+                if (r0 + m < L) best = fmaxf(best, __ldg(s + r0 + m));
             return score_key(best);
         }
-        case kPoolRows: {
-            const int32_t blk = prow[i >> 3];
+        if (S == kPoolRows) {
+            const int32_t blk = __ldg(prow + (i >> 3));
             const int64_t row = static_cast<int64_t>(blk) * kPoolBlock + (i & 7);
-            return (blk >= 0 && row < L) ? score_key(s[i]) : 0u;
+            return (blk >= 0 && row < L) ? score_key(__ldg(s + i)) : 0u;
         }
-        default: return ids[i] >= 0 ? score_key(s[i]) : 0u;
-        }
+        return __ldg(ids + i) >= 0 ? score_key(__ldg(s + i)) : 0u;
     }
     __device__ __forceinline__ int32_t id(int64_t i) const
     {
-        switch (source) {
-        case kPoolRows: return prow[i >> 3] * kPoolBlock + static_cast<int32_t>(i & 7);
-        case kPairs: return ids[i];
-        default: return static_cast<int32_t>(i);
-        }
+        if (S == kPoolRows) return __ldg(prow + (i >> 3)) * kPoolBlock + static_cast<int32_t>(i & 7);
+        if (S == kPairs) return __ldg(ids + i);
+        return static_cast<int32_t>(i);
     }
 };
 
@@ -113,6 +116,39 @@ __device__ __forceinline__ float key_score(uint32_t k)
 {
     const uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
     return __uint_as_float(b);
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(const void *local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_red_add(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_store(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_barrier()
+{
+    cluster_arrive();
+    cluster_wait();
 }
 
 // Block-wide exclusive scan of one value per thread; *total gets the sum.
@@ -143,49 +179,50 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
     return before;
 }
 
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t *warp_tot)
+// Adds this CTA's non-zero bins into every cluster CTA's copy of the histogram.
+__device__ __forceinline__ void push_histogram(const uint32_t *local, const uint32_t *global, int nb, int C)
 {
-    uint32_t t;
-    block_exclusive_scan(v, warp_tot, &t);
-    return t;
+    for (int b = threadIdx.x; b < nb; b += kSelThreads) {
+        const uint32_t v = local[b];
+        if (v)
+            for (int q = 0; q < C; ++q) cluster_red_add(cluster_addr(global + b, q), v);
+    }
 }
 
-__device__ __forceinline__ uint32_t block_min(uint32_t v, uint32_t *scratch)
+// Finds, in a cluster-wide histogram h of nb bins, the bin b holding the
+// need-th largest key: fewer than `need` keys lie in the bins above b and at
+// least `need` in b and above.  Thread t owns the nb/T bins just below the top
+// t*nb/T ones, so an exclusive scan over threads is the count above its range.
+// Returns the histogram total; sh.res_bin and sh.res_above (the count above
+// the bin) are set when the total is at least `need`.
+__device__ __forceinline__ uint32_t find_bin(const uint32_t *h, int nb, uint32_t need, SelShared &sh)
 {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    const int tid = threadIdx.x;
+    const int per = nb >= kSelThreads ? nb / kSelThreads : 1;
+    const int hi = nb - tid * per;
+    const int lo = hi - per;
+    uint32_t s = 0;
+    if (lo >= 0)
+        for (int b = lo; b < hi; ++b) s += h[b];
+    uint32_t total;
+    const uint32_t excl = block_exclusive_scan(s, sh.warp_tot, &total);
+    if (lo >= 0 && s && excl < need && excl + s >= need) {
+        uint32_t cum = excl;
+        for (int b = hi - 1; b >= lo; --b) {
+            if (cum + h[b] >= need) {
+                sh.res_bin = static_cast<uint32_t>(b);
+                sh.res_above = cum;
+                break;
+            }
+            cum += h[b];
+        }
+    }
     __syncthreads();
-    uint32_t r = 0xFFFFFFFFu;
-    for (int w = 0; w < kSelWarps; ++w) r = min(r, scratch[w]);
-    __syncthreads();
-    return r;
+    return total;
 }
 
-__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t *scratch)
-{
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    uint32_t r = 0;
-    for (int w = 0; w < kSelWarps; ++w) r = max(r, scratch[w]);
-    __syncthreads();
-    return r;
-}
-
-enum Rule { kAll, kRange, kTies };
-
-__device__ __forceinline__ bool selected(Rule rule, uint32_t k, uint32_t lo, uint32_t hi, uint32_t &tie_rank,
-                                         uint32_t take)
-{
-    if (rule == kAll) return k != 0;
-    if (rule == kRange) return k != 0 && k >= lo;
-    if (k == lo) return tie_rank++ < take;
-    return k > hi;
-}
-
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
+template <int S>
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
@@ -193,12 +230,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
     extern __shared__ __align__(16) uint8_t dyn_smem[];
     SelShared &sh = *reinterpret_cast<SelShared *>(dyn_smem);
     uint32_t *cache = reinterpret_cast<uint32_t *>(dyn_smem + sizeof(SelShared));
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const int row = blockIdx.y / a.segments, seg = blockIdx.y % a.segments;
     int64_t n;
-    RowView rv{a.source, nullptr, nullptr, nullptr, 0};
-    if (a.source == kPairs) {
+    RowView<S> rv{nullptr, nullptr, nullptr, 0};
+    if (S == kPairs) {
         n = a.n_pairs;
         rv.s = a.scores + static_cast<int64_t>(row) * a.n_pairs;
         rv.ids = a.pair_ids + static_cast<int64_t>(row) * a.n_pairs;
@@ -207,211 +244,141 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
         const int L = a.lengths[b] - a.P + 1 + p;
         rv.s = a.scores + static_cast<int64_t>(row) * a.ld;
         rv.L = L;
-        if (a.source == kPoolRows) {
+        if (S == kPoolRows) {
             n = static_cast<int64_t>(a.pool_blocks) * kPoolBlock;
             rv.prow = a.pool + static_cast<int64_t>(row) * a.pool_blocks;
         } else {
-            n = L <= 0 ? 0 : (a.source == kRows ? L : (L + kPoolBlock - 1) / kPoolBlock);
+            n = L <= 0 ? 0 : (S == kRows ? L : (L + kPoolBlock - 1) / kPoolBlock);
         }
     }
     const int64_t s0 = min(n, seg * a.seg_len), s1 = min(n, s0 + a.seg_len);
     const int64_t chunk = (s1 - s0 + C - 1) / C;
     const int64_t e0 = min(s1, s0 + rank * chunk), e1 = min(s1, e0 + chunk);
-    const int m = static_cast<int>(e1 - e0);  // <= kSelCache (the host sizes the cluster so)
+    const int m = static_cast<int>(e1 - e0);  // <= kSelCacheMax (the host sizes the cluster so)
 
-    // Pass 0: keys into shared memory; count, min and max of the candidates.
-    uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0;
-    for (int i = tid; i < m; i += kSelThreads) {
-        const uint32_t k = rv.key(e0 + i);
-        cache[i] = k;
-        if (k) {
-            ++cnt;
-            kmin = min(kmin, k);
-            kmax = max(kmax, k);
+    {
+        uint4 *z = reinterpret_cast<uint4 *>(sh.l0);
+        for (int i = tid; i < kZeroWords / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    cluster_arrive();  // the zeroed cluster-wide histograms may now receive additions
+
+    // Pass 0: keys into shared memory and the digit-0 histogram.  Loads are
+    // issued U at a time so that their latencies overlap.
+    constexpr int U = S == kBlocks ? 2 : 8;
+    for (int base = 0; base < m; base += U * kSelThreads) {
+        uint32_t k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * kSelThreads + tid;
+            k[u] = i < m ? rv.key(e0 + i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * kSelThreads + tid;
+            if (i < m) {
+                cache[i] = k[u];
+                if (k[u]) atomicAdd(&sh.l0[k[u] >> 20], 1u);
+            }
         }
     }
-    cnt = block_sum(cnt, sh.warp_tot);
-    kmin = block_min(kmin, sh.scratch);
-    kmax = block_max(kmax, sh.scratch);
-    if (tid < C) {
-        SelShared *dst = cluster.map_shared_rank(&sh, tid);
-        dst->cnt_all[rank] = cnt;
-        dst->min_all[rank] = kmin;
-        dst->max_all[rank] = kmax;
-    }
-    cluster.sync();
-    uint32_t total = 0, lo = 0xFFFFFFFFu, hi = 0;
-    for (int q = 0; q < C; ++q) {
-        total += sh.cnt_all[q];
-        lo = min(lo, sh.min_all[q]);
-        hi = max(hi, sh.max_all[q]);
-    }
+    __syncthreads();
+    cluster_wait();
+    push_histogram(sh.l0, sh.g0, kDigit0Bins, C);
+    cluster_barrier();
 
+    // Selection: every key > thr_gt, plus the first `need` keys equal to
+    // thr_eq in id order.
     const uint32_t K = static_cast<uint32_t>(a.K);
-    // Selection rule after the passes:
-    //   kAll  : every candidate (total <= K)
-    //   kRange: every key >= lo
-    //   kTies : keys > hi, plus the first `need` keys equal to lo (== hi) in id order
-    Rule rule = kAll;
-    uint32_t need = 0, local_above = 0, local_eq = 0;
+    uint32_t thr_gt = 0, thr_eq = 0, need = 0;
+    const uint32_t total = find_bin(sh.g0, kDigit0Bins, K, sh);
     if (total > K) {
-        uint32_t above = 0;
-        rule = kRange;
-        for (int pass = 0; pass < 4; ++pass) {
-            if (lo == hi) {  // every live key is equal: the ties rule decides
-                rule = kTies;
-                need = K - above;
-                uint32_t le = 0;
-                for (int i = tid; i < m; i += kSelThreads) le += cache[i] == lo;
-                local_eq = block_sum(le, sh.warp_tot);
-                break;
-            }
-            const uint32_t span = hi - lo;
-            const int bits = 32 - __clz(span);
-            const int shift = bits > 11 ? bits - 11 : 0;
-            const int nb = static_cast<int>(span >> shift) + 1;  // <= 2048 buckets
-            const int bpc = (nb + C - 1) / C;                    // buckets owned per CTA
-            for (int i = tid; i < kBins; i += kSelThreads) sh.hist[i] = 0;
-            if (tid == 0) {
-                sh.res_bucket = 0;
-                sh.res_gt = above;
-                sh.res_class = 0;
+        const uint32_t d0 = sh.res_bin;
+        uint32_t above = sh.res_above;
+        if (sh.g0[d0] == K - above) {
+            thr_gt = d0 ? (d0 << 20) - 1u : 0u;
+        } else {
+            for (int i = tid; i < m; i += kSelThreads) {
+                const uint32_t k = cache[i];
+                if (k && (k >> 20) == d0) atomicAdd(&sh.l1[(k >> 8) & 0xFFFu], 1u);
             }
             __syncthreads();
-            for (int base = 0; base < m; base += kSelThreads) {
-                const int i = base + tid;
-                const uint32_t k = i < m ? cache[i] : 0u;
-                const bool in = k != 0 && k >= lo && k <= hi;
-                const uint32_t bkt = in ? (k - lo) >> shift : 0xFFFFFFFFu;
-                const unsigned peers = __match_any_sync(0xFFFFFFFFu, bkt);
-                if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bkt], static_cast<uint32_t>(__popc(peers)));
-            }
-            __syncthreads();
-            for (int i = tid; i < nb; i += kSelThreads) {
-                const int owner = i / bpc;
-                cluster.map_shared_rank(sh.stage, owner)[rank * bpc + (i - owner * bpc)] = sh.hist[i];
-            }
-            cluster.sync();
-            uint32_t part = 0;
-            const int own0 = rank * bpc, own_n = max(0, min(nb - own0, bpc));
-            for (int j = tid; j < own_n; j += kSelThreads) {
-                uint32_t g = 0;
-                for (int q = 0; q < C; ++q) g += sh.stage[q * bpc + j];
-                sh.slice[j] = g;
-                part += g;
-            }
-            part = block_sum(part, sh.warp_tot);
-            if (tid < C) cluster.map_shared_rank(&sh, tid)->totals[rank] = part;
-            cluster.sync();
-            int owner = 0;
-            uint32_t cum = above;
-            for (int q = C - 1; q >= 0; --q) {
-                if (cum + sh.totals[q] >= K) {
-                    owner = q;
-                    break;
-                }
-                cum += sh.totals[q];
-            }
-            if (rank == owner) {
-                // Suffix sums over the owned buckets, highest first: each thread
-                // takes `per` consecutive buckets; threads are scanned in reverse.
-                const int per = (own_n + kSelThreads - 1) / kSelThreads;
-                uint32_t mine = 0;
-                for (int j = 0; j < per; ++j) {
-                    const int bkt = tid * per + j;
-                    if (bkt < own_n) mine += sh.slice[bkt];
-                }
-                sh.scratch[kSelThreads - 1 - tid] = mine;
-                __syncthreads();
-                const uint32_t mirrored = sh.scratch[tid];
-                __syncthreads();
-                uint32_t t_;
-                const uint32_t excl = block_exclusive_scan(mirrored, sh.warp_tot, &t_);
-                sh.scratch[kSelThreads - 1 - tid] = excl;
-                __syncthreads();
-                uint32_t suf = cum + sh.scratch[tid];
-                for (int j = per - 1; j >= 0; --j) {
-                    const int bkt = tid * per + j;
-                    if (bkt >= own_n) continue;
-                    const uint32_t gt = suf;
-                    suf += sh.slice[bkt];
-                    if (gt < K && suf >= K) {
-                        sh.res_bucket = static_cast<uint32_t>(own0 + bkt);
-                        sh.res_gt = gt;
-                        sh.res_class = sh.slice[bkt];
-                    }
+            push_histogram(sh.l1, sh.g1, kDigit1Bins, C);
+            cluster_barrier();
+            find_bin(sh.g1, kDigit1Bins, K - above, sh);
+            const uint32_t p24 = (d0 << 12) | sh.res_bin;
+            above += sh.res_above;
+            if (sh.g1[sh.res_bin] == K - above) {
+                thr_gt = p24 ? (p24 << 8) - 1u : 0u;
+            } else {
+                for (int i = tid; i < m; i += kSelThreads) {
+                    const uint32_t k = cache[i];
+                    if (k && (k >> 8) == p24) atomicAdd(&sh.l2[k & 0xFFu], 1u);
                 }
                 __syncthreads();
-                if (tid < C) {
-                    SelShared *dst = cluster.map_shared_rank(&sh, tid);
-                    dst->res_bucket = sh.res_bucket;
-                    dst->res_gt = sh.res_gt;
-                    dst->res_class = sh.res_class;
+                push_histogram(sh.l2, sh.g2, kDigit2Bins, C);
+                cluster_barrier();
+                find_bin(sh.g2, kDigit2Bins, K - above, sh);
+                const uint32_t t = (p24 << 8) | sh.res_bin;  // >= 1: key 0 is never counted
+                above += sh.res_above;
+                need = K - above;  // 1 <= need <= g2[res_bin]
+                if (need == sh.g2[sh.res_bin]) {
+                    thr_gt = t - 1u;
+                    need = 0;
+                } else {
+                    thr_gt = t;
+                    thr_eq = t;
                 }
-            }
-            cluster.sync();
-            const uint32_t d = sh.res_bucket;
-            const uint32_t cls = sh.res_class;
-            above = sh.res_gt;
-            uint32_t la = 0;
-            for (int i = tid; i < nb; i += kSelThreads)
-                if (static_cast<uint32_t>(i) > d) la += sh.hist[i];
-            local_above += block_sum(la, sh.warp_tot);
-            local_eq = sh.hist[d];
-            const uint32_t nlo = lo + (d << shift);
-            const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << shift) - 1);
-            hi = static_cast<uint32_t>(nhi < hi ? nhi : hi);
-            lo = nlo;
-            need = K - above;
-            if (need == cls) {  // the whole bucket is selected
-                rule = kRange;
-                break;
             }
         }
     }
 
-    // Per-CTA selected counts (and counts at the threshold) to every CTA.
-    const uint32_t mine_sel = rule == kAll ? cnt : (rule == kRange ? local_above + local_eq : local_above);
-    if (tid < C) {
-        SelShared *dst = cluster.map_shared_rank(&sh, tid);
-        dst->sel_all[rank] = mine_sel;
-        dst->eq_all[rank] = local_eq;
+    // Per (iteration, warp) counts of keys above the threshold and at it.
+    const int J = (m + kSelThreads - 1) / kSelThreads;
+    for (int j = 0; j < J; ++j) {
+        const int i = j * kSelThreads + tid;
+        const uint32_t k = i < m ? cache[i] : 0u;
+        const unsigned ba = __ballot_sync(0xFFFFFFFFu, k > thr_gt);
+        const unsigned be = __ballot_sync(0xFFFFFFFFu, need && k == thr_eq);
+        if (lane == 0) sh.jw[j * kSelWarps + warp] = (static_cast<uint32_t>(__popc(ba)) << 16) | __popc(be);
     }
-    cluster.sync();  // last remote write: from here on CTAs touch only their own memory
-    uint32_t out_before = 0, tie_before = 0, take = 0;
-    for (int q = 0; q < C; ++q) {
-        uint32_t tq = 0;
-        if (rule == kTies) tq = tie_before >= need ? 0u : min(sh.eq_all[q], need - tie_before);
-        if (q < rank) out_before += sh.sel_all[q] + tq;
-        if (q == rank) take = tq;
-        tie_before += sh.eq_all[q];
+    __syncthreads();
+    uint32_t cta_tot;
+    {
+        const uint32_t v = tid < J * kSelWarps ? sh.jw[tid] : 0u;
+        const uint32_t ex = block_exclusive_scan(v, sh.warp_tot, &cta_tot);
+        if (tid < J * kSelWarps) sh.jw[tid] = ex;
+    }
+    if (tid < C) {
+        cluster_store(cluster_addr(&sh.cnt_above[rank], tid), cta_tot >> 16);
+        cluster_store(cluster_addr(&sh.cnt_eq[rank], tid), cta_tot & 0xFFFFu);
+    }
+    cluster_barrier();  // last remote write: from here on CTAs touch only their own memory
+    uint32_t above0 = 0, tie0 = 0;
+    for (int q = 0; q < rank; ++q) {
+        above0 += sh.cnt_above[q];
+        tie0 += sh.cnt_eq[q];
     }
 
-    // Collect: thread t owns keys [t*E, t*E+E) of the chunk, so the block scans
-    // give each thread its tie rank and its output position in id order.
-    const int E = (m + kSelThreads - 1) / kSelThreads;
-    const int i0 = min(m, tid * E), i1 = min(m, i0 + E);
-    uint32_t t_;
-    uint32_t my_ties = 0;
-    if (rule == kTies)
-        for (int i = i0; i < i1; ++i) my_ties += cache[i] == lo;
-    const uint32_t ties_before_me = rule == kTies ? block_exclusive_scan(my_ties, sh.warp_tot, &t_) : 0u;
-    uint32_t my_sel = 0;
-    {
-        uint32_t tr = ties_before_me;
-        for (int i = i0; i < i1; ++i) my_sel += selected(rule, cache[i], lo, hi, tr, take);
-    }
-    const uint32_t pos0 = out_before + block_exclusive_scan(my_sel, sh.warp_tot, &t_);
+    // Output position of a selected key = selected keys with a lower id.
     const int64_t obase = static_cast<int64_t>(blockIdx.y) * a.K;
-    {
-        uint32_t tr = ties_before_me, pos = pos0;
-        for (int i = i0; i < i1; ++i) {
-            const uint32_t k = cache[i];
-            if (selected(rule, k, lo, hi, tr, take)) {
-                a.out_ids[obase + pos] = rv.id(e0 + i);
-                if (a.out_scores) a.out_scores[obase + pos] = key_score(k);
-                ++pos;
-            }
+    const unsigned lt = (1u << lane) - 1u;
+    for (int j = 0; j < J; ++j) {
+        const int i = j * kSelThreads + tid;
+        const uint32_t k = i < m ? cache[i] : 0u;
+        const bool is_above = k > thr_gt;
+        const bool is_tie = need && k == thr_eq;
+        const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
+        const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
+        const uint32_t base = sh.jw[j * kSelWarps + warp];
+        const uint32_t a_before = above0 + (base >> 16) + __popc(ba & lt);
+        const uint32_t t_before = tie0 + (base & 0xFFFFu) + __popc(be & lt);
+        int64_t pos = -1;
+        if (is_above) pos = a_before + min(t_before, need);
+        else if (is_tie && t_before < need) pos = a_before + t_before;
+        if (pos >= 0) {
+            a.out_ids[obase + pos] = rv.id(e0 + i);
+            if (a.out_scores) a.out_scores[obase + pos] = key_score(k);
         }
     }
     const uint32_t selected_total = total > K ? K : total;
@@ -422,47 +389,36 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(SelArgs a)
         }
 }
 
-int g_max_cluster = 0;
-
-cudaError_t launch(const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)
+size_t select_smem(int64_t chunk)
 {
-    const size_t smem = sizeof(SelShared) + kSelCache * sizeof(uint32_t);
-    if (g_max_cluster == 0) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    return sizeof(SelShared) + static_cast<size_t>((chunk + 3) / 4 * 4) * sizeof(uint32_t);
+}
+
+template <int S>
+cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)
+{
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(select_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(select_smem(kSelCacheMax)));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(select_kernel<S>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        g_max_cluster = 1;
-        for (int cs = kMaxCluster; cs >= 2; cs >>= 1) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(cs, 1, 1);
-            cfg.blockDim = dim3(kSelThreads, 1, 1);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = cs;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int nclusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&nclusters, select_kernel, &cfg) == cudaSuccess && nclusters > 0) {
-                g_max_cluster = cs;
-                break;
-            }
-            cudaGetLastError();
-        }
+        configured = true;
     }
+    // Smallest cluster whose chunks fit shared memory, widened (down to
+    // kMinChunk keys per CTA) while the grid is under one CTA per SM.
     int C = 1;
-    while (C < g_max_cluster &&
-           ((n_per_cluster + C - 1) / C > kSelCache || static_cast<int64_t>(grid_rows) * C < 2 * 148))
+    while (C < kMaxCluster &&
+           ((n_per_cluster + C - 1) / C > kSelCacheMax ||
+            (static_cast<int64_t>(grid_rows) * C < 148 && (n_per_cluster + 2 * C - 1) / (2 * C) >= kMinChunk)))
         C *= 2;
-    if ((n_per_cluster + C - 1) / C > kSelCache) return cudaErrorInvalidValue;
+    const int64_t chunk = (n_per_cluster + C - 1) / C;
+    if (chunk > kSelCacheMax) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, grid_rows, 1);
     cfg.blockDim = dim3(kSelThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = select_smem(chunk);
     cfg.stream = st;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -471,9 +427,19 @@ cudaError_t launch(const SelArgs &args, int grid_rows, int64_t n_per_cluster, cu
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, args);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel<S>, args);
     if (e == cudaSuccess) count_launch();
     return e;
+}
+
+cudaError_t launch(int source, const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)
+{
+    switch (source) {
+    case kRows: return launch_source<kRows>(args, grid_rows, n_per_cluster, st);
+    case kBlocks: return launch_source<kBlocks>(args, grid_rows, n_per_cluster, st);
+    case kPoolRows: return launch_source<kPoolRows>(args, grid_rows, n_per_cluster, st);
+    default: return launch_source<kPairs>(args, grid_rows, n_per_cluster, st);
+    }
 }
 
 struct SelPlan {
@@ -488,10 +454,10 @@ SelPlan sel_plan(const CacheView &c, const int32_t *pool, int pool_blocks, int b
     SelPlan p;
     p.n_max = pool ? static_cast<int64_t>(pool_blocks) * kPoolBlock
                    : (block == 1 ? c.cap : (c.cap + kPoolBlock - 1) / kPoolBlock);
-    const int64_t one_cluster = static_cast<int64_t>(kMaxCluster) * kSelCache;
-    p.segments = static_cast<int>((p.n_max + one_cluster - 1) / one_cluster);
-    if (p.segments < 1) p.segments = 1;
+    const int64_t one_cluster = static_cast<int64_t>(kMaxCluster) * kSelCacheMax;
+    p.segments = p.n_max <= one_cluster ? 1 : static_cast<int>((p.n_max + kSegmentLen - 1) / kSegmentLen);
     p.seg_len = (p.n_max + p.segments - 1) / p.segments;
+    if (p.seg_len < 1) p.seg_len = 1;
     p.k_seg = static_cast<int>(p.seg_len < K ? p.seg_len : K);
     return p;
 }
@@ -510,7 +476,7 @@ int select_supported(const CacheView &c, const int32_t *pool, int pool_blocks, i
 {
     const SelPlan p = sel_plan(c, pool, pool_blocks, block, K);
     return p.segments == 1 ||
-           static_cast<int64_t>(p.segments) * p.k_seg <= static_cast<int64_t>(kMaxCluster) * kSelCache;
+           static_cast<int64_t>(p.segments) * p.k_seg <= static_cast<int64_t>(kMaxCluster) * kSelCacheMax;
 }
 
 cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
@@ -520,8 +486,8 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
     const int rows = c.B * P;
     if (rows == 0) return cudaSuccess;
     const SelPlan p = sel_plan(c, pool, pool_blocks, block, K);
+    const int source = pool ? kPoolRows : (block == 1 ? kRows : kBlocks);
     SelArgs a{};
-    a.source = pool ? kPoolRows : (block == 1 ? kRows : kBlocks);
     a.scores = scores;
     a.ld = ld;
     a.lengths = c.lengths;
@@ -533,7 +499,7 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
         a.seg_len = p.n_max;
         a.K = K;
         a.out_ids = out;
-        return launch(a, rows, p.n_max, st);
+        return launch(source, a, rows, p.n_max, st);
     }
     // Stage 1: each segment's own top k_seg, with scores, into the workspace.
     if (!ws || ws_bytes < select_workspace_bytes(c, P, pool, pool_blocks, block, K)) return cudaErrorInvalidValue;
@@ -545,11 +511,10 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
     a.K = p.k_seg;
     a.out_ids = cand_i;
     a.out_scores = cand_s;
-    cudaError_t e = launch(a, rows * p.segments, p.seg_len, st);
+    cudaError_t e = launch(source, a, rows * p.segments, p.seg_len, st);
     if (e != cudaSuccess) return e;
     // Stage 2: the row's top K among the segments' candidates (in id order).
     SelArgs b{};
-    b.source = kPairs;
     b.scores = cand_s;
     b.pair_ids = cand_i;
     b.n_pairs = p.segments * p.k_seg;
@@ -558,7 +523,7 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
     b.seg_len = b.n_pairs;
     b.K = K;
     b.out_ids = out;
-    return launch(b, rows, b.n_pairs, st);
+    return launch(kPairs, b, rows, b.n_pairs, st);
 }
 
 }  // namespace csa
