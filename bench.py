@@ -14,6 +14,7 @@ the data path).
 """
 import argparse
 import json
+import re
 import os
 import statistics
 import sys
@@ -252,16 +253,8 @@ def bench_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.barrier()
-        total_ms = float(t.item())
+    total_ms, value = aggregate_over_ranks(sum(step_ms), wl.B * wl.P, args.steps, world, dev)
     ms_per_step = total_ms / args.steps
-    units = wl.B * wl.P
-    value = world * units * args.steps / (total_ms / 1e3)
     sbytes, ibytes = step_bytes(wl)
     gbs = sbytes / (ms_per_step / 1e3) / 1e9
 
@@ -274,6 +267,20 @@ def bench_ours(args, wl, rank, world, local_rank):
     return dict(value=value, ms_per_step=ms_per_step, gbs=gbs, step_bytes=sbytes, index_bytes=ibytes,
                 clocks=clock_info, launches=launches_per_step * args.steps, stages=stages, e2e=e2e,
                 step_ms=step_ms)
+
+
+def aggregate_over_ranks(total_ms, units_per_rank, steps, world, device):
+    """The job's time is its slowest rank's (max over ranks); its throughput is
+    the units every rank processed over that time (weak scaling: each rank runs
+    the same per-GPU workload on its own sequences, with no data exchange)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        total_ms = float(t.item())
+    return total_ms, world * units_per_rank * steps / (total_ms / 1e3)
 
 
 def capture(fn):
@@ -433,6 +440,30 @@ def config_of(wl):
             "l2": "flushed between timed steps (256 MiB write outside the timed events)"}
 
 
+def index_traffic_from_profile():
+    """DRAM bytes per index_score launch from the committed ncu summary, or None
+    when the kernel's sources have changed since that capture (the summary
+    records the sha256 of the sources it was taken with)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "index_score_full_64k.md")
+    csrc = os.path.join(ROOT, "fp4_compressed_sparse_append_b300", "csrc")
+    try:
+        text = open(path).read()
+        h = hashlib.sha256()
+        for name in ("index_score.cu", "common.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None, "no ncu summary"
+    want = re.search(r"kernel_sources_sha256:\s*([0-9a-f]{64})", text)
+    val = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    if not want or not val:
+        return None, "no ncu summary"
+    if want.group(1) != h.hexdigest():
+        return None, "kernel changed since the ncu capture"
+    return int(val.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/index_score_full_64k.md)"
+
+
 def main():
     args = parse_args()
     rank, world, local_rank = dist_env()
@@ -460,13 +491,15 @@ def main():
     peak_src = "measured" if peak_hbm else "fallback"
     peak_hbm = peak_hbm or 6400.0
     idx_ms = r["stages"].get("index_score")
+    traffic, traffic_src = index_traffic_from_profile()
     dominant = max(r["stages"], key=r["stages"].get) if r["stages"] else None
     roof = None
     if idx_ms:
         ach = r["index_bytes"] / (idx_ms / 1e3) / 1e9
         roof = {"kernel": "index_score", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
                 "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
-                "algorithmic_bytes_per_launch": r["index_bytes"], "launch_ms": idx_ms, "traffic": None}
+                "algorithmic_bytes_per_launch": r["index_bytes"], "launch_ms": idx_ms, "traffic": traffic,
+                "traffic_source": traffic_src}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         rate, cores, sample, el = oracle_sample(wl, args.seed, 20.0)
