@@ -158,6 +158,21 @@ class Clocks:
 # Our arm
 # ---------------------------------------------------------------------------
 
+class L2Flush:
+    """Evicts the L2 (126 MB) between timed iterations by reading a 256 MiB
+    buffer.  A read leaves clean lines behind, so the timed kernels do not pay
+    for writing back the flush's own data."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.out = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        import torch
+        torch.sum(self.buf, dim=0, out=self.out)
+
+
 def build_state(wl, seed, device):
     """Untimed setup: the cache (built through csa_quantize_append) and the
     per-layer arguments with their workspaces."""
@@ -211,13 +226,13 @@ def bench_ours(args, wl, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     cache, layers, base_len = build_state(wl, args.seed, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def reset():
         if wl.n_append:
             cache.lengths.copy_(base_len)      # the step appends rows: start each step from the same cache
-        flush.fill_(1)                         # L2 flush between timed iterations
+        flush()                                # L2 flush between timed iterations
 
     for _ in range(max(3, args.warmup)):
         reset()
@@ -316,7 +331,7 @@ def stage_times(cache, layers, wl, flush, steps, stream):
         g = capture(fn)
         ts = []
         for i in range(max(3, steps) + 3):
-            flush.fill_(1)
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             g.replay()
@@ -353,7 +368,7 @@ def e2e_run(cache, layers, base_len, wl, args, stream, flush):
     for i in range(args.steps + 2):
         if wl.n_append:
             cache.lengths.copy_(base_len)
-        flush.fill_(1)
+        flush()
         if i >= 2:
             ev[i - 2][0].record(stream)
         for la, row in zip(layers, hin):
@@ -437,7 +452,7 @@ def config_of(wl):
             "layers": "".join({W.FULL: "F", W.REINDEX: "X", W.REUSE: "R"}[m] for m in wl.layers),
             "pool_blocks": wl.pool_blocks, "appended_rows": wl.n_append,
             "kv_format": "E2M1 codes + E4M3 scale per 16 channels; FP8 E4M3 indexer keys",
-            "l2": "flushed between timed steps (256 MiB write outside the timed events)"}
+            "l2": "flushed between timed steps (a 256 MiB read outside the timed events)"}
 
 
 def index_traffic_from_profile():

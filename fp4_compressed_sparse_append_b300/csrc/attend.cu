@@ -24,9 +24,14 @@
 //                  memory as one row, so max, exp2 and sums need no cross-thread
 //                  traffic; the running maximum is rescaled lazily (only when
 //                  it grows by more than 2^8).
-// The accumulator O^T [D x heads] stays in tensor memory across the CTA's tiles;
-// at the end the softmax warps write the final output (one split) or a partial
-// (O, m, l) that the merge kernel combines.
+// The accumulator O^T [D x heads] stays in tensor memory across the CTA's tiles.
+// At the end the softmax warps write the final output (one split).  With
+// several splits of one query launched as a thread-block cluster, each split
+// copies its unnormalised O, m and l into its own shared memory and, after a
+// cluster barrier, each CTA combines one slice of the dims over every split by
+// distributed-shared-memory loads and writes it; with more splits than a
+// cluster holds, the partials go through global memory to the merge kernel.
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -43,6 +48,7 @@ constexpr int kMaxHeads = 64;       // S uses M = 64 (heads, zero-padded)
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxClusterSplit = 8;  // portable cluster size
 
 struct AttArgs {
     CacheView c;
@@ -52,6 +58,7 @@ struct AttArgs {
     float scale;
     const int32_t *idx;
     int nsplit, tiles_per_split, tiles_total;
+    int cluster;      // 1: the nsplit CTAs of a query form a cluster and merge in shared memory
     float *part_o;    // [units][nsplit][H][D]   (nsplit > 1)
     float2 *part_ml;  // [units][nsplit][H] (m in log2 units, l)
     float *out;       // [units][H][D]           (nsplit == 1)
@@ -109,7 +116,7 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float sc)
 }
 
 struct AttSmem {
-    uint64_t vfull[2], vempty[2], sfull[2], sempty[2], pfull[2], pempty[2], xbar, done;
+    uint64_t vfull[2], vempty[2], sfull[2], sempty[2], pfull[2], pempty[2], xbar, done, qbar;
     uint32_t valid[2][2];     // row-valid bits of each V buffer
     float fac[2][kMaxHeads];  // rescale factor per head, by tile parity
     float cfac[kMaxHeads];    // scale * log2(e) * 2^-e per head (e: power of two applied to Q)
@@ -120,7 +127,7 @@ struct AttSmem {
     int abort;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
+__global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_constant__ CUtensorMap qmap, AttArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -136,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.y, split = blockIdx.x;
     const int b = unit / a.P;
-    const int len = a.c.lengths[b];
+    int len = 0;
     const int t_first = split * a.tiles_per_split;
     const int t_last = min(a.tiles_total, t_first + a.tiles_per_split);
     const int n_tiles = max(0, t_last - t_first);
@@ -157,13 +164,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         }
         mbar_init(&sm.xbar, 32 * kSoftWarps);
         mbar_init(&sm.done, 1);
+        mbar_init(&sm.qbar, 1);
         sm.abort = 0;
         fence_mbar_init();
+        prefetch_tensormap(&qmap);
     }
     if (warp == mma_warp) {
         tmem_alloc(&sm.tmem_slot, a.tmem_cols);
         tmem_relinquish();
     }
+    __syncthreads();  // barrier initialisation visible to every waiting thread
+    // Above: this CTA only.  Below: reads of what earlier work on the stream wrote.
+    pdl_wait();
+    pdl_trigger();
+    // The query block [64 head rows][D] bf16 arrives by TMA, 128B-swizzled in
+    // 64-dim boxes, in the second V buffer (free until the first tile is done).
+    uint8_t *q_stage = v_s + kRows * D * 2;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(kMaxHeads * D * 2));
+        for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(q_stage + kb * kMaxHeads * 128, &qmap, &sm.qbar, kb * 128, unit * H);
+    }
+    len = a.c.lengths[b];
 
     // Gather-warp state: the rows of tile i+1 are loaded while tile i is used;
     // thread (row gr, half grh) holds half of one FP4 row.
@@ -193,13 +215,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
     if (is_gather && n_tiles > 0) prefetch(t_first);  // in flight while Q is staged
 
     // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15: thread (head
-    // qh, quarter qq) of the first 256 threads converts dims [qq*D/4, (qq+1)*D/4).
-    if (tid < 4 * kMaxHeads) {
+    // qh, quarter qq) of the first 256 threads converts dims [qq*D/4, (qq+1)*D/4)
+    // from the bf16 block in shared memory.
+    if (!mbar_wait(&sm.qbar, 0, abort_flag)) {
+        // timed out: the status bit is raised at the end; the CTA drains below
+    } else if (tid < 4 * kMaxHeads) {
         const int qh = tid >> 2, qq = tid & 3, qn = D / 32;
         uint4 qreg[16];
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(unit) * H + qh) * D) + qq * qn;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) qreg[i] = (qh < H && i < qn) ? src[i] : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i) {
+            // 16-byte chunk i of this quarter: dims qq*D/4 + 8i .. +8
+            const int dim = qq * (D / 4) + i * 8;
+            const int kb = dim >> 6, c = (dim >> 3) & 7;
+            qreg[i] = (qh < H && i < qn)
+                          ? *reinterpret_cast<const uint4 *>(q_stage + kb * kMaxHeads * 128 + qh * 128 +
+                                                             ((c ^ (qh & 7)) << 4))
+                          : make_uint4(0, 0, 0, 0);
+        }
         uint32_t emax = 0;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -237,8 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
             const uint64_t dv = smem_desc(smem_u32(v_s), 16, 1024, 2);
             const uint64_t dvt = smem_desc(smem_u32(v_s), kRows * 128 /*next 64 dims*/, 1024 /*next 8 rows*/, 2);
             const uint64_t dp = smem_desc(smem_u32(p_s), 16, 1024, 2);
-            auto issue_pv = [&](int i) -> bool {
-                if (!mbar_wait(&sm.pfull[i & 1], (i >> 1) & 1, abort_flag)) return false;
+            auto issue_s = [&](int i) {
+                tc_fence_after();
+                const uint64_t vb = dv + (((i & 1) * v_bytes) >> 4);
+                for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(t_s + (i & 1) * kRows, dq + ((kb * kMaxHeads * 128 + ks * 32) >> 4),
+                                vb + ((kb * kRows * 128 + ks * 32) >> 4), idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&sm.sfull[i & 1]);
+            };
+            auto issue_pv = [&](int i) {
                 tc_fence_after();
                 const uint64_t vb = dvt + (((i & 1) * v_bytes) >> 4);
                 for (int mt = 0; mt < D / 128; ++mt)
@@ -251,24 +292,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
                     }
                 mma_commit(&sm.pempty[i & 1]);
                 mma_commit(&sm.vempty[i & 1]);
-                return true;
             };
-            bool ok = true;
-            for (int i = 0; i < n_tiles && ok; ++i) {
-                const uint32_t par = (i >> 1) & 1;
-                if (!mbar_wait(&sm.vfull[i & 1], par, abort_flag)) break;
-                if (!mbar_wait(&sm.sempty[i & 1], par ^ 1, abort_flag)) break;
-                tc_fence_after();
-                const uint64_t vb = dv + (((i & 1) * v_bytes) >> 4);
-                for (int kb = 0; kb < D / 64; ++kb)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f16(t_s + (i & 1) * kRows, dq + ((kb * kMaxHeads * 128 + ks * 32) >> 4),
-                                vb + ((kb * kRows * 128 + ks * 32) >> 4), idesc_s, (kb > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(&sm.sfull[i & 1]);
-                if (i > 0) ok = issue_pv(i - 1);
+            // Issue in order of readiness: O^T of tile i as soon as its P is
+            // written (which also frees its V buffer for the gather sooner),
+            // S of tile i+1 as soon as its V is gathered and its S buffer is
+            // free.  Polling is non-blocking so neither waits behind the other.
+            int ns = 0, npv = 0;
+            unsigned long long t_idle = global_ns();
+            while (npv < n_tiles) {
+                if (npv < ns && mbar_test(&sm.pfull[npv & 1], (npv >> 1) & 1)) {
+                    issue_pv(npv++);
+                    t_idle = global_ns();
+                } else if (ns < n_tiles && ns < npv + 2 && mbar_test(&sm.vfull[ns & 1], (ns >> 1) & 1) &&
+                           mbar_test(&sm.sempty[ns & 1], ((ns >> 1) & 1) ^ 1)) {
+                    issue_s(ns++);
+                    t_idle = global_ns();
+                } else if (*abort_flag) {
+                    break;
+                } else if (global_ns() - t_idle > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    break;
+                }
             }
-            if (ok && !*abort_flag) issue_pv(n_tiles - 1);
             mma_commit(&sm.done);
             const unsigned long long t0 = global_ns();
             while (!mbar_try_wait(&sm.done, 0) && global_ns() - t0 < kWaitLimitNs) {
@@ -419,7 +464,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
         }
         mbar_arrive(&sm.xbar);
         if (ok) ok = mbar_wait(&sm.xbar, n_tiles & 1, abort_flag);
-        if (ok) {
+        if (ok && a.cluster) {
+            // This split's unnormalised O -> shared memory [H][D] fp32 over the
+            // V buffers (free: the last O^T update has completed).
+            tc_fence_after();
+            float *obuf = reinterpret_cast<float *>(v_s);
+            for (int mt = 0; mt < D / 128; ++mt) {
+                const int d = mt * 128 + warp * 32 + lane;
+                uint32_t r[kMaxHeads];
+#pragma unroll
+                for (int c0 = 0; c0 < kMaxHeads; c0 += 16)
+                    if (c0 < NH) tmem_ld16(t_o + mt * NH + lane_off + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+                tmem_ld_wait();
+#pragma unroll
+                for (int hh = 0; hh < kMaxHeads; ++hh) {
+                    if (hh >= H) break;
+                    obuf[hh * D + d] = n_tiles > 0 ? __uint_as_float(r[hh]) : 0.f;
+                }
+            }
+        } else if (ok) {
             tc_fence_after();
             const bool final_out = a.nsplit == 1;
             float *obase = final_out ? a.out + static_cast<int64_t>(unit) * H * D
@@ -454,6 +517,53 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(AttArgs a)
 
     tc_fence_before();
     __syncthreads();
+    if (a.cluster) {
+        // Every split's O, m and l are in its shared memory after this barrier;
+        // each CTA merges dims [d0, d1) of every head over the splits.
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int C = a.nsplit, rank = static_cast<int>(cluster.block_rank());
+        const int slice = (D / C + 3) & ~3;
+        const int d0 = min(D, rank * slice), d1 = min(D, d0 + slice);
+        float *wq = reinterpret_cast<float *>(p_s);  // [split][head] normalised weights (P buffers are free)
+        if (tid < H) {
+            float mq[kMaxClusterSplit], lq[kMaxClusterSplit];
+            float M = -INFINITY;
+            for (int q = 0; q < C; ++q) {
+                const AttSmem *rs = cluster.map_shared_rank(&sm, q);
+                mq[q] = rs->m_fin[tid];
+                lq[q] = rs->l_fin[tid];
+                if (lq[q] > 0.f) M = fmaxf(M, mq[q]);
+            }
+            float L = 0.f;
+            for (int q = 0; q < C; ++q) {
+                mq[q] = lq[q] > 0.f ? exp2f(mq[q] - M) : 0.f;
+                L = fmaf(mq[q], lq[q], L);
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            for (int q = 0; q < C; ++q) wq[q * kMaxHeads + tid] = mq[q] * inv;
+            if (rank == 0 && a.lse)
+                a.lse[static_cast<int64_t>(unit) * H + tid] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+        __syncthreads();
+        const int nd4 = (d1 - d0) / 4;
+        const float *obuf = reinterpret_cast<const float *>(v_s);
+        for (int w = tid; w < H * nd4; w += kThreads) {
+            const int hh = w / nd4, d = d0 + 4 * (w - hh * nd4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q = 0; q < C; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(obuf, q) + hh * D + d);
+                const float wgt = wq[q * kMaxHeads + hh];
+                acc.x = fmaf(wgt, v.x, acc.x);
+                acc.y = fmaf(wgt, v.y, acc.y);
+                acc.z = fmaf(wgt, v.z, acc.z);
+                acc.w = fmaf(wgt, v.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(unit) * H + hh) * D + d) = acc;
+        }
+        cluster.sync();  // no CTA leaves while another still reads its shared memory
+    }
     if (*abort_flag && tid == 0) raise_status(a.status, CSA_DEV_TIMEOUT);
     if (warp == mma_warp) {
         tc_fence_after();
@@ -470,6 +580,7 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
                                                           const float2 *__restrict__ part_ml, float *__restrict__ out,
                                                           float *__restrict__ lse)
 {
+    pdl_wait();
     __shared__ float wsh[kMaxSplit];
     __shared__ float inv_l;
     const int d = blockIdx.x * 128 + threadIdx.x, h = blockIdx.y, unit = blockIdx.z;
@@ -502,15 +613,17 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
 }
 
 struct Plan {
-    int nsplit, tiles_per_split, tiles_total;
+    int nsplit, tiles_per_split, tiles_total, cluster;
 };
 
-// Splits of one query's selection: about one wave of CTAs, at most kMaxSplit.
+// Splits of one query's selection: at most one wave of CTAs.  Up to
+// kMaxClusterSplit splits form a cluster and merge on chip; more (only for
+// very few queries) merge through global memory.
 Plan plan(const CacheView &c, int P, int K)
 {
     const int units = c.B * P;
     const int tiles = (K + kRows - 1) / kRows;
-    int want = (148 + units - 1) / units;
+    int want = 148 / units;  // splits x queries within one wave of CTAs (one per SM)
     if (want > tiles) want = tiles;
     if (want > kMaxSplit) want = kMaxSplit;
     if (want < 1) want = 1;
@@ -518,6 +631,7 @@ Plan plan(const CacheView &c, int P, int K)
     p.tiles_total = tiles;
     p.tiles_per_split = (tiles + want - 1) / want;
     p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    p.cluster = p.nsplit > 1 && p.nsplit <= kMaxClusterSplit;
     return p;
 }
 
@@ -532,7 +646,7 @@ size_t smem_bytes(int D, int NH)
 size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K)
 {
     const Plan p = plan(c, P, K);
-    if (p.nsplit == 1) return 0;
+    if (p.nsplit == 1 || p.cluster) return 0;
     const size_t units = static_cast<size_t>(c.B) * P;
     size_t o = units * p.nsplit * H * c.D * sizeof(float);
     o = (o + 255) / 256 * 256;
@@ -559,6 +673,7 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     a.nsplit = p.nsplit;
     a.tiles_per_split = p.tiles_per_split;
     a.tiles_total = p.tiles_total;
+    a.cluster = p.cluster;
     size_t o_bytes = static_cast<size_t>(units) * p.nsplit * H * c.D * sizeof(float);
     o_bytes = (o_bytes + 255) / 256 * 256;
     a.part_o = static_cast<float *>(ws);
@@ -570,20 +685,20 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     a.tmem_cols = cols;
     a.status = status;
     const size_t smem = smem_bytes(c.D, a.NH);
+    // Query rows [units*H][D] bf16 as bytes: 64-dim (128-byte) boxes of 64 rows.
+    CUtensorMap qm;
+    if (encode_tensor_map_2d_u8(&qm, q, static_cast<uint64_t>(c.D) * 2, static_cast<uint64_t>(units) * H, 128,
+                                kMaxHeads, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attend_kernel<<<dim3(p.nsplit, units), kThreads, smem, st>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    count_launch();
-    if (p.nsplit > 1) {
-        attend_merge_kernel<<<dim3((c.D + 127) / 128, H, units), 128, 0, st>>>(c.D, H, p.nsplit, a.part_o, a.part_ml,
-                                                                               out, lse);
-        e = cudaGetLastError();
-        if (e == cudaSuccess) count_launch();
-    }
-    return e;
+    e = launch_kernel(attend_kernel, dim3(p.nsplit, units), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0, qm,
+                      a);
+    if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
+    return launch_kernel(attend_merge_kernel, dim3((c.D + 127) / 128, H, units), dim3(128), 0, st, 0, c.D, H,
+                         p.nsplit, static_cast<const float *>(a.part_o), static_cast<const float2 *>(a.part_ml), out,
+                         lse);
 }
 
 }  // namespace csa

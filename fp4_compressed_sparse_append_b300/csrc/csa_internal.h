@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace csa {
 
 struct CacheView {
@@ -37,6 +39,38 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
 
 // Host-side count of kernel launches issued by the library (csa_kernel_launches).
 void count_launch(int n = 1);
+
+// Launches `kernel` with programmatic stream serialization (it may begin while
+// the previous kernel on the stream finishes; the kernel calls pdl_wait()
+// before reading anything earlier work wrote) and, if cluster_x > 0, with
+// thread-block clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          int cluster_x, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
 
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,

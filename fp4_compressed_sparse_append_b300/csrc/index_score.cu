@@ -13,12 +13,21 @@
 // cross-thread traffic; the [128 x N] product never leaves the SM.
 //
 // Persistent, warp-specialised CTA (one per SM):
-//   warp 0      TMA producer: key tiles (128 rows, or 16 pool blocks of 8 rows)
-//               into a ring of shared-memory stages; the unit's query rows.
-//   warp 1      TMEM owner and MMA issuer (one thread): kind::f8f6f4, M=128,
-//               fp32 accumulators double-buffered in tensor memory.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, weighted ReLU sum,
-//               coalesced fp32 score stores.
+//   warp 0      TMA producer: each job is up to 4 consecutive 128-row key tiles
+//               of one unit (or 16 pool blocks of 8 rows) in one stage of a
+//               shared-memory ring; the unit's query rows.
+//   warp 1      TMEM owner and MMA issuer (one thread): kind::f8f6f4, M=128 per
+//               key tile, all tiles of a stage into one accumulator slot of a
+//               ring in tensor memory, so one barrier round trip and one commit
+//               cover a whole stage and the MMAs run ahead of the epilogue.
+//   warps 2..9  epilogue, two groups of four warps (each group covers the four
+//               tensor-memory lane quarters): with several key tiles per job
+//               the groups split each slot's tiles, otherwise they take
+//               alternate slots; tcgen05.ld, weighted ReLU sum, coalesced fp32
+//               score stores.
+// The stage size matters: the MMA thread's fixed cost per stage (barrier waits,
+// commits) is several hundred cycles, so 16 KB stages cap a CTA near 25 GB/s
+// while 64 KB stages leave the key stream bound by HBM.
 // Every wait is bounded (kWaitLimitNs); a wait that runs out raises
 // CSA_DEV_TIMEOUT and the CTA drains its copies and returns.
 #include "common.cuh"
@@ -32,6 +41,9 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 8;
 constexpr int kMaxCols = 512;
+constexpr int kMaxAcc = 8;
+constexpr int kMaxTilesPerJob = 4;
+constexpr int kMaxUnitsSmem = 2048;  // units whose tile counts are prefix-summed in shared memory
 
 struct IdxArgs {
     int B, P, HI, cap, DI;
@@ -39,12 +51,15 @@ struct IdxArgs {
     int pool_mode;
     int groups;      // query positions per unit: P (full) or 1 (pool)
     int n_real;      // query rows (MMA columns) per unit: groups * HI
-    int n_sub;       // column sub-chunks per tile (each its own accumulator)
+    int n_sub;       // column sub-chunks per key tile
     int gps;         // groups per sub-chunk
     int sub_cols;    // MMA N of a sub-chunk (gps*HI rounded up to 16, <= 256)
+    int mt;          // 128-row key tiles per job (and per stage)
+    int n_acc;       // accumulator slots in tensor memory (a power of two, 2..kMaxAcc)
     int stages;
     int b_rows, b_loads, b_box_rows;
     uint32_t tmem_cols;
+    int prefix_smem; // units <= kMaxUnitsSmem: per-unit job counts prefix-summed in shared memory
     const int32_t *lengths;
     const int32_t *pool;
     int pool_blocks;
@@ -54,44 +69,78 @@ struct IdxArgs {
     int *status;
 };
 
-struct JobIter {
-    int u, tile, tiles_u;
-};
-
-__device__ __forceinline__ int unit_tiles(const IdxArgs &a, int u)
+// Jobs of one unit: ceil(rows / (mt*128)) for a full scan, 16 pool blocks
+// (one 128-row tile) per job for a pool.
+__device__ __forceinline__ int unit_jobs_global(const IdxArgs &a, int u)
 {
     if (a.pool_mode) return (a.pool_blocks + 15) / 16;
     const int len = min(a.lengths[u], a.cap);
-    return len > 0 ? (len + kTileRows - 1) / kTileRows : 0;
+    const int rows = a.mt * kTileRows;
+    return len > 0 ? (len + rows - 1) / rows : 0;
 }
 
-__device__ __forceinline__ void job_seek(const IdxArgs &a, int64_t j, JobIter &it)
-{
-    int64_t acc = 0;
-    it.u = 0;
-    while (it.u < a.units) {
-        const int t = unit_tiles(a, it.u);
-        if (acc + t > j) {
-            it.tiles_u = t;
-            it.tile = static_cast<int>(j - acc);
+struct JobIter {
+    int u, job, jobs_u;
+};
+
+struct Jobs {
+    const IdxArgs &a;
+    const int *prefix;  // [units + 1] in shared memory, or nullptr
+    __device__ __forceinline__ int count(int u) const
+    {
+        return prefix ? prefix[u + 1] - prefix[u] : unit_jobs_global(a, u);
+    }
+    __device__ __forceinline__ int64_t total() const
+    {
+        if (prefix) return prefix[a.units];
+        int64_t t = 0;
+        for (int u = 0; u < a.units; ++u) t += unit_jobs_global(a, u);
+        return t;
+    }
+    __device__ __forceinline__ void seek(int64_t j, JobIter &it) const
+    {
+        if (prefix) {
+            int lo = 0, hi = a.units;  // last u with prefix[u] <= j
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (prefix[mid] <= j) lo = mid;
+                else hi = mid;
+            }
+            it.u = lo;
+            it.jobs_u = count(lo);
+            it.job = static_cast<int>(j - prefix[lo]);
+            while (it.job >= it.jobs_u && it.u < a.units - 1) {  // skip empty units
+                it.job -= it.jobs_u;
+                ++it.u;
+                it.jobs_u = count(it.u);
+            }
             return;
         }
-        acc += t;
-        ++it.u;
+        int64_t acc = 0;
+        it.u = 0;
+        while (it.u < a.units) {
+            const int t = unit_jobs_global(a, it.u);
+            if (acc + t > j) {
+                it.jobs_u = t;
+                it.job = static_cast<int>(j - acc);
+                return;
+            }
+            acc += t;
+            ++it.u;
+        }
+        it.jobs_u = 0;
+        it.job = 0;
     }
-    it.tiles_u = 0;
-    it.tile = 0;
-}
-
-__device__ __forceinline__ void job_next(const IdxArgs &a, JobIter &it)
-{
-    if (++it.tile < it.tiles_u) return;
-    it.tile = 0;
-    do {
-        ++it.u;
-        it.tiles_u = it.u < a.units ? unit_tiles(a, it.u) : 1;
-    } while (it.u < a.units && it.tiles_u == 0);
-}
+    __device__ __forceinline__ void next(JobIter &it) const
+    {
+        if (++it.job < it.jobs_u) return;
+        it.job = 0;
+        do {
+            ++it.u;
+            it.jobs_u = it.u < a.units ? count(it.u) : 1;
+        } while (it.u < a.units && it.jobs_u == 0);
+    }
+};
 
 __device__ __forceinline__ uint32_t swizzle_mode(int di)
 {
@@ -105,6 +154,26 @@ __device__ __forceinline__ uint32_t swizzle_mode(int di)
 __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *w, int HI)
 {
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    if (HI == 64) {  // both loads in flight before one wait
+        uint32_t r[32], t[32];
+        tmem_ld32(taddr, r);
+        tmem_ld32(taddr + 32, t);
+        tmem_ld_wait();
+        const float4 *w4 = reinterpret_cast<const float4 *>(w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 ww = w4[k], wv = w4[k + 8];
+            s0 = fmaf(ww.x, fmaxf(__uint_as_float(r[4 * k + 0]), 0.f), s0);
+            s1 = fmaf(ww.y, fmaxf(__uint_as_float(r[4 * k + 1]), 0.f), s1);
+            s2 = fmaf(ww.z, fmaxf(__uint_as_float(r[4 * k + 2]), 0.f), s2);
+            s3 = fmaf(ww.w, fmaxf(__uint_as_float(r[4 * k + 3]), 0.f), s3);
+            s0 = fmaf(wv.x, fmaxf(__uint_as_float(t[4 * k + 0]), 0.f), s0);
+            s1 = fmaf(wv.y, fmaxf(__uint_as_float(t[4 * k + 1]), 0.f), s1);
+            s2 = fmaf(wv.z, fmaxf(__uint_as_float(t[4 * k + 2]), 0.f), s2);
+            s3 = fmaf(wv.w, fmaxf(__uint_as_float(t[4 * k + 3]), 0.f), s3);
+        }
+        return (s0 + s1) + (s2 + s3);
+    }
     for (int c0 = 0; c0 < HI; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c0, r);
@@ -122,6 +191,23 @@ __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *
     return (s0 + s1) + (s2 + s3);
 }
 
+// Same sum for any HI: 16-column loads masked to this position's columns.
+__device__ __forceinline__ float weighted_relu_sum_any(uint32_t taddr, int col, const float *w, int HI)
+{
+    float s = 0.f;
+    for (int c0 = col & ~15; c0 < col + HI; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int c = c0 + k;
+            if (c >= col && c < col + HI) s = fmaf(w[c - col], fmaxf(__uint_as_float(r[k]), 0.f), s);
+        }
+    }
+    return s;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap keys128, const __grid_constant__ CUtensorMap keys8,
                        const __grid_constant__ CUtensorMap qmap, IdxArgs a)
@@ -130,9 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte aligned carve-up (swizzle atoms need it).
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *base = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    const int a_bytes = kTileRows * a.DI;
+    const int tile_bytes = kTileRows * a.DI;
+    const int stage_bytes = a.mt * tile_bytes;
     uint8_t *a_smem = base;
-    uint8_t *b_smem = a_smem + a.stages * a_bytes;
+    uint8_t *b_smem = a_smem + a.stages * stage_bytes;
     float *w_smem = reinterpret_cast<float *>(b_smem + ((a.b_rows * a.DI + 1023) & ~1023));  // [kEpiWarps][n_pad]
     const int n_pad = (a.n_real + 3) & ~3;
     uint64_t *bars = reinterpret_cast<uint64_t *>(w_smem + kEpiWarps * n_pad);
@@ -140,11 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *empty = full + kMaxStages;         // [kMaxStages]
     uint64_t *bfull = empty + kMaxStages;
     uint64_t *bempty = bfull + 1;
-    uint64_t *tfull = bempty + 1;                // [2]
-    uint64_t *tempty = tfull + 2;                // [2]
-    uint64_t *mma_done = tempty + 2;
+    uint64_t *tfull = bempty + 1;                // [kMaxAcc]
+    uint64_t *tempty = tfull + kMaxAcc;          // [kMaxAcc]
+    uint64_t *mma_done = tempty + kMaxAcc;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *prefix = const_cast<int *>(reinterpret_cast<volatile int *>(tmem_slot + 2));  // [units + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -154,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bfull, 1);
         mbar_init(bempty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < a.n_acc; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 32 * kEpiWarps);
+            mbar_init(&tempty[i], a.mt > 1 ? 32 * kEpiWarps : 32 * (kEpiWarps / 2));
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -171,14 +259,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&keys8);
         prefetch_tensormap(&qmap);
     }
+    // Everything above touches only this CTA; from here on the kernel reads
+    // what earlier work on the stream wrote (lengths, keys, queries).
+    pdl_wait();
+    if (warp == 2 && a.prefix_smem) {
+        int carry = 0;
+        for (int u0 = 0; u0 < a.units; u0 += 32) {
+            const int u = u0 + lane;
+            int t = u < a.units ? unit_jobs_global(a, u) : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+                if (lane >= o) t += y;
+            }
+            if (u < a.units) prefix[u + 1] = carry + t;
+            carry += __shfl_sync(0xFFFFFFFFu, t, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_trigger();
     const uint32_t tmem = *tmem_slot;
+    const Jobs jobs{a, a.prefix_smem ? prefix : nullptr};
 
-    // This CTA's contiguous share of the flattened (unit, tile) jobs.
-    int64_t total = 0;
-    for (int u = 0; u < a.units; ++u) total += unit_tiles(a, u);
+    // This CTA's contiguous share of the flattened (unit, job) list.
+    const int64_t total = jobs.total();
     const int64_t j0 = total * blockIdx.x / gridDim.x;
     const int64_t j1 = total * (blockIdx.x + 1) / gridDim.x;
 
@@ -186,12 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------- producer
         if (lane == 0 && j0 < j1) {
             JobIter it;
-            job_seek(a, j0, it);
+            jobs.seek(j0, it);
             int stage = 0;
             uint32_t phase = 0, bphase = 0;
             int cur = -1;
             uint32_t issued_mask = 0, issued_parity = 0;
-            for (int64_t j = j0; j < j1; ++j, job_next(a, it)) {
+            for (int64_t j = j0; j < j1; ++j, jobs.next(it)) {
                 if (it.u != cur) {
                     if (cur >= 0) {
                         if (!mbar_wait(bempty, bphase, abort_flag)) break;
@@ -204,10 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cur = it.u;
                 }
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
-                uint8_t *dst = a_smem + stage * a_bytes;
+                uint8_t *dst = a_smem + stage * stage_bytes;
                 if (!a.pool_mode) {
-                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(a_bytes));
-                    tma_load_2d(dst, &keys128, &full[stage], 0, it.u * a.cap + it.tile * kTileRows);
+                    // mt whole boxes; rows past the cache's end read as zeros
+                    // and rows past the unit's length are never stored.
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
+                    const int row0 = it.u * a.cap + it.job * a.mt * kTileRows;
+                    for (int m = 0; m < a.mt; ++m)
+                        tma_load_2d(dst + m * tile_bytes, &keys128, &full[stage], 0, row0 + m * kTileRows);
                 } else {
                     const int b = it.u / a.P;
                     const int32_t *prow = a.pool + static_cast<int64_t>(it.u) * a.pool_blocks;
@@ -215,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int32_t blk[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        const int jb = it.tile * 16 + k;
+                        const int jb = it.job * 16 + k;
                         blk[k] = jb < a.pool_blocks ? prow[jb] : -1;
                         if (blk[k] >= 0 && blk[k] * kPoolBlock < a.cap)
                             ++nv;
@@ -252,10 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && j0 < j1) {
             const uint32_t sw = swizzle_mode(a.DI);
             const uint32_t sbo = 8 * a.DI;  // bytes between 8-row swizzle atoms
-            const uint32_t a_base = smem_u32(a_smem), b_base = smem_u32(b_smem);
+            // Descriptors of stage 0 / query row 0; the address field is the
+            // low 14 bits (in 16-byte units), so offsets are added in place.
+            const uint64_t da0 = smem_desc(smem_u32(a_smem), 16, sbo, sw);
+            const uint64_t db0 = smem_desc(smem_u32(b_smem), 16, sbo, sw);
             const uint32_t idesc = instr_desc(128, a.sub_cols, 0, 0, 0, 0);
+            const int slot_cols = a.mt * a.sub_cols;
+            const int ksteps = a.DI / 32;
             JobIter it;
-            job_seek(a, j0, it);
+            jobs.seek(j0, it);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, bphase = 0;
             int cur = -1;
@@ -267,22 +383,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cur = it.u;
                 }
                 if (!mbar_wait(&full[stage], phase, abort_flag)) break;
-                const uint32_t a_stage = a_base + stage * a_bytes;
+                const uint64_t da_stage = da0 + static_cast<uint64_t>((stage * stage_bytes) >> 4);
                 for (int sub = 0; sub < a.n_sub; ++sub) {
                     if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_sub = b_base + sub * a.gps * a.HI * a.DI;
-                    const uint32_t d_col = tmem + acc * a.sub_cols;
-                    for (int k = 0; k < a.DI / 32; ++k) {
-                        const uint64_t da = smem_desc(a_stage + k * 32, 16, sbo, sw);
-                        const uint64_t db = smem_desc(b_sub + k * 32, 16, sbo, sw);
-                        mma_f8f6f4(d_col, da, db, idesc, k > 0 ? 1u : 0u);
+                    const uint64_t db_sub = db0 + static_cast<uint64_t>((sub * a.gps * a.HI * a.DI) >> 4);
+                    const uint32_t d_slot = tmem + acc * slot_cols;
+                    for (int m = 0; m < a.mt; ++m) {
+                        const uint64_t da_m = da_stage + static_cast<uint64_t>((m * tile_bytes) >> 4);
+                        for (int k = 0; k < ksteps; ++k)
+                            mma_f8f6f4(d_slot + m * a.sub_cols, da_m + 2 * k, db_sub + 2 * k, idesc, k > 0 ? 1u : 0u);
                     }
                     mma_commit(&tfull[acc]);
-                    if (++acc == 2) {
+                    if (++acc == a.n_acc) {
                         acc = 0;
                         acc_phase ^= 1;
                     }
@@ -290,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 mma_commit(&empty[stage]);
                 JobIter nx = it;
-                job_next(a, nx);
+                jobs.next(nx);
                 if (j + 1 == j1 || nx.u != it.u) mma_commit(bempty);
                 it = nx;
                 if (++stage == a.stages) {
@@ -308,16 +424,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------- epilogue
         const int ew = warp - 2;
-        const int q = warp & 3;   // tensor-memory lane quarter this warp may access
-        const int half = ew >> 2;  // the two warps of a quarter split the positions
+        const int q = warp & 3;     // tensor-memory lane quarter this warp may access
+        const int grp = ew >> 2;    // the two groups split each slot's tiles, or take alternate slots
+        const bool split_tiles = a.mt > 1;
         const int row_in_tile = q * 32 + lane;
+        const int slot_cols = a.mt * a.sub_cols;
         float *wcopy = w_smem + ew * n_pad;
         JobIter it;
-        if (j0 < j1) job_seek(a, j0, it);
-        int acc = 0;
-        uint32_t acc_phase = 0;
+        if (j0 < j1) jobs.seek(j0, it);
+        uint32_t seq = 0;           // (job, sub-chunk) slots in MMA order
         int cur = -1, len_b = 0;
-        for (int64_t j = j0; j < j1; ++j, job_next(a, it)) {
+        for (int64_t j = j0; j < j1; ++j, jobs.next(it)) {
             if (it.u != cur) {
                 __syncwarp();
                 const float *wsrc = a.w + static_cast<int64_t>(it.u) * a.n_real;
@@ -327,49 +444,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cur = it.u;
             }
             bool ok = true;
-            for (int sub = 0; sub < a.n_sub; ++sub) {
-                if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+            for (int sub = 0; sub < a.n_sub; ++sub, ++seq) {
+                if (!split_tiles && static_cast<int>(seq & 1u) != grp) continue;
+                const int acc = static_cast<int>(seq & static_cast<uint32_t>(a.n_acc - 1));
+                const uint32_t par = (seq / static_cast<uint32_t>(a.n_acc)) & 1u;
+                if (!mbar_wait(&tfull[acc], par, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * a.sub_cols;
+                const uint32_t t_slot = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * slot_cols;
                 const int g0 = sub * a.gps, g1 = min(a.groups, g0 + a.gps);
-                for (int g = g0 + half; g < g1; g += 2) {
-                    const int col = (g - g0) * a.HI;
-                    float s;
-                    if ((a.HI & 31) == 0) {
-                        s = weighted_relu_sum(t_base + col, wcopy + g * a.HI, a.HI);
-                    } else {
-                        // General head counts: 16-column loads, masked to this position.
-                        s = 0.f;
-                        for (int c0 = col & ~15; c0 < col + a.HI; c0 += 16) {
-                            uint32_t r[16];
-                            tmem_ld16(t_base + c0, r);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                const int c = c0 + k;
-                                if (c >= col && c < col + a.HI)
-                                    s = fmaf(wcopy[g * a.HI + c - col], fmaxf(__uint_as_float(r[k]), 0.f), s);
-                            }
+                for (int m = split_tiles ? grp : 0; m < a.mt; m += split_tiles ? 2 : 1) {
+                    const uint32_t t_base = t_slot + m * a.sub_cols;
+                    const int r = (it.job * a.mt + m) * kTileRows + row_in_tile;
+                    for (int g = g0; g < g1; ++g) {
+                        const int col = (g - g0) * a.HI;
+                        const float s = (a.HI & 31) == 0 ? weighted_relu_sum(t_base + col, wcopy + g * a.HI, a.HI)
+                                                         : weighted_relu_sum_any(t_base, col, wcopy + g * a.HI, a.HI);
+                        if (!a.pool_mode) {
+                            const int Lp = len_b - a.P + 1 + g;
+                            if (r < Lp) a.scores[(static_cast<int64_t>(it.u) * a.P + g) * a.ld + r] = s;
+                        } else {
+                            if (r < a.pool_blocks * kPoolBlock) a.scores[static_cast<int64_t>(it.u) * a.ld + r] = s;
                         }
-                    }
-                    if (!a.pool_mode) {
-                        const int t = it.tile * kTileRows + row_in_tile;
-                        const int Lp = len_b - a.P + 1 + g;
-                        if (t < Lp) a.scores[(static_cast<int64_t>(it.u) * a.P + g) * a.ld + t] = s;
-                    } else {
-                        const int c = it.tile * kTileRows + row_in_tile;
-                        if (c < a.pool_blocks * kPoolBlock) a.scores[static_cast<int64_t>(it.u) * a.ld + c] = s;
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&tempty[acc]);
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1;
-                }
             }
             if (!ok) break;
         }
@@ -405,21 +507,27 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     a.n_real = a.groups * HI;
     if (a.n_real > kMaxCols || HI > 256) return cudaErrorInvalidValue;
     // Column sub-chunks: whole positions per chunk, at most 256 MMA columns
-    // each, so that two accumulators always fit the 512 tensor-memory columns.
+    // each, so that two accumulator slots always fit the 512 tensor-memory columns.
     int n_sub = 1;
     while ((((a.groups + n_sub - 1) / n_sub) * HI + 15) / 16 * 16 > 256) ++n_sub;
     a.n_sub = n_sub;
     a.gps = (a.groups + n_sub - 1) / n_sub;
     a.sub_cols = (a.gps * HI + 15) / 16 * 16;
     if (n_sub > 1 && (a.gps * HI) % 8) return cudaErrorInvalidValue;
+    // Key tiles per job: as many as keep two slots within tensor memory.
+    a.mt = 1;
+    while (!a.pool_mode && 2 * a.mt <= kMaxTilesPerJob && 2 * (2 * a.mt) * a.sub_cols <= kMaxCols) a.mt *= 2;
+    a.n_acc = 2;
+    while (2 * a.n_acc <= kMaxAcc && 2 * a.n_acc * a.mt * a.sub_cols <= kMaxCols) a.n_acc *= 2;
     uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(2 * a.sub_cols)) cols *= 2;
+    while (cols < static_cast<uint32_t>(a.n_acc * a.mt * a.sub_cols)) cols *= 2;
     a.tmem_cols = cols;
     // Query rows staged per unit: every sub-chunk's MMA reads sub_cols rows.
     const int need_rows = (n_sub - 1) * a.gps * HI + a.sub_cols;
     a.b_loads = (need_rows + 255) / 256;
     a.b_box_rows = ((need_rows + a.b_loads - 1) / a.b_loads + 7) / 8 * 8;
     a.b_rows = a.b_loads * a.b_box_rows;
+    a.prefix_smem = a.units <= kMaxUnitsSmem;
     a.lengths = c.lengths;
     a.pool = pool;
     a.pool_blocks = pool_blocks;
@@ -428,16 +536,18 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     a.ld = ld;
     a.status = status;
 
-    const size_t a_bytes = static_cast<size_t>(kTileRows) * c.DI;
+    const size_t stage_bytes = static_cast<size_t>(a.mt) * kTileRows * c.DI;
     const size_t b_bytes = (static_cast<size_t>(a.b_rows) * c.DI + 1023) & ~size_t(1023);
     const size_t w_bytes = static_cast<size_t>(kEpiWarps) * ((a.n_real + 3) & ~3) * sizeof(float);
-    const size_t fixed = 1024 /*align*/ + b_bytes + w_bytes + (2 * kMaxStages + 8) * 8 + 64;
-    const size_t budget = 220 * 1024;
-    int stages = static_cast<int>((budget - fixed) / a_bytes);
+    const size_t prefix_bytes = a.prefix_smem ? (static_cast<size_t>(a.units) + 1) * sizeof(int) : 0;
+    const size_t fixed =
+        1024 /*align*/ + b_bytes + w_bytes + (2 * kMaxStages + 2 * kMaxAcc + 4) * 8 + 16 + prefix_bytes;
+    const size_t budget = 224 * 1024;
+    int stages = static_cast<int>((budget - fixed) / stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
     a.stages = stages;
-    const size_t smem = fixed + stages * a_bytes;
+    const size_t smem = fixed + stages * stage_bytes;
 
     const CUtensorMapSwizzle sw = c.DI == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : c.DI == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -456,13 +566,10 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
         cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (g_num_sms <= 0) g_num_sms = 148;
     }
-    cudaError_t e =
+    const cudaError_t e =
         cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    index_score_kernel<<<g_num_sms, kThreads, smem, st>>>(k128, k8, qm, a);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) count_launch();
-    return e;
+    return launch_kernel(index_score_kernel, dim3(g_num_sms), dim3(kThreads), smem, st, 0, k128, k8, qm, a);
 }
 
 }  // namespace csa

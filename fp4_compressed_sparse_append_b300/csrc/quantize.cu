@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(256) quantize_append_kernel(CacheView c, const
                                                               const uint8_t *__restrict__ ikeys_new, int n_new,
                                                               int *status)
 {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.y;
     const int len0 = c.lengths[b];
     if (len0 < 0 || len0 + n_new > c.cap) {
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(256) quantize_append_kernel(CacheView c, const
 
 __global__ void advance_lengths_kernel(int32_t *lengths, int B, int cap, int n_new)
 {
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) {
         const int len0 = lengths[b];
@@ -121,13 +124,11 @@ cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, con
     if (blocks_x > want * 8) blocks_x = want * 8;
     if (blocks_x < 1) blocks_x = 1;
     dim3 grid(static_cast<unsigned>(blocks_x), c.B);
-    quantize_append_kernel<<<grid, 256, 0, st>>>(c, rows, ikeys_new, n_new, status);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_kernel(quantize_append_kernel, grid, dim3(256), 0, st, 0, c, rows, ikeys_new, n_new,
+                                        status);
     if (e != cudaSuccess) return e;
-    advance_lengths_kernel<<<(c.B + 127) / 128, 128, 0, st>>>(c.lengths, c.B, c.cap, n_new);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) count_launch(2);
-    return e;
+    return launch_kernel(advance_lengths_kernel, dim3((c.B + 127) / 128), dim3(128), 0, st, 0, c.lengths, c.B, c.cap,
+                         n_new);
 }
 
 }  // namespace csa

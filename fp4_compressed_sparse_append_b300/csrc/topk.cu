@@ -232,6 +232,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     uint32_t *cache = reinterpret_cast<uint32_t *>(dyn_smem + sizeof(SelShared));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    {
+        uint4 *z = reinterpret_cast<uint4 *>(sh.l0);
+        for (int i = tid; i < kZeroWords / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    // Above: this CTA only.  Below: reads of what earlier work on the stream wrote.
+    pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.y / a.segments, seg = blockIdx.y % a.segments;
     int64_t n;
     RowView<S> rv{nullptr, nullptr, nullptr, 0};
@@ -256,10 +263,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     const int64_t e0 = min(s1, s0 + rank * chunk), e1 = min(s1, e0 + chunk);
     const int m = static_cast<int>(e1 - e0);  // <= kSelCacheMax (the host sizes the cluster so)
 
-    {
-        uint4 *z = reinterpret_cast<uint4 *>(sh.l0);
-        for (int i = tid; i < kZeroWords / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
-    }
     __syncthreads();
     cluster_arrive();  // the zeroed cluster-wide histograms may now receive additions
 
@@ -415,21 +418,7 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
         C *= 2;
     const int64_t chunk = (n_per_cluster + C - 1) / C;
     if (chunk > kSelCacheMax) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C, grid_rows, 1);
-    cfg.blockDim = dim3(kSelThreads, 1, 1);
-    cfg.dynamicSmemBytes = select_smem(chunk);
-    cfg.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = C;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel<S>, args);
-    if (e == cudaSuccess) count_launch();
-    return e;
+    return launch_kernel(select_kernel<S>, dim3(C, grid_rows), dim3(kSelThreads), select_smem(chunk), st, C, args);
 }
 
 cudaError_t launch(int source, const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)

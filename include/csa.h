@@ -200,8 +200,11 @@ CSA_API csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, 
  *    each other's partials: order them on one stream or with events.
  *  - The array keeps whatever the last call left in it; nothing in it has to
  *    start at zero, because each call writes every partial it later reads.
+ *  - Only calls with few queries (at most 9) split a query over more CTAs than
+ *    a thread-block cluster holds and need partials in memory at all; 17 MiB
+ *    holds them for up to 8 queries of 64 heads x 512 dims.
  */
-#define CSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define CSA_NOALLOC_SCRATCH_BYTES (17u << 20)
 
 CSA_API csa_status csa_sparse_attend_noalloc(const csa_cache *cache, int32_t P, int32_t H, const uint16_t *q,
                                              float scale, const int32_t *idx, int32_t K, float *out, float *lse,
