@@ -9,10 +9,15 @@
 // memory as order-preserving 32-bit keys (0 = no candidate).  The K-th largest
 // key is found by a most-significant-digit radix select with fixed digits of
 // 12, 12 and 8 bits: each pass histograms, in shared memory, the keys whose
-// higher digits equal the threshold found so far, then every CTA adds its
-// non-zero bins into every CTA's cluster-wide histogram (distributed shared
-// memory reductions) and one cluster barrier later all CTAs hold the same
-// histogram and find the same threshold bin.  A pass stops early when the
+// higher digits equal the threshold found so far; the cluster sums the CTAs'
+// histograms in distributed shared memory: each CTA owns a slice of the bins,
+// every CTA adds its non-zero counts into the owners' slices (one remote
+// reduction per non-zero bin), and each owner stores its summed slice into
+// every CTA with 16-byte stores, so after two cluster barriers all CTAs hold
+// the same histogram and find the same threshold bin.  Indexer scores crowd
+// into a few coarse bins (a weighted sum over many heads varies little
+// relative to its size) and then spread over many fine bins, so the exchange
+// must stay cheap for sparse and dense histograms alike.  A pass stops early when the
 // threshold bin is taken whole, so typical data needs one or two passes.  Ties
 // at the final key go to the lower row id.  Output ids are written in ascending
 // order: per (iteration, warp) counts from warp ballots, one block scan, and
@@ -37,7 +42,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kDigit0Bins = 4096;    // key bits 31..20
 constexpr int kDigit1Bins = 4096;    // key bits 19..8
 constexpr int kDigit2Bins = 256;     // key bits 7..0
-constexpr int kSelCacheMax = 11264;  // keys held per CTA at most (44 KB): two CTAs fit one SM
+constexpr int kSelCacheMax = 15360;  // keys held per CTA at most (60 KB): two CTAs fit one SM
 constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
 constexpr int kMinChunk = 4096;      // a row is not spread thinner than this per CTA
@@ -61,23 +66,20 @@ struct SelArgs {
     float *out_scores;         // segments > 1: [rows*segments][K]
 };
 
-// Per-CTA shared state.  Other CTAs of the cluster only ever add into g0/g1/g2
-// and store into cnt_above/cnt_eq, and every such write is followed by a
+// Per-CTA shared state.  Other CTAs of the cluster only ever add into acc and
+// store into hist_g, cnt_above and cnt_eq, and every such write is followed by a
 // cluster barrier before it is read; no CTA loads another CTA's shared memory.
 struct SelShared {
-    uint32_t l0[kDigit0Bins];  // this CTA's histogram, digit 0
-    uint32_t g0[kDigit0Bins];  // cluster-wide histogram, digit 0
-    uint32_t l1[kDigit1Bins];
-    uint32_t g1[kDigit1Bins];
-    uint32_t l2[kDigit2Bins];
-    uint32_t g2[kDigit2Bins];
+    uint32_t hist_l[kDigit0Bins];  // this CTA's histogram of the current pass
+    uint32_t acc[kDigit0Bins];     // sums of the bins this CTA owns (other CTAs add into it)
+    uint32_t hist_g[kDigit0Bins];  // cluster-wide histogram of the current pass
     uint32_t cnt_above[kMaxCluster];     // per-CTA count of keys above the threshold
     uint32_t cnt_eq[kMaxCluster];        // per-CTA count of keys at the threshold
     uint32_t jw[kMaxIters * kSelWarps];  // per (iteration, warp): above << 16 | equal
     uint32_t warp_tot[kSelWarps];
     uint32_t res_bin, res_above;
 };
-constexpr int kZeroWords = 2 * (kDigit0Bins + kDigit1Bins + kDigit2Bins);
+static_assert(kDigit1Bins <= kDigit0Bins && kDigit2Bins <= kDigit0Bins, "one histogram size serves every pass");
 
 template <int S>
 struct RowView {
@@ -179,14 +181,51 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
     return before;
 }
 
-// Adds this CTA's non-zero bins into every cluster CTA's copy of the histogram.
-__device__ __forceinline__ void push_histogram(const uint32_t *local, const uint32_t *global, int nb, int C)
+__device__ __forceinline__ void cluster_store4(uint32_t addr, uint4 v)
 {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Sums the cluster's per-CTA histograms of nb bins: CTA r owns bins
+// [r*nb/C, (r+1)*nb/C); every CTA adds its non-zero counts into the owners'
+// acc; after a barrier each owner stores its slice into every CTA's hist_g and
+// clears its acc for the next pass; after a second barrier every CTA holds the
+// whole histogram.  Returns the histogram to search (the CTA's own when it is
+// alone).
+__device__ __forceinline__ const uint32_t *reduce_histogram(SelShared &sh, int nb, int C, int rank)
+{
+    __syncthreads();  // the local histogram is complete
+    if (C == 1) return sh.hist_l;
+    const int S = nb / C;  // >= 16
     for (int b = threadIdx.x; b < nb; b += kSelThreads) {
-        const uint32_t v = local[b];
-        if (v)
-            for (int q = 0; q < C; ++q) cluster_red_add(cluster_addr(global + b, q), v);
+        const uint32_t v = sh.hist_l[b];
+        if (v) cluster_red_add(cluster_addr(&sh.acc[b], b / S), v);
     }
+    cluster_barrier();
+    const int nv = S / 4;
+    const uint4 *mine = reinterpret_cast<const uint4 *>(sh.acc + rank * S);
+    for (int i = threadIdx.x; i < nv * C; i += kSelThreads) {
+        const int q = i / nv, j = i - q * nv;
+        cluster_store4(cluster_addr(&sh.hist_g[rank * S + 4 * j], q), mine[j]);
+    }
+    __syncthreads();  // every store above has read its values
+    for (int j = threadIdx.x; j < S; j += kSelThreads) sh.acc[rank * S + j] = 0;
+    cluster_barrier();
+    return sh.hist_g;
+}
+
+__device__ __forceinline__ void zero_histogram(SelShared &sh, int nb)
+{
+    uint4 *z = reinterpret_cast<uint4 *>(sh.hist_l);
+    for (int i = threadIdx.x; i < nb / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void zero_owned(SelShared &sh)
+{
+    uint4 *z = reinterpret_cast<uint4 *>(sh.acc);
+    for (int i = threadIdx.x; i < kDigit0Bins / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
 }
 
 // Finds, in a cluster-wide histogram h of nb bins, the bin b holding the
@@ -232,10 +271,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     uint32_t *cache = reinterpret_cast<uint32_t *>(dyn_smem + sizeof(SelShared));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    {
-        uint4 *z = reinterpret_cast<uint4 *>(sh.l0);
-        for (int i = tid; i < kZeroWords / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
-    }
+    zero_histogram(sh, kDigit0Bins);
+    zero_owned(sh);
     // Above: this CTA only.  Below: reads of what earlier work on the stream wrote.
     pdl_wait();
     pdl_trigger();
@@ -263,8 +300,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     const int64_t e0 = min(s1, s0 + rank * chunk), e1 = min(s1, e0 + chunk);
     const int m = static_cast<int>(e1 - e0);  // <= kSelCacheMax (the host sizes the cluster so)
 
-    __syncthreads();
-    cluster_arrive();  // the zeroed cluster-wide histograms may now receive additions
+    __syncthreads();   // histogram zeroed before any thread counts into it
+    // Every CTA of the cluster runs before any stores into another's memory.
+    cluster_arrive();
 
     // Pass 0: keys into shared memory and the digit-0 histogram.  Loads are
     // issued U at a time so that their latencies overlap.
@@ -281,51 +319,51 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             const int i = base + u * kSelThreads + tid;
             if (i < m) {
                 cache[i] = k[u];
-                if (k[u]) atomicAdd(&sh.l0[k[u] >> 20], 1u);
+                if (k[u]) atomicAdd(&sh.hist_l[k[u] >> 20], 1u);
             }
         }
     }
-    __syncthreads();
     cluster_wait();
-    push_histogram(sh.l0, sh.g0, kDigit0Bins, C);
-    cluster_barrier();
+    const uint32_t *h0 = reduce_histogram(sh, kDigit0Bins, C, rank);
 
     // Selection: every key > thr_gt, plus the first `need` keys equal to
     // thr_eq in id order.
     const uint32_t K = static_cast<uint32_t>(a.K);
     uint32_t thr_gt = 0, thr_eq = 0, need = 0;
-    const uint32_t total = find_bin(sh.g0, kDigit0Bins, K, sh);
+    const uint32_t total = find_bin(h0, kDigit0Bins, K, sh);
     if (total > K) {
         const uint32_t d0 = sh.res_bin;
         uint32_t above = sh.res_above;
-        if (sh.g0[d0] == K - above) {
+        if (h0[d0] == K - above) {
             thr_gt = d0 ? (d0 << 20) - 1u : 0u;
         } else {
+            __syncthreads();  // every thread has read h0 (the CTA's own histogram when alone)
+            zero_histogram(sh, kDigit1Bins);
+            __syncthreads();
             for (int i = tid; i < m; i += kSelThreads) {
                 const uint32_t k = cache[i];
-                if (k && (k >> 20) == d0) atomicAdd(&sh.l1[(k >> 8) & 0xFFFu], 1u);
+                if (k && (k >> 20) == d0) atomicAdd(&sh.hist_l[(k >> 8) & 0xFFFu], 1u);
             }
-            __syncthreads();
-            push_histogram(sh.l1, sh.g1, kDigit1Bins, C);
-            cluster_barrier();
-            find_bin(sh.g1, kDigit1Bins, K - above, sh);
+            const uint32_t *h1 = reduce_histogram(sh, kDigit1Bins, C, rank);
+            find_bin(h1, kDigit1Bins, K - above, sh);
             const uint32_t p24 = (d0 << 12) | sh.res_bin;
             above += sh.res_above;
-            if (sh.g1[sh.res_bin] == K - above) {
+            if (h1[sh.res_bin] == K - above) {
                 thr_gt = p24 ? (p24 << 8) - 1u : 0u;
             } else {
+                __syncthreads();  // every thread has read h1 before the histogram is reused
+                zero_histogram(sh, kDigit2Bins);
+                __syncthreads();
                 for (int i = tid; i < m; i += kSelThreads) {
                     const uint32_t k = cache[i];
-                    if (k && (k >> 8) == p24) atomicAdd(&sh.l2[k & 0xFFu], 1u);
+                    if (k && (k >> 8) == p24) atomicAdd(&sh.hist_l[k & 0xFFu], 1u);
                 }
-                __syncthreads();
-                push_histogram(sh.l2, sh.g2, kDigit2Bins, C);
-                cluster_barrier();
-                find_bin(sh.g2, kDigit2Bins, K - above, sh);
+                const uint32_t *h2 = reduce_histogram(sh, kDigit2Bins, C, rank);
+                find_bin(h2, kDigit2Bins, K - above, sh);
                 const uint32_t t = (p24 << 8) | sh.res_bin;  // >= 1: key 0 is never counted
                 above += sh.res_above;
-                need = K - above;  // 1 <= need <= g2[res_bin]
-                if (need == sh.g2[sh.res_bin]) {
+                need = K - above;  // 1 <= need <= h2[res_bin]
+                if (need == h2[sh.res_bin]) {
                     thr_gt = t - 1u;
                     need = 0;
                 } else {
