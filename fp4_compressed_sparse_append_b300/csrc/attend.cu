@@ -8,8 +8,8 @@
 //
 // One CTA = one (sequence, position) query and a contiguous share of its
 // selection, in tiles of 64 selected rows, as a warp-specialised pipeline:
-//   gather warps   fetch one tile ahead: each thread holds half of one FP4 row
-//                  (D/4 code bytes + D/32 scale bytes) in registers, then
+//   gather warps   fetch one tile ahead: each thread holds a quarter of one FP4
+//                  row (D/8 code bytes + D/64 scale bytes) in registers, then
 //                  dequantises it to fp16 (E2M1 x E4M3 is exact in fp16) into a
 //                  K-major 128B-swizzled tile V[64 rows][D] (two buffers);
 //   MMA thread     S = Q . V^T (M = 64 heads, N = 64 rows, K = D; Q staged once
@@ -42,7 +42,9 @@ namespace {
 
 constexpr int kRows = 64;           // selected rows per tile (MMA N of S, K of O^T)
 constexpr int kSoftWarps = 4;       // one per tensor-memory lane quarter
-constexpr int kGatherWarps = 4;     // two threads per selected row
+constexpr int kGatherWarps = 8;     // four threads per selected row
+constexpr int kParts = kGatherWarps * 32 / 64;  // row parts (threads per row)
+constexpr int kMaxPieces = 512 / (32 * kParts); // 16-byte code pieces per part at D = 512
 constexpr int kThreads = 32 * (kSoftWarps + kGatherWarps + 1);  // + the MMA warp
 constexpr int kMaxHeads = 64;       // S uses M = 64 (heads, zero-padded)
 constexpr float kRescaleLog2 = 8.f;
@@ -188,29 +190,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     len = a.c.lengths[b];
 
     // Gather-warp state: the rows of tile i+1 are loaded while tile i is used;
-    // thread (row gr, half grh) holds half of one FP4 row.
+    // thread (row gr, part gp) holds D/kParts channels of one FP4 row: nc
+    // 16-byte code pieces (32 channels each) and their two scale bytes each.
     const bool is_gather = warp >= kSoftWarps && warp < mma_warp;
     const int gt = tid - 32 * kSoftWarps;
-    const int gr = gt & (kRows - 1), grh = (gt >> 6) & 1;
-    const int nc = D / 64;  // 16-byte code pieces per half row
+    const int gr = gt & (kRows - 1), gp = gt >> 6;
+    const int nc = D / (32 * kParts);
     int32_t nrow = -1;
-    uint4 ncw[8];
-    uint32_t nsw[4];
+    uint4 ncw[kMaxPieces];
+    uint32_t nsw[kMaxPieces];  // two scale bytes per code piece
     auto prefetch = [&](int tile) {
         const int j = tile * kRows + gr;
         int32_t row = j < a.K ? irow[j] : -1;
         if (row >= len) {
-            if (grh == 0) raise_status(a.status, CSA_DEV_BAD_INDEX);
+            if (gp == 0) raise_status(a.status, CSA_DEV_BAD_INDEX);
             row = -1;
         }
         nrow = row;
         const int64_t g = static_cast<int64_t>(b) * a.c.cap + (row >= 0 ? row : 0);
-        const uint4 *cp = reinterpret_cast<const uint4 *>(a.c.codes + g * (D / 2)) + grh * nc;
-        const uint32_t *sp = reinterpret_cast<const uint32_t *>(a.c.scales + g * (D / 16)) + grh * (D / 128);
+        const uint4 *cp = reinterpret_cast<const uint4 *>(a.c.codes + g * (D / 2)) + gp * nc;
+        const uint16_t *sp = reinterpret_cast<const uint16_t *>(a.c.scales + g * (D / 16)) + gp * nc;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ncw[i] = (row >= 0 && i < nc) ? cp[i] : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < kMaxPieces; ++i) ncw[i] = (row >= 0 && i < nc) ? cp[i] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) nsw[i] = (row >= 0 && i < D / 128) ? sp[i] : 0u;
+        for (int i = 0; i < kMaxPieces; ++i) nsw[i] = (row >= 0 && i < nc) ? sp[i] : 0u;
     };
     if (is_gather && n_tiles > 0) prefetch(t_first);  // in flight while Q is staged
 
@@ -326,14 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             if (!mbar_wait(&sm.vempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag)) break;
             uint8_t *vb = v_s + (i & 1) * kRows * D * 2;
             const unsigned vbits = __ballot_sync(0xFFFFFFFFu, nrow >= 0);
-            if (grh == 0 && lane == 0) sm.valid[i & 1][gr >> 5] = vbits;
+            if (gp == 0 && lane == 0) sm.valid[i & 1][gr >> 5] = vbits;
 #pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
+            for (int c16 = 0; c16 < kMaxPieces; ++c16) {
                 if (c16 >= nc) break;
-                const uint32_t sc = (nsw[c16 >> 1] >> (16 * (c16 & 1))) & 0xFFFF;  // 2 scales of 32 channels
+                const uint32_t sc = nsw[c16];  // the scales of this piece's two 16-channel groups
                 const uint32_t s0 = e4m3_to_h2(sc & 0xFF), s1 = e4m3_to_h2(sc >> 8);
                 const uint32_t words[4] = {ncw[c16].x, ncw[c16].y, ncw[c16].z, ncw[c16].w};
-                const int ch0 = grh * (D / 2) + c16 * 32;
+                const int ch0 = gp * (D / kParts) + c16 * 32;
 #pragma unroll
                 for (int h8 = 0; h8 < 4; ++h8) {
                     const uint32_t sv = h8 < 2 ? s0 : s1;
