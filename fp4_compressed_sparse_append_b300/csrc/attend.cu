@@ -176,17 +176,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         tmem_relinquish();
     }
     __syncthreads();  // barrier initialisation visible to every waiting thread
-    // Above: this CTA only.  Below: reads of what earlier work on the stream wrote.
-    pdl_wait();
-    pdl_trigger();
     // The query block [64 head rows][D] bf16 arrives by TMA, 128B-swizzled in
     // 64-dim boxes, in the second V buffer (free until the first tile is done).
+    // The query is an input of the step, never written by this library's
+    // kernels, so it is fetched before waiting on the previous kernel.
     uint8_t *q_stage = v_s + kRows * D * 2;
     if (tid == 0) {
         mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(kMaxHeads * D * 2));
         for (int kb = 0; kb < D / 64; ++kb)
             tma_load_2d(q_stage + kb * kMaxHeads * 128, &qmap, &sm.qbar, kb * 128, unit * H);
     }
+    // Below: reads of what earlier kernels on the stream wrote (lengths, indices, cache).
+    pdl_wait();
+    pdl_trigger();
     len = a.c.lengths[b];
 
     // Gather-warp state: the rows of tile i+1 are loaded while tile i is used;

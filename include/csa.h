@@ -27,6 +27,14 @@
  *    device pointer must be 16-byte aligned (cache lengths: 4-byte).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  No call synchronises the host, except csa_device_status.
+ *  - Kernels are launched with programmatic dependent launch: each may start
+ *    while the kernel before it on the stream finishes, and waits for it
+ *    before reading anything that kernel could have written.  One exception:
+ *    the attention kernels fetch the main query q before that wait, so q
+ *    must not be written by a kernel that lets its dependents start early
+ *    (griddepcontrol.launch_dependents) and runs immediately before the call.
+ *    Kernels that do not use that instruction, copies and the library's own
+ *    kernels are all safe producers of q.
  *  - Argument errors return CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED before
  *    anything is launched.  Launch failures return CSA_ERR_CUDA.
  *  - Faults found on the device (a row index outside [0, length), an append
