@@ -12,7 +12,9 @@
 // tensor memory and reduces sum_h w_h ReLU(.) over its own columns with no
 // cross-thread traffic; the [128 x N] product never leaves the SM.
 //
-// Persistent, warp-specialised CTA (one per SM):
+// Persistent, warp-specialised CTAs (two per SM when their tensor-memory
+// slots fit in half of it, so that two MMA threads keep the tensor core and the
+// key stream busy while either one waits on a barrier):
 //   warp 0      TMA producer: each job is up to 4 consecutive 128-row key tiles
 //               of one unit (or 16 pool blocks of 8 rows) in one stage of a
 //               shared-memory ring; the unit's query rows.
@@ -26,8 +28,8 @@
 //               alternate slots; tcgen05.ld, weighted ReLU sum, coalesced fp32
 //               score stores.
 // The stage size matters: the MMA thread's fixed cost per stage (barrier waits,
-// commits) is several hundred cycles, so 16 KB stages cap a CTA near 25 GB/s
-// while 64 KB stages leave the key stream bound by HBM.
+// commits) is several hundred cycles, so a single CTA with 16 KB stages caps
+// near 25 GB/s; 32 KB stages with two CTAs per SM stream fastest.
 // Every wait is bounded (kWaitLimitNs); a wait that runs out raises
 // CSA_DEV_TIMEOUT and the CTA drains its copies and returns.
 #include "common.cuh"
@@ -208,7 +210,7 @@ __device__ __forceinline__ float weighted_relu_sum_any(uint32_t taddr, int col, 
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     index_score_kernel(const __grid_constant__ CUtensorMap keys128, const __grid_constant__ CUtensorMap keys8,
                        const __grid_constant__ CUtensorMap qmap, IdxArgs a)
 {
@@ -514,11 +516,15 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     a.gps = (a.groups + n_sub - 1) / n_sub;
     a.sub_cols = (a.gps * HI + 15) / 16 * 16;
     if (n_sub > 1 && (a.gps * HI) % 8) return cudaErrorInvalidValue;
-    // Key tiles per job: as many as keep two slots within tensor memory.
+    // Two CTAs per SM when two accumulator slots of two key tiles (or one,
+    // for a pool) fit in half of tensor memory; key tiles per job: as many as
+    // keep two slots within the CTA's share of tensor memory.
+    const int per_sm = 2 * (a.pool_mode ? 1 : 2) * a.sub_cols <= kMaxCols / 2 ? 2 : 1;
+    const int cols_cta = kMaxCols / per_sm;
     a.mt = 1;
-    while (!a.pool_mode && 2 * a.mt <= kMaxTilesPerJob && 2 * (2 * a.mt) * a.sub_cols <= kMaxCols) a.mt *= 2;
+    while (!a.pool_mode && 2 * a.mt <= kMaxTilesPerJob / per_sm && 2 * (2 * a.mt) * a.sub_cols <= cols_cta) a.mt *= 2;
     a.n_acc = 2;
-    while (2 * a.n_acc <= kMaxAcc && 2 * a.n_acc * a.mt * a.sub_cols <= kMaxCols) a.n_acc *= 2;
+    while (2 * a.n_acc <= kMaxAcc && 2 * a.n_acc * a.mt * a.sub_cols <= cols_cta) a.n_acc *= 2;
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(a.n_acc * a.mt * a.sub_cols)) cols *= 2;
     a.tmem_cols = cols;
@@ -542,7 +548,7 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     const size_t prefix_bytes = a.prefix_smem ? (static_cast<size_t>(a.units) + 1) * sizeof(int) : 0;
     const size_t fixed =
         1024 /*align*/ + b_bytes + w_bytes + (2 * kMaxStages + 2 * kMaxAcc + 4) * 8 + 16 + prefix_bytes;
-    const size_t budget = 224 * 1024;
+    const size_t budget = per_sm == 1 ? 224 * 1024 : 110 * 1024;
     int stages = static_cast<int>((budget - fixed) / stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -569,7 +575,8 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     const cudaError_t e =
         cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_kernel(index_score_kernel, dim3(g_num_sms), dim3(kThreads), smem, st, 0, k128, k8, qm, a);
+    return launch_kernel(index_score_kernel, dim3(g_num_sms * per_sm), dim3(kThreads), smem, st, 0, k128, k8, qm,
+                         a);
 }
 
 }  // namespace csa
