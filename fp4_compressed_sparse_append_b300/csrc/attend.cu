@@ -556,14 +556,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         const float *obuf = reinterpret_cast<const float *>(v_s);
         for (int w = tid; w < H * nd4; w += kThreads) {
             const int hh = w / nd4, d = d0 + 4 * (w - hh * nd4);
+            // All the splits' loads are issued before any is used.
+            float4 v[kMaxClusterSplit];
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplit; ++q)
+                if (q < C) v[q] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(obuf, q) + hh * D + d);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int q = 0; q < C; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(obuf, q) + hh * D + d);
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplit; ++q) {
+                if (q >= C) break;
                 const float wgt = wq[q * kMaxHeads + hh];
-                acc.x = fmaf(wgt, v.x, acc.x);
-                acc.y = fmaf(wgt, v.y, acc.y);
-                acc.z = fmaf(wgt, v.z, acc.z);
-                acc.w = fmaf(wgt, v.w, acc.w);
+                acc.x = fmaf(wgt, v[q].x, acc.x);
+                acc.y = fmaf(wgt, v[q].y, acc.y);
+                acc.z = fmaf(wgt, v[q].z, acc.z);
+                acc.w = fmaf(wgt, v[q].w, acc.w);
             }
             *reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(unit) * H + hh) * D + d) = acc;
         }
@@ -623,7 +629,8 @@ struct Plan {
 
 // Splits of one query's selection: at most one wave of CTAs.  Up to
 // kMaxClusterSplit splits form a cluster and merge on chip; more (only for
-// very few queries) merge through global memory.
+// very few queries) merge through global memory, which measures faster than a
+// cluster of 16 for them.
 Plan plan(const CacheView &c, int P, int K)
 {
     const int units = c.B * P;
@@ -664,7 +671,11 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     const int units = c.B * P;
     if (units == 0) return cudaSuccess;
     if (H > kMaxHeads || c.D % 128 || c.D > 512) return cudaErrorInvalidValue;
+    const size_t smem = smem_bytes(c.D, (H + 15) / 16 * 16);
     const Plan p = plan(c, P, K);
+    cudaError_t e =
+        cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     if (ws_bytes < attend_workspace_bytes(c, P, H, K)) return cudaErrorInvalidValue;
     AttArgs a{};
     a.c = c;
@@ -689,15 +700,11 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     while (cols < static_cast<uint32_t>(2 * kRows + (c.D / 128) * a.NH)) cols *= 2;
     a.tmem_cols = cols;
     a.status = status;
-    const size_t smem = smem_bytes(c.D, a.NH);
     // Query rows [units*H][D] bf16 as bytes: 64-dim (128-byte) boxes of 64 rows.
     CUtensorMap qm;
     if (encode_tensor_map_2d_u8(&qm, q, static_cast<uint64_t>(c.D) * 2, static_cast<uint64_t>(units) * H, 128,
                                 kMaxHeads, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    cudaError_t e =
-        cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     e = launch_kernel(attend_kernel, dim3(p.nsplit, units), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0, qm,
                       a);
     if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;

@@ -42,7 +42,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kDigit0Bins = 4096;    // key bits 31..20
 constexpr int kDigit1Bins = 4096;    // key bits 19..8
 constexpr int kDigit2Bins = 256;     // key bits 7..0
-constexpr int kSelCacheMax = 15360;  // keys held per CTA at most (60 KB): two CTAs fit one SM
+constexpr int kSelCacheMax = 16384;  // keys held per CTA at most (64 KB; up to 15,360 two CTAs fit one SM)
 constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
 constexpr int kMinChunk = 4096;      // a row is not spread thinner than this per CTA
@@ -302,7 +302,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 
     __syncthreads();   // histogram zeroed before any thread counts into it
     // Every CTA of the cluster runs before any stores into another's memory.
-    cluster_arrive();
+    // A CTA alone needs no cluster barrier anywhere (they cost ~10x a CTA barrier).
+    const bool solo = C == 1;
+    if (!solo) cluster_arrive();
 
     // Pass 0: keys into shared memory and the digit-0 histogram.  Loads are
     // issued U at a time so that their latencies overlap.
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
             }
         }
     }
-    cluster_wait();
+    if (!solo) cluster_wait();
     const uint32_t *h0 = reduce_histogram(sh, kDigit0Bins, C, rank);
 
     // Selection: every key > thr_gt, plus the first `need` keys equal to
@@ -390,11 +392,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         const uint32_t ex = block_exclusive_scan(v, sh.warp_tot, &cta_tot);
         if (tid < J * kSelWarps) sh.jw[tid] = ex;
     }
-    if (tid < C) {
-        cluster_store(cluster_addr(&sh.cnt_above[rank], tid), cta_tot >> 16);
-        cluster_store(cluster_addr(&sh.cnt_eq[rank], tid), cta_tot & 0xFFFFu);
+    if (!solo) {
+        if (tid < C) {
+            cluster_store(cluster_addr(&sh.cnt_above[rank], tid), cta_tot >> 16);
+            cluster_store(cluster_addr(&sh.cnt_eq[rank], tid), cta_tot & 0xFFFFu);
+        }
+        cluster_barrier();  // last remote write: from here on CTAs touch only their own memory
     }
-    cluster_barrier();  // last remote write: from here on CTAs touch only their own memory
     uint32_t above0 = 0, tie0 = 0;
     for (int q = 0; q < rank; ++q) {
         above0 += sh.cnt_above[q];
@@ -448,7 +452,9 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
         configured = true;
     }
     // Smallest cluster whose chunks fit shared memory, widened (down to
-    // kMinChunk keys per CTA) while the grid is under one CTA per SM.
+    // kMinChunk keys per CTA) while the grid is under one CTA per SM: spreading
+    // a row's keys over more CTAs also spreads the contention of its shared-
+    // memory histogram, which crowded indexer scores make high.
     int C = 1;
     while (C < kMaxCluster &&
            ((n_per_cluster + C - 1) / C > kSelCacheMax ||
