@@ -585,19 +585,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
 // Combines the split partials: block = (128 dims, head, query); each thread
 // loads its dim from every split at once.  out = sum_s 2^(m_s - M) O_s / L,
 // L = sum_s 2^(m_s - M) l_s, lse = ln 2 * (M + log2 L).
-constexpr int kMaxSplit = 16;
+constexpr int kMaxSplit = 32;  // one warp holds every split's (m, l) in the merge
 
+template <int MS>
 __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsplit, const float *__restrict__ part_o,
                                                           const float2 *__restrict__ part_ml, float *__restrict__ out,
                                                           float *__restrict__ lse)
 {
     pdl_wait();
-    __shared__ float wsh[kMaxSplit];
+    __shared__ float wsh[MS];
     __shared__ float inv_l;
     const int d = blockIdx.x * 128 + threadIdx.x, h = blockIdx.y, unit = blockIdx.z;
-    float pv[kMaxSplit];
+    float pv[MS];
 #pragma unroll
-    for (int s = 0; s < kMaxSplit; ++s)
+    for (int s = 0; s < MS; ++s)
         pv[s] = (s < nsplit && d < D) ? part_o[((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d] : 0.f;
     if (threadIdx.x < 32) {
         const int s = threadIdx.x;
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
         float L = w * ml.y;
 #pragma unroll
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
-        if (s < kMaxSplit) wsh[s] = w;
+        if (s < MS) wsh[s] = w;
         if (s == 0) {
             inv_l = L > 0.f ? 1.f / L : 0.f;
             if (lse && blockIdx.x == 0) lse[static_cast<int64_t>(unit) * H + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
@@ -619,7 +620,7 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
     __syncthreads();
     float acc = 0.f;
 #pragma unroll
-    for (int s = 0; s < kMaxSplit; ++s) acc = fmaf(wsh[s], pv[s], acc);
+    for (int s = 0; s < MS; ++s) acc = fmaf(wsh[s], pv[s], acc);
     if (d < D) out[(static_cast<int64_t>(unit) * H + h) * D + d] = acc * inv_l;
 }
 
@@ -708,9 +709,10 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     e = launch_kernel(attend_kernel, dim3(p.nsplit, units), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0, qm,
                       a);
     if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
-    return launch_kernel(attend_merge_kernel, dim3((c.D + 127) / 128, H, units), dim3(128), 0, st, 0, c.D, H,
-                         p.nsplit, static_cast<const float *>(a.part_o), static_cast<const float2 *>(a.part_ml), out,
-                         lse);
+    // The merge loads every split's value at once: 16 or 32 registers.
+    auto merge = p.nsplit <= 16 ? attend_merge_kernel<16> : attend_merge_kernel<kMaxSplit>;
+    return launch_kernel(merge, dim3((c.D + 127) / 128, H, units), dim3(128), 0, st, 0, c.D, H, p.nsplit,
+                         static_cast<const float *>(a.part_o), static_cast<const float2 *>(a.part_ml), out, lse);
 }
 
 }  // namespace csa

@@ -98,12 +98,16 @@ struct RowView {
                 if (r0 + m < L) best = fmaxf(best, __ldg(s + r0 + m));
             return score_key(best);
         }
+        // Both loads are issued before either is tested, so they overlap.
         if (S == kPoolRows) {
             const int32_t blk = __ldg(prow + (i >> 3));
+            const float v = __ldg(s + i);
             const int64_t row = static_cast<int64_t>(blk) * kPoolBlock + (i & 7);
-            return (blk >= 0 && row < L) ? score_key(__ldg(s + i)) : 0u;
+            return (blk >= 0 && row < L) ? score_key(v) : 0u;
         }
-        return __ldg(ids + i) >= 0 ? score_key(__ldg(s + i)) : 0u;
+        const int32_t id = __ldg(ids + i);
+        const float v = __ldg(s + i);
+        return id >= 0 ? score_key(v) : 0u;
     }
     __device__ __forceinline__ int32_t id(int64_t i) const
     {
@@ -408,22 +412,36 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     // Output position of a selected key = selected keys with a lower id.
     const int64_t obase = static_cast<int64_t>(blockIdx.y) * a.K;
     const unsigned lt = (1u << lane) - 1u;
-    for (int j = 0; j < J; ++j) {
-        const int i = j * kSelThreads + tid;
-        const uint32_t k = i < m ? cache[i] : 0u;
-        const bool is_above = k > thr_gt;
-        const bool is_tie = need && k == thr_eq;
-        const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
-        const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
-        const uint32_t base = sh.jw[j * kSelWarps + warp];
-        const uint32_t a_before = above0 + (base >> 16) + __popc(ba & lt);
-        const uint32_t t_before = tie0 + (base & 0xFFFFu) + __popc(be & lt);
-        int64_t pos = -1;
-        if (is_above) pos = a_before + min(t_before, need);
-        else if (is_tie && t_before < need) pos = a_before + t_before;
-        if (pos >= 0) {
-            a.out_ids[obase + pos] = rv.id(e0 + i);
-            if (a.out_scores) a.out_scores[obase + pos] = key_score(k);
+    // Ids that live in memory (pool rows, stage-2 pairs) are fetched eight
+    // iterations at a time, so their latencies overlap instead of adding up.
+    constexpr int W = (S == kPoolRows || S == kPairs) ? 8 : 1;
+    for (int j0 = 0; j0 < J; j0 += W) {
+        int32_t idv[W];
+#pragma unroll
+        for (int u = 0; u < W; ++u) {
+            const int i = (j0 + u) * kSelThreads + tid;
+            idv[u] = (W > 1 && j0 + u < J && i < m) ? rv.id(e0 + i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < W; ++u) {
+            const int j = j0 + u;
+            if (j >= J) break;
+            const int i = j * kSelThreads + tid;
+            const uint32_t k = i < m ? cache[i] : 0u;
+            const bool is_above = k > thr_gt;
+            const bool is_tie = need && k == thr_eq;
+            const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
+            const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
+            const uint32_t base = sh.jw[j * kSelWarps + warp];
+            const uint32_t a_before = above0 + (base >> 16) + __popc(ba & lt);
+            const uint32_t t_before = tie0 + (base & 0xFFFFu) + __popc(be & lt);
+            int64_t pos = -1;
+            if (is_above) pos = a_before + min(t_before, need);
+            else if (is_tie && t_before < need) pos = a_before + t_before;
+            if (pos >= 0) {
+                a.out_ids[obase + pos] = W > 1 ? idv[u] : rv.id(e0 + i);
+                if (a.out_scores) a.out_scores[obase + pos] = key_score(k);
+            }
         }
     }
     const uint32_t selected_total = total > K ? K : total;
