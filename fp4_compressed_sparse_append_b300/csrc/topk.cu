@@ -42,7 +42,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kDigit0Bins = 4096;    // key bits 31..20
 constexpr int kDigit1Bins = 4096;    // key bits 19..8
 constexpr int kDigit2Bins = 256;     // key bits 7..0
-constexpr int kSelCacheMax = 16384;  // keys held per CTA at most (64 KB; up to 15,360 two CTAs fit one SM)
+constexpr int kSelCacheMax = 16384;  // keys held per CTA at most (64 KB): two CTAs fit one SM
 constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
 constexpr int kMinChunk = 4096;      // a row is not spread thinner than this per CTA
@@ -71,7 +71,7 @@ struct SelArgs {
 // cluster barrier before it is read; no CTA loads another CTA's shared memory.
 struct SelShared {
     uint32_t hist_l[kDigit0Bins];  // this CTA's histogram of the current pass
-    uint32_t acc[kDigit0Bins];     // sums of the bins this CTA owns (other CTAs add into it)
+    uint32_t acc[kDigit0Bins / 2]; // sums of the bins this CTA owns, at most half (other CTAs add into it)
     uint32_t hist_g[kDigit0Bins];  // cluster-wide histogram of the current pass
     uint32_t cnt_above[kMaxCluster];     // per-CTA count of keys above the threshold
     uint32_t cnt_eq[kMaxCluster];        // per-CTA count of keys at the threshold
@@ -202,20 +202,21 @@ __device__ __forceinline__ const uint32_t *reduce_histogram(SelShared &sh, int n
 {
     __syncthreads();  // the local histogram is complete
     if (C == 1) return sh.hist_l;
-    const int S = nb / C;  // >= 16
+    const int S = nb / C;  // >= 16, <= nb / 2
     for (int b = threadIdx.x; b < nb; b += kSelThreads) {
         const uint32_t v = sh.hist_l[b];
-        if (v) cluster_red_add(cluster_addr(&sh.acc[b], b / S), v);
+        const int owner = b / S;
+        if (v) cluster_red_add(cluster_addr(&sh.acc[b - owner * S], owner), v);
     }
     cluster_barrier();
     const int nv = S / 4;
-    const uint4 *mine = reinterpret_cast<const uint4 *>(sh.acc + rank * S);
+    const uint4 *mine = reinterpret_cast<const uint4 *>(sh.acc);
     for (int i = threadIdx.x; i < nv * C; i += kSelThreads) {
         const int q = i / nv, j = i - q * nv;
         cluster_store4(cluster_addr(&sh.hist_g[rank * S + 4 * j], q), mine[j]);
     }
     __syncthreads();  // every store above has read its values
-    for (int j = threadIdx.x; j < S; j += kSelThreads) sh.acc[rank * S + j] = 0;
+    for (int j = threadIdx.x; j < S; j += kSelThreads) sh.acc[j] = 0;
     cluster_barrier();
     return sh.hist_g;
 }
@@ -229,7 +230,7 @@ __device__ __forceinline__ void zero_histogram(SelShared &sh, int nb)
 __device__ __forceinline__ void zero_owned(SelShared &sh)
 {
     uint4 *z = reinterpret_cast<uint4 *>(sh.acc);
-    for (int i = threadIdx.x; i < kDigit0Bins / 4; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kDigit0Bins / 8; i += kSelThreads) z[i] = make_uint4(0, 0, 0, 0);
 }
 
 // Finds, in a cluster-wide histogram h of nb bins, the bin b holding the
