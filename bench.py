@@ -31,7 +31,7 @@ L2_FLUSH_BYTES = 256 << 20
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="full_64k")
@@ -79,31 +79,61 @@ def step_bytes(wl):
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes; no
+    Python NVML package is needed).  Clock-event reason bits are NVML's."""
+
+    SW_POWER_CAP, HW_SLOWDOWN, SW_THERMAL, HW_THERMAL = 0x4, 0x8, 0x20, 0x40
+    CLOCK_SM = 1
+
+    def __init__(self, index):
+        import ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self._ct = ctypes
+
+    def clock(self, fn):
+        v = self._ct.c_uint()
+        if getattr(self.lib, fn)(self.h, self._ct.c_int(self.CLOCK_SM), self._ct.byref(v)) != 0:
+            raise RuntimeError(fn + " failed")
+        return v.value
+
+    def reasons(self):
+        v = self._ct.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(self.h, self._ct.byref(v)) != 0:
+            raise RuntimeError("clock event reasons failed")
+        return v.value
+
+
 class Clocks:
     """Samples the SM clock and the clock-event reasons while the timed region
-    runs (read-only queries: NVML when importable, else nvidia-smi one-shot
-    queries), in a background thread; one sample is always taken at start and
-    one at stop."""
+    runs (read-only queries: NVML through the driver library every couple of
+    milliseconds, else nvidia-smi one-shot queries), in a background thread;
+    one sample is always taken at start and one at stop."""
 
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
     QUERY = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index, period_s=0.05):
+    def __init__(self, gpu_index, period_s=0.002):
         self.gpu, self.period = gpu_index, period_s
         self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
         self._stop, self._thread, self._nvml = None, None, None
 
     def _sample(self):
         if self._nvml is not None:
-            N, h = self._nvml
-            self.samples.append(N.nvmlDeviceGetClockInfo(h, N.NVML_CLOCK_SM))
-            self.max_mhz = N.nvmlDeviceGetMaxClockInfo(h, N.NVML_CLOCK_SM)
-            bits = N.nvmlDeviceGetCurrentClocksEventReasons(h)
-            consts = (N.nvmlClocksEventReasonHwSlowdown, N.nvmlClocksEventReasonHwThermalSlowdown,
-                      N.nvmlClocksEventReasonSwThermalSlowdown, N.nvmlClocksEventReasonSwPowerCap)
-            for name, c in zip(self.REASONS, consts):
+            N = self._nvml
+            self.samples.append(N.clock("nvmlDeviceGetClockInfo"))
+            self.max_mhz = N.clock("nvmlDeviceGetMaxClockInfo")
+            bits = N.reasons()
+            for name, c in zip(self.REASONS, (N.HW_SLOWDOWN, N.HW_THERMAL, N.SW_THERMAL, N.SW_POWER_CAP)):
                 if bits & c:
                     self.reasons.add(name)
             return
@@ -127,11 +157,10 @@ class Clocks:
     def start(self):
         import threading
         try:
-            import pynvml as N
-            N.nvmlInit()
-            self._nvml = (N, N.nvmlDeviceGetHandleByIndex(self.gpu))
+            self._nvml = _Nvml(self.gpu)
         except Exception:
             self._nvml = None
+            self.period = max(self.period, 0.05)
         try:
             self._sample()
         except Exception as e:
@@ -468,11 +497,14 @@ def config_of(wl):
             "l2": "flushed between timed steps (a 256 MiB read outside the timed events)"}
 
 
-def index_traffic_from_profile():
-    """DRAM bytes per index_score launch from the committed ncu summary, or None
-    when the kernel's sources have changed since that capture (the summary
-    records the sha256 of the sources it was taken with)."""
+def index_traffic_from_profile(workload):
+    """DRAM bytes per index_score launch from the committed ncu summary of the
+    full_64k step, or None for another workload, or when the kernel's sources
+    have changed since that capture (the summary records the sha256 of the
+    sources it was taken with)."""
     import hashlib
+    if workload != "full_64k":
+        return None, "no ncu capture of this workload"
     path = os.path.join(ROOT, "profiles", "index_score_full_64k.md")
     csrc = os.path.join(ROOT, "fp4_compressed_sparse_append_b300", "csrc")
     try:
@@ -519,7 +551,7 @@ def main():
     peak_src = "measured" if peak_hbm else "fallback"
     peak_hbm = peak_hbm or 6400.0
     idx_ms = r["stages"].get("index_score")
-    traffic, traffic_src = index_traffic_from_profile()
+    traffic, traffic_src = index_traffic_from_profile(wl.name)
     dominant = max(r["stages"], key=r["stages"].get) if r["stages"] else None
     roof = None
     if idx_ms:
