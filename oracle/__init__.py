@@ -77,6 +77,7 @@ def lib():
         L.oracle_topk.argtypes = [P, P, i64, i64, P]
         L.oracle_block_max.argtypes = [P, i64, i32, P]
         L.oracle_attend.argtypes = [P, i32, i32, dbl, P, P, P, i64, P, P]
+        L.oracle_attend_swa.argtypes = [P, i32, i32, dbl, P, P, P, i64, P, i64, i64, P, P]
         for f in (L.oracle_quantize_rows, L.oracle_dequantize_rows, L.oracle_index_score,
                   L.oracle_topk, L.oracle_block_max, L.oracle_attend):
             f.restype = None
@@ -278,6 +279,33 @@ def attend(q_bits, codes_b, scales_b, idx, scale: float):
     lse = np.zeros(H, np.float32)
     lib().oracle_attend(_ptr(q), H, D, float(scale), _ptr(c), _ptr(s), _ptr(ix), ix.shape[0],
                         _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def swa_window(n_swa: int, P: int, p: int, window: int):
+    """Rows [lo, hi) of a sequence's local cache that position p attends to:
+    the `window` most recent tokens up to and including its own, whose row is
+    n_swa - P + p (the step's P positions are the last P local rows).
+    "G2C Brief - DeepSeek V4.1-Flash", section "Two attention paths in every
+    layer": exact sliding-window attention over the most recent 128 tokens."""
+    own = n_swa - P + p
+    return max(0, own - window + 1), own + 1
+
+
+def attend_swa(q_bits, codes_b, scales_b, idx, swa_b, lo: int, hi: int, scale: float):
+    """Joint softmax over the selected FP4 rows and the FP8 E4M3 window rows
+    swa_b[lo:hi] (one shared latent per token, K = V).  q [H, D] bf16 bits;
+    swa_b [n_swa, D] E4M3 bytes -> (out fp32 [H, D], lse fp32 [H])."""
+    q = _np(q_bits, np.uint16)
+    c = _np(codes_b, np.uint8)
+    s = _np(scales_b, np.uint8)
+    w = _np(swa_b, np.uint8)
+    ix = np.ascontiguousarray(np.asarray(idx, np.int64))
+    H, D = q.shape
+    out = np.zeros((H, D), np.float32)
+    lse = np.zeros(H, np.float32)
+    lib().oracle_attend_swa(_ptr(q), H, D, float(scale), _ptr(c), _ptr(s), _ptr(ix), ix.shape[0], _ptr(w),
+                            int(lo), int(hi), _ptr(out), _ptr(lse))
     return out, lse
 
 

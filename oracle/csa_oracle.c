@@ -338,3 +338,74 @@ void oracle_attend(const uint16_t *q, int H, int D, double scale,
     free(z);
     free(v);
 }
+
+/* Joint attention of the sparse global branch and the local sliding window.
+ * [FPR] "The Paper": the selected entries are glued onto the sliding-window
+ * KV and the query attends to both with one softmax; [G2C] "Two attention
+ * paths in every layer": the local branch is exact attention over the most
+ * recent 128 tokens; "FP4 cache entries, and why they're safe": the local
+ * cache stays in FP8.  Window rows are FP8 E4M3 vectors of D channels (no
+ * scale), one shared latent per token (K = V, as for the global entries).
+ * swa holds the sequence's local rows; rows [lo, hi) are the window.  The
+ * softmax runs over the selected dequantised FP4 rows and the window rows
+ * together, in double precision. */
+void oracle_attend_swa(const uint16_t *q, int H, int D, double scale,
+                       const uint8_t *codes, const uint8_t *scales,
+                       const int64_t *idx, int64_t K,
+                       const uint8_t *swa, int64_t lo, int64_t hi,
+                       float *out, float *lse)
+{
+    int64_t nv = 0;
+    for (int64_t j = 0; j < K; ++j)
+        if (idx[j] >= 0)
+            ++nv;
+    const int64_t nw = hi > lo ? hi - lo : 0;
+    const int64_t n = nv + nw;
+    double *v = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
+    int64_t r = 0;
+    for (int64_t j = 0; j < K; ++j)
+        if (idx[j] >= 0) {
+            oracle_dequantize_rows(codes + idx[j] * (int64_t)(D / 2), scales + idx[j] * (int64_t)(D / 16),
+                                   1, D, v + r * D);
+            ++r;
+        }
+    for (int64_t t = lo; t < hi; ++t, ++r)
+        for (int d = 0; d < D; ++d)
+            v[r * D + d] = oracle_e4m3_value(swa[t * (int64_t)D + d]);
+    double *z = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double *acc = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int h = 0; h < H; ++h) {
+        if (n == 0) {
+            for (int d = 0; d < D; ++d)
+                out[h * D + d] = 0.0f;
+            if (lse)
+                lse[h] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += oracle_bf16_value(q[h * D + d]) * v[j * D + d];
+            z[j] = scale * dot;
+            if (z[j] > m)
+                m = z[j];
+        }
+        double l = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc[d] = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            double p = exp(z[j] - m);
+            l += p;
+            for (int d = 0; d < D; ++d)
+                acc[d] += p * v[j * D + d];
+        }
+        for (int d = 0; d < D; ++d)
+            out[h * D + d] = (float)(acc[d] / l);
+        if (lse)
+            lse[h] = (float)(m + log(l));
+    }
+    free(acc);
+    free(z);
+    free(v);
+}
