@@ -70,6 +70,9 @@ def step_bytes(wl):
             if mode == W.FULL and wl.pool_blocks:
                 pool_built = True
         total += units * min(wl.K, L) * row + q
+        if wl.window:
+            # the local FP8 rows of each sequence's windows (positions share rows)
+            total += wl.B * (wl.window + wl.P - 1) * wl.D
     if wl.n_append:
         total += wl.B * wl.n_append * (wl.D * 2 + wl.DI + row + wl.DI)
     return total, index_bytes
@@ -218,6 +221,7 @@ def build_state(wl, seed, device):
     del lat, ik
     torch.cuda.synchronize()
     app = W.append_rows(wl, seed, device=device) if wl.n_append else None
+    swa = B.Swa(W.local_rows(wl, seed, device=device), wl.window) if wl.window else None
     layers, prev, pool = [], None, None
     for li, mode in enumerate(wl.layers):
         inp = W.layer_inputs(wl, seed, li, device=device)
@@ -226,7 +230,7 @@ def build_state(wl, seed, device):
                          rows_new=app["rows"] if (app and li == 0) else None,
                          ikeys_new=app["ikeys"] if (app and li == 0) else None,
                          pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
-                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None))
+                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None), swa=swa)
         if mode != W.REUSE:
             prev = la.idx
         if la.pool_out is not None:
@@ -351,7 +355,9 @@ def stage_times(cache, layers, wl, flush, steps, stream):
     scores = B.csa_index_score(cache, iq, w)
     ws_sel = torch.empty(max(16, B.topk_workspace_size(cache, wl.P, wl.K)), dtype=torch.uint8, device=dev)
     idx, _ = B.csa_topk(cache, scores, wl.K, workspace=ws_sel)
-    ws_att = torch.empty(max(16, B.attend_workspace_size(cache, wl.P, wl.H, wl.K)), dtype=torch.uint8, device=dev)
+    swa = la.swa
+    ws_att = torch.empty(max(16, B.attend_swa_workspace_size(cache, wl.P, wl.H, wl.K, swa)), dtype=torch.uint8,
+                         device=dev)
     o = torch.empty(q.shape, dtype=torch.float32, device=dev)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
@@ -372,8 +378,8 @@ def stage_times(cache, layers, wl, flush, steps, stream):
 
     out["index_score"] = timed(lambda: B.csa_index_score(cache, iq, w, scores=scores))
     out["topk"] = timed(lambda: B.csa_topk(cache, scores, wl.K, workspace=ws_sel))
-    out["sparse_attend"] = timed(lambda: B.csa_sparse_attend(cache, q, idx, wl.scale, workspace=ws_att, out=o,
-                                                             lse=lse))
+    out["sparse_attend"] = timed(lambda: B.csa_sparse_attend_swa(cache, q, idx, wl.scale, swa, workspace=ws_att,
+                                                                 out=o, lse=lse))
     return out
 
 
@@ -448,10 +454,11 @@ def oracle_sample(wl, seed, max_seconds):
         oc.append(app["rows"][:1].numpy(), app["ikeys"][:1].numpy())
     inputs = [{k: v[:1].numpy() for k, v in W.layer_inputs(wl, seed, li, device="cpu").items()}
               for li in range(len(wl.layers))]
+    swa = (W.local_rows(wl, seed, device="cpu")[:1].numpy(), wl.window) if wl.window else None
     done, t0 = 0, time.perf_counter()
     while True:
         oracle.run_chain(oc, wl.layers, inputs, wl.K, wl.scale, P=wl.P, pool_keep=wl.pool_blocks,
-                         units=[(0, 0)], score_threads=cores)
+                         units=[(0, 0)], score_threads=cores, swa=swa)
         done += 1
         el = time.perf_counter() - t0
         if el > max_seconds or done >= 50:

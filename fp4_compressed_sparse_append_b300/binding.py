@@ -22,7 +22,7 @@ CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
     "csa_quantize_append", "csa_index_score", "csa_topk", "csa_topk_workspace_size", "csa_sparse_attend",
-    "csa_sparse_attend_noalloc",
+    "csa_sparse_attend_noalloc", "csa_sparse_attend_swa", "csa_attend_swa_workspace_size",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
 )
@@ -40,6 +40,11 @@ class csa_cache(ctypes.Structure):
                 ("ikeys", ctypes.c_void_p), ("lengths", ctypes.c_void_p)]
 
 
+class csa_swa(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_void_p), ("lengths", ctypes.c_void_p), ("n", ctypes.c_int32),
+                ("window", ctypes.c_int32)]
+
+
 class csa_layer_args(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("P", ctypes.c_int32), ("H", ctypes.c_int32), ("HI", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("scale", ctypes.c_float), ("q", ctypes.c_void_p),
@@ -47,7 +52,7 @@ class csa_layer_args(ctypes.Structure):
                 ("ikeys_new", ctypes.c_void_p), ("n_new", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
                 ("pool_in", ctypes.c_void_p), ("pool_out", ctypes.c_void_p), ("idx", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("swa", ctypes.c_void_p)]
 
 
 _lib = None
@@ -70,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.csa_sparse_attend.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V, SZ, V]
         L.csa_sparse_attend_noalloc.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V]
         L.csa_attend_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
+        S = ctypes.POINTER(csa_swa)
+        L.csa_sparse_attend_swa.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, S, V, V, V, SZ, V]
+        L.csa_attend_swa_workspace_size.argtypes = [C, I32, I32, I32, S, ctypes.POINTER(SZ)]
         L.csa_layer_step.argtypes = [C, ctypes.POINTER(csa_layer_args), V]
         L.csa_layer_workspace_size.argtypes = [C, ctypes.POINTER(csa_layer_args), ctypes.POINTER(SZ)]
         L.csa_device_status.argtypes = [ctypes.POINTER(I32), I32, V]
@@ -215,11 +223,51 @@ def csa_sparse_attend_noalloc(cache: Cache, q: torch.Tensor, idx: torch.Tensor, 
                                            _stream(stream)), "csa_sparse_attend_noalloc")
 
 
+class Swa:
+    """The local window of csa_swa: rows [B, n, D] FP8 E4M3 bytes (uint8) and
+    lengths [B] int32 (local rows per sequence) or None (n for every sequence)."""
+
+    def __init__(self, rows: torch.Tensor, window: int, lengths: Optional[torch.Tensor] = None):
+        self.rows, self.lengths, self.window = rows, lengths, window
+        self._struct = csa_swa(_ptr(rows), _ptr(lengths), rows.shape[1], window)
+
+    @property
+    def ref(self):
+        return ctypes.byref(self._struct)
+
+
+def attend_swa_workspace_size(cache: Cache, P: int, H: int, K: int, swa: Optional[Swa]) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().csa_attend_swa_workspace_size(cache.ref, P, H, K, swa.ref if swa is not None else None,
+                                               ctypes.byref(n)), "csa_attend_swa_workspace_size")
+    return n.value
+
+
+def csa_sparse_attend_swa(cache: Cache, q: torch.Tensor, idx: torch.Tensor, scale: float, swa: Optional[Swa],
+                          workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Joint softmax over the selected rows and the local window -> (out [B, P, H, D], lse [B, P, H])."""
+    B, P, H, D = q.shape
+    K = idx.shape[-1]
+    if workspace is None:
+        workspace = torch.empty(max(attend_swa_workspace_size(cache, P, H, K, swa), 16), dtype=torch.uint8,
+                                device=cache.device)
+    if out is None:
+        out = torch.empty((B, P, H, D), dtype=torch.float32, device=cache.device)
+    if lse is None:
+        lse = torch.empty((B, P, H), dtype=torch.float32, device=cache.device)
+    _check(lib().csa_sparse_attend_swa(cache.ref, P, H, _ptr(q), scale, _ptr(idx), K,
+                                       swa.ref if swa is not None else None, _ptr(out), _ptr(lse),
+                                       _ptr(workspace), workspace.numel(), _stream(stream)), "csa_sparse_attend_swa")
+    return out, lse
+
+
 class LayerArgs:
     """Owns the tensors of one csa_layer_step call and its csa_layer_args struct."""
 
     def __init__(self, cache: Cache, mode: int, q, K: int, scale: float, iq=None, w=None, idx=None,
-                 rows_new=None, ikeys_new=None, pool_in=None, pool_blocks: int = 0, make_pool: bool = False):
+                 rows_new=None, ikeys_new=None, pool_in=None, pool_blocks: int = 0, make_pool: bool = False,
+                 swa: Optional[Swa] = None):
         B, P, H, D = q.shape
         dev = cache.device
         self.tensors = dict(q=q, iq=iq, w=w, rows_new=rows_new, ikeys_new=ikeys_new, pool_in=pool_in)
@@ -232,7 +280,9 @@ class LayerArgs:
         n_new = rows_new.shape[1] if rows_new is not None else 0
         self.struct = csa_layer_args(mode, P, H, HI, K, scale, _ptr(q), _ptr(iq), _ptr(w), _ptr(rows_new),
                                      _ptr(ikeys_new), n_new, pool_blocks, _ptr(pool_in), _ptr(self.pool_out),
-                                     _ptr(self.idx), _ptr(self.out), _ptr(self.lse), None, 0)
+                                     _ptr(self.idx), _ptr(self.out), _ptr(self.lse), None, 0,
+                                     ctypes.addressof(swa._struct) if swa is not None else None)
+        self.swa = swa
         n = ctypes.c_size_t(0)
         _check(lib().csa_layer_workspace_size(cache.ref, ctypes.byref(self.struct), ctypes.byref(n)),
                "csa_layer_workspace_size")

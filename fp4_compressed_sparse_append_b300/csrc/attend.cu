@@ -61,6 +61,11 @@ struct AttArgs {
     const int32_t *idx;
     int nsplit, tiles_per_split, tiles_total;
     int cluster;      // 1: the nsplit CTAs of a query form a cluster and merge in shared memory
+    // Local branch: split swa_split (the last) attends to the window of the
+    // FP8 local rows [batch][swa_n][D] instead of selected FP4 rows; -1: none.
+    const uint8_t *swa;
+    const int32_t *swa_len;  // local rows per sequence, or null: swa_n each
+    int swa_n, swa_window, swa_split;
     float *part_o;    // [units][nsplit][H][D]   (nsplit > 1)
     float2 *part_ml;  // [units][nsplit][H] (m in log2 units, l)
     float *out;       // [units][H][D]           (nsplit == 1)
@@ -92,6 +97,15 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t byte, uint32_t scale_h
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(scale_h2));
     return r;
+}
+
+// Two E4M3 bytes (low byte = first value) -> two fp16 values, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t pair)
+{
+    uint32_t v;
+    const uint16_t p16 = static_cast<uint16_t>(pair);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(v) : "h"(p16));
+    return v;
 }
 
 // E4M3 byte -> fp16 value replicated in both halves.
@@ -146,9 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     const int unit = blockIdx.y, split = blockIdx.x;
     const int b = unit / a.P;
     int len = 0;
-    const int t_first = split * a.tiles_per_split;
-    const int t_last = min(a.tiles_total, t_first + a.tiles_per_split);
-    const int n_tiles = max(0, t_last - t_first);
+    const bool win = split == a.swa_split;
     const int32_t *irow = a.idx + static_cast<int64_t>(unit) * a.K;
     const int mma_warp = kSoftWarps + kGatherWarps;
 
@@ -190,6 +202,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     pdl_wait();
     pdl_trigger();
     len = a.c.lengths[b];
+    // The window split's rows: [w_lo, w_hi) of the sequence's local rows, the
+    // window of tokens that ends at this position's own row (L - P + p for a
+    // sequence of L local rows).  A length outside [P, swa_n] is a caller
+    // error: flagged, and the window left empty.
+    int w_lo = 0, w_hi = 0;
+    if (win) {
+        const int L = a.swa_len ? a.swa_len[b] : a.swa_n;
+        if (L < a.P || L > a.swa_n) {
+            if (tid == 0) raise_status(a.status, CSA_DEV_BAD_INDEX);
+        } else {
+            w_hi = L - a.P + unit % a.P + 1;
+            w_lo = max(0, w_hi - a.swa_window);
+        }
+    }
+    const int t_first = win ? 0 : split * a.tiles_per_split;
+    const int t_last = win ? (w_hi - w_lo + kRows - 1) / kRows : min(a.tiles_total, t_first + a.tiles_per_split);
+    const int n_tiles = max(0, t_last - t_first);
 
     // Gather-warp state: the rows of tile i+1 are loaded while tile i is used;
     // thread (row gr, part gp) holds D/kParts channels of one FP4 row: nc
@@ -199,9 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     const int gr = gt & (kRows - 1), gp = gt >> 6;
     const int nc = D / (32 * kParts);
     int32_t nrow = -1;
-    uint4 ncw[kMaxPieces];
-    uint32_t nsw[kMaxPieces];  // two scale bytes per code piece
+    uint4 ncw[2 * kMaxPieces];  // FP4: nc pieces; FP8 window rows: 2 nc pieces (16 channels each)
+    uint32_t nsw[kMaxPieces];   // two scale bytes per FP4 code piece
     auto prefetch = [&](int tile) {
+        if (win) {
+            const int row = w_lo + tile * kRows + gr;
+            nrow = row < w_hi ? row : -1;
+            const uint4 *wp = reinterpret_cast<const uint4 *>(
+                                  a.swa + (static_cast<int64_t>(b) * a.swa_n + (nrow >= 0 ? row : 0)) * D) +
+                              gp * 2 * nc;
+#pragma unroll
+            for (int i = 0; i < 2 * kMaxPieces; ++i) ncw[i] = (nrow >= 0 && i < 2 * nc) ? wp[i] : make_uint4(0, 0, 0, 0);
+            return;
+        }
         const int j = tile * kRows + gr;
         int32_t row = j < a.K ? irow[j] : -1;
         if (row >= len) {
@@ -332,6 +371,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             uint8_t *vb = v_s + (i & 1) * kRows * D * 2;
             const unsigned vbits = __ballot_sync(0xFFFFFFFFu, nrow >= 0);
             if (gp == 0 && lane == 0) sm.valid[i & 1][gr >> 5] = vbits;
+            if (win) {
+                // FP8 E4M3 window rows: exact in fp16, two channels per conversion.
+#pragma unroll
+                for (int c = 0; c < 2 * kMaxPieces; ++c) {
+                    if (c >= 2 * nc) break;
+                    const uint32_t words[4] = {ncw[c].x, ncw[c].y, ncw[c].z, ncw[c].w};
+                    const int ch0 = gp * (D / kParts) + c * 16;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 o;
+                        o.x = e4m3x2_to_h2(words[2 * h] & 0xFFFF);
+                        o.y = e4m3x2_to_h2(words[2 * h] >> 16);
+                        o.z = e4m3x2_to_h2(words[2 * h + 1] & 0xFFFF);
+                        o.w = e4m3x2_to_h2(words[2 * h + 1] >> 16);
+                        *reinterpret_cast<uint4 *>(vb + sw128_off(gr, ch0 + h * 8, kRows)) = o;
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(&sm.vfull[i & 1]);
+                if (i + 1 < n_tiles) prefetch(t_first + i + 1);
+                continue;
+            }
 #pragma unroll
             for (int c16 = 0; c16 < kMaxPieces; ++c16) {
                 if (c16 >= nc) break;
@@ -626,24 +687,37 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
 
 struct Plan {
     int nsplit, tiles_per_split, tiles_total, cluster;
+    int swa_split;  // index of the local-window split, or -1
 };
 
 // Splits of one query's selection: at most one wave of CTAs.  Up to
 // kMaxClusterSplit splits form a cluster and merge on chip; more (only for
 // very few queries) merge through global memory, which measures faster than a
-// cluster of 16 for them.
-Plan plan(const CacheView &c, int P, int K)
+// cluster of 16 for them.  With a local window, one more split per query
+// attends to the window and is merged like the others.
+Plan plan(const CacheView &c, int P, int K, const SwaView *swa)
 {
     const int units = c.B * P;
+    const int extra = swa ? 1 : 0;
     const int tiles = (K + kRows - 1) / kRows;
-    int want = 148 / units;  // splits x queries within one wave of CTAs (one per SM)
+    int want = 148 / units - extra;  // splits x queries within one wave of CTAs (one per SM)
     if (want > tiles) want = tiles;
-    if (want > kMaxSplit) want = kMaxSplit;
+    if (want > kMaxSplit - extra) want = kMaxSplit - extra;
     if (want < 1) want = 1;
     Plan p;
+    if (tiles == 0) {  // nothing selected: one split
+        p.tiles_total = 0;
+        p.tiles_per_split = 1;
+        p.nsplit = 1 + extra;
+        p.swa_split = swa ? 1 : -1;
+        p.cluster = p.nsplit > 1;
+        return p;
+    }
     p.tiles_total = tiles;
     p.tiles_per_split = (tiles + want - 1) / want;
-    p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int main_splits = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    p.nsplit = main_splits + extra;
+    p.swa_split = swa ? main_splits : -1;
     p.cluster = p.nsplit > 1 && p.nsplit <= kMaxClusterSplit;
     return p;
 }
@@ -656,9 +730,9 @@ size_t smem_bytes(int D, int NH)
 
 }  // namespace
 
-size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K)
+size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K, const SwaView *swa)
 {
-    const Plan p = plan(c, P, K);
+    const Plan p = plan(c, P, K, swa);
     if (p.nsplit == 1 || p.cluster) return 0;
     const size_t units = static_cast<size_t>(c.B) * P;
     size_t o = units * p.nsplit * H * c.D * sizeof(float);
@@ -667,17 +741,19 @@ size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K)
 }
 
 cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, float scale, const int32_t *idx,
-                          int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st)
+                          int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st,
+                          const SwaView *swa)
 {
     const int units = c.B * P;
     if (units == 0) return cudaSuccess;
     if (H > kMaxHeads || c.D % 128 || c.D > 512) return cudaErrorInvalidValue;
+    if (swa && (!swa->rows || swa->n < P || swa->window < 1)) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(c.D, (H + 15) / 16 * 16);
-    const Plan p = plan(c, P, K);
+    const Plan p = plan(c, P, K, swa);
     cudaError_t e =
         cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    if (ws_bytes < attend_workspace_bytes(c, P, H, K)) return cudaErrorInvalidValue;
+    if (ws_bytes < attend_workspace_bytes(c, P, H, K, swa)) return cudaErrorInvalidValue;
     AttArgs a{};
     a.c = c;
     a.P = P;
@@ -691,6 +767,11 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     a.tiles_per_split = p.tiles_per_split;
     a.tiles_total = p.tiles_total;
     a.cluster = p.cluster;
+    a.swa = swa ? swa->rows : nullptr;
+    a.swa_len = swa ? swa->lengths : nullptr;
+    a.swa_n = swa ? swa->n : 0;
+    a.swa_window = swa ? swa->window : 0;
+    a.swa_split = p.swa_split;
     size_t o_bytes = static_cast<size_t>(units) * p.nsplit * H * c.D * sizeof(float);
     o_bytes = (o_bytes + 255) / 256 * 256;
     a.part_o = static_cast<float *>(ws);

@@ -210,6 +210,54 @@ csa_status csa_sparse_attend(const csa_cache *cache, int32_t P, int32_t H, const
     return from_cuda(csa::launch_attend(v, P, H, q, scale, idx, K, out, lse, workspace, workspace_bytes, st, stream));
 }
 
+// The local window descriptor: rows 16-byte aligned, n >= P, 1 <= window <= 1024.
+static csa_status check_swa(const csa_swa *swa, int32_t P)
+{
+    if (!swa) return CSA_OK;
+    if (!swa->rows || !aligned16(swa->rows) || swa->n < P || swa->window < 1 || swa->window > 1024)
+        return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
+static csa::SwaView swa_view(const csa_swa *swa)
+{
+    return csa::SwaView{swa->rows, swa->lengths, swa->n, swa->window};
+}
+
+csa_status csa_attend_swa_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K, const csa_swa *swa,
+                                         size_t *bytes)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (!bytes || P < 1 || H < 1 || K < 1) return CSA_ERR_INVALID_ARG;
+    if (H > 64) return CSA_ERR_UNSUPPORTED;
+    if ((s = check_swa(swa, P)) != CSA_OK) return s;
+    const csa::SwaView sv = swa ? swa_view(swa) : csa::SwaView{};
+    *bytes = csa::attend_workspace_bytes(view(cache), P, H, K, swa ? &sv : nullptr);
+    return CSA_OK;
+}
+
+csa_status csa_sparse_attend_swa(const csa_cache *cache, int32_t P, int32_t H, const uint16_t *q, float scale,
+                                 const int32_t *idx, int32_t K, const csa_swa *swa, float *out, float *lse,
+                                 void *workspace, size_t workspace_bytes, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (P < 1 || H < 1 || K < 1 || !q || !idx || !out) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse))) return CSA_ERR_INVALID_ARG;
+    if (H > 64) return CSA_ERR_UNSUPPORTED;
+    if ((s = check_swa(swa, P)) != CSA_OK) return s;
+    const csa::CacheView v = view(cache);
+    const csa::SwaView sv = swa ? swa_view(swa) : csa::SwaView{};
+    const csa::SwaView *svp = swa ? &sv : nullptr;
+    const size_t need = csa::attend_workspace_bytes(v, P, H, K, svp);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CSA_ERR_WORKSPACE;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(
+        csa::launch_attend(v, P, H, q, scale, idx, K, out, lse, workspace, workspace_bytes, st, stream, svp));
+}
+
 static size_t layer_scores_ld(const csa_cache *cache, const csa_layer_args *a)
 {
     if (a->mode == CSA_REINDEX && a->pool_in) return round_up(static_cast<size_t>(a->pool_blocks) * CSA_POOL_BLOCK, 4);
@@ -232,6 +280,7 @@ static csa_status check_layer(const csa_cache *cache, const csa_layer_args *a)
     if ((a->pool_in || a->pool_out) && (a->pool_blocks < 1 || a->pool_blocks > 16384)) return CSA_ERR_INVALID_ARG;
     if (a->pool_in && a->mode != CSA_REINDEX) return CSA_ERR_INVALID_ARG;
     if (a->pool_out && a->mode != CSA_FULL) return CSA_ERR_INVALID_ARG;
+    if ((s = check_swa(a->swa, a->P)) != CSA_OK) return s;
     if (a->mode != CSA_REUSE) {
         const int has_pool = a->mode == CSA_REINDEX && a->pool_in != nullptr;
         const int has_pool_out = a->mode == CSA_FULL && a->pool_out != nullptr;
@@ -260,7 +309,8 @@ csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args
         total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_scores_ld(cache, a) * sizeof(float), 256);
         total += round_up(layer_select_ws(cache, a), 256);
     }
-    total += round_up(csa::attend_workspace_bytes(v, a->P, a->H, a->K), 256);
+    const csa::SwaView sv = a->swa ? swa_view(a->swa) : csa::SwaView{};
+    total += round_up(csa::attend_workspace_bytes(v, a->P, a->H, a->K, a->swa ? &sv : nullptr), 256);
     *bytes = total;
     return CSA_OK;
 }
@@ -298,8 +348,10 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
                                    sel_bytes, stream);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
     }
-    const size_t att = csa::attend_workspace_bytes(v, a->P, a->H, a->K);
-    e = csa::launch_attend(v, a->P, a->H, a->q, a->scale, a->idx, a->K, a->out, a->lse, ws, att, st, stream);
+    const csa::SwaView sv = a->swa ? swa_view(a->swa) : csa::SwaView{};
+    const csa::SwaView *svp = a->swa ? &sv : nullptr;
+    const size_t att = csa::attend_workspace_bytes(v, a->P, a->H, a->K, svp);
+    e = csa::launch_attend(v, a->P, a->H, a->q, a->scale, a->idx, a->K, a->out, a->lse, ws, att, st, stream, svp);
     return from_cuda(e);
 }
 

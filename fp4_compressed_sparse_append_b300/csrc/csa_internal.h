@@ -32,10 +32,16 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
                           int pool_blocks, int block, int K, int32_t *out, void *ws, size_t ws_bytes,
                           cudaStream_t st);
 
-// a5/a6
-size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K);
+// a5/a6, and the local window of the joint softmax (rows [B][n][D] FP8 E4M3).
+struct SwaView {
+    const uint8_t *rows;
+    const int32_t *lengths;  // [B] local rows per sequence, or null: n each
+    int n, window;
+};
+size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K, const SwaView *swa = nullptr);
 cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, float scale, const int32_t *idx,
-                          int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st);
+                          int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st,
+                          const SwaView *swa = nullptr);
 
 // Host-side count of kernel launches issued by the library (csa_kernel_launches).
 void count_launch(int n = 1);

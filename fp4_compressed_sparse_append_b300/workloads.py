@@ -25,6 +25,7 @@ full_64k           8   65536     64  512  64  128  2048  1  Full (1% outlier cha
 chain_128k         32  131072    64  512  64  128  2048  1  Full, 3x Reindex, 4x Reuse
 hier_1m            1   1048576   64  512  64  128  2048  1  Full+pool, 7x Reindex(pool)
 verify_append_32k  64  32768     64  512  64  128  2048  6  append 6 rows, then Full
+full_64k_swa       8   65536     64  512  64  128  2048  1  Full + 128-row local window
 =================  ==  ========  ==  ===  ==  ===  ====  =  =========================
 """
 from __future__ import annotations
@@ -58,6 +59,7 @@ class Workload:
     outlier_channels: int = 0   # latent channels scaled x8 (same channels in every row)
     planted: int = 0        # length of a planted high-similarity block (0 = none)
     n_append: int = 0       # rows appended (quantised) at the start of the step
+    window: int = 0         # >0: every query also attends to this many local FP8 rows
 
     @property
     def capacity(self) -> int:
@@ -85,10 +87,12 @@ WORKLOADS: Dict[str, Workload] = {
                         layers=(FULL,) + (REINDEX,) * 7, pool_blocks=2048, planted=512),
     "verify_append_32k": Workload("verify_append_32k", B=64, L=32768, H=64, D=512, HI=64,
                                   DI=128, K=2048, P=6, n_append=6),
+    "full_64k_swa": Workload("full_64k_swa", B=8, L=65536, H=64, D=512, HI=64, DI=128, K=2048,
+                             outlier_channels=5, window=128),
 }
 
 # Tensor tags for the per-tensor streams.
-_T_LATENT, _T_IKEY, _T_Q, _T_IQ, _T_W, _T_NEWROW, _T_NEWIKEY, _T_OUTLIER, _T_PLANT = range(9)
+_T_LATENT, _T_IKEY, _T_Q, _T_IQ, _T_W, _T_NEWROW, _T_NEWIKEY, _T_OUTLIER, _T_PLANT, _T_LOCAL = range(10)
 
 
 def _mix(*vals: int) -> int:
@@ -209,6 +213,18 @@ def append_rows(wl: Workload, seed: int, device="cpu") -> Dict[str, torch.Tensor
     if out_ch.numel():
         lat[..., out_ch] *= 8.0
     return {"rows": to_bf16_bits(lat), "ikeys": to_e4m3_bytes(ik)}
+
+
+def local_rows(wl: Workload, seed: int, device="cpu", n: Optional[int] = None) -> torch.Tensor:
+    """The local window's rows of every sequence: E4M3 bytes [B, n, D] (default
+    n = window + P - 1, enough for the full window of each of the P positions),
+    latents drawn like the cached rows (N(0,1), the same outlier channels x8)."""
+    n = wl.window + wl.P - 1 if n is None else n
+    lat = _randn((wl.B, n, wl.D), device, seed, _T_LOCAL)
+    out_ch = outlier_channels(wl, seed).to(device)
+    if out_ch.numel():
+        lat[..., out_ch] *= 8.0
+    return to_e4m3_bytes(lat)
 
 
 def random_bf16_bits(shape, seed: int, tag: int = 0, device="cpu", std: float = 1.0) -> torch.Tensor:

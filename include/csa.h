@@ -186,6 +186,45 @@ CSA_API csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, 
                                      size_t *bytes);
 
 /*
+ * The local branch and the joint softmax.  ("G2C Brief", "Two attention
+ * paths in every layer": besides the selected global entries every query sees
+ * a sliding window of the 128 most recent tokens; "FP4 cache entries, and why
+ * they're safe": that local cache stays in FP8; "Pushing the Limits", "The
+ * Paper": the selected entries are joined to the window's KV for one attention.)
+ * Plain reading: one softmax over the union of the selected FP4 rows and the
+ * window rows, with K == V for both.
+ *   rows    : [batch][n][d_latent] FP8 E4M3 bytes (device, 16-byte aligned),
+ *             the sequence's local rows in token order; position p of P is
+ *             the row L - P + p of a sequence with L local rows.
+ *   lengths : [batch] int32 device array of L per sequence, or NULL (L = n for
+ *             every sequence).  L outside [P, n] sets CSA_DEV_BAD_INDEX in the
+ *             status word and that sequence's windows are left empty.
+ *   n       : row capacity per sequence (the stride of rows), n >= P.
+ *   window  : rows attended per query, 1..1024: local rows
+ *             [max(0, own - window + 1), own] of a query whose own row is own.
+ * The caller owns the window array and fills it (e.g. the last `window`
+ * tokens' latent rows converted to E4M3); the library only reads it.
+ */
+typedef struct csa_swa {
+    const uint8_t *rows;
+    const int32_t *lengths;
+    int32_t n;
+    int32_t window;
+} csa_swa;
+
+/*
+ * csa_sparse_attend with the local window: out and lse are those of the joint
+ * softmax over the selected rows of idx and the window rows of swa (NULL swa:
+ * exactly csa_sparse_attend).  workspace: csa_attend_swa_workspace_size bytes.
+ */
+CSA_API csa_status csa_sparse_attend_swa(const csa_cache *cache, int32_t P, int32_t H, const uint16_t *q,
+                                         float scale, const int32_t *idx, int32_t K, const csa_swa *swa, float *out,
+                                         float *lse, void *workspace, size_t workspace_bytes, csa_stream_t stream);
+
+CSA_API csa_status csa_attend_swa_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K,
+                                                 const csa_swa *swa, size_t *bytes);
+
+/*
  * csa_sparse_attend without a workspace argument and without any allocation.
  * The pages describe no counterpart of this call; it exists for callers that
  * cannot allocate device memory themselves: code running under a framework
@@ -225,8 +264,9 @@ CSA_API csa_status csa_sparse_attend_noalloc(const csa_cache *cache, int32_t P, 
  *   REINDEX : scores over every visible row, or over pool_in's rows when
  *             pool_in != NULL -> idx (fresh top K) -> attention
  *   REUSE   : attention over the given idx
- * idx is written by FULL/REINDEX and read by REUSE.  All arrays are laid out
- * as in the calls above.  workspace: csa_layer_workspace_size bytes.
+ * idx is written by FULL/REINDEX and read by REUSE.  With swa set, every mode's
+ * attention is the joint softmax of csa_sparse_attend_swa.  All arrays are
+ * laid out as in the calls above.  workspace: csa_layer_workspace_size bytes.
  */
 typedef struct csa_layer_args {
     csa_mode mode;
@@ -249,6 +289,7 @@ typedef struct csa_layer_args {
     float *lse;                  /* [batch][P][H] fp32 or NULL */
     void *workspace;
     size_t workspace_bytes;
+    const csa_swa *swa;          /* local window joined to the softmax, or NULL */
 } csa_layer_args;
 
 CSA_API csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *args, csa_stream_t stream);

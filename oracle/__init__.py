@@ -314,7 +314,8 @@ def attend_swa(q_bits, codes_b, scales_b, idx, swa_b, lo: int, hi: int, scale: f
 # --------------------------------------------------------------------------
 
 def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int, scale: float,
-               prev_idx=None, pool_in=None, pool_keep: int = 0, threads: int = 1) -> Dict[str, np.ndarray]:
+               prev_idx=None, pool_in=None, pool_keep: int = 0, threads: int = 1,
+               swa=None) -> Dict[str, np.ndarray]:
     """One (sequence b, position p) through one CSA2 layer.
 
     Full    : score every visible row, keep the top K (and, with pool_keep > 0,
@@ -322,7 +323,9 @@ def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int
     Reindex : score the visible rows again with this layer's own indexer
               query, or only the pool's rows when pool_in is given; fresh top K.
     Reuse   : take prev_idx unchanged.
-    Then attend over the selected rows with this layer's own query.
+    Then attend over the selected rows with this layer's own query; with
+    swa = (rows_b [n, D] E4M3 bytes of this sequence, window), jointly with the
+    local window of this position (attend_swa).
     """
     L_p = visible_length(cache.lengths[b], P, p)
     res: Dict[str, np.ndarray] = {}
@@ -341,16 +344,23 @@ def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int
         res["scores"] = sc
         if mode == FULL and pool_keep:
             res["pool"] = build_pool(sc, pool_keep)
-    out, lse = attend(q, cache.codes[b], cache.scales[b], idx, scale)
+    if swa is None:
+        out, lse = attend(q, cache.codes[b], cache.scales[b], idx, scale)
+    else:
+        rows_b, window = swa
+        lo, hi = swa_window(rows_b.shape[0], P, p, window)
+        out, lse = attend_swa(q, cache.codes[b], cache.scales[b], idx, rows_b, lo, hi, scale)
     res.update(idx=idx, out=out, lse=lse)
     return res
 
 
 def run_layer(cache: Cache, mode: int, inputs: Dict, K: int, scale: float, P: int = 1,
               prev_idx=None, pool_in=None, pool_keep: int = 0,
-              units: Optional[Sequence] = None, threads: int = 1, score_threads: int = 1) -> Dict:
+              units: Optional[Sequence] = None, threads: int = 1, score_threads: int = 1,
+              swa=None) -> Dict:
     """One layer for every (b, p) unit (or the listed units).  inputs holds
-    q [B,P,H,D] bf16 bits, iq [B,P,HI,DI], w [B,P,HI].  Returns per-unit dicts."""
+    q [B,P,H,D] bf16 bits, iq [B,P,HI,DI], w [B,P,HI]; swa = (rows [B, n, D]
+    E4M3 bytes, window) or None.  Returns per-unit dicts."""
     q = _np(inputs["q"], np.uint16)
     iq = _np(inputs["iq"], np.uint8)
     w = _np(inputs["w"], np.float32)
@@ -361,7 +371,8 @@ def run_layer(cache: Cache, mode: int, inputs: Dict, K: int, scale: float, P: in
         b, p = u
         return u, unit_layer(cache, b, p, P, mode, q[b, p], iq[b, p], w[b, p], K, scale,
                              None if prev_idx is None else prev_idx[u],
-                             None if pool_in is None else pool_in[u], pool_keep, score_threads)
+                             None if pool_in is None else pool_in[u], pool_keep, score_threads,
+                             None if swa is None else (swa[0][b], swa[1]))
 
     if threads > 1:
         with ThreadPoolExecutor(threads) as ex:
@@ -370,17 +381,19 @@ def run_layer(cache: Cache, mode: int, inputs: Dict, K: int, scale: float, P: in
 
 
 def run_chain(cache: Cache, modes: Sequence[int], layer_inputs: Sequence[Dict], K: int, scale: float,
-              P: int = 1, pool_keep: int = 0, units=None, threads: int = 1, score_threads: int = 1):
+              P: int = 1, pool_keep: int = 0, units=None, threads: int = 1, score_threads: int = 1,
+              swa=None):
     """A chain of layers sharing one cache.  Reuse takes the nearest preceding
     Full/Reindex selection; Reindex uses the pool of the first Full layer when
-    pool_keep > 0.  Returns a list of per-layer results."""
+    pool_keep > 0; swa = (rows [B, n, D], window) joins every layer's attention
+    to the local window.  Returns a list of per-layer results."""
     results, prev, pool = [], None, None
     for li, mode in enumerate(modes):
         r = run_layer(cache, mode, layer_inputs[li], K, scale, P,
                       prev_idx=prev if mode == REUSE else None,
                       pool_in=pool if mode == REINDEX else None,
                       pool_keep=pool_keep if (mode == FULL and pool is None) else 0,
-                      units=units, threads=threads, score_threads=score_threads)
+                      units=units, threads=threads, score_threads=score_threads, swa=swa)
         if mode != REUSE:
             prev = {u: v["idx"] for u, v in r.items()}
         if mode == FULL and pool is None and pool_keep:

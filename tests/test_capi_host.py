@@ -107,3 +107,34 @@ def test_layer_args_checks(lib):
     # workspace missing -> rejected before launch
     a.mode, a.n_new = B.CSA_FULL, 0
     assert lib.csa_layer_step(c, ctypes.byref(a), None) == 5
+
+
+def test_local_window_checks(lib):
+    c = ctypes.byref(fake_cache())
+    V = ctypes.c_void_p
+    n = ctypes.c_size_t(0)
+    ok = B.csa_swa(rows=0x7000, lengths=None, n=128, window=128)
+    assert lib.csa_attend_swa_workspace_size(c, 1, 16, 8, ctypes.byref(ok), ctypes.byref(n)) == 0
+    for bad in (B.csa_swa(rows=None, lengths=None, n=128, window=128),     # no rows
+                B.csa_swa(rows=0x7008, lengths=None, n=128, window=128),   # misaligned rows
+                B.csa_swa(rows=0x7000, lengths=None, n=0, window=128),     # fewer rows than positions
+                B.csa_swa(rows=0x7000, lengths=None, n=128, window=0),     # empty window
+                B.csa_swa(rows=0x7000, lengths=None, n=2048, window=1025)):
+        assert lib.csa_attend_swa_workspace_size(c, 1, 16, 8, ctypes.byref(bad), ctypes.byref(n)) == 1
+        assert lib.csa_sparse_attend_swa(c, 1, 16, V(0x1000), 1.0, V(0x2000), 8, ctypes.byref(bad), V(0x3000),
+                                         None, V(0x4000), 1 << 20, None) == 1
+    # no window: the same sizes as csa_attend_workspace_size
+    m = ctypes.c_size_t(0)
+    assert lib.csa_attend_swa_workspace_size(c, 1, 16, 2048, None, ctypes.byref(n)) == 0
+    assert lib.csa_attend_workspace_size(c, 1, 16, 2048, ctypes.byref(m)) == 0 and m.value == n.value
+    # with a window, 2 queries still split over more CTAs than a cluster holds
+    assert lib.csa_attend_swa_workspace_size(c, 1, 16, 2048, ctypes.byref(ok), ctypes.byref(n)) == 0
+    assert n.value > 0
+    # a layer step validates its window too
+    a = B.csa_layer_args(mode=B.CSA_REUSE, P=2, H=16, K=8, scale=1.0, q=0x1000, idx=0x4000, out=0x5000)
+    bad = B.csa_swa(rows=0x7000, lengths=None, n=1, window=8)
+    a.swa = ctypes.addressof(bad)
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 1
+    good = B.csa_swa(rows=0x7000, lengths=None, n=4, window=8)
+    a.swa = ctypes.addressof(good)
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 0

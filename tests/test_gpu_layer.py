@@ -21,6 +21,7 @@ THREADS = max(1, min(32, os.cpu_count() or 1))
 
 
 def run_gpu_chain(wl, seed, cache):
+    swa = B.Swa(W.local_rows(wl, seed, device="cuda"), wl.window) if wl.window else None
     layers, prev, pool = [], None, None
     for li, mode in enumerate(wl.layers):
         inp = W.layer_inputs(wl, seed, li, device="cuda")
@@ -29,7 +30,7 @@ def run_gpu_chain(wl, seed, cache):
                          idx=prev if mode == W.REUSE else None,
                          rows_new=app["rows"] if app else None, ikeys_new=app["ikeys"] if app else None,
                          pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
-                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None))
+                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None), swa=swa)
         B.csa_layer_step(cache, la)
         if mode != W.REUSE:
             prev = la.idx
@@ -52,8 +53,9 @@ def oracle_chain(wl, seed, lat, ik, seqs):
     for li in range(len(wl.layers)):
         inp = W.layer_inputs(wl, seed, li, device="cuda")
         inputs.append({k: v[seqs].cpu().numpy() for k, v in inp.items()})
+    swa = (W.local_rows(wl, seed, device="cuda")[seqs].cpu().numpy(), wl.window) if wl.window else None
     return oracle.run_chain(cache, wl.layers, inputs, wl.K, wl.scale, P=wl.P, pool_keep=wl.pool_blocks,
-                            threads=min(THREADS, len(seqs) * wl.P), score_threads=THREADS)
+                            threads=min(THREADS, len(seqs) * wl.P), score_threads=THREADS, swa=swa)
 
 
 def compare_chain(wl, gpu_layers, ora_layers, seqs):
@@ -98,6 +100,8 @@ SMALL = [
     W.Workload("hier_small", B=1, L=40000, H=64, D=512, HI=64, DI=128, K=512,
                layers=(W.FULL, W.REINDEX, W.REINDEX, W.REUSE), pool_blocks=128, planted=64),
     W.Workload("verify_small", B=3, L=3000, H=8, D=128, HI=32, DI=64, K=700, P=6, n_append=6),
+    W.Workload("chain_swa_small", B=3, L=4000, H=32, D=512, HI=16, DI=128, K=512, P=2, outlier_channels=5,
+               layers=(W.FULL, W.REINDEX, W.REUSE), window=128),
 ]
 
 
@@ -116,7 +120,8 @@ def test_small_workloads_every_query(wl):
             assert set(range(off, off + wl.planted)) <= sel
 
 
-FULL_SIZE = [("full_64k", [0, 5]), ("chain_128k", [17]), ("hier_1m", [0]), ("verify_append_32k", [40])]
+FULL_SIZE = [("full_64k", [0, 5]), ("chain_128k", [17]), ("hier_1m", [0]), ("verify_append_32k", [40]),
+             ("full_64k_swa", [3])]
 
 
 @pytest.mark.slow
