@@ -126,7 +126,8 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float sc)
     for (int k = 0; k < 4; ++k) {
         const float lo = __uint_as_float(w4[k] << 16) * sc;
         const float hi = __uint_as_float(w4[k] & 0xFFFF0000u) * sc;
-        r4[k] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
+        const __half2 h = __floats2half2_rn(lo, hi);  // one conversion for the pair; lo in the low half
+        r4[k] = *reinterpret_cast<const uint32_t *>(&h);
     }
     return make_uint4(r4[0], r4[1], r4[2], r4[3]);
 }
@@ -200,7 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
     // Below: reads of what earlier kernels on the stream wrote (lengths, indices, cache).
     pdl_wait();
-    pdl_trigger();
     len = a.c.lengths[b];
     // The window split's rows: [w_lo, w_hi) of the sequence's local rows, the
     // window of tokens that ends at this position's own row (L - P + p for a
@@ -264,33 +264,42 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     if (!mbar_wait(&sm.qbar, 0, abort_flag)) {
         // timed out: the status bit is raised at the end; the CTA drains below
     } else if (tid < 4 * kMaxHeads) {
-        const int qh = tid >> 2, qq = tid & 3, qn = D / 32;
-        uint4 qreg[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        // Two passes over this thread's 16-byte chunks, both unrolled with
+        // independent work per chunk: the exponent scan (four max chains), then
+        // the conversion, re-reading shared memory.  Lane = 8 * quarter + head
+        // (mod 8): each 8-lane phase of a 16-byte access covers 8 heads, whose
+        // swizzled chunks fall in 8 different bank groups.
+        const int qh = warp * 8 + (lane & 7), qq = lane >> 3, qn = D / 32;
+        const uint32_t qst = smem_u32(q_stage), qs = smem_u32(q_s);
+        auto chunk = [&](int i) -> uint4 {
             // 16-byte chunk i of this quarter: dims qq*D/4 + 8i .. +8
             const int dim = qq * (D / 4) + i * 8;
             const int kb = dim >> 6, c = (dim >> 3) & 7;
-            qreg[i] = (qh < H && i < qn)
-                          ? *reinterpret_cast<const uint4 *>(q_stage + kb * kMaxHeads * 128 + qh * 128 +
-                                                             ((c ^ (qh & 7)) << 4))
-                          : make_uint4(0, 0, 0, 0);
-        }
-        uint32_t emax = 0;
+            return ld_shared_v4(qst + kb * kMaxHeads * 128 + qh * 128 + ((c ^ (qh & 7)) << 4));
+        };
+        constexpr uint32_t kExp = 0x7F807F80u;  // the exponent fields of two bf16
+        uint32_t m4[4] = {0u, 0u, 0u, 0u};
+        if (qh < H) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t w4[4] = {qreg[i].x, qreg[i].y, qreg[i].z, qreg[i].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) emax = max(emax, max((w4[k] >> 7) & 0xFFu, (w4[k] >> 23) & 0xFFu));
+            for (int i = 0; i < 16; ++i) {
+                if (i < qn) {
+                    const uint4 v = chunk(i);
+                    m4[i & 3] = __vmaxu2(m4[i & 3], __vmaxu2(__vmaxu2(v.x & kExp, v.y & kExp),
+                                                             __vmaxu2(v.z & kExp, v.w & kExp)));
+                }
+            }
         }
-        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 1));
-        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 2));
+        const uint32_t m2 = __vmaxu2(__vmaxu2(m4[0], m4[1]), __vmaxu2(m4[2], m4[3]));
+        uint32_t emax = max((m2 >> 7) & 0xFFu, m2 >> 23);
+        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 8));
+        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 16));
         const float e = emax > 0 ? 14.f - (static_cast<float>(emax) - 127.f) : 0.f;
         const float qscale = exp2f(e);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            if (i < qn) *reinterpret_cast<uint4 *>(q_s + sw128_off(qh, qq * (D / 4) + i * 8, kMaxHeads)) =
-                            bf16x8_to_f16x8(qreg[i], qscale);
+            if (i < qn)
+                st_shared_v4(qs + sw128_off(qh, qq * (D / 4) + i * 8, kMaxHeads),
+                             qh < H ? bf16x8_to_f16x8(chunk(i), qscale) : make_uint4(0, 0, 0, 0));
         if (qq == 0) sm.cfac[qh] = a.scale * kLog2e * exp2f(-e);
     }
     fence_async_smem();
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         // ------------------------------------------------------------ gather warps
         for (int i = 0; i < n_tiles; ++i) {
             if (!mbar_wait(&sm.vempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag)) break;
-            uint8_t *vb = v_s + (i & 1) * kRows * D * 2;
+            const uint32_t vb = smem_u32(v_s) + (i & 1) * kRows * D * 2;
             const unsigned vbits = __ballot_sync(0xFFFFFFFFu, nrow >= 0);
             if (gp == 0 && lane == 0) sm.valid[i & 1][gr >> 5] = vbits;
             if (win) {
@@ -385,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                         o.y = e4m3x2_to_h2(words[2 * h] >> 16);
                         o.z = e4m3x2_to_h2(words[2 * h + 1] & 0xFFFF);
                         o.w = e4m3x2_to_h2(words[2 * h + 1] >> 16);
-                        *reinterpret_cast<uint4 *>(vb + sw128_off(gr, ch0 + h * 8, kRows)) = o;
+                        st_shared_v4(vb + sw128_off(gr, ch0 + h * 8, kRows), o);
                     }
                 }
                 fence_async_smem();
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     o.y = dequant_pair((wd >> 8) & 0xFF, sv);
                     o.z = dequant_pair((wd >> 16) & 0xFF, sv);
                     o.w = dequant_pair(wd >> 24, sv);
-                    *reinterpret_cast<uint4 *>(vb + sw128_off(gr, ch0 + h8 * 8, kRows)) = o;
+                    st_shared_v4(vb + sw128_off(gr, ch0 + h8 * 8, kRows), o);
                 }
             }
             fence_async_smem();
@@ -493,27 +502,31 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             l_run *= f;
             float lsum = 0.f;
             if (h < NH) {
-                uint8_t *ph_s = p_s + (i & 1) * 2 * p_bytes, *pl_s = ph_s + p_bytes;
+                const uint32_t ph_s = smem_u32(p_s) + (i & 1) * 2 * p_bytes, pl_s = ph_s + p_bytes;
 #pragma unroll
                 for (int k8 = 0; k8 < 4; ++k8) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int k2 = 0; k2 < 4; ++k2) {
-                        __half ph[2], pl[2];
+                        // p = hi + lo: hi keeps p's leading 11 significant bits
+                        // (exact in fp16 for p >= 2^-14), lo the exact fp32
+                        // remainder rounded to fp16; one conversion per pair each.
+                        float hf[2], lf[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const float zz = __uint_as_float(z[k8 * 8 + k2 * 2 + e]);
                             const float pv = (active && zz > -INFINITY) ? fast_exp2(zz - m_run) : 0.f;
                             lsum += pv;
-                            ph[e] = __float2half_rn(pv);
-                            pl[e] = __float2half_rn(pv - __half2float(ph[e]));
+                            hf[e] = __uint_as_float(__float_as_uint(pv) & 0xFFFFE000u);
+                            lf[e] = pv - hf[e];
                         }
-                        hw[k2] = pack_half2(ph[0], ph[1]);
-                        lw[k2] = pack_half2(pl[0], pl[1]);
+                        const __half2 h2 = __floats2half2_rn(hf[0], hf[1]), l2 = __floats2half2_rn(lf[0], lf[1]);
+                        hw[k2] = *reinterpret_cast<const uint32_t *>(&h2);
+                        lw[k2] = *reinterpret_cast<const uint32_t *>(&l2);
                     }
                     const uint32_t off = sw128_off(h, ch * 32 + k8 * 8, NH);
-                    *reinterpret_cast<uint4 *>(ph_s + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4 *>(pl_s + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    st_shared_v4(ph_s + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                    st_shared_v4(pl_s + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
                 }
             }
             lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
@@ -522,60 +535,59 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             tc_fence_before();
             mbar_arrive(&sm.pfull[i & 1]);
         }
-        // ---- epilogue: the last O^T update done -> result or partial
+        // ---- the last O^T update done: final (m, l) per head
         if (ok && n_tiles > 0) ok = mbar_wait(&sm.pempty[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag);
         if (lane < 16) {
             sm.l_fin[h] = l_run;
             sm.m_fin[h] = m_run;
         }
-        mbar_arrive(&sm.xbar);
-        if (ok) ok = mbar_wait(&sm.xbar, n_tiles & 1, abort_flag);
-        if (ok && a.cluster) {
-            // This split's unnormalised O -> shared memory [H][D] fp32 over the
-            // V buffers (free: the last O^T update has completed).
-            tc_fence_after();
-            float *obuf = reinterpret_cast<float *>(v_s);
-            for (int mt = 0; mt < D / 128; ++mt) {
-                const int d = mt * 128 + warp * 32 + lane;
-                uint32_t r[kMaxHeads];
-#pragma unroll
-                for (int c0 = 0; c0 < kMaxHeads; c0 += 16)
-                    if (c0 < NH) tmem_ld16(t_o + mt * NH + lane_off + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
-                tmem_ld_wait();
-#pragma unroll
-                for (int hh = 0; hh < kMaxHeads; ++hh) {
-                    if (hh >= H) break;
-                    obuf[hh * D + d] = n_tiles > 0 ? __uint_as_float(r[hh]) : 0.f;
-                }
+        if (lane < 16 && active && !a.cluster) {
+            if (a.nsplit == 1) {
+                if (a.lse)
+                    a.lse[static_cast<int64_t>(unit) * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            } else {
+                a.part_ml[(static_cast<int64_t>(unit) * a.nsplit + split) * H + h] = make_float2(m_run, l_run);
             }
-        } else if (ok) {
-            tc_fence_after();
-            const bool final_out = a.nsplit == 1;
+        }
+    }
+
+    // ---- epilogue over all softmax and gather warps: O^T from tensor memory
+    // (warp w reads lane quadrant w % 4, i.e. 32 dims of each 128-dim block)
+    // to the split partial in global memory, to the final output (one split),
+    // or to shared memory [H][D] over the V buffers for the cluster merge.
+    // Work items are (dim block, 16 heads); the three warps of a quadrant
+    // take every third item.
+    if (warp < mma_warp) {
+        named_barrier_sync(1, 32 * mma_warp);  // the softmax warps have seen the last O^T update
+        tc_fence_after();
+        if (!*abort_flag) {
+            const int q4 = warp & 3, grp = warp >> 2, ngrp = mma_warp / 4;
+            const uint32_t loff = static_cast<uint32_t>(q4 * 32) << 16;
+            const int nc16 = NH / 16, items = (D / 128) * nc16;
+            const bool final_out = a.nsplit == 1 && !a.cluster;
+            float *obuf = reinterpret_cast<float *>(v_s);
             float *obase = final_out ? a.out + static_cast<int64_t>(unit) * H * D
                                      : a.part_o + (static_cast<int64_t>(unit) * a.nsplit + split) * H * D;
-            for (int mt = 0; mt < D / 128; ++mt) {
-                const int d = mt * 128 + warp * 32 + lane;
-                uint32_t r[kMaxHeads];
-#pragma unroll
-                for (int c0 = 0; c0 < kMaxHeads; c0 += 16)
-                    if (c0 < NH) tmem_ld16(t_o + mt * NH + lane_off + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+            for (int it = grp; it < items; it += ngrp) {
+                const int mt = it / nc16, c0 = (it - mt * nc16) * 16;
+                const int d = mt * 128 + q4 * 32 + lane;
+                uint32_t r[16];
+                tmem_ld16(t_o + mt * NH + loff + c0, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int hh = 0; hh < kMaxHeads; ++hh) {
+                for (int k = 0; k < 16; ++k) {
+                    const int hh = c0 + k;
                     if (hh >= H) break;
-                    float v = n_tiles > 0 ? __uint_as_float(r[hh]) : 0.f;
-                    const float lh = sm.l_fin[hh];
-                    if (final_out) v = lh > 0.f ? v * __frcp_rn(lh) : 0.f;
-                    obase[static_cast<int64_t>(hh) * D + d] = v;
-                }
-            }
-            if (lane < 16 && active) {
-                if (final_out) {
-                    if (a.lse)
-                        a.lse[static_cast<int64_t>(unit) * H + h] =
-                            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-                } else {
-                    a.part_ml[(static_cast<int64_t>(unit) * a.nsplit + split) * H + h] = make_float2(m_run, l_run);
+                    float v = n_tiles > 0 ? __uint_as_float(r[k]) : 0.f;
+                    if (a.cluster) {
+                        obuf[hh * D + d] = v;
+                    } else {
+                        if (final_out) {
+                            const float lh = sm.l_fin[hh];
+                            v = lh > 0.f ? v * __frcp_rn(lh) : 0.f;
+                        }
+                        obase[static_cast<int64_t>(hh) * D + d] = v;
+                    }
                 }
             }
         }
@@ -636,6 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         }
         cluster.sync();  // no CTA leaves while another still reads its shared memory
     }
+    // The next kernel (the split merge) is released only now: its CTAs are
+    // small enough to share this CTA's SM, and waiting there they slow it.
+    pdl_trigger();
     if (*abort_flag && tid == 0) raise_status(a.status, CSA_DEV_TIMEOUT);
     if (warp == mma_warp) {
         tc_fence_after();
@@ -643,9 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
 }
 
-// Combines the split partials: block = (128 dims, head, query); each thread
-// loads its dim from every split at once.  out = sum_s 2^(m_s - M) O_s / L,
-// L = sum_s 2^(m_s - M) l_s, lse = ln 2 * (M + log2 L).
+// Combines the split partials: block = (512 dims, head, query); each thread
+// loads its 4 dims (one 16-byte load) from every split at once.
+// out = sum_s 2^(m_s - M) O_s / L, L = sum_s 2^(m_s - M) l_s,
+// lse = ln 2 * (M + log2 L).
 constexpr int kMaxSplit = 32;  // one warp holds every split's (m, l) in the merge
 
 template <int MS>
@@ -656,11 +672,13 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
     pdl_wait();
     __shared__ float wsh[MS];
     __shared__ float inv_l;
-    const int d = blockIdx.x * 128 + threadIdx.x, h = blockIdx.y, unit = blockIdx.z;
-    float pv[MS];
+    const int d = (blockIdx.x * 128 + threadIdx.x) * 4, h = blockIdx.y, unit = blockIdx.z;
+    float4 pv[MS];
 #pragma unroll
     for (int s = 0; s < MS; ++s)
-        pv[s] = (s < nsplit && d < D) ? part_o[((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d] : 0.f;
+        pv[s] = (s < nsplit && d < D) ? *reinterpret_cast<const float4 *>(
+                                            part_o + ((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
     if (threadIdx.x < 32) {
         const int s = threadIdx.x;
         float2 ml = make_float2(-INFINITY, 0.f);
@@ -679,10 +697,19 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsp
         }
     }
     __syncthreads();
-    float acc = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int s = 0; s < MS; ++s) acc = fmaf(wsh[s], pv[s], acc);
-    if (d < D) out[(static_cast<int64_t>(unit) * H + h) * D + d] = acc * inv_l;
+    for (int s = 0; s < MS; ++s) {
+        const float w = wsh[s];
+        acc.x = fmaf(w, pv[s].x, acc.x);
+        acc.y = fmaf(w, pv[s].y, acc.y);
+        acc.z = fmaf(w, pv[s].z, acc.z);
+        acc.w = fmaf(w, pv[s].w, acc.w);
+    }
+    const float il = inv_l;
+    if (d < D)
+        *reinterpret_cast<float4 *>(out + (static_cast<int64_t>(unit) * H + h) * D + d) =
+            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
 }
 
 struct Plan {
@@ -792,7 +819,7 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
     // The merge loads every split's value at once: 16 or 32 registers.
     auto merge = p.nsplit <= 16 ? attend_merge_kernel<16> : attend_merge_kernel<kMaxSplit>;
-    return launch_kernel(merge, dim3((c.D + 127) / 128, H, units), dim3(128), 0, st, 0, c.D, H, p.nsplit,
+    return launch_kernel(merge, dim3((c.D + 511) / 512, H, units), dim3(128), 0, st, 0, c.D, H, p.nsplit,
                          static_cast<const float *>(a.part_o), static_cast<const float2 *>(a.part_ml), out, lse);
 }
 
