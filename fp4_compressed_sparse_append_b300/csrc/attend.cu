@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
         const int C = a.nsplit, rank = static_cast<int>(cluster.block_rank());
-        const int slice = (D / C + 3) & ~3;
+        const int slice = ((D + C - 1) / C + 3) & ~3;  // C slices of a multiple of 4 dims cover D
         const int d0 = min(D, rank * slice), d1 = min(D, d0 + slice);
         float *wq = reinterpret_cast<float *>(p_s);  // [split][head] normalised weights (P buffers are free)
         if (tid < H) {

@@ -15,12 +15,15 @@ def host_cache(cache):
     return cache.codes.cpu().numpy(), cache.scales.cpu().numpy()
 
 
-# Split plans covered: a cluster of 4 splits (1 query, 4 tiles), 16 splits
-# merged through global memory (2 queries), a cluster of 2 (6 queries), one
-# split, a cluster of 7 (odd size: ragged dim slices; 20 queries), and 11
-# splits through global memory with 48 heads and D = 384 (12 queries).
+# Split plans covered: a cluster of 4 splits (1 query, 4 tiles), 32 splits
+# merged by the merge kernel (2 queries), a cluster of 2 (6 queries), one
+# split, a cluster of 7 (odd size: ragged dim slices; 20 queries), 11 splits
+# merged by the merge kernel with 48 heads and D = 384 (12 queries), 16 splits
+# (8 queries, the 64K decode shape), and clusters of 5 at D = 384 and of 7 at
+# D = 256, whose last dim slice is shorter than the others.
 @pytest.mark.parametrize("H,D,K,Bn,P", [(16, 128, 256, 1, 1), (64, 512, 2048, 2, 1), (7, 256, 100, 2, 3),
-                                        (64, 512, 1, 1, 1), (64, 512, 2048, 20, 1), (48, 384, 700, 12, 1)])
+                                        (64, 512, 1, 1, 1), (64, 512, 2048, 20, 1), (48, 384, 700, 12, 1),
+                                        (64, 512, 2048, 8, 1), (8, 384, 320, 29, 1), (8, 256, 448, 21, 1)])
 def test_attention_matches_oracle(H, D, K, Bn, P):
     need_gpu()
     wl = W.Workload("t", B=Bn, L=5000, H=H, D=D, HI=4, DI=64, K=K, P=P, outlier_channels=5)

@@ -41,8 +41,8 @@ def check_units(out, lse, q, lat, idx, local, lens, wl, units):
 # cluster of 5 (1 query), 16 + 1 splits merged through global memory (2
 # queries), a cluster of 3 with a different window per position (6 queries), a
 # cluster of 7 (20 queries), a window of 16 tiles with ragged local lengths
-# (windows of 1 and 2 rows at the start of a sequence), and one selected row
-# beside a full window.
+# (windows of 1 and 2 rows at the start of a sequence), one selected row
+# beside a full window, and 11 + 1 splits through the merge kernel.
 @pytest.mark.parametrize("H,D,K,Bn,P,window,lens", [
     (16, 128, 256, 1, 1, 128, None),
     (64, 512, 2048, 2, 1, 128, None),
@@ -50,6 +50,7 @@ def check_units(out, lse, q, lat, idx, local, lens, wl, units):
     (64, 512, 2048, 20, 1, 128, None),
     (32, 256, 64, 3, 2, 1000, (2, 700, 1001)),
     (64, 512, 1, 1, 1, 128, None),
+    (64, 512, 2048, 9, 1, 128, None),
 ])
 def test_joint_softmax_matches_oracle(H, D, K, Bn, P, window, lens):
     need_gpu()
