@@ -199,6 +199,51 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         for (int kb = 0; kb < D / 64; ++kb)
             tma_load_2d(q_stage + kb * kMaxHeads * 128, &qmap, &sm.qbar, kb * 128, unit * H);
     }
+    // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15, before the
+    // wait on the previous kernel (q is an input of the step): thread (head
+    // qh, quarter qq) of the first 256 threads converts dims [qq*D/4, (qq+1)*D/4)
+    // from the bf16 block in shared memory.
+    if (!mbar_wait(&sm.qbar, 0, abort_flag)) {
+        // timed out: the status bit is raised at the end; the CTA drains below
+    } else if (tid < 4 * kMaxHeads) {
+        // Two passes over this thread's 16-byte chunks, both unrolled with
+        // independent work per chunk: the exponent scan (four max chains), then
+        // the conversion, re-reading shared memory.  Lane = 8 * quarter + head
+        // (mod 8): each 8-lane phase of a 16-byte access covers 8 heads, whose
+        // swizzled chunks fall in 8 different bank groups.
+        const int qh = warp * 8 + (lane & 7), qq = lane >> 3, qn = D / 32;
+        const uint32_t qst = smem_u32(q_stage), qs = smem_u32(q_s);
+        auto chunk = [&](int i) -> uint4 {
+            // 16-byte chunk i of this quarter: dims qq*D/4 + 8i .. +8
+            const int dim = qq * (D / 4) + i * 8;
+            const int kb = dim >> 6, c = (dim >> 3) & 7;
+            return ld_shared_v4(qst + kb * kMaxHeads * 128 + qh * 128 + ((c ^ (qh & 7)) << 4));
+        };
+        constexpr uint32_t kExp = 0x7F807F80u;  // the exponent fields of two bf16
+        uint32_t m4[4] = {0u, 0u, 0u, 0u};
+        if (qh < H) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i < qn) {
+                    const uint4 v = chunk(i);
+                    m4[i & 3] = __vmaxu2(m4[i & 3], __vmaxu2(__vmaxu2(v.x & kExp, v.y & kExp),
+                                                             __vmaxu2(v.z & kExp, v.w & kExp)));
+                }
+            }
+        }
+        const uint32_t m2 = __vmaxu2(__vmaxu2(m4[0], m4[1]), __vmaxu2(m4[2], m4[3]));
+        uint32_t emax = max((m2 >> 7) & 0xFFu, m2 >> 23);
+        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 8));
+        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 16));
+        const float e = emax > 0 ? 14.f - (static_cast<float>(emax) - 127.f) : 0.f;
+        const float qscale = exp2f(e);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < qn)
+                st_shared_v4(qs + sw128_off(qh, qq * (D / 4) + i * 8, kMaxHeads),
+                             qh < H ? bf16x8_to_f16x8(chunk(i), qscale) : make_uint4(0, 0, 0, 0));
+        if (qq == 0) sm.cfac[qh] = a.scale * kLog2e * exp2f(-e);
+    }
     // Below: reads of what earlier kernels on the stream wrote (lengths, indices, cache).
     pdl_wait();
     len = a.c.lengths[b];
@@ -256,52 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < kMaxPieces; ++i) nsw[i] = (row >= 0 && i < nc) ? sp[i] : 0u;
     };
-    if (is_gather && n_tiles > 0) prefetch(t_first);  // in flight while Q is staged
+    if (is_gather && n_tiles > 0) prefetch(t_first);
 
-    // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15: thread (head
-    // qh, quarter qq) of the first 256 threads converts dims [qq*D/4, (qq+1)*D/4)
-    // from the bf16 block in shared memory.
-    if (!mbar_wait(&sm.qbar, 0, abort_flag)) {
-        // timed out: the status bit is raised at the end; the CTA drains below
-    } else if (tid < 4 * kMaxHeads) {
-        // Two passes over this thread's 16-byte chunks, both unrolled with
-        // independent work per chunk: the exponent scan (four max chains), then
-        // the conversion, re-reading shared memory.  Lane = 8 * quarter + head
-        // (mod 8): each 8-lane phase of a 16-byte access covers 8 heads, whose
-        // swizzled chunks fall in 8 different bank groups.
-        const int qh = warp * 8 + (lane & 7), qq = lane >> 3, qn = D / 32;
-        const uint32_t qst = smem_u32(q_stage), qs = smem_u32(q_s);
-        auto chunk = [&](int i) -> uint4 {
-            // 16-byte chunk i of this quarter: dims qq*D/4 + 8i .. +8
-            const int dim = qq * (D / 4) + i * 8;
-            const int kb = dim >> 6, c = (dim >> 3) & 7;
-            return ld_shared_v4(qst + kb * kMaxHeads * 128 + qh * 128 + ((c ^ (qh & 7)) << 4));
-        };
-        constexpr uint32_t kExp = 0x7F807F80u;  // the exponent fields of two bf16
-        uint32_t m4[4] = {0u, 0u, 0u, 0u};
-        if (qh < H) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (i < qn) {
-                    const uint4 v = chunk(i);
-                    m4[i & 3] = __vmaxu2(m4[i & 3], __vmaxu2(__vmaxu2(v.x & kExp, v.y & kExp),
-                                                             __vmaxu2(v.z & kExp, v.w & kExp)));
-                }
-            }
-        }
-        const uint32_t m2 = __vmaxu2(__vmaxu2(m4[0], m4[1]), __vmaxu2(m4[2], m4[3]));
-        uint32_t emax = max((m2 >> 7) & 0xFFu, m2 >> 23);
-        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 8));
-        emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, 16));
-        const float e = emax > 0 ? 14.f - (static_cast<float>(emax) - 127.f) : 0.f;
-        const float qscale = exp2f(e);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i < qn)
-                st_shared_v4(qs + sw128_off(qh, qq * (D / 4) + i * 8, kMaxHeads),
-                             qh < H ? bf16x8_to_f16x8(chunk(i), qscale) : make_uint4(0, 0, 0, 0));
-        if (qq == 0) sm.cfac[qh] = a.scale * kLog2e * exp2f(-e);
-    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
