@@ -531,6 +531,47 @@ def index_traffic_from_profile(workload):
     return int(val.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/index_score_full_64k.md)"
 
 
+def stage_rooflines(wl, stages, index_bytes, peak_hbm, peak_src, peak_tf, peak_tf_src, traffic, traffic_src):
+    """Roofline of each stage of the first layer, each timed alone (stage_times):
+    index_score is bound by HBM (indexer keys scanned + queries and weights);
+    sparse_attend (the attention kernel and its split merge) by the tensor
+    cores: S = Q.V^T and O = P.V, 2*H*D flops each per selected row and query
+    (fp16 operands, the dense bf16 rate); topk is reported against HBM for the
+    scores it reads and the ids it writes."""
+    units = wl.B * wl.P
+    L = wl.length_after_append
+    out = {}
+    ms = stages.get("index_score")
+    if ms:
+        ach = index_bytes / (ms / 1e3) / 1e9
+        out["index_score"] = {
+            "kernel": "index_score_kernel", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
+            "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
+            "algorithmic_bytes_per_launch": index_bytes, "launch_ms": ms, "traffic": traffic,
+            "traffic_source": traffic_src}
+    ms = stages.get("topk")
+    if ms:
+        nbytes = units * min(L, wl.capacity) * 4 + units * wl.K * 4
+        ach = nbytes / (ms / 1e3) / 1e9
+        out["topk"] = {
+            "kernel": "select_kernel", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
+            "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
+            "algorithmic_bytes_per_launch": nbytes, "launch_ms": ms, "traffic": None,
+            "traffic_source": "not captured"}
+    ms = stages.get("sparse_attend")
+    if ms:
+        kk = min(wl.K, L)
+        flops = units * 4.0 * wl.H * kk * wl.D
+        ach = flops / (ms / 1e3) / 1e12
+        out["sparse_attend"] = {
+            "kernel": "attend_kernel + attend_merge_kernel", "bound": "tensor", "achieved": ach, "peak": peak_tf,
+            "unit": "TFLOP/s", "frac": ach / peak_tf, "peak_source": peak_tf_src + " (bf16 dense, burst)",
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": units * (kk * (wl.D // 2 + wl.D // 16) + wl.H * wl.D * (2 + 4)),
+            "launch_ms": ms, "traffic": None, "traffic_source": "not captured"}
+    return out
+
+
 def main():
     args = parse_args()
     rank, world, local_rank = dist_env()
@@ -557,16 +598,14 @@ def main():
     peak_hbm = peaks.get("hbm_gbs")
     peak_src = "measured" if peak_hbm else "fallback"
     peak_hbm = peak_hbm or 6400.0
-    idx_ms = r["stages"].get("index_score")
+    peak_tf = peaks.get("bf16_tflops")
+    peak_tf_src = "measured" if peak_tf else "fallback"
+    peak_tf = peak_tf or 1800.0
     traffic, traffic_src = index_traffic_from_profile(wl.name)
     dominant = max(r["stages"], key=r["stages"].get) if r["stages"] else None
-    roof = None
-    if idx_ms:
-        ach = r["index_bytes"] / (idx_ms / 1e3) / 1e9
-        roof = {"kernel": "index_score", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
-                "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
-                "algorithmic_bytes_per_launch": r["index_bytes"], "launch_ms": idx_ms, "traffic": traffic,
-                "traffic_source": traffic_src}
+    rooflines = stage_rooflines(wl, r["stages"], r["index_bytes"], peak_hbm, peak_src, peak_tf, peak_tf_src,
+                                traffic, traffic_src)
+    roof = rooflines.get(dominant)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         rate, cores, sample, el = oracle_sample(wl, args.seed, 20.0)
@@ -581,7 +620,7 @@ def main():
         "hbm_gbs": r["gbs"], "frac_of_8tbs": r["gbs"] / NOMINAL_HBM_GBS, "frac_of_measured_hbm": r["gbs"] / peak_hbm,
         "step_algorithmic_bytes": r["step_bytes"],
         "stages_ms": r["stages"], "dominant_stage": dominant,
-        "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],
+        "roofline": roof, "roofline_stages": rooflines, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
     print(json.dumps(line))
