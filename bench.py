@@ -308,11 +308,12 @@ def bench_ours(args, wl, rank, world, local_rank):
 
     # Stage timings (the dominant kernel for the roofline): each stage alone.
     stages = stage_times(cache, layers, wl, flush, args.steps, stream)
+    layer_ms = layer_times(cache, layers, base_len, wl, flush, args.steps, stream)
     # e2e through the public API with host buffers
     e2e = e2e_run(cache, layers, base_len, wl, args, stream, flush)
     if B.csa_device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
-    return dict(value=value, ms_per_step=ms_per_step, gbs=gbs, step_bytes=sbytes, index_bytes=ibytes,
+    return dict(value=value, ms_per_step=ms_per_step, gbs=gbs, step_bytes=sbytes, index_bytes=ibytes, layer_ms=layer_ms,
                 clocks=clock_info, launches=launches_per_step * args.steps, stages=stages, e2e=e2e,
                 step_ms=step_ms)
 
@@ -380,6 +381,33 @@ def stage_times(cache, layers, wl, flush, steps, stream):
     out["topk"] = timed(lambda: B.csa_topk(cache, scores, wl.K, workspace=ws_sel))
     out["sparse_attend"] = timed(lambda: B.csa_sparse_attend_swa(cache, q, idx, wl.scale, swa, workspace=ws_att,
                                                                  out=o, lse=lse))
+    return out
+
+
+def layer_times(cache, layers, base_len, wl, flush, steps, stream):
+    """Each layer of the step alone (chains: Full, Reindex, Reuse in order),
+    captured as its own graph and replayed with L2 flushed before every
+    replay; mean device time per layer in ms.  Layers are sequential calls,
+    so no layer reads another's keys from L2."""
+    import torch
+    from fp4_compressed_sparse_append_b300 import binding as B
+    out = []
+    n = max(3, min(steps, 50))
+    for la in layers:
+        g = capture(lambda la=la: B.csa_layer_step(cache, la))
+        ts = []
+        for i in range(n + 2):
+            if wl.n_append:
+                cache.lengths.copy_(base_len)
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            if i >= 2:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        out.append(statistics.mean(x.elapsed_time(y) for x, y in ts))
     return out
 
 
@@ -620,6 +648,8 @@ def main():
         "hbm_gbs": r["gbs"], "frac_of_8tbs": r["gbs"] / NOMINAL_HBM_GBS, "frac_of_measured_hbm": r["gbs"] / peak_hbm,
         "step_algorithmic_bytes": r["step_bytes"],
         "stages_ms": r["stages"], "dominant_stage": dominant,
+        "layers_ms": {"modes": [W.MODE_NAMES[m] for m in wl.layers], "ms": r["layer_ms"],
+                      "how": "each layer alone as a graph, L2 flushed before each replay"},
         "roofline": roof, "roofline_stages": rooflines, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }

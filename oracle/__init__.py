@@ -78,6 +78,10 @@ def lib():
         L.oracle_block_max.argtypes = [P, i64, i32, P]
         L.oracle_attend.argtypes = [P, i32, i32, dbl, P, P, P, i64, P, P]
         L.oracle_attend_swa.argtypes = [P, i32, i32, dbl, P, P, P, i64, P, i64, i64, P, P]
+        L.oracle_project_ikeys.argtypes = [P, P, i64, i32, P, i32, P]
+        L.oracle_project_ikeys.restype = None
+        L.oracle_e4m3_round.argtypes = [dbl]
+        L.oracle_e4m3_round.restype = ctypes.c_uint8
         for f in (L.oracle_quantize_rows, L.oracle_dequantize_rows, L.oracle_index_score,
                   L.oracle_topk, L.oracle_block_max, L.oracle_attend):
             f.restype = None
@@ -149,6 +153,28 @@ def quantize_rows(x_bits, threads: int = 1) -> tuple:
     elif n:
         part((0, n))
     return codes, scales
+
+
+def e4m3_round(x: float) -> int:
+    """Signed E4M3 byte of a real: nearest value, ties to the even code, 448 beyond."""
+    return int(lib().oracle_e4m3_round(float(x)))
+
+
+def project_ikeys(codes, scales, w_bits) -> np.ndarray:
+    """Indexer keys projected from stored rows: codes [..., D/2], scales
+    [..., D/16], w [D][DI] bf16 bits -> [..., DI] E4M3 bytes.
+    "G2C Brief - DeepSeek V4.1-Flash", section "The global branch: compress,
+    index, select": the indexer's keys are a projection of the main cache entries."""
+    c = _np(codes, np.uint8)
+    s = _np(scales, np.uint8)
+    w = _np(w_bits, np.uint16)
+    D = c.shape[-1] * 2
+    DI = w.shape[1]
+    assert w.shape[0] == D
+    n = int(np.prod(c.shape[:-1])) if c.ndim > 1 else 1
+    out = np.zeros(c.shape[:-1] + (DI,), np.uint8)
+    lib().oracle_project_ikeys(_ptr(c), _ptr(s), n, D, _ptr(w), DI, _ptr(out))
+    return out
 
 
 def dequantize_rows(codes, scales) -> np.ndarray:

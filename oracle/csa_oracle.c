@@ -169,6 +169,48 @@ void oracle_dequantize_rows(const uint8_t *codes, const uint8_t *scales, int64_t
         }
 }
 
+/* Signed E4M3 of a real x: the magnitude rounded as oracle_e4m3_round_ratio
+ * (nearest, ties to the even code, 448 beyond the largest value), the sign of
+ * x kept (a zero result of a negative x keeps its sign bit). */
+uint8_t oracle_e4m3_round(double x)
+{
+    uint8_t m = oracle_e4m3_round_ratio(fabs(x), 1.0);
+    return (uint8_t)(x < 0.0 ? (m | 0x80) : m);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Indexer keys projected from the main cache entries ([G2C] "The global     */
+/* branch: compress, index, select": the indexer's keys are a projection of  */
+/* the main cache entries rather than a separately computed cache)           */
+/* ------------------------------------------------------------------------- */
+/*
+ * For each stored row (FP4 codes + E4M3 scales, dequantised exactly):
+ *     ik[j] = E4M3( sum_c v[c] * w[c][j] ),   j < DI
+ * with w a [D][DI] matrix of bf16 values.  Every product has at most 8 + 6
+ * significant bits and the sum over c is taken in double; it is exact while
+ * the products' exponents span at most 30 binades (53 bits less 14
+ * significant bits less 9 carry bits for up to 512 terms), which holds for
+ * weights and rows of ordinary size (the workloads' w is N(0, 1/D) in bf16).
+ *
+ * codes  : [n_rows][D/2]      scales : [n_rows][D/16]
+ * w      : [D][DI] bf16 bits  ik     : [n_rows][DI] E4M3 bytes (out)
+ */
+void oracle_project_ikeys(const uint8_t *codes, const uint8_t *scales, int64_t n_rows, int D,
+                          const uint16_t *w, int DI, uint8_t *ik)
+{
+    double *v = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int64_t r = 0; r < n_rows; ++r) {
+        oracle_dequantize_rows(codes + r * (D / 2), scales + r * (D / 16), 1, D, v);
+        for (int j = 0; j < DI; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < D; ++c)
+                acc += v[c] * oracle_bf16_value(w[(int64_t)c * DI + j]);
+            ik[r * DI + j] = oracle_e4m3_round(acc);
+        }
+    }
+    free(v);
+}
+
 /* ------------------------------------------------------------------------- */
 /* a2/a4: indexer score ([G2C] "The global branch", item 3; [FPR] Full mode)  */
 /* ------------------------------------------------------------------------- */
