@@ -151,11 +151,17 @@ __device__ __forceinline__ uint32_t swizzle_mode(int di)
 
 // sum_h w[h] * ReLU(acc[h]) over one query position's HI columns (HI a multiple
 // of 32), which start at tensor-memory address `taddr` of this warp's lane
-// quarter; w is this warp's copy in shared memory.  Four partial sums keep the
-// FMA chains short.
+// quarter; w is this warp's copy in shared memory.  ReLU one value at a time,
+// the weighting two at a time (packed fp32 FMA), into four paired partial sums
+// that keep the FMA chains short.
+__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b)
+{
+    return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
+}
+
 __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *w, int HI)
 {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
     if (HI == 64) {  // both loads in flight before one wait
         uint32_t r[32], t[32];
         tmem_ld32(taddr, r);
@@ -165,16 +171,12 @@ __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float4 ww = w4[k], wv = w4[k + 8];
-            s0 = fmaf(ww.x, fmaxf(__uint_as_float(r[4 * k + 0]), 0.f), s0);
-            s1 = fmaf(ww.y, fmaxf(__uint_as_float(r[4 * k + 1]), 0.f), s1);
-            s2 = fmaf(ww.z, fmaxf(__uint_as_float(r[4 * k + 2]), 0.f), s2);
-            s3 = fmaf(ww.w, fmaxf(__uint_as_float(r[4 * k + 3]), 0.f), s3);
-            s0 = fmaf(wv.x, fmaxf(__uint_as_float(t[4 * k + 0]), 0.f), s0);
-            s1 = fmaf(wv.y, fmaxf(__uint_as_float(t[4 * k + 1]), 0.f), s1);
-            s2 = fmaf(wv.z, fmaxf(__uint_as_float(t[4 * k + 2]), 0.f), s2);
-            s3 = fmaf(wv.w, fmaxf(__uint_as_float(t[4 * k + 3]), 0.f), s3);
+            s0 = __ffma2_rn(make_float2(ww.x, ww.y), relu2(r[4 * k + 0], r[4 * k + 1]), s0);
+            s1 = __ffma2_rn(make_float2(ww.z, ww.w), relu2(r[4 * k + 2], r[4 * k + 3]), s1);
+            s2 = __ffma2_rn(make_float2(wv.x, wv.y), relu2(t[4 * k + 0], t[4 * k + 1]), s2);
+            s3 = __ffma2_rn(make_float2(wv.z, wv.w), relu2(t[4 * k + 2], t[4 * k + 3]), s3);
         }
-        return (s0 + s1) + (s2 + s3);
+        return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
     }
     for (int c0 = 0; c0 < HI; c0 += 32) {
         uint32_t r[32];
@@ -182,15 +184,15 @@ __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *
         tmem_ld_wait();
         const float4 *w4 = reinterpret_cast<const float4 *>(w + c0);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 ww = w4[k];
-            s0 = fmaf(ww.x, fmaxf(__uint_as_float(r[4 * k + 0]), 0.f), s0);
-            s1 = fmaf(ww.y, fmaxf(__uint_as_float(r[4 * k + 1]), 0.f), s1);
-            s2 = fmaf(ww.z, fmaxf(__uint_as_float(r[4 * k + 2]), 0.f), s2);
-            s3 = fmaf(ww.w, fmaxf(__uint_as_float(r[4 * k + 3]), 0.f), s3);
+        for (int k = 0; k < 8; k += 2) {
+            const float4 ww = w4[k], wv = w4[k + 1];
+            s0 = __ffma2_rn(make_float2(ww.x, ww.y), relu2(r[4 * k + 0], r[4 * k + 1]), s0);
+            s1 = __ffma2_rn(make_float2(ww.z, ww.w), relu2(r[4 * k + 2], r[4 * k + 3]), s1);
+            s2 = __ffma2_rn(make_float2(wv.x, wv.y), relu2(r[4 * k + 4], r[4 * k + 5]), s2);
+            s3 = __ffma2_rn(make_float2(wv.z, wv.w), relu2(r[4 * k + 6], r[4 * k + 7]), s3);
         }
     }
-    return (s0 + s1) + (s2 + s3);
+    return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
 }
 
 // Same sum for any HI: 16-column loads masked to this position's columns.
