@@ -217,7 +217,11 @@ def build_state(wl, seed, device):
     ik = torch.empty((wl.B, wl.L, wl.DI), dtype=torch.uint8, device=device)
     for b in range(wl.B):
         lat[b], ik[b] = W.cache_rows(wl, seed, b, device=device)
-    B.csa_quantize_append(cache, lat, ik)
+    w_ik = W.ikey_projection(wl, seed, device=device) if wl.project else None
+    if wl.project:
+        B.csa_quantize_append_project(cache, lat, w_ik)
+    else:
+        B.csa_quantize_append(cache, lat, ik)
     del lat, ik
     torch.cuda.synchronize()
     app = W.append_rows(wl, seed, device=device) if wl.n_append else None
@@ -228,7 +232,8 @@ def build_state(wl, seed, device):
         la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
                          idx=prev if mode == W.REUSE else None,
                          rows_new=app["rows"] if (app and li == 0) else None,
-                         ikeys_new=app["ikeys"] if (app and li == 0) else None,
+                         ikeys_new=app["ikeys"] if (app and li == 0 and not wl.project) else None,
+                         w_ik=w_ik if (app and li == 0) else None,
                          pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
                          make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None), swa=swa)
         if mode != W.REUSE:
@@ -476,10 +481,15 @@ def oracle_sample(wl, seed, max_seconds):
     cores = os.cpu_count() or 1
     lat, ik = W.cache_rows(wl, seed, 0, device="cpu")
     oc = oracle.Cache(1, wl.capacity, wl.D, wl.DI)
-    oc.append(lat[None].numpy(), ik[None].numpy(), threads=cores)
+    w_ik = W.ikey_projection(wl, seed, device="cpu").numpy() if wl.project else None
+
+    def keys(rows_bits, given):
+        return oracle.project_ikeys(*oracle.quantize_rows(rows_bits), w_ik) if wl.project else given
+
+    oc.append(lat[None].numpy(), keys(lat.numpy(), ik.numpy())[None], threads=cores)
     if wl.n_append:
         app = W.append_rows(wl, seed, device="cpu")
-        oc.append(app["rows"][:1].numpy(), app["ikeys"][:1].numpy())
+        oc.append(app["rows"][:1].numpy(), keys(app["rows"][0].numpy(), app["ikeys"][0].numpy())[None])
     inputs = [{k: v[:1].numpy() for k, v in W.layer_inputs(wl, seed, li, device="cpu").items()}
               for li in range(len(wl.layers))]
     swa = (W.local_rows(wl, seed, device="cpu")[:1].numpy(), wl.window) if wl.window else None

@@ -21,7 +21,7 @@ CSA_POOL_BLOCK = 8
 CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
-    "csa_quantize_append", "csa_index_score", "csa_topk", "csa_topk_workspace_size", "csa_sparse_attend",
+    "csa_quantize_append", "csa_quantize_append_project", "csa_index_score", "csa_topk", "csa_topk_workspace_size", "csa_sparse_attend",
     "csa_sparse_attend_noalloc", "csa_sparse_attend_swa", "csa_attend_swa_workspace_size",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
@@ -52,7 +52,7 @@ class csa_layer_args(ctypes.Structure):
                 ("ikeys_new", ctypes.c_void_p), ("n_new", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
                 ("pool_in", ctypes.c_void_p), ("pool_out", ctypes.c_void_p), ("idx", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("swa", ctypes.c_void_p)]
+                ("workspace_bytes", ctypes.c_size_t), ("swa", ctypes.c_void_p), ("w_ik", ctypes.c_void_p)]
 
 
 _lib = None
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         C = ctypes.POINTER(csa_cache)
         L.csa_quantize_append.argtypes = [C, V, V, I32, V]
+        L.csa_quantize_append_project.argtypes = [C, V, V, I32, V]
         L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
         L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, SZ, V]
         L.csa_topk_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
@@ -151,6 +152,14 @@ def csa_quantize_append(cache: Cache, rows: torch.Tensor, ikeys_new: Optional[to
     n = rows.shape[1]
     _check(lib().csa_quantize_append(cache.ref, _ptr(rows), _ptr(ikeys_new), n, _stream(stream)),
            "csa_quantize_append")
+
+
+def csa_quantize_append_project(cache: Cache, rows: torch.Tensor, w_ik: torch.Tensor, stream=None) -> None:
+    """rows: [B, n, D] bf16 bits; w_ik: [D, DI] bf16 bits.  The appended rows'
+    indexer keys are projected from their stored FP4 entries."""
+    n = rows.shape[1]
+    _check(lib().csa_quantize_append_project(cache.ref, _ptr(rows), _ptr(w_ik), n, _stream(stream)),
+           "csa_quantize_append_project")
 
 
 def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optional[torch.Tensor] = None,
@@ -267,7 +276,7 @@ class LayerArgs:
 
     def __init__(self, cache: Cache, mode: int, q, K: int, scale: float, iq=None, w=None, idx=None,
                  rows_new=None, ikeys_new=None, pool_in=None, pool_blocks: int = 0, make_pool: bool = False,
-                 swa: Optional[Swa] = None):
+                 swa: Optional[Swa] = None, w_ik=None):
         B, P, H, D = q.shape
         dev = cache.device
         self.tensors = dict(q=q, iq=iq, w=w, rows_new=rows_new, ikeys_new=ikeys_new, pool_in=pool_in)
@@ -281,8 +290,9 @@ class LayerArgs:
         self.struct = csa_layer_args(mode, P, H, HI, K, scale, _ptr(q), _ptr(iq), _ptr(w), _ptr(rows_new),
                                      _ptr(ikeys_new), n_new, pool_blocks, _ptr(pool_in), _ptr(self.pool_out),
                                      _ptr(self.idx), _ptr(self.out), _ptr(self.lse), None, 0,
-                                     ctypes.addressof(swa._struct) if swa is not None else None)
+                                     ctypes.addressof(swa._struct) if swa is not None else None, _ptr(w_ik))
         self.swa = swa
+        self.tensors["w_ik"] = w_ik
         n = ctypes.c_size_t(0)
         _check(lib().csa_layer_workspace_size(cache.ref, ctypes.byref(self.struct), ctypes.byref(n)),
                "csa_layer_workspace_size")

@@ -106,6 +106,21 @@ csa_status csa_quantize_append(const csa_cache *cache, const uint16_t *rows, con
     return from_cuda(csa::launch_quantize_append(view(cache), rows, ikeys_new, n_new, st, stream));
 }
 
+csa_status csa_quantize_append_project(const csa_cache *cache, const uint16_t *rows, const uint16_t *w_ik,
+                                       int32_t n_new, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (n_new < 0 || !w_ik || !aligned16(w_ik)) return CSA_ERR_INVALID_ARG;
+    if (cache->d_index != 32 && cache->d_index != 64 && cache->d_index != 128) return CSA_ERR_UNSUPPORTED;
+    if (n_new == 0) return CSA_OK;
+    if (!rows || !aligned16(rows)) return CSA_ERR_INVALID_ARG;
+    if (n_new > cache->capacity) return CSA_ERR_INVALID_ARG;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_quantize_append(view(cache), rows, nullptr, n_new, st, stream, w_ik));
+}
+
 csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
                            const int32_t *pool, int32_t pool_blocks, float *scores, int64_t ld, csa_stream_t stream)
 {
@@ -277,6 +292,9 @@ static csa_status check_layer(const csa_cache *cache, const csa_layer_args *a)
         if (a->HI * a->P > 512 || a->HI > 256) return CSA_ERR_UNSUPPORTED;
     }
     if (a->n_new < 0 || (a->n_new > 0 && (a->mode != CSA_FULL || !a->rows_new))) return CSA_ERR_INVALID_ARG;
+    if (a->w_ik && (a->ikeys_new || !aligned16(a->w_ik))) return CSA_ERR_INVALID_ARG;
+    if (a->w_ik && a->n_new > 0 && cache->d_index != 32 && cache->d_index != 64 && cache->d_index != 128)
+        return CSA_ERR_UNSUPPORTED;
     if ((a->pool_in || a->pool_out) && (a->pool_blocks < 1 || a->pool_blocks > 16384)) return CSA_ERR_INVALID_ARG;
     if (a->pool_in && a->mode != CSA_REINDEX) return CSA_ERR_INVALID_ARG;
     if (a->pool_out && a->mode != CSA_FULL) return CSA_ERR_INVALID_ARG;
@@ -335,7 +353,7 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         const size_t sel_bytes = layer_select_ws(cache, a);
         ws += round_up(sel_bytes, 256);
         if (a->n_new > 0) {
-            e = csa::launch_quantize_append(v, a->rows_new, a->ikeys_new, a->n_new, st, stream);
+            e = csa::launch_quantize_append(v, a->rows_new, a->ikeys_new, a->n_new, st, stream, a->w_ik);
             if (e != cudaSuccess) return CSA_ERR_CUDA;
         }
         const int32_t *pool = a->mode == CSA_REINDEX ? a->pool_in : nullptr;

@@ -17,8 +17,10 @@ struct CacheView {
 };
 
 // a1
+// w_ik (optional): [D][DI] bf16; the appended rows' indexer keys are then
+// projected from their stored entries instead of copied from ikeys_new.
 cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, const uint8_t *ikeys_new, int n_new,
-                                   int *status, cudaStream_t st);
+                                   int *status, cudaStream_t st, const uint16_t *w_ik = nullptr);
 
 // a2/a4
 cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,

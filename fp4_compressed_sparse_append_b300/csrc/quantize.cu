@@ -102,6 +102,122 @@ __global__ void __launch_bounds__(256) quantize_append_kernel(CacheView c, const
     }
 }
 
+// Indexer keys projected from the just-stored main cache entries.
+// "G2C Brief - DeepSeek V4.1-Flash", section "The global branch: compress,
+// index, select": the indexer's keys are a projection of the main cache
+// entries rather than a separately computed cache.
+//     ik[j] = E4M3( sum_c v[c] * w[c][j] ),  v = E2M1(code) * E4M3(scale)
+// One CTA per (up to kProjRows new rows, sequence, kProjCols key channels);
+// runs after the append kernel, before the lengths advance, and reads the rows
+// it stored (from L2).  The dequantised rows are exact in fp32 and held in
+// shared memory as [channel][row]; thread (channel slice, row half, group of 4
+// key channels) accumulates 4 rows x 4 key channels over its slice in fp32
+// (w read as 4 bf16 at a time, coalesced along the key channels); the slices
+// are summed, and each sum is rounded once to E4M3 (nearest, ties to even,
+// saturating at 448).
+constexpr int kProjThreads = 256;
+constexpr int kProjRows = 8;
+constexpr int kProjCols = 32;                                 // key channels per CTA
+constexpr int kProjGroups = kProjCols / 4;                    // groups of 4 key channels
+constexpr int kProjSlices = kProjThreads / (2 * kProjGroups);  // channel slices (16)
+
+__device__ __forceinline__ float e4m3_byte_to_float(uint8_t byte)
+{
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3)));
+}
+
+__device__ __forceinline__ float2 e2m1_pair(uint8_t byte)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(uint32_t(byte)));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+}
+
+__global__ void __launch_bounds__(kProjThreads) project_ikeys_kernel(CacheView c, const uint16_t *__restrict__ w,
+                                                                     int n_new)
+{
+    extern __shared__ __align__(16) float psm[];
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.y, tid = threadIdx.x;
+    const int len0 = c.lengths[b];
+    if (len0 < 0 || len0 + n_new > c.cap) return;  // left unchanged (and flagged) by the append kernel
+    const int D = c.D, DI = c.DI;
+    const int j0 = blockIdx.x * kProjRows, col0 = blockIdx.z * kProjCols;
+    const int nr = min(kProjRows, n_new - j0);
+    const int64_t row0 = static_cast<int64_t>(b) * c.cap + len0 + j0;
+    float *v = psm;                                // [D][kProjRows]
+    float *part = psm + D * kProjRows;             // [kProjSlices][kProjRows][kProjCols]
+    // Dequantise: thread (code byte, row), rows fastest; the loads of all its
+    // iterations are issued before any is used.
+    constexpr int kDq = 8;
+    for (int i0 = 0; i0 < kProjRows * (D / 2); i0 += kDq * kProjThreads) {
+        uint8_t cb8[kDq], sb8[kDq];
+#pragma unroll
+        for (int u = 0; u < kDq; ++u) {
+            const int i = i0 + u * kProjThreads + tid;
+            const int r = i % kProjRows, cb = i / kProjRows;
+            const bool live = i < kProjRows * (D / 2) && r < nr;
+            cb8[u] = live ? c.codes[(row0 + r) * (D / 2) + cb] : 0;
+            sb8[u] = live ? c.scales[(row0 + r) * (D / 16) + cb / 8] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kDq; ++u) {
+            const int i = i0 + u * kProjThreads + tid;
+            if (i >= kProjRows * (D / 2)) break;
+            const int r = i % kProjRows, cb = i / kProjRows;
+            const float s = e4m3_byte_to_float(sb8[u]);
+            const float2 x = e2m1_pair(cb8[u]);
+            v[(2 * cb) * kProjRows + r] = x.x * s;
+            v[(2 * cb + 1) * kProjRows + r] = x.y * s;
+        }
+    }
+    __syncthreads();
+    const int ks = tid / (2 * kProjGroups), rh = (tid / kProjGroups) & 1, jg = tid % kProjGroups;
+    const int cpk = D / kProjSlices;
+    float acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+    const uint16_t *wp = w + static_cast<int64_t>(ks * cpk) * DI + col0 + jg * 4;
+    const float *vp = v + ks * cpk * kProjRows + rh * 4;
+    // w comes from L2: sixteen channels' loads are issued before their use.
+    constexpr int kBatch = 16;
+    for (int cc0 = 0; cc0 < cpk; cc0 += kBatch) {
+        uint2 wb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            wb[u] = cc0 + u < cpk ? __ldg(reinterpret_cast<const uint2 *>(wp + static_cast<int64_t>(cc0 + u) * DI))
+                                  : make_uint2(0u, 0u);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (cc0 + u >= cpk) break;
+            const float4 vv = *reinterpret_cast<const float4 *>(vp + (cc0 + u) * kProjRows);
+            const float wq[4] = {__uint_as_float(wb[u].x << 16), __uint_as_float(wb[u].x & 0xFFFF0000u),
+                                 __uint_as_float(wb[u].y << 16), __uint_as_float(wb[u].y & 0xFFFF0000u)};
+            const float vr[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(vr[r], wq[q], acc[r][q]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4 *>(part + (ks * kProjRows + rh * 4 + r) * kProjCols + jg * 4) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    __syncthreads();
+    for (int i = tid; i < nr * kProjCols; i += kProjThreads) {
+        const int r = i / kProjCols, j = i - r * kProjCols;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kProjSlices; ++q) sum += part[(q * kProjRows + r) * kProjCols + j];
+        c.ikeys[(row0 + r) * DI + col0 + j] =
+            static_cast<uint8_t>(__nv_cvt_float_to_fp8(sum, __NV_SATFINITE, __NV_E4M3));
+    }
+}
+
 __global__ void advance_lengths_kernel(int32_t *lengths, int B, int cap, int n_new)
 {
     pdl_wait();
@@ -114,8 +230,14 @@ __global__ void advance_lengths_kernel(int32_t *lengths, int B, int cap, int n_n
 
 }  // namespace
 
+size_t project_smem_bytes(const CacheView &c)
+{
+    return static_cast<size_t>(c.D) * kProjRows * sizeof(float) +
+           static_cast<size_t>(kProjSlices) * kProjRows * kProjCols * sizeof(float);
+}
+
 cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, const uint8_t *ikeys_new, int n_new,
-                                   int *status, cudaStream_t st)
+                                   int *status, cudaStream_t st, const uint16_t *w_ik)
 {
     if (n_new <= 0) return cudaSuccess;
     const int64_t work = static_cast<int64_t>(n_new) * (c.D / 8);
@@ -124,9 +246,19 @@ cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, con
     if (blocks_x > want * 8) blocks_x = want * 8;
     if (blocks_x < 1) blocks_x = 1;
     dim3 grid(static_cast<unsigned>(blocks_x), c.B);
-    const cudaError_t e = launch_kernel(quantize_append_kernel, grid, dim3(256), 0, st, 0, c, rows, ikeys_new, n_new,
-                                        status);
+    cudaError_t e = launch_kernel(quantize_append_kernel, grid, dim3(256), 0, st, 0, c, rows, ikeys_new, n_new,
+                                  status);
     if (e != cudaSuccess) return e;
+    if (w_ik) {
+        if (c.DI != 32 && c.DI != 64 && c.DI != 128) return cudaErrorInvalidValue;
+        const size_t smem = project_smem_bytes(c);
+        e = cudaFuncSetAttribute(project_ikeys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        e = launch_kernel(project_ikeys_kernel, dim3((n_new + kProjRows - 1) / kProjRows, c.B, c.DI / kProjCols),
+                          dim3(kProjThreads), smem, st, 0, c, w_ik, n_new);
+        if (e != cudaSuccess) return e;
+    }
     return launch_kernel(advance_lengths_kernel, dim3((c.B + 127) / 128), dim3(128), 0, st, 0, c.lengths, c.B, c.cap,
                          n_new);
 }

@@ -26,6 +26,7 @@ chain_128k         32  131072    64  512  64  128  2048  1  Full, 3x Reindex, 4x
 hier_1m            1   1048576   64  512  64  128  2048  1  Full+pool, 7x Reindex(pool)
 verify_append_32k  64  32768     64  512  64  128  2048  6  append 6 rows, then Full
 full_64k_swa       8   65536     64  512  64  128  2048  1  Full + 128-row local window
+verify_project_32k 64  32768     64  512  64  128  2048  6  as verify_append_32k, keys projected
 =================  ==  ========  ==  ===  ==  ===  ====  =  =========================
 """
 from __future__ import annotations
@@ -60,6 +61,7 @@ class Workload:
     planted: int = 0        # length of a planted high-similarity block (0 = none)
     n_append: int = 0       # rows appended (quantised) at the start of the step
     window: int = 0         # >0: every query also attends to this many local FP8 rows
+    project: bool = False   # indexer keys projected from the stored rows by a seeded [D][DI] matrix
 
     @property
     def capacity(self) -> int:
@@ -89,10 +91,12 @@ WORKLOADS: Dict[str, Workload] = {
                                   DI=128, K=2048, P=6, n_append=6),
     "full_64k_swa": Workload("full_64k_swa", B=8, L=65536, H=64, D=512, HI=64, DI=128, K=2048,
                              outlier_channels=5, window=128),
+    "verify_project_32k": Workload("verify_project_32k", B=64, L=32768, H=64, D=512, HI=64,
+                                   DI=128, K=2048, P=6, n_append=6, project=True),
 }
 
 # Tensor tags for the per-tensor streams.
-_T_LATENT, _T_IKEY, _T_Q, _T_IQ, _T_W, _T_NEWROW, _T_NEWIKEY, _T_OUTLIER, _T_PLANT, _T_LOCAL = range(10)
+_T_LATENT, _T_IKEY, _T_Q, _T_IQ, _T_W, _T_NEWROW, _T_NEWIKEY, _T_OUTLIER, _T_PLANT, _T_LOCAL, _T_WIK = range(11)
 
 
 def _mix(*vals: int) -> int:
@@ -213,6 +217,12 @@ def append_rows(wl: Workload, seed: int, device="cpu") -> Dict[str, torch.Tensor
     if out_ch.numel():
         lat[..., out_ch] *= 8.0
     return {"rows": to_bf16_bits(lat), "ikeys": to_e4m3_bytes(ik)}
+
+
+def ikey_projection(wl: Workload, seed: int, device="cpu") -> torch.Tensor:
+    """The [D][DI] matrix that projects stored rows to indexer keys: N(0, 1/D)
+    in bf16 (bits as int16), so a key channel has about the spread of a latent."""
+    return to_bf16_bits(_randn((wl.D, wl.DI), device, seed, _T_WIK) / math.sqrt(wl.D))
 
 
 def local_rows(wl: Workload, seed: int, device="cpu", n: Optional[int] = None) -> torch.Tensor:

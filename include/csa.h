@@ -121,6 +121,24 @@ CSA_API csa_status csa_quantize_append(const csa_cache *cache, const uint16_t *r
                                const uint8_t *ikeys_new, int32_t n_new, csa_stream_t stream);
 
 /*
+ * a1 with indexer keys projected from the stored rows.  ("G2C Brief", section
+ * "The global branch: compress, index, select": the indexer's keys are a
+ * projection of the main cache entries rather than a separately computed
+ * cache.)  Appends rows as csa_quantize_append does, then writes each appended
+ * row's indexer key
+ *     ik[j] = E4M3( sum_c v[c] * w_ik[c][j] ),  j < d_index,
+ * from its stored entry v = E2M1(code) * E4M3(scale) (exact), summed in fp32
+ * and rounded once: nearest, ties to even, saturating at 448 (a zero sum is
+ * +0).  The sum's order differs from an exact one, so a key can differ by one
+ * code from the exactly rounded product where that product lies within fp32
+ * rounding of the midpoint between two E4M3 values.
+ *   w_ik : [d_latent][d_index] bf16 bits, device, 16-byte aligned (read only)
+ * d_index must be 32, 64 or 128 (else CSA_ERR_UNSUPPORTED).
+ */
+CSA_API csa_status csa_quantize_append_project(const csa_cache *cache, const uint16_t *rows, const uint16_t *w_ik,
+                                               int32_t n_new, csa_stream_t stream);
+
+/*
  * a2/a4: indexer scores for B*P queries.
  * ("G2C Brief", sections "The global branch" and "The hierarchical indexer".)
  *   iq     : [batch][P][HI][d_index] E4M3 indexer queries
@@ -290,6 +308,9 @@ typedef struct csa_layer_args {
     void *workspace;
     size_t workspace_bytes;
     const csa_swa *swa;          /* local window joined to the softmax, or NULL */
+    const uint16_t *w_ik;        /* FULL with n_new > 0: project the new rows' indexer keys
+                                    ([d_latent][d_index] bf16, as csa_quantize_append_project)
+                                    instead of copying ikeys_new (which must then be NULL); or NULL */
 } csa_layer_args;
 
 CSA_API csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *args, csa_stream_t stream);

@@ -35,7 +35,12 @@ def device_cache(wl: W.Workload, seed: int, device="cuda"):
     ik = torch.empty((wl.B, wl.L, wl.DI), dtype=torch.uint8, device=device)
     for b in range(wl.B):
         lat[b], ik[b] = W.cache_rows(wl, seed, b, device=device)
-    B.csa_quantize_append(cache, lat, ik)
+    if wl.project:
+        # keys projected from the stored rows (the drawn keys are not used)
+        B.csa_quantize_append_project(cache, lat, W.ikey_projection(wl, seed, device=device))
+        ik = cache.ikeys[:, : wl.L].clone()
+    else:
+        B.csa_quantize_append(cache, lat, ik)
     return cache, lat, ik
 
 

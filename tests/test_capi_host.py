@@ -138,3 +138,19 @@ def test_local_window_checks(lib):
     good = B.csa_swa(rows=0x7000, lengths=None, n=4, window=8)
     a.swa = ctypes.addressof(good)
     assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 0
+
+
+def test_projected_append_checks(lib):
+    c = ctypes.byref(fake_cache())
+    V = ctypes.c_void_p
+    assert lib.csa_quantize_append_project(c, V(0x50000), None, 1, None) == 1            # no matrix
+    assert lib.csa_quantize_append_project(c, V(0x50000), V(0x60008), 1, None) == 1      # misaligned matrix
+    assert lib.csa_quantize_append_project(ctypes.byref(fake_cache(d_index=48)), V(0x50000), V(0x60000), 1,
+                                           None) == 2                                     # d_index not 32/64/128
+    assert lib.csa_quantize_append_project(c, V(0x50000), V(0x60000), 0, None) == 0       # nothing to append
+    a = B.csa_layer_args(mode=B.CSA_FULL, P=1, H=16, HI=4, K=8, scale=1.0, q=0x1000, iq=0x2000, w=0x3000,
+                         idx=0x4000, out=0x5000, rows_new=0x7000, ikeys_new=0x8000, n_new=1, w_ik=0x9000)
+    n = ctypes.c_size_t(0)
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 1        # keys given and projected
+    a.ikeys_new = None
+    assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 0

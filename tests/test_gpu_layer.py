@@ -22,13 +22,16 @@ THREADS = max(1, min(32, os.cpu_count() or 1))
 
 def run_gpu_chain(wl, seed, cache):
     swa = B.Swa(W.local_rows(wl, seed, device="cuda"), wl.window) if wl.window else None
+    w_ik = W.ikey_projection(wl, seed, device="cuda") if wl.project else None
     layers, prev, pool = [], None, None
     for li, mode in enumerate(wl.layers):
         inp = W.layer_inputs(wl, seed, li, device="cuda")
         app = W.append_rows(wl, seed, device="cuda") if (li == 0 and wl.n_append) else None
         la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
                          idx=prev if mode == W.REUSE else None,
-                         rows_new=app["rows"] if app else None, ikeys_new=app["ikeys"] if app else None,
+                         rows_new=app["rows"] if app else None,
+                         ikeys_new=app["ikeys"] if (app and not wl.project) else None,
+                         w_ik=w_ik if app else None,
                          pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
                          make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None), swa=swa)
         B.csa_layer_step(cache, la)
@@ -45,10 +48,20 @@ def run_gpu_chain(wl, seed, cache):
 def oracle_chain(wl, seed, lat, ik, seqs):
     """Oracle chain for the listed sequences (host copies of the same draws)."""
     cache = oracle.Cache(len(seqs), wl.capacity, wl.D, wl.DI)
-    cache.append(lat[seqs].cpu().numpy(), ik[seqs].cpu().numpy(), threads=THREADS)
+    w_ik = W.ikey_projection(wl, seed, device="cuda").cpu().numpy() if wl.project else None
+
+    def keys(rows_bits, given):
+        # projected workloads: the oracle projects the keys itself, from its own quantisation
+        if not wl.project:
+            return given
+        return np.stack([oracle.project_ikeys(*oracle.quantize_rows(r), w_ik) for r in rows_bits])
+
+    lat_s = lat[seqs].cpu().numpy()
+    cache.append(lat_s, keys(lat_s, ik[seqs].cpu().numpy()), threads=THREADS)
     if wl.n_append:
         app = W.append_rows(wl, seed, device="cuda")
-        cache.append(app["rows"][seqs].cpu().numpy(), app["ikeys"][seqs].cpu().numpy())
+        rows_s = app["rows"][seqs].cpu().numpy()
+        cache.append(rows_s, keys(rows_s, app["ikeys"][seqs].cpu().numpy()))
     inputs = []
     for li in range(len(wl.layers)):
         inp = W.layer_inputs(wl, seed, li, device="cuda")
@@ -102,6 +115,8 @@ SMALL = [
     W.Workload("verify_small", B=3, L=3000, H=8, D=128, HI=32, DI=64, K=700, P=6, n_append=6),
     W.Workload("chain_swa_small", B=3, L=4000, H=32, D=512, HI=16, DI=128, K=512, P=2, outlier_channels=5,
                layers=(W.FULL, W.REINDEX, W.REUSE), window=128),
+    W.Workload("verify_project_small", B=3, L=3000, H=8, D=256, HI=32, DI=64, K=700, P=6, n_append=6,
+               project=True),
 ]
 
 
@@ -121,7 +136,7 @@ def test_small_workloads_every_query(wl):
 
 
 FULL_SIZE = [("full_64k", [0, 5]), ("chain_128k", [17]), ("hier_1m", [0]), ("verify_append_32k", [40]),
-             ("full_64k_swa", [3])]
+             ("full_64k_swa", [3]), ("verify_project_32k", [11])]
 
 
 @pytest.mark.slow
