@@ -45,7 +45,8 @@ constexpr int kDigit2Bins = 256;     // key bits 7..0
 constexpr int kSelCacheMax = 16384;  // keys held per CTA at most (64 KB): two CTAs fit one SM
 constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
-constexpr int kMinChunk = 4096;      // a row is not spread thinner than this per CTA
+constexpr int kMinChunk = 4096;      // a row of up to 2x this stays whole in one CTA (no cluster barrier)
+constexpr int kMinChunkLong = 1024;  // a longer row is not spread thinner than this per CTA
 constexpr int64_t kSegmentLen = static_cast<int64_t>(kMaxCluster) * 8192;
 
 enum SelSource { kRows = 0, kBlocks = 1, kPoolRows = 2, kPairs = 3 };
@@ -471,13 +472,16 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
         configured = true;
     }
     // Smallest cluster whose chunks fit shared memory, widened (down to
-    // kMinChunk keys per CTA) while the grid is under one CTA per SM: spreading
+    // kMinChunkLong keys per CTA) while the grid is under one CTA per SM: spreading
     // a row's keys over more CTAs also spreads the contention of its shared-
     // memory histogram, which crowded indexer scores make high.
+    // Rows of at most 2 * kMinChunk keys stay in one CTA: there the cluster
+    // barriers cost more than the spread saves.
+    const int64_t min_chunk = n_per_cluster <= 2 * kMinChunk ? kMinChunk : kMinChunkLong;
     int C = 1;
     while (C < kMaxCluster &&
            ((n_per_cluster + C - 1) / C > kSelCacheMax ||
-            (static_cast<int64_t>(grid_rows) * C < 148 && (n_per_cluster + 2 * C - 1) / (2 * C) >= kMinChunk)))
+            (static_cast<int64_t>(grid_rows) * C < 148 && (n_per_cluster + 2 * C - 1) / (2 * C) >= min_chunk)))
         C *= 2;
     const int64_t chunk = (n_per_cluster + C - 1) / C;
     if (chunk > kSelCacheMax) return cudaErrorInvalidValue;
