@@ -79,6 +79,16 @@ def lib():
         L.oracle_attend.argtypes = [P, i32, i32, dbl, P, P, P, i64, P, P]
         L.oracle_attend_swa.argtypes = [P, i32, i32, dbl, P, P, P, i64, P, i64, i64, P, P]
         L.oracle_project_ikeys.argtypes = [P, P, i64, i32, P, i32, P]
+        L.oracle_mx_exponent.argtypes = [dbl]
+        L.oracle_mx_exponent.restype = ctypes.c_int
+        L.oracle_mx_quantize.argtypes = [P, i64, i32, P, P]
+        L.oracle_mx_quantize.restype = None
+        L.oracle_mx_dequantize.argtypes = [P, P, i64, i32, P]
+        L.oracle_mx_dequantize.restype = None
+        L.oracle_index_score_mx.argtypes = [P, P, i32, i32, P, P, P, i64, P]
+        L.oracle_index_score_mx.restype = None
+        L.oracle_project_ikeys_mx.argtypes = [P, P, i64, i32, P, i32, P, P]
+        L.oracle_project_ikeys_mx.restype = None
         L.oracle_project_ikeys.restype = None
         L.oracle_e4m3_round.argtypes = [dbl]
         L.oracle_e4m3_round.restype = ctypes.c_uint8
@@ -177,6 +187,67 @@ def project_ikeys(codes, scales, w_bits) -> np.ndarray:
     return out
 
 
+# --------------------------------------------------------------------------
+# MXFP4 indexer keys ("G2C Brief - DeepSeek V4.1-Flash", section "FP4 cache
+# entries, and why they're safe": 128 values x 4 bits + one 8-bit scale per 32
+# values = 68 B).  A packed key row is its DI/2 code bytes then its DI/32
+# scale bytes.
+# --------------------------------------------------------------------------
+
+def mx_exponent(amax: float) -> int:
+    """Block exponent X = floor(log2 amax) - 2, clamped to [-8, 6] (-8 for 0)."""
+    return int(lib().oracle_mx_exponent(float(amax)))
+
+
+def mx_quantize(x) -> tuple:
+    """Reals [..., DI] (float64) -> (codes [..., DI/2], scales [..., DI/32])."""
+    a = _np(x, np.float64)
+    DI = a.shape[-1]
+    n = int(np.prod(a.shape[:-1])) if a.ndim > 1 else 1
+    codes = np.zeros(a.shape[:-1] + (DI // 2,), np.uint8)
+    scales = np.zeros(a.shape[:-1] + (DI // 32,), np.uint8)
+    lib().oracle_mx_quantize(_ptr(a), n, DI, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mx_quantize_bf16(x_bits) -> tuple:
+    bits = _np(x_bits, np.uint16).astype(np.uint32) << 16
+    return mx_quantize(bits.view(np.float32).astype(np.float64))
+
+
+def mx_dequantize(codes, scales) -> np.ndarray:
+    c = _np(codes, np.uint8)
+    s = _np(scales, np.uint8)
+    DI = c.shape[-1] * 2
+    n = int(np.prod(c.shape[:-1])) if c.ndim > 1 else 1
+    out = np.zeros(c.shape[:-1] + (DI,), np.float64)
+    lib().oracle_mx_dequantize(_ptr(c), _ptr(s), n, DI, _ptr(out))
+    return out
+
+
+def mx_pack(codes, scales) -> np.ndarray:
+    return np.ascontiguousarray(np.concatenate([_np(codes, np.uint8), _np(scales, np.uint8)], axis=-1))
+
+
+def mx_unpack(keys, DI: int) -> tuple:
+    k = _np(keys, np.uint8)
+    return np.ascontiguousarray(k[..., : DI // 2]), np.ascontiguousarray(k[..., DI // 2:])
+
+
+def project_ikeys_mx(codes, scales, w_bits) -> np.ndarray:
+    """Projected keys (as project_ikeys) in MXFP4: packed rows [..., DI/2 + DI/32]."""
+    c = _np(codes, np.uint8)
+    s = _np(scales, np.uint8)
+    w = _np(w_bits, np.uint16)
+    D = c.shape[-1] * 2
+    DI = w.shape[1]
+    n = int(np.prod(c.shape[:-1])) if c.ndim > 1 else 1
+    kc = np.zeros(c.shape[:-1] + (DI // 2,), np.uint8)
+    ks = np.zeros(c.shape[:-1] + (DI // 32,), np.uint8)
+    lib().oracle_project_ikeys_mx(_ptr(c), _ptr(s), n, D, _ptr(w), DI, _ptr(kc), _ptr(ks))
+    return mx_pack(kc, ks)
+
+
 def dequantize_rows(codes, scales) -> np.ndarray:
     c = _np(codes, np.uint8)
     s = _np(scales, np.uint8)
@@ -188,17 +259,20 @@ def dequantize_rows(codes, scales) -> np.ndarray:
 
 
 class Cache:
-    """Host copy of one global cache: rows [0, lengths[b]) of each sequence are valid."""
+    """Host copy of one global cache: rows [0, lengths[b]) of each sequence are valid.
+    Indexer keys are E4M3 rows [DI] ("e4m3") or packed MXFP4 rows [DI/2 + DI/32] ("mxfp4")."""
 
-    def __init__(self, B: int, capacity: int, D: int, DI: int):
+    def __init__(self, B: int, capacity: int, D: int, DI: int, key_format: str = "e4m3"):
         self.B, self.capacity, self.D, self.DI = B, capacity, D, DI
+        self.key_format = key_format
         self.codes = np.zeros((B, capacity, D // 2), np.uint8)
         self.scales = np.zeros((B, capacity, D // 16), np.uint8)
-        self.ikeys = np.zeros((B, capacity, DI), np.uint8)
+        kb = DI if key_format == "e4m3" else DI // 2 + DI // 32
+        self.ikeys = np.zeros((B, capacity, kb), np.uint8)
         self.lengths = np.zeros(B, np.int64)
 
     def append(self, rows_bits, ikeys, threads: int = 1) -> None:
-        """Quantise rows [B, n, D] and write them, with their ikeys [B, n, DI],
+        """Quantise rows [B, n, D] and write them, with their ikeys [B, n, key bytes],
         at positions lengths[b] .. lengths[b]+n-1; then lengths += n."""
         rows = _np(rows_bits, np.uint16)
         ik = _np(ikeys, np.uint8)
@@ -237,6 +311,28 @@ def index_scores(iq, w, ikeys_b, rows, threads: int = 1) -> np.ndarray:
     def part(c):
         a, b = c
         lib().oracle_index_score(_ptr(q), _ptr(ww), HI, DI, _ptr(ik), _ptr(r[a:b]), b - a, _ptr(out[a:b]))
+
+    if threads > 1 and r.shape[0] > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(part, _chunks(r.shape[0], threads)))
+    elif r.shape[0]:
+        part((0, r.shape[0]))
+    return out
+
+
+def index_scores_mx(iq, w, keys_b, rows, threads: int = 1) -> np.ndarray:
+    """index_scores with MXFP4 keys: keys_b [n_rows_total, DI/2 + DI/32] packed rows."""
+    q = _np(iq, np.uint8)
+    ww = _np(w, np.float32)
+    HI, DI = q.shape
+    kc, ks = mx_unpack(keys_b, DI)
+    r = np.ascontiguousarray(np.asarray(rows, np.int64))
+    out = np.zeros(r.shape[0], np.float32)
+
+    def part(c):
+        a, b = c
+        lib().oracle_index_score_mx(_ptr(q), _ptr(ww), HI, DI, _ptr(kc), _ptr(ks), _ptr(r[a:b]), b - a,
+                                    _ptr(out[a:b]))
 
     if threads > 1 and r.shape[0] > 1:
         with ThreadPoolExecutor(threads) as ex:
@@ -359,13 +455,13 @@ def unit_layer(cache: Cache, b: int, p: int, P: int, mode: int, q, iq, w, K: int
         idx = np.asarray(prev_idx, np.int64)
     elif mode == REINDEX and pool_in is not None:
         rows, valid = pool_rows(pool_in, L_p)
-        sc = index_scores(iq, w, cache.ikeys[b], rows, threads)
+        sc = (index_scores_mx if cache.key_format == "mxfp4" else index_scores)(iq, w, cache.ikeys[b], rows, threads)
         sel = topk(sc, K, valid)
         idx = np.where(sel >= 0, rows[np.maximum(sel, 0)], -1)
         res["scores"], res["rows"], res["valid"] = sc, rows, valid
     else:
         rows = np.arange(L_p, dtype=np.int64)
-        sc = index_scores(iq, w, cache.ikeys[b], rows, threads)
+        sc = (index_scores_mx if cache.key_format == "mxfp4" else index_scores)(iq, w, cache.ikeys[b], rows, threads)
         idx = topk(sc, K)
         res["scores"] = sc
         if mode == FULL and pool_keep:

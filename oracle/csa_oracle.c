@@ -252,6 +252,127 @@ void oracle_index_score(const uint8_t *iq, const float *w, int HI, int DI,
 }
 
 /* ------------------------------------------------------------------------- */
+/* MXFP4 indexer keys ([G2C] "FP4 cache entries, and why they're safe": the   */
+/* indexer K entry of 128 values x 4 bits plus one 8-bit scale per 32 values, */
+/* 68 B, the OCP MXFP4 format the report says V4 adopted)                    */
+/* ------------------------------------------------------------------------- */
+/*
+ * Per block of 32 consecutive channels with largest magnitude amax:
+ *   X = floor(log2(amax)) - 2     (2 is the exponent of E2M1's largest value, 6)
+ *   clamped to [-8, 6], and X = -8 for an all-zero block;
+ *   scale byte = X + 127 (UE8M0: the value 2^X);
+ *   code = sign(x) | E2M1 magnitude nearest to |x| / 2^X (ties to the even
+ *   code, 6 beyond), packed two per byte, the even channel in the low nibble.
+ * The clamp is this build's addition to the OCP rule: with X in [-8, 6] every
+ * stored value 2^X * E2M1 is exactly an E4M3 value (6 * 2^6 = 384 <= 448, and
+ * 0.5 * 2^-8 = 2^-9 is E4M3's smallest step), so a key decodes exactly.
+ */
+int oracle_mx_exponent(double amax)
+{
+    if (!(amax > 0.0))
+        return -8;
+    int e;
+    frexp(amax, &e);                 /* amax = f * 2^e, f in [0.5, 1): floor(log2 amax) = e - 1 */
+    int X = (e - 1) - 2;
+    if (X < -8)
+        X = -8;
+    if (X > 6)
+        X = 6;
+    return X;
+}
+
+/* Quantise rows of reals x [n][DI] (DI a multiple of 32) to MXFP4:
+ * codes [n][DI/2], scales [n][DI/32]. */
+void oracle_mx_quantize(const double *x, int64_t n, int DI, uint8_t *codes, uint8_t *scales)
+{
+    for (int64_t r = 0; r < n; ++r)
+        for (int blk = 0; blk < DI / 32; ++blk) {
+            const double *xb = x + r * DI + blk * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i)
+                if (fabs(xb[i]) > amax)
+                    amax = fabs(xb[i]);
+            const int X = oracle_mx_exponent(amax);
+            const double s = ldexp(1.0, X);
+            scales[r * (DI / 32) + blk] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; ++i) {
+                uint8_t code = oracle_e2m1_round_ratio(fabs(xb[i]), s);
+                if (signbit(xb[i]))
+                    code |= 0x8;
+                const int ch = blk * 32 + i;
+                uint8_t *dst = codes + r * (DI / 2) + ch / 2;
+                if ((ch & 1) == 0)
+                    *dst = (uint8_t)((*dst & 0xF0) | code);
+                else
+                    *dst = (uint8_t)((*dst & 0x0F) | (code << 4));
+            }
+        }
+}
+
+/* MXFP4 decode: 2^(scale - 127) * E2M1(code). */
+double oracle_mx_value(uint8_t code, uint8_t scale)
+{
+    return ldexp(oracle_e2m1_value(code), (int)scale - 127);
+}
+
+void oracle_mx_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t n, int DI, double *out)
+{
+    for (int64_t r = 0; r < n; ++r)
+        for (int ch = 0; ch < DI; ++ch) {
+            uint8_t byte = codes[r * (DI / 2) + ch / 2];
+            uint8_t code = (ch & 1) ? (byte >> 4) : (byte & 0xF);
+            out[r * DI + ch] = oracle_mx_value(code, scales[r * (DI / 32) + ch / 32]);
+        }
+}
+
+/* Indexer scores with MXFP4 keys: the score formula of oracle_index_score,
+ * with each key decoded from its codes and block scales (products exact in
+ * double, as there). */
+void oracle_index_score_mx(const uint8_t *iq, const float *w, int HI, int DI, const uint8_t *kcodes,
+                           const uint8_t *kscales, const int64_t *rows, int64_t n, float *out)
+{
+    double *q = (double *)malloc(sizeof(double) * (size_t)HI * DI);
+    for (int i = 0; i < HI * DI; ++i)
+        q[i] = oracle_e4m3_value(iq[i]);
+    double *k = (double *)malloc(sizeof(double) * (size_t)DI);
+    for (int64_t j = 0; j < n; ++j) {
+        oracle_mx_dequantize(kcodes + rows[j] * (int64_t)(DI / 2), kscales + rows[j] * (int64_t)(DI / 32), 1, DI, k);
+        double acc = 0.0;
+        for (int h = 0; h < HI; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < DI; ++d)
+                dot += q[h * DI + d] * k[d];
+            double relu = dot > 0.0 ? dot : 0.0;
+            acc += (double)w[h] * relu;
+        }
+        out[j] = (float)acc;
+    }
+    free(k);
+    free(q);
+}
+
+/* Projected indexer keys in MXFP4: the exact products of oracle_project_ikeys,
+ * quantised per block of 32 key channels by oracle_mx_quantize. */
+void oracle_project_ikeys_mx(const uint8_t *codes, const uint8_t *scales, int64_t n_rows, int D, const uint16_t *w,
+                             int DI, uint8_t *kcodes, uint8_t *kscales)
+{
+    double *v = (double *)malloc(sizeof(double) * (size_t)D);
+    double *ik = (double *)malloc(sizeof(double) * (size_t)DI);
+    for (int64_t r = 0; r < n_rows; ++r) {
+        oracle_dequantize_rows(codes + r * (D / 2), scales + r * (D / 16), 1, D, v);
+        for (int j = 0; j < DI; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < D; ++c)
+                acc += v[c] * oracle_bf16_value(w[(int64_t)c * DI + j]);
+            ik[j] = acc;
+        }
+        oracle_mx_quantize(ik, 1, DI, kcodes + r * (DI / 2), kscales + r * (DI / 32));
+    }
+    free(ik);
+    free(v);
+}
+
+/* ------------------------------------------------------------------------- */
 /* a3: top-K selection ([FPR] "keep the best 512"; [G2C] "The global branch") */
 /* ------------------------------------------------------------------------- */
 
