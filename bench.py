@@ -212,9 +212,9 @@ def build_state(wl, seed, device):
     from fp4_compressed_sparse_append_b300 import binding as B
     from fp4_compressed_sparse_append_b300 import workloads as W
 
-    cache = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=device)
+    cache = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=device, key_format=wl.key_format)
     lat = torch.empty((wl.B, wl.L, wl.D), dtype=torch.int16, device=device)
-    ik = torch.empty((wl.B, wl.L, wl.DI), dtype=torch.uint8, device=device)
+    ik = torch.empty((wl.B, wl.L, W.key_bytes(wl)), dtype=torch.uint8, device=device)
     for b in range(wl.B):
         lat[b], ik[b] = W.cache_rows(wl, seed, b, device=device)
     w_ik = W.ikey_projection(wl, seed, device=device) if wl.project else None
@@ -480,11 +480,12 @@ def oracle_sample(wl, seed, max_seconds):
 
     cores = os.cpu_count() or 1
     lat, ik = W.cache_rows(wl, seed, 0, device="cpu")
-    oc = oracle.Cache(1, wl.capacity, wl.D, wl.DI)
+    oc = oracle.Cache(1, wl.capacity, wl.D, wl.DI, key_format=wl.key_format)
     w_ik = W.ikey_projection(wl, seed, device="cpu").numpy() if wl.project else None
+    project = oracle.project_ikeys_mx if wl.key_format == "mxfp4" else oracle.project_ikeys
 
     def keys(rows_bits, given):
-        return oracle.project_ikeys(*oracle.quantize_rows(rows_bits), w_ik) if wl.project else given
+        return project(*oracle.quantize_rows(rows_bits), w_ik) if wl.project else given
 
     oc.append(lat[None].numpy(), keys(lat.numpy(), ik.numpy())[None], threads=cores)
     if wl.n_append:

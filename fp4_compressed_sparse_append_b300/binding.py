@@ -34,10 +34,14 @@ class CsaError(RuntimeError):
         self.status = status
 
 
+CSA_IKEY_E4M3, CSA_IKEY_MXFP4 = 0, 1
+
+
 class csa_cache(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("capacity", ctypes.c_int32), ("d_latent", ctypes.c_int32),
                 ("d_index", ctypes.c_int32), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
-                ("ikeys", ctypes.c_void_p), ("lengths", ctypes.c_void_p)]
+                ("ikeys", ctypes.c_void_p), ("lengths", ctypes.c_void_p), ("ikey_format", ctypes.c_int32),
+                ("iscales", ctypes.c_void_p)]
 
 
 class csa_swa(ctypes.Structure):
@@ -120,18 +124,30 @@ def _stream(stream=None):
 class Cache:
     """A global FP4 cache in device memory (torch tensors), laid out as csa_cache says.
 
-    codes [B, cap, D/2] u8, scales [B, cap, D/16] u8, ikeys [B, cap, DI] u8, lengths [B] i32.
+    codes [B, cap, D/2] u8, scales [B, cap, D/16] u8, lengths [B] i32; indexer keys
+    ikeys [B, cap, DI] u8 (E4M3), or for key_format="mxfp4" ikeys [B, cap, DI/2]
+    (E2M1 codes) and iscales [B, cap, DI/32] (UE8M0 block scales).
     """
 
-    def __init__(self, batch: int, capacity: int, d_latent: int, d_index: int, device="cuda"):
+    def __init__(self, batch: int, capacity: int, d_latent: int, d_index: int, device="cuda",
+                 key_format: str = "e4m3"):
         self.batch, self.capacity, self.d_latent, self.d_index = batch, capacity, d_latent, d_index
+        self.key_format = key_format
+        mx = key_format == "mxfp4"
         dev = torch.device(device)
         self.codes = torch.zeros((batch, capacity, d_latent // 2), dtype=torch.uint8, device=dev)
         self.scales = torch.zeros((batch, capacity, d_latent // 16), dtype=torch.uint8, device=dev)
-        self.ikeys = torch.zeros((batch, capacity, d_index), dtype=torch.uint8, device=dev)
+        self.ikeys = torch.zeros((batch, capacity, d_index // 2 if mx else d_index), dtype=torch.uint8, device=dev)
+        self.iscales = torch.zeros((batch, capacity, d_index // 32), dtype=torch.uint8, device=dev) if mx else None
         self.lengths = torch.zeros((batch,), dtype=torch.int32, device=dev)
         self._struct = csa_cache(batch, capacity, d_latent, d_index, self.codes.data_ptr(),
-                                 self.scales.data_ptr(), self.ikeys.data_ptr(), self.lengths.data_ptr())
+                                 self.scales.data_ptr(), self.ikeys.data_ptr(), self.lengths.data_ptr(),
+                                 CSA_IKEY_MXFP4 if mx else CSA_IKEY_E4M3,
+                                 self.iscales.data_ptr() if mx else None)
+
+    def packed_keys(self) -> torch.Tensor:
+        """MXFP4 keys as packed rows [B, cap, DI/2 + DI/32] (codes then scales)."""
+        return torch.cat([self.ikeys, self.iscales], dim=-1)
 
     @property
     def ref(self):

@@ -43,12 +43,19 @@ csa_status check_cache(const csa_cache *c)
     if (c->d_index <= 0 || c->d_index % 16) return CSA_ERR_INVALID_ARG;
     if (c->d_latent % 128 || c->d_latent > 512) return CSA_ERR_UNSUPPORTED;
     if (c->d_index != 32 && c->d_index != 64 && c->d_index != 128) return CSA_ERR_UNSUPPORTED;
+    if (c->ikey_format != CSA_IKEY_E4M3 && c->ikey_format != CSA_IKEY_MXFP4) return CSA_ERR_INVALID_ARG;
+    if (c->ikey_format == CSA_IKEY_MXFP4) {
+        if (!c->iscales || !aligned16(c->iscales)) return CSA_ERR_INVALID_ARG;
+        if (c->d_index != 128 || c->capacity % 4) return CSA_ERR_UNSUPPORTED;
+    }
     return CSA_OK;
 }
 
 csa::CacheView view(const csa_cache *c)
 {
-    return csa::CacheView{c->batch, c->capacity, c->d_latent, c->d_index, c->codes, c->scales, c->ikeys, c->lengths};
+    return csa::CacheView{c->batch,  c->capacity, c->d_latent, c->d_index,
+                          c->codes,  c->scales,   c->ikeys,    c->lengths,
+                          c->ikey_format == CSA_IKEY_MXFP4 ? 1 : 0, c->iscales};
 }
 
 csa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }

@@ -14,6 +14,8 @@ struct CacheView {
     int B, cap, D, DI;
     uint8_t *codes, *scales, *ikeys;
     int32_t *lengths;
+    int mx;            // MXFP4 indexer keys: ikeys holds DI/2 code bytes per row, iscales DI/32
+    uint8_t *iscales;
 };
 
 // a1

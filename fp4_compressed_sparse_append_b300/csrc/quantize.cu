@@ -89,7 +89,21 @@ __global__ void __launch_bounds__(256) quantize_append_kernel(CacheView c, const
         *reinterpret_cast<uint32_t *>(c.codes + row * (c.D / 2) + h * 4) = packed;
         if ((h & 1) == 0) c.scales[row * (c.D / 16) + h / 2] = static_cast<uint8_t>(sbyte);
     }
-    if (ikeys_new) {
+    if (ikeys_new && c.mx) {
+        // packed MXFP4 rows (codes then scales), 4-byte words: DI/8 of codes, DI/128 of scales
+        const int64_t wpr = c.DI / 8 + c.DI / 128;
+        const int64_t total_k = static_cast<int64_t>(n_new) * wpr;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_k;
+             i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            const int64_t j = i / wpr, k = i % wpr;
+            const uint32_t x = *reinterpret_cast<const uint32_t *>(ikeys_new + (static_cast<int64_t>(b) * n_new + j) *
+                                                                                   (wpr * 4) + k * 4);
+            if (k < c.DI / 8)
+                *reinterpret_cast<uint32_t *>(c.ikeys + (base_row + j) * (c.DI / 2) + k * 4) = x;
+            else
+                *reinterpret_cast<uint32_t *>(c.iscales + (base_row + j) * (c.DI / 32) + (k - c.DI / 8) * 4) = x;
+        }
+    } else if (ikeys_new) {
         const int64_t vec_per_row = c.DI / 16;
         const int64_t total_k = static_cast<int64_t>(n_new) * vec_per_row;
         for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_k;
@@ -208,13 +222,33 @@ __global__ void __launch_bounds__(kProjThreads) project_ikeys_kernel(CacheView c
         *reinterpret_cast<float4 *>(part + (ks * kProjRows + rh * 4 + r) * kProjCols + jg * 4) =
             make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
     __syncthreads();
+    // One warp per row (nr * 32 <= kProjThreads): lane j sums key channel col0 + j.
     for (int i = tid; i < nr * kProjCols; i += kProjThreads) {
         const int r = i / kProjCols, j = i - r * kProjCols;
         float sum = 0.f;
 #pragma unroll
         for (int q = 0; q < kProjSlices; ++q) sum += part[(q * kProjRows + r) * kProjCols + j];
-        c.ikeys[(row0 + r) * DI + col0 + j] =
-            static_cast<uint8_t>(__nv_cvt_float_to_fp8(sum, __NV_SATFINITE, __NV_E4M3));
+        if (!c.mx) {
+            c.ikeys[(row0 + r) * DI + col0 + j] =
+                static_cast<uint8_t>(__nv_cvt_float_to_fp8(sum, __NV_SATFINITE, __NV_E4M3));
+            continue;
+        }
+        // MXFP4: the 32 channels of this CTA are one block.  X = floor(log2
+        // amax) - 2 clamped to [-8, 6] (amax's exponent field; -8 for zero or
+        // a subnormal), codes from |sum| * 2^-X (exact) against the E2M1
+        // midpoints, ties to the even code, 6 beyond.
+        float amax = fabsf(sum);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+        const int X = ex == 0 ? -8 : min(6, max(-8, ex - 127 - 2));
+        const float q = fabsf(sum) * __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
+        const uint32_t code = ((q > 0.25f) + (q >= 0.75f) + (q > 1.25f) + (q >= 1.75f) + (q > 2.5f) + (q >= 3.5f) +
+                               (q > 5.0f)) |
+                              (__float_as_uint(sum) >> 28 & 0x8u);
+        const uint32_t pair = code | (__shfl_down_sync(0xFFFFFFFFu, code, 1) << 4);
+        if ((j & 1) == 0) c.ikeys[(row0 + r) * (DI / 2) + (col0 + j) / 2] = static_cast<uint8_t>(pair);
+        if (j == 0) c.iscales[(row0 + r) * (DI / 32) + col0 / 32] = static_cast<uint8_t>(X + 127);
     }
 }
 

@@ -26,6 +26,8 @@ chain_128k         32  131072    64  512  64  128  2048  1  Full, 3x Reindex, 4x
 hier_1m            1   1048576   64  512  64  128  2048  1  Full+pool, 7x Reindex(pool)
 verify_append_32k  64  32768     64  512  64  128  2048  6  append 6 rows, then Full
 full_64k_swa       8   65536     64  512  64  128  2048  1  Full + 128-row local window
+full_64k_mx        8   65536     64  512  64  128  2048  1  Full, MXFP4 indexer keys (68 B)
+chain_128k_mx      32  131072    64  512  64  128  2048  1  as chain_128k, MXFP4 indexer keys
 verify_project_32k 64  32768     64  512  64  128  2048  6  as verify_append_32k, keys projected
 =================  ==  ========  ==  ===  ==  ===  ====  =  =========================
 """
@@ -62,6 +64,7 @@ class Workload:
     n_append: int = 0       # rows appended (quantised) at the start of the step
     window: int = 0         # >0: every query also attends to this many local FP8 rows
     project: bool = False   # indexer keys projected from the stored rows by a seeded [D][DI] matrix
+    key_format: str = "e4m3"  # "mxfp4": E2M1 codes + one UE8M0 scale per 32 key channels (d_index 128)
 
     @property
     def capacity(self) -> int:
@@ -93,10 +96,15 @@ WORKLOADS: Dict[str, Workload] = {
                              outlier_channels=5, window=128),
     "verify_project_32k": Workload("verify_project_32k", B=64, L=32768, H=64, D=512, HI=64,
                                    DI=128, K=2048, P=6, n_append=6, project=True),
+    "full_64k_mx": Workload("full_64k_mx", B=8, L=65536, H=64, D=512, HI=64, DI=128, K=2048,
+                            outlier_channels=5, key_format="mxfp4"),
+    "chain_128k_mx": Workload("chain_128k_mx", B=32, L=131072, H=64, D=512, HI=64, DI=128, K=2048,
+                              layers=(FULL, REINDEX, REINDEX, REINDEX, REUSE, REUSE, REUSE, REUSE),
+                              key_format="mxfp4"),
 }
 
 # Tensor tags for the per-tensor streams.
-_T_LATENT, _T_IKEY, _T_Q, _T_IQ, _T_W, _T_NEWROW, _T_NEWIKEY, _T_OUTLIER, _T_PLANT, _T_LOCAL, _T_WIK = range(11)
+_T_LATENT, _T_IKEY, _T_Q, _T_IQ, _T_W, _T_NEWROW, _T_NEWIKEY, _T_OUTLIER, _T_PLANT, _T_LOCAL, _T_WIK, _T_MXKEY = range(12)
 
 
 def _mix(*vals: int) -> int:
@@ -184,7 +192,10 @@ def cache_rows(wl: Workload, seed: int, b: int, device="cpu",
                 ik[p0 - c0:p1 - c0] = c_ik + 0.25 * z_ik
         s0, s1 = max(r0, c0) - c0, min(r1, c1) - c0
         lat_parts.append(to_bf16_bits(lat[s0:s1]))
-        ik_parts.append(to_e4m3_bytes(ik[s0:s1]))
+        if wl.key_format == "mxfp4":
+            ik_parts.append(random_mx_keys(c1 - c0, wl.DI, device, seed, b, c0)[s0:s1])
+        else:
+            ik_parts.append(to_e4m3_bytes(ik[s0:s1]))
     return torch.cat(lat_parts), torch.cat(ik_parts)
 
 
@@ -209,14 +220,32 @@ def layer_inputs(wl: Workload, seed: int, layer: int, device="cpu") -> Dict[str,
 
 
 def append_rows(wl: Workload, seed: int, device="cpu") -> Dict[str, torch.Tensor]:
-    """Rows appended at the start of the step: bf16 latents [B, n, D], E4M3 ikeys [B, n, DI]."""
+    """Rows appended at the start of the step: bf16 latents [B, n, D], ikeys [B, n, key bytes]."""
     n = wl.n_append
     lat = _randn((wl.B, n, wl.D), device, seed, _T_NEWROW)
     ik = _randn((wl.B, n, wl.DI), device, seed, _T_NEWIKEY)
     out_ch = outlier_channels(wl, seed).to(device)
     if out_ch.numel():
         lat[..., out_ch] *= 8.0
-    return {"rows": to_bf16_bits(lat), "ikeys": to_e4m3_bytes(ik)}
+    if wl.key_format == "mxfp4":
+        keys = random_mx_keys(wl.B * n, wl.DI, device, seed, _T_NEWIKEY).view(wl.B, n, -1)
+    else:
+        keys = to_e4m3_bytes(ik)
+    return {"rows": to_bf16_bits(lat), "ikeys": keys}
+
+
+def key_bytes(wl: Workload) -> int:
+    """Bytes of one indexer key row as the tests and the C ABI's append take it."""
+    return wl.DI // 2 + wl.DI // 32 if wl.key_format == "mxfp4" else wl.DI
+
+
+def random_mx_keys(n: int, DI: int, device, *tag) -> torch.Tensor:
+    """Packed MXFP4 key rows [n, DI/2 + DI/32]: uniform code bytes (every E2M1
+    code), then scale bytes uniform over [119, 133] (block exponents -8..6)."""
+    g = _gen(device, _T_MXKEY, *tag)
+    codes = torch.randint(0, 256, (n, DI // 2), generator=g, device=device, dtype=torch.int32)
+    scales = torch.randint(119, 134, (n, DI // 32), generator=g, device=device, dtype=torch.int32)
+    return torch.cat([codes, scales], dim=1).to(torch.uint8)
 
 
 def ikey_projection(wl: Workload, seed: int, device="cpu") -> torch.Tensor:

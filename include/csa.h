@@ -89,10 +89,27 @@ typedef enum csa_mode { CSA_FULL = 0, CSA_REINDEX = 1, CSA_REUSE = 2 } csa_mode;
  *   codes   : [batch][capacity][d_latent/2]  two E2M1 codes per byte, the even
  *             channel in the low nibble, sign in bit 3 of each nibble
  *   scales  : [batch][capacity][d_latent/16] one E4M3 scale per 16 channels
- *   ikeys   : [batch][capacity][d_index]     FP8 E4M3 indexer key per row
+ *   ikeys   : CSA_IKEY_E4M3:  [batch][capacity][d_index]    FP8 E4M3 indexer key per row
+ *             CSA_IKEY_MXFP4: [batch][capacity][d_index/2]  E2M1 codes of the key
+ *                             (even channel in the low nibble)
+ *   iscales : CSA_IKEY_MXFP4: [batch][capacity][d_index/32] UE8M0 block scales
+ *             (2^(byte - 127) per 32 channels); unused (may be NULL) for E4M3
  *   lengths : [batch] int32                  valid rows per sequence
  * d_latent is 128, 256, 384 or 512; d_index is 32, 64 or 128; capacity >= 1.
+ * MXFP4 keys ("G2C Brief", section "FP4 cache entries, and why they're safe":
+ * 128 values x 4 bits + one 8-bit scale per 32 values = 68 B, the OCP MXFP4
+ * format the pages assume) need d_index = 128 and capacity a multiple of 4.
+ * Their rule, where the library writes them (csa_quantize_append_project): per
+ * block of 32 channels, X = floor(log2 amax) - 2 clamped to [-8, 6] (-8 for an
+ * all-zero block), scale byte X + 127, codes the E2M1 values nearest to
+ * x / 2^X (ties to even, 6 beyond) with the sign of x.  With X in [-8, 6]
+ * every decoded key channel is exactly an E4M3 value; scale bytes outside
+ * [119, 133] written by a caller are read, but their keys are then rounded to
+ * E4M3 (saturating at 448) before scoring.
  */
+#define CSA_IKEY_E4M3 0
+#define CSA_IKEY_MXFP4 1
+
 typedef struct csa_cache {
     int32_t batch;
     int32_t capacity;
@@ -102,13 +119,17 @@ typedef struct csa_cache {
     uint8_t *scales;
     uint8_t *ikeys;
     int32_t *lengths;
+    int32_t ikey_format;          /* CSA_IKEY_E4M3 (0) or CSA_IKEY_MXFP4 */
+    uint8_t *iscales;             /* CSA_IKEY_MXFP4 only */
 } csa_cache;
 
 /*
  * a1: quantise new latent rows to FP4 and append them.
  * ("G2C Brief", section "FP4 cache entries, and why they're safe".)
  *   rows      : [batch][n_new][d_latent] bf16 bits
- *   ikeys_new : [batch][n_new][d_index] E4M3 bytes, or NULL to leave ikeys as is
+ *   ikeys_new : [batch][n_new][d_index] E4M3 bytes (MXFP4 cache: [batch][n_new]
+ *               [d_index/2 + d_index/32], each row's codes then its scales),
+ *               copied as given; or NULL to leave the keys as they are
  * Per 16-channel group: scale = E4M3 round-to-nearest-even(amax / 6), saturating
  * at 448; each channel's code is the E2M1 value nearest to x / scale (ties to
  * the even code, beyond 6 clamped to 6) with the sign of x kept; a group whose
@@ -129,9 +150,10 @@ CSA_API csa_status csa_quantize_append(const csa_cache *cache, const uint16_t *r
  *     ik[j] = E4M3( sum_c v[c] * w_ik[c][j] ),  j < d_index,
  * from its stored entry v = E2M1(code) * E4M3(scale) (exact), summed in fp32
  * and rounded once: nearest, ties to even, saturating at 448 (a zero sum is
- * +0).  The sum's order differs from an exact one, so a key can differ by one
- * code from the exactly rounded product where that product lies within fp32
- * rounding of the midpoint between two E4M3 values.
+ * +0); for an MXFP4 cache each block of 32 sums is quantised by the MXFP4
+ * rule above instead.  The sum's order differs from an exact one, so a key can
+ * differ by one code (or a block by its exponent) from the exactly rounded
+ * product where that product lies within fp32 rounding of a rounding boundary.
  *   w_ik : [d_latent][d_index] bf16 bits, device, 16-byte aligned (read only)
  * d_index must be 32, 64 or 128 (else CSA_ERR_UNSUPPORTED).
  */

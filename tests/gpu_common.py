@@ -30,15 +30,15 @@ def need_gpu():
 def device_cache(wl: W.Workload, seed: int, device="cuda"):
     """Draw the workload's cached rows on the device, quantise-append them through
     the C ABI.  Returns (cache, latents [B, L, D] int16 bits, ikeys [B, L, DI] u8), on the device."""
-    cache = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=device)
+    cache = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=device, key_format=wl.key_format)
     lat = torch.empty((wl.B, wl.L, wl.D), dtype=torch.int16, device=device)
-    ik = torch.empty((wl.B, wl.L, wl.DI), dtype=torch.uint8, device=device)
+    ik = torch.empty((wl.B, wl.L, W.key_bytes(wl)), dtype=torch.uint8, device=device)
     for b in range(wl.B):
         lat[b], ik[b] = W.cache_rows(wl, seed, b, device=device)
     if wl.project:
         # keys projected from the stored rows (the drawn keys are not used)
         B.csa_quantize_append_project(cache, lat, W.ikey_projection(wl, seed, device=device))
-        ik = cache.ikeys[:, : wl.L].clone()
+        ik = None          # the oracle projects its own keys
     else:
         B.csa_quantize_append(cache, lat, ik)
     return cache, lat, ik

@@ -47,17 +47,18 @@ def run_gpu_chain(wl, seed, cache):
 
 def oracle_chain(wl, seed, lat, ik, seqs):
     """Oracle chain for the listed sequences (host copies of the same draws)."""
-    cache = oracle.Cache(len(seqs), wl.capacity, wl.D, wl.DI)
+    cache = oracle.Cache(len(seqs), wl.capacity, wl.D, wl.DI, key_format=wl.key_format)
     w_ik = W.ikey_projection(wl, seed, device="cuda").cpu().numpy() if wl.project else None
+    project = oracle.project_ikeys_mx if wl.key_format == "mxfp4" else oracle.project_ikeys
 
     def keys(rows_bits, given):
         # projected workloads: the oracle projects the keys itself, from its own quantisation
         if not wl.project:
             return given
-        return np.stack([oracle.project_ikeys(*oracle.quantize_rows(r), w_ik) for r in rows_bits])
+        return np.stack([project(*oracle.quantize_rows(r), w_ik) for r in rows_bits])
 
     lat_s = lat[seqs].cpu().numpy()
-    cache.append(lat_s, keys(lat_s, ik[seqs].cpu().numpy()), threads=THREADS)
+    cache.append(lat_s, keys(lat_s, None if ik is None else ik[seqs].cpu().numpy()), threads=THREADS)
     if wl.n_append:
         app = W.append_rows(wl, seed, device="cuda")
         rows_s = app["rows"][seqs].cpu().numpy()
@@ -117,6 +118,10 @@ SMALL = [
                layers=(W.FULL, W.REINDEX, W.REUSE), window=128),
     W.Workload("verify_project_small", B=3, L=3000, H=8, D=256, HI=32, DI=64, K=700, P=6, n_append=6,
                project=True),
+    W.Workload("chain_mx_small", B=2, L=5002, H=16, D=256, HI=16, DI=128, K=300, P=2, n_append=2,
+               layers=(W.FULL, W.REINDEX, W.REUSE), key_format="mxfp4"),
+    W.Workload("hier_mx_small", B=1, L=40000, H=64, D=512, HI=64, DI=128, K=512,
+               layers=(W.FULL, W.REINDEX, W.REINDEX, W.REUSE), pool_blocks=128, key_format="mxfp4"),
 ]
 
 
@@ -136,7 +141,7 @@ def test_small_workloads_every_query(wl):
 
 
 FULL_SIZE = [("full_64k", [0, 5]), ("chain_128k", [17]), ("hier_1m", [0]), ("verify_append_32k", [40]),
-             ("full_64k_swa", [3]), ("verify_project_32k", [11])]
+             ("full_64k_swa", [3]), ("verify_project_32k", [11]), ("full_64k_mx", [2]), ("chain_128k_mx", [9])]
 
 
 @pytest.mark.slow
