@@ -53,6 +53,7 @@ def step_bytes(wl):
     from fp4_compressed_sparse_append_b300 import workloads as W
     units = wl.B * wl.P
     row = wl.D // 2 + wl.D // 16
+    kb = W.key_bytes(wl)                      # stored bytes of one indexer key
     L = wl.length_after_append
     total, index_bytes = 0, 0
     pool_built = False
@@ -61,10 +62,10 @@ def step_bytes(wl):
         if mode != W.REUSE:
             q += units * wl.HI * (wl.DI + 4)
             if mode == W.REINDEX and wl.pool_blocks and pool_built:
-                keys = units * wl.pool_blocks * 8 * wl.DI
+                keys = units * wl.pool_blocks * 8 * kb
             else:
                 # P positions of a sequence share one scan of the keys
-                keys = wl.B * L * wl.DI
+                keys = wl.B * L * kb
             total += keys
             index_bytes = max(index_bytes, keys + units * wl.HI * (wl.DI + 4))
             if mode == W.FULL and wl.pool_blocks:
@@ -74,7 +75,10 @@ def step_bytes(wl):
             # the local FP8 rows of each sequence's windows (positions share rows)
             total += wl.B * (wl.window + wl.P - 1) * wl.D
     if wl.n_append:
-        total += wl.B * wl.n_append * (wl.D * 2 + wl.DI + row + wl.DI)
+        # bf16 rows in, FP4 rows and keys out; given keys are read, projected ones are not
+        total += wl.B * wl.n_append * (wl.D * 2 + (0 if wl.project else kb) + row + kb)
+        if wl.project:
+            total += wl.D * wl.DI * 2                 # the projection matrix, once
     return total, index_bytes
 
 
@@ -539,7 +543,9 @@ def config_of(wl):
             "d_latent": wl.D, "indexer_heads": wl.HI, "indexer_dim": wl.DI, "top_k": wl.K,
             "layers": "".join({W.FULL: "F", W.REINDEX: "X", W.REUSE: "R"}[m] for m in wl.layers),
             "pool_blocks": wl.pool_blocks, "appended_rows": wl.n_append,
-            "kv_format": "E2M1 codes + E4M3 scale per 16 channels; FP8 E4M3 indexer keys",
+            "kv_format": "E2M1 codes + E4M3 scale per 16 channels; " + (
+                "MXFP4 indexer keys (E2M1 codes + UE8M0 scale per 32 channels)" if wl.key_format == "mxfp4"
+                else "FP8 E4M3 indexer keys"),
             "l2": "flushed between timed steps (a 256 MiB read outside the timed events)"}
 
 

@@ -45,7 +45,9 @@ csa_status check_cache(const csa_cache *c)
     if (c->d_index != 32 && c->d_index != 64 && c->d_index != 128) return CSA_ERR_UNSUPPORTED;
     if (c->ikey_format != CSA_IKEY_E4M3 && c->ikey_format != CSA_IKEY_MXFP4) return CSA_ERR_INVALID_ARG;
     if (c->ikey_format == CSA_IKEY_MXFP4) {
-        if (!c->iscales || !aligned16(c->iscales)) return CSA_ERR_INVALID_ARG;
+        // the packed key copy reads from a 32-byte-aligned base
+        if (!c->iscales || !aligned16(c->iscales) || (reinterpret_cast<uintptr_t>(c->ikeys) & 31u))
+            return CSA_ERR_INVALID_ARG;
         if (c->d_index != 128 || c->capacity % 4) return CSA_ERR_UNSUPPORTED;
     }
     return CSA_OK;
@@ -407,13 +409,15 @@ std::atomic<uint64_t> &launch_counter()
 
 void count_launch(int n) { launch_counter() += static_cast<uint64_t>(n); }
 
-CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
-                                 uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle)
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn()
 {
-    using Fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                            const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                            CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    static Fn fn = nullptr;
+    static EncodeFn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
         void *p = nullptr;
@@ -421,8 +425,17 @@ CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t in
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<Fn>(p);
+            fn = reinterpret_cast<EncodeFn>(p);
     });
+    return fn;
+}
+
+}  // namespace
+
+CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                                 uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle)
+{
+    const EncodeFn fn = encode_fn();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
     const cuuint64_t dims[2] = {inner_bytes, rows};
     const cuuint64_t strides[1] = {inner_bytes};
@@ -430,6 +443,19 @@ CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t in
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tensor_map_2d_packed4(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows)
+{
+    const EncodeFn fn = encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {128, rows};  // in 4-bit values
+    const cuuint64_t strides[1] = {64};      // bytes per row
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 

@@ -85,5 +85,10 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
                                  uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// Rows of 128 packed 4-bit values (64 bytes): a box of box_rows rows lands in
+// shared memory as 128-byte rows, each 16-byte chunk holding 8 code bytes then
+// 8 untouched bytes, with the 128-byte swizzle; the copy completes 64 bytes a
+// row on its barrier.  base must be 32-byte aligned.
+CUresult encode_tensor_map_2d_packed4(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows);
 
 }  // namespace csa

@@ -43,19 +43,24 @@ namespace {
 constexpr int kTileRows = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-// MXFP4 keys: four warps expand each staged key tile (E2M1 codes and one
-// UE8M0 scale per 32 channels, 68 B a key) into E4M3 bytes in the layout the
-// MMA reads (128 B a key), exactly: with block exponents in [-8, 6] every
-// 2^X * E2M1 value is an E4M3 value.  They take the place of the second
-// epilogue group, so the CTA keeps 320 threads and two CTAs fit an SM.
+// MXFP4 keys (E2M1 codes and one UE8M0 scale per 32 channels, 68 B a key)
+// go to the tensor core as they are stored: the TMA reads each key's 64 code
+// bytes and writes them 8 bytes to every 16 (the padded 4-bit operand layout),
+// and the MMA is the block-scaled kind::mxf8f6f4 with an E2M1 A operand and
+// the E4M3 queries as B.  Four scale warps copy each tile's block scales from
+// shared memory to tensor memory (row r at lane r, one 32-bit word holding its
+// four block exponents; the instruction descriptor picks the byte of each
+// 32-channel step), where the MMA applies them.  They take the place of the
+// second epilogue group, so the CTA keeps 320 threads and two CTAs fit an SM.
 constexpr int kEpiWarpsMx = 4;
-constexpr int kCvtWarp0 = 2 + kEpiWarpsMx;
-constexpr int kCvtThreads = 128;  // thread = row of a 128-row tile
-constexpr int kMxAbuf = 2;        // expanded (E4M3) tile buffers between the converters and the MMA
-static_assert(2 + kEpiWarpsMx + kCvtThreads / 32 == kThreads / 32, "same block size as the E4M3 variant");
+constexpr int kSclWarp0 = 2 + kEpiWarpsMx;
+constexpr int kSclThreads = 128;  // thread = row of a 128-row tile
+static_assert(2 + kEpiWarpsMx + kSclThreads / 32 == kThreads / 32, "same block size as the E4M3 variant");
 constexpr int kMxCodeRow = 64;    // E2M1 code bytes per key (d_index 128)
 constexpr int kMxScaleRow = 4;    // UE8M0 scale bytes per key
 constexpr int kMxPoolScaleSlot = 128;  // pool: each 8-key block's 32 scale bytes in a 128-byte-aligned TMA slot
+constexpr int kSfbCols = 16;      // tensor-memory columns of the queries' block scales (all 2^0)
+constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;  // four UE8M0 bytes of 2^0
 constexpr int kMaxStages = 8;
 constexpr int kMaxCols = 512;
 constexpr int kMaxAcc = 8;
@@ -77,8 +82,10 @@ struct IdxArgs {
     int b_rows, b_loads, b_box_rows;
     uint32_t tmem_cols;
     int prefix_smem; // units <= kMaxUnitsSmem: per-unit job counts prefix-summed in shared memory
-    int mx;          // MXFP4 keys (staged, then expanded by the converter warps)
+    int mx;          // MXFP4 keys (block-scaled MMA)
     int mx_scale_stage;  // staged scale bytes per stage: mt*128*4, or 16 slots of 128 for a pool
+    int sfa_col;     // MXFP4: tensor-memory column of the keys' scales, 4 columns per (stage, tile)
+    int sfb_col;     // MXFP4: tensor-memory column of the queries' scales (kSfbCols columns)
     const int32_t *lengths;
     const int32_t *pool;
     int pool_blocks;
@@ -229,29 +236,31 @@ __device__ __forceinline__ float weighted_relu_sum_any(uint32_t taddr, int col, 
     return s;
 }
 
-// Expands 8 E2M1 codes (channel k in nibble k) to 8 E4M3 bytes: magnitude by
-// byte permute from the block's 8-entry table (lut_lo: codes 0..3, lut_hi:
-// 4..7), sign bit 3 of each nibble to bit 7 of its byte (the code bytes
-// doubled by a byte permute put nibbles 1 and 3's sign bits in place and
-// nibbles 0 and 2's four bits low).
-__device__ __forceinline__ uint32_t mx_sign_bytes(uint32_t x16)
+// The block-scaled MMA: D (+)= (A * 2^scale_A) * (B * 2^scale_B)^T over one
+// 32-channel step; the scale words sit in tensor memory, the descriptor's
+// scale ids (bits 29-30 for A, 4-5 for B) pick their byte.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
-    const uint32_t z = __byte_perm(x16, 0u, 0x1100u);  // bytes b0, b0, b1, b1 of the codes
-    return ((z << 4) & 0x00800080u) | (z & 0x80008000u);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
 }
 
-__device__ __forceinline__ uint2 mx_expand8(uint32_t w, uint32_t lut_lo, uint32_t lut_hi)
+// Instruction descriptor of the block-scaled MMA: A E2M1 (5), B E4M3 (0),
+// both K-major, UE8M0 scales (bit 23), fp32 accumulation implied.
+__host__ __device__ constexpr uint32_t instr_desc_mx(uint32_t M, uint32_t N)
 {
-    const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-    return make_uint2(__byte_perm(lut_lo, lut_hi, lo & 0x7777u) | mx_sign_bytes(lo),
-                      __byte_perm(lut_lo, lut_hi, hi & 0x7777u) | mx_sign_bytes(hi));
+    return (5u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
 }
 
-// E4M3 byte of E2M1 magnitude m times 2^X (exact for X in [-8, 6]; else rounded, saturating).
-__device__ __forceinline__ uint32_t mx_mag_byte(int m, int X)
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v)
 {
-    const float g = m < 4 ? 0.5f * m : (m == 4 ? 2.f : (m == 5 ? 3.f : (m == 6 ? 4.f : 6.f)));
-    return static_cast<uint32_t>(__nv_cvt_float_to_fp8(ldexpf(g, X), __NV_SATFINITE, __NV_E4M3));
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%1,%1,%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
 template <bool MX>
@@ -266,17 +275,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *base = smem_raw + ((1024 - (raw & 1023)) & 1023);
     const int tile_bytes = kTileRows * a.DI;
     const int stage_bytes = a.mt * tile_bytes;
-    uint8_t *a_smem = base;
-    // MXFP4: per stage, the staged codes [mt][128][64] (64-byte swizzle) and
-    // scales [mt][128][4] ahead of the expansion into a_smem.
-    // E4M3: one operand buffer per stage.  MXFP4: the stages hold the packed
-    // keys only, and kMxAbuf operand buffers sit between the converters and the
-    // MMA, so that the key stream keeps many compact stages in flight.
-    uint8_t *stg_codes = a_smem + (MX ? kMxAbuf : a.stages) * stage_bytes;
-    uint8_t *stg_scales = stg_codes + (MX ? a.stages * a.mt * kTileRows * kMxCodeRow : 0);
-    const int stg_bytes =
-        MX ? (a.stages * (a.mt * kTileRows * kMxCodeRow + a.mx_scale_stage) + 1023) & ~1023 : 0;
-    uint8_t *b_smem = stg_codes + stg_bytes;
+    uint8_t *a_smem = base;  // [stages][mt][128 rows][DI bytes] key tiles (MXFP4: padded 4-bit codes)
+    // MXFP4: each stage's block scales, [mt][128][4] (or 16 pool slots of 128 bytes).
+    uint8_t *stg_scales = a_smem + a.stages * stage_bytes;
+    const int stg_bytes = MX ? (a.stages * a.mx_scale_stage + 1023) & ~1023 : 0;
+    uint8_t *b_smem = stg_scales + stg_bytes;
     constexpr int EW = MX ? kEpiWarpsMx : kEpiWarps;  // epilogue warps (groups of four)
     float *w_smem = reinterpret_cast<float *>(b_smem + ((a.b_rows * a.DI + 1023) & ~1023));  // [EW][n_pad]
     const int n_pad = (a.n_real + 3) & ~3;
@@ -288,10 +291,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *tfull = bempty + 1;                // [kMaxAcc]
     uint64_t *tempty = tfull + kMaxAcc;          // [kMaxAcc]
     uint64_t *mma_done = tempty + kMaxAcc;
-    uint64_t *afull = mma_done + 1;              // [kMxAbuf] MXFP4: operand buffer expanded
-    uint64_t *aempty = afull + kMxAbuf;          // [kMxAbuf] MXFP4: operand buffer read by the MMA
-    uint32_t *mx_lut = reinterpret_cast<uint32_t *>(aempty + kMxAbuf + 4);  // [15][2] E4M3 bytes, X = -8..6
-    uint32_t *tmem_slot = mx_lut + 30;
+    uint64_t *sready = mma_done + 1;             // [kMaxStages] MXFP4: the stage's scales are in tensor memory
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sready + kMaxStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *prefix = const_cast<int *>(reinterpret_cast<volatile int *>(tmem_slot + 2));  // [units + 1]
 
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], MX ? kCvtThreads : 1);  // MXFP4: freed by the converters
+            mbar_init(&empty[s], 1);
+            if (MX) mbar_init(&sready[s], kSclThreads);
         }
         mbar_init(bfull, 1);
         mbar_init(bempty, 1);
@@ -308,19 +310,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&tempty[i], (a.mt > 1 || EW == 4) ? 32 * EW : 32 * (EW / 2));
         }
         mbar_init(mma_done, 1);
-        if (MX)
-            for (int i = 0; i < kMxAbuf; ++i) {
-                mbar_init(&afull[i], kCvtThreads);
-                mbar_init(&aempty[i], 1);
-            }
         *abort_flag = 0;
         fence_mbar_init();
-    }
-    if (MX && threadIdx.x < 30) {
-        // table of the 15 in-range block exponents: word 2i (codes 0..3) and 2i+1 (4..7) of X = i - 8
-        const int X = threadIdx.x / 2 - 8, m0 = (threadIdx.x & 1) * 4;
-        mx_lut[threadIdx.x] = mx_mag_byte(m0, X) | (mx_mag_byte(m0 + 1, X) << 8) | (mx_mag_byte(m0 + 2, X) << 16) |
-                              (mx_mag_byte(m0 + 3, X) << 24);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, a.tmem_cols);
@@ -389,14 +380,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
                 uint8_t *dst = a_smem + stage * stage_bytes;
                 if (!a.pool_mode && MX) {
-                    // codes and scales of mt tiles; the scales as 16-byte rows of 4 keys
-                    uint8_t *dc = stg_codes + stage * a.mt * kTileRows * kMxCodeRow;
+                    // codes of mt tiles, padded to the MMA's layout by the copy
+                    // (which counts the bytes it reads: 64 a key), and their
+                    // scales as 16-byte rows of 4 keys
                     uint8_t *ds = stg_scales + stage * a.mx_scale_stage;
                     mbar_arrive_expect_tx(&full[stage],
                                           static_cast<uint32_t>(a.mt * kTileRows * (kMxCodeRow + kMxScaleRow)));
                     const int row0 = it.u * a.cap + it.job * a.mt * kTileRows;
                     for (int m = 0; m < a.mt; ++m) {
-                        tma_load_2d(dc + m * kTileRows * kMxCodeRow, &keys128, &full[stage], 0, row0 + m * kTileRows);
+                        tma_load_2d(dst + m * tile_bytes, &keys128, &full[stage], 0, row0 + m * kTileRows);
                         tma_load_2d(ds + m * kTileRows * kMxScaleRow, &scl128, &full[stage], 0,
                                     (row0 + m * kTileRows) / 4);
                     }
@@ -422,14 +414,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                             blk[k] = -1;
                     }
                     if (MX) {
-                        uint8_t *dc = stg_codes + stage * a.mt * kTileRows * kMxCodeRow;
                         uint8_t *ds = stg_scales + stage * a.mx_scale_stage;
                         mbar_arrive_expect_tx(&full[stage],
                                               static_cast<uint32_t>(nv * kPoolBlock * (kMxCodeRow + kMxScaleRow)));
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
                             if (blk[k] >= 0) {
-                                tma_load_2d(dc + k * kPoolBlock * kMxCodeRow, &keys8, &full[stage], 0,
+                                tma_load_2d(dst + k * kPoolBlock * a.DI, &keys8, &full[stage], 0,
                                             b * a.cap + blk[k] * kPoolBlock);
                                 tma_load_2d(ds + k * kMxPoolScaleSlot, &scl8, &full[stage], 0,
                                             (b * a.cap + blk[k] * kPoolBlock) / 4);
@@ -470,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // low 14 bits (in 16-byte units), so offsets are added in place.
             const uint64_t da0 = smem_desc(smem_u32(a_smem), 16, sbo, sw);
             const uint64_t db0 = smem_desc(smem_u32(b_smem), 16, sbo, sw);
-            const uint32_t idesc = instr_desc(128, a.sub_cols, 0, 0, 0, 0);
+            const uint32_t idesc = MX ? instr_desc_mx(128, a.sub_cols) : instr_desc(128, a.sub_cols, 0, 0, 0, 0);
             const int slot_cols = a.mt * a.sub_cols;
             const int ksteps = a.DI / 32;
             JobIter it;
@@ -485,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bphase ^= 1;
                     cur = it.u;
                 }
-                // MXFP4: `stage` and `phase` walk the kMxAbuf operand buffers.
-                if (!mbar_wait(MX ? &afull[stage] : &full[stage], phase, abort_flag)) break;
+                if (!mbar_wait(&full[stage], phase, abort_flag)) break;
+                if (MX && !mbar_wait(&sready[stage], phase, abort_flag)) break;
                 const uint64_t da_stage = da0 + static_cast<uint64_t>((stage * stage_bytes) >> 4);
                 for (int sub = 0; sub < a.n_sub; ++sub) {
                     if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
@@ -498,8 +489,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint32_t d_slot = tmem + acc * slot_cols;
                     for (int m = 0; m < a.mt; ++m) {
                         const uint64_t da_m = da_stage + static_cast<uint64_t>((m * tile_bytes) >> 4);
-                        for (int k = 0; k < ksteps; ++k)
-                            mma_f8f6f4(d_slot + m * a.sub_cols, da_m + 2 * k, db_sub + 2 * k, idesc, k > 0 ? 1u : 0u);
+                        if (MX) {
+                            const uint32_t sfa = tmem + a.sfa_col + (stage * a.mt + m) * 4;
+                            for (uint32_t k = 0; k < static_cast<uint32_t>(ksteps); ++k)
+                                mma_mxf8f6f4(d_slot + m * a.sub_cols, da_m + 2 * k, db_sub + 2 * k,
+                                             idesc | (k << 29) | (k << 4), sfa, tmem + a.sfb_col, k > 0 ? 1u : 0u);
+                        } else {
+                            for (int k = 0; k < ksteps; ++k)
+                                mma_f8f6f4(d_slot + m * a.sub_cols, da_m + 2 * k, db_sub + 2 * k, idesc,
+                                           k > 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&tfull[acc]);
                     if (++acc == a.n_acc) {
@@ -508,12 +507,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
                 if (!ok) break;
-                mma_commit(MX ? &aempty[stage] : &empty[stage]);
+                mma_commit(&empty[stage]);
                 JobIter nx = it;
                 jobs.next(nx);
                 if (j + 1 == j1 || nx.u != it.u) mma_commit(bempty);
                 it = nx;
-                if (++stage == (MX ? kMxAbuf : a.stages)) {
+                if (++stage == a.stages) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -525,63 +524,36 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
         __syncwarp();
-    } else if (MX && warp >= kCvtWarp0) {
-        // ------------------------------------------------------------- MXFP4 expansion
-        // Thread ct owns row ct of every 128-row tile: its 64 code bytes (four
-        // 16-byte chunks, 64-byte swizzle: chunk c at c ^ ((row >> 1) & 3)) and
-        // 4 scale bytes become 128 E4M3 bytes at the MMA layout (128-byte
-        // swizzle: chunk c at c ^ (row & 7)).  Pool tiles (16 boxes of 8 rows)
-        // have the same row layout; rows of skipped pool blocks hold stale
-        // bytes whose scores are never used.
-        const int ct = threadIdx.x - 32 * kCvtWarp0;
-        int stage = 0, ab = 0;
-        uint32_t phase = 0, aphase = 0;
+    } else if (MX && warp >= kSclWarp0) {
+        // ------------------------------------------------------------- MXFP4 block scales
+        // The warp of lane quarter q copies the scale word of rows 32q..32q+31
+        // of each staged tile to tensor-memory lanes 32q..32q+31 (the same
+        // word in the tile's four columns), after the queries' unit scales.
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        for (int c = 0; c < kSfbCols; c += 4) tmem_st4(tl + a.sfb_col + c, kUnitScales);
+        int stage = 0;
+        uint32_t phase = 0;
         for (int64_t j = j0; j < j1; ++j) {
             if (!mbar_wait(&full[stage], phase, abort_flag)) break;
-            if (!mbar_wait(&aempty[ab], aphase ^ 1, abort_flag)) break;
-            const uint32_t sc = smem_u32(stg_codes + stage * a.mt * kTileRows * kMxCodeRow);
             const uint8_t *ss = stg_scales + stage * a.mx_scale_stage;
-            const uint32_t dst = smem_u32(a_smem + ab * stage_bytes);
             for (int m = 0; m < a.mt; ++m) {
-                const uint32_t rc = sc + (m * kTileRows + ct) * kMxCodeRow;
-                uint4 cw[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) cw[c] = ld_shared_v4(rc + ((c ^ ((ct >> 1) & 3)) << 4));
-                const uint32_t sw = *reinterpret_cast<const uint32_t *>(
-                    a.pool_mode ? ss + (ct >> 3) * kMxPoolScaleSlot + (ct & 7) * kMxScaleRow
-                                : ss + (m * kTileRows + ct) * kMxScaleRow);
-                const uint32_t rd = dst + m * tile_bytes + (ct >> 3) * 1024 + (ct & 7) * 128;
-#pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    const int X = static_cast<int>((sw >> (8 * blk)) & 0xFFu) - 127;
-                    uint32_t lut_lo, lut_hi;
-                    if (X >= -8 && X <= 6) {
-                        lut_lo = mx_lut[2 * (X + 8)];
-                        lut_hi = mx_lut[2 * (X + 8) + 1];
-                    } else {
-                        lut_lo = mx_mag_byte(0, X) | (mx_mag_byte(1, X) << 8) | (mx_mag_byte(2, X) << 16) |
-                                 (mx_mag_byte(3, X) << 24);
-                        lut_hi = mx_mag_byte(4, X) | (mx_mag_byte(5, X) << 8) | (mx_mag_byte(6, X) << 16) |
-                                 (mx_mag_byte(7, X) << 24);
-                    }
-                    const uint2 e0 = mx_expand8(cw[blk].x, lut_lo, lut_hi), e1 = mx_expand8(cw[blk].y, lut_lo, lut_hi);
-                    const uint2 e2 = mx_expand8(cw[blk].z, lut_lo, lut_hi), e3 = mx_expand8(cw[blk].w, lut_lo, lut_hi);
-                    st_shared_v4(rd + (((2 * blk) ^ (ct & 7)) << 4), make_uint4(e0.x, e0.y, e1.x, e1.y));
-                    st_shared_v4(rd + (((2 * blk + 1) ^ (ct & 7)) << 4), make_uint4(e2.x, e2.y, e3.x, e3.y));
-                }
+                // pool tiles: block row >> 3 in its own 128-byte slot
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(
+                    a.pool_mode ? ss + (row >> 3) * kMxPoolScaleSlot + (row & 7) * kMxScaleRow
+                                : ss + (m * kTileRows + row) * kMxScaleRow);
+                tmem_st4(tl + a.sfa_col + (stage * a.mt + m) * 4, w);
             }
-            fence_async_smem();
-            mbar_arrive(&afull[ab]);
-            mbar_arrive(&empty[stage]);  // the staged keys have been read
-            if (++ab == kMxAbuf) {
-                ab = 0;
-                aphase ^= 1;
-            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&sready[stage]);
             if (++stage == a.stages) {
                 stage = 0;
                 phase ^= 1;
             }
         }
+        tmem_st_wait();
     } else {
         // ------------------------------------------------------------- epilogue
         const int ew = warp - 2;
@@ -684,16 +656,18 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     a.mx = c.mx;
     const int per_sm = 2 * (a.pool_mode ? 1 : 2) * a.sub_cols <= kMaxCols / 2 ? 2 : 1;
     const int cols_cta = kMaxCols / per_sm;
+    // MXFP4: tensor memory also holds the keys' scales (4 columns per tile of
+    // every stage, reserved for kMaxStages) and the queries' unit scales.
+    auto sf_cols = [&](int mt) { return a.mx ? kMaxStages * mt * 4 + kSfbCols : 0; };
     a.mt = 1;
-    // MXFP4: at most 2 tiles a stage, so that four stages (each also staging its
-    // packed keys) keep the expansion overlapped with the key stream.
-    const int max_mt = a.mx ? (per_sm == 2 ? 1 : 2) : kMaxTilesPerJob / per_sm;
-    while (!a.pool_mode && 2 * a.mt <= max_mt && 2 * (2 * a.mt) * a.sub_cols <= cols_cta) a.mt *= 2;
-    a.n_acc = 2;
-    while (2 * a.n_acc <= kMaxAcc && 2 * a.n_acc * a.mt * a.sub_cols <= cols_cta) a.n_acc *= 2;
-    uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(a.n_acc * a.mt * a.sub_cols)) cols *= 2;
-    a.tmem_cols = cols;
+    const int max_mt = kMaxTilesPerJob / per_sm;
+    while (!a.pool_mode && 2 * a.mt <= max_mt && 2 * (2 * a.mt) * a.sub_cols + sf_cols(2 * a.mt) <= cols_cta)
+        a.mt *= 2;
+    // Accumulator slots: a power of two, two or more where they fit (one only
+    // when an MXFP4 cache's scales leave room for a single slot of 256 columns).
+    a.n_acc = 2 * a.mt * a.sub_cols + sf_cols(a.mt) <= cols_cta ? 2 : 1;
+    while (2 * a.n_acc <= kMaxAcc && 2 * a.n_acc * a.mt * a.sub_cols + sf_cols(a.mt) <= cols_cta) a.n_acc *= 2;
+    const int acc_cols = a.n_acc * a.mt * a.sub_cols;
     // Query rows staged per unit: every sub-chunk's MMA reads sub_cols rows.
     const int need_rows = (n_sub - 1) * a.gps * HI + a.sub_cols;
     a.b_loads = (need_rows + 255) / 256;
@@ -712,20 +686,23 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     const size_t b_bytes = (static_cast<size_t>(a.b_rows) * c.DI + 1023) & ~size_t(1023);
     const size_t w_bytes = static_cast<size_t>(a.mx ? kEpiWarpsMx : kEpiWarps) * ((a.n_real + 3) & ~3) * sizeof(float);
     const size_t prefix_bytes = a.prefix_smem ? (static_cast<size_t>(a.units) + 1) * sizeof(int) : 0;
-    const size_t fixed = 1024 /*align*/ + b_bytes + w_bytes + (2 * kMaxStages + 2 * kMaxAcc + 2 * kMxAbuf + 8) * 8 +
-                         30 * 4 + 16 + prefix_bytes + (a.mx ? 1024 : 0) /*staging round-up*/;
+    const size_t fixed = 1024 /*align*/ + b_bytes + w_bytes + (3 * kMaxStages + 2 * kMaxAcc + 4) * 8 + 16 +
+                         prefix_bytes + (a.mx ? 1024 : 0) /*scale staging round-up*/;
     const size_t budget = per_sm == 1 ? 224 * 1024 : 110 * 1024;
-    // MXFP4: each stage also stages its keys' codes and scales before expansion.
+    // MXFP4: each stage also stages its keys' block scales.
     a.mx_scale_stage = a.pool_mode ? 16 * kMxPoolScaleSlot : a.mt * kTileRows * kMxScaleRow;
-    // E4M3: stages of key tiles.  MXFP4: stages of packed keys plus kMxAbuf
-    // fixed operand buffers.
-    const size_t per_stage = a.mx ? static_cast<size_t>(a.mt) * kTileRows * kMxCodeRow + a.mx_scale_stage : stage_bytes;
-    const size_t abuf_bytes = a.mx ? kMxAbuf * stage_bytes : 0;
-    if (budget < fixed + abuf_bytes + 2 * per_stage) return cudaErrorInvalidValue;
-    int stages = static_cast<int>((budget - fixed - abuf_bytes) / per_stage);
+    const size_t per_stage = stage_bytes + (a.mx ? a.mx_scale_stage : 0);
+    if (budget < fixed + 2 * per_stage) return cudaErrorInvalidValue;
+    int stages = static_cast<int>((budget - fixed) / per_stage);
     if (stages > kMaxStages) stages = kMaxStages;
     a.stages = stages;
-    const size_t smem = fixed + abuf_bytes + stages * per_stage;
+    const size_t smem = fixed + stages * per_stage;
+    a.sfa_col = acc_cols;
+    a.sfb_col = acc_cols + stages * a.mt * 4;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(a.mx ? a.sfb_col + kSfbCols : acc_cols)) cols *= 2;
+    if (cols > static_cast<uint32_t>(cols_cta)) return cudaErrorInvalidValue;
+    a.tmem_cols = cols;
 
     const CUtensorMapSwizzle sw = c.DI == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : c.DI == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -736,12 +713,11 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (a.mx) {
-        // codes [rows][64] with the 64-byte swizzle; scales [rows][4] as [rows / 4][16]
+        // codes [rows][128 four-bit values], written 8 bytes to every 16 with
+        // the 128-byte swizzle; scales [rows][4] as [rows / 4][16]
         if (c.DI != 128 || c.cap % 4) return cudaErrorInvalidValue;
-        if (encode_tensor_map_2d_u8(&k128, c.ikeys, kMxCodeRow, rows, kMxCodeRow, kTileRows,
-                                    CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS ||
-            encode_tensor_map_2d_u8(&k8, c.ikeys, kMxCodeRow, rows, kMxCodeRow, kPoolBlock,
-                                    CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS ||
+        if (encode_tensor_map_2d_packed4(&k128, c.ikeys, rows, kTileRows) != CUDA_SUCCESS ||
+            encode_tensor_map_2d_packed4(&k8, c.ikeys, rows, kPoolBlock) != CUDA_SUCCESS ||
             encode_tensor_map_2d_u8(&s128, c.iscales, 16, rows / 4, 16, kTileRows / 4, CU_TENSOR_MAP_SWIZZLE_NONE) !=
                 CUDA_SUCCESS ||
             encode_tensor_map_2d_u8(&s8, c.iscales, 16, rows / 4, 16, kPoolBlock / 4, CU_TENSOR_MAP_SWIZZLE_NONE) !=

@@ -102,10 +102,11 @@ typedef enum csa_mode { CSA_FULL = 0, CSA_REINDEX = 1, CSA_REUSE = 2 } csa_mode;
  * Their rule, where the library writes them (csa_quantize_append_project): per
  * block of 32 channels, X = floor(log2 amax) - 2 clamped to [-8, 6] (-8 for an
  * all-zero block), scale byte X + 127, codes the E2M1 values nearest to
- * x / 2^X (ties to even, 6 beyond) with the sign of x.  With X in [-8, 6]
- * every decoded key channel is exactly an E4M3 value; scale bytes outside
- * [119, 133] written by a caller are read, but their keys are then rounded to
- * E4M3 (saturating at 448) before scoring.
+ * x / 2^X (ties to even, 6 beyond) with the sign of x.  A key given by the
+ * caller may carry any scale byte but 255 (NaN in the OCP format, which gives
+ * unspecified scores): the scan applies 2^(byte - 127) exactly in the tensor
+ * core's block-scaled product, accumulating in fp32.  The ikeys base must be
+ * 32-byte aligned (the scan's 4-bit copy requires it).
  */
 #define CSA_IKEY_E4M3 0
 #define CSA_IKEY_MXFP4 1

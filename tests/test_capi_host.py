@@ -154,3 +154,19 @@ def test_projected_append_checks(lib):
     assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 1        # keys given and projected
     a.ikeys_new = None
     assert lib.csa_layer_workspace_size(c, ctypes.byref(a), ctypes.byref(n)) == 0
+
+
+def test_mxfp4_cache_checks(lib):
+    V = ctypes.c_void_p
+    ok = dict(d_index=128, ikey_format=B.CSA_IKEY_MXFP4, iscales=0x60000)
+    assert lib.csa_quantize_append(ctypes.byref(fake_cache(**ok)), V(0x50000), None, 0, None) == 0
+    bad = [
+        (dict(ok, ikey_format=7), 1),                 # unknown key format
+        (dict(ok, iscales=None), 1),                  # no block scales
+        (dict(ok, iscales=0x60008), 1),               # misaligned scales
+        (dict(ok, ikeys=0x30010), 1),                 # keys 16- but not 32-byte aligned
+        (dict(ok, d_index=64), 2),                    # MXFP4 keys are 128 channels
+        (dict(ok, capacity=62), 2),                   # capacity a multiple of 4
+    ]
+    for kw, want in bad:
+        assert lib.csa_quantize_append(ctypes.byref(fake_cache(**kw)), V(0x50000), None, 0, None) == want, kw

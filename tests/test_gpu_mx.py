@@ -56,6 +56,27 @@ def test_full_scan_scores(HI, P):
             compare(s[b, p, :L], ora, iqh[b, p], wh[b, p], ikh[b, :L], (b, p))
 
 
+def test_scales_outside_the_written_range_apply_exactly():
+    """Block scales the library never writes (bytes 100..150, X = -27..23) are
+    applied as 2^(byte - 127) by the block-scaled MMA, as the oracle decodes them."""
+    need_gpu()
+    Bn, L, DI, HI = 2, 1100, 128, 16
+    wl = W.Workload("t", B=Bn, L=L, H=4, D=128, HI=HI, DI=DI, K=8, key_format="mxfp4")
+    cache = B.Cache(Bn, L, 128, DI, device="cuda", key_format="mxfp4")
+    keys = W.random_mx_keys(Bn * L, DI, "cuda", 77).view(Bn, L, -1)
+    keys[..., DI // 2:] = W.random_ints((Bn, L, DI // 32), 100, 151, seed=78).to(torch.uint8).cuda()
+    B.csa_quantize_append(cache, W.random_bf16_bits((Bn, L, 128), seed=79, device="cuda"), keys)
+    inp = W.layer_inputs(wl, 77, 0, device="cuda")
+    scores = B.csa_index_score(cache, inp["iq"], inp["w"])
+    torch.cuda.synchronize()
+    assert B.csa_device_status() == 0
+    s = scores.cpu().numpy()
+    ikh, iqh, wh = keys.cpu().numpy(), inp["iq"].cpu().numpy(), inp["w"].cpu().numpy()
+    for b in range(Bn):
+        ora = oracle.index_scores_mx(iqh[b, 0], wh[b, 0], ikh[b], np.arange(L))
+        compare(s[b, 0, :L], ora, iqh[b, 0], wh[b, 0], ikh[b], b)
+
+
 def test_pool_scores():
     need_gpu()
     wl = W.Workload("t", B=2, L=2004, H=4, D=128, HI=16, DI=128, K=8, key_format="mxfp4")
