@@ -550,14 +550,14 @@ def config_of(wl):
 
 
 def index_traffic_from_profile(workload):
-    """DRAM bytes per index_score launch from the committed ncu summary of the
-    full_64k step, or None for another workload, or when the kernel's sources
-    have changed since that capture (the summary records the sha256 of the
-    sources it was taken with)."""
+    """DRAM bytes per index_score launch from the committed ncu summary of this
+    workload's step (profiles/index_score_<workload>.md), or None where there
+    is none, or when the kernel's sources have changed since that capture (the
+    summary records the sha256 of the sources it was taken with)."""
     import hashlib
-    if workload != "full_64k":
+    path = os.path.join(ROOT, "profiles", "index_score_%s.md" % workload)
+    if not os.path.exists(path):
         return None, "no ncu capture of this workload"
-    path = os.path.join(ROOT, "profiles", "index_score_full_64k.md")
     csrc = os.path.join(ROOT, "fp4_compressed_sparse_append_b300", "csrc")
     try:
         text = open(path).read()
@@ -573,7 +573,7 @@ def index_traffic_from_profile(workload):
         return None, "no ncu summary"
     if want.group(1) != h.hexdigest():
         return None, "kernel changed since the ncu capture"
-    return int(val.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/index_score_full_64k.md)"
+    return int(val.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/%s)" % os.path.basename(path)
 
 
 def stage_rooflines(wl, stages, index_bytes, peak_hbm, peak_src, peak_tf, peak_tf_src, traffic, traffic_src):

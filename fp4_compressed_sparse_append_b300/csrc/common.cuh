@@ -110,6 +110,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware for up to
+// kSleepHintNs while the phase is incomplete (it wakes when the phase
+// completes), instead of returning at once: a waiting warp then takes no issue
+// slots from the warps that share its scheduler.
+constexpr uint32_t kSleepHintNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kSleepHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Non-blocking test of a phase (for threads that poll several barriers).
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {
@@ -126,13 +145,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 
 // Waits until the barrier's phase with the given parity completes.  Returns
 // false (and raises *abort) when the wait runs past kWaitLimitNs or another
-// thread of the CTA has already raised *abort.
+// thread of the CTA has already raised *abort.  Sleep: the hinted try-wait
+// (mbar_try_wait_sleep) between checks.
+template <bool Sleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (Sleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort = 1;

@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int64_t j = j0; j < j1; ++j, jobs.next(it)) {
                 if (it.u != cur) {
                     if (cur >= 0) {
-                        if (!mbar_wait(bempty, bphase, abort_flag)) break;
+                        if (!mbar_wait<true>(bempty, bphase, abort_flag)) break;
                         bphase ^= 1;
                     }
                     mbar_arrive_expect_tx(bfull, static_cast<uint32_t>(a.b_loads * a.b_box_rows * a.DI));
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     it.u * a.n_real + i * a.b_box_rows);
                     cur = it.u;
                 }
-                if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
+                if (!mbar_wait<true>(&empty[stage], phase ^ 1, abort_flag)) break;
                 uint8_t *dst = a_smem + stage * stage_bytes;
                 if (!a.pool_mode && MX) {
                     // codes of mt tiles, padded to the MMA's layout by the copy
@@ -472,15 +472,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             bool ok = true;
             for (int64_t j = j0; j < j1 && ok; ++j) {
                 if (it.u != cur) {
-                    if (!mbar_wait(bfull, bphase, abort_flag)) break;
+                    if (!mbar_wait<true>(bfull, bphase, abort_flag)) break;
                     bphase ^= 1;
                     cur = it.u;
                 }
-                if (!mbar_wait(&full[stage], phase, abort_flag)) break;
-                if (MX && !mbar_wait(&sready[stage], phase, abort_flag)) break;
+                if (!mbar_wait<true>(&full[stage], phase, abort_flag)) break;
+                if (MX && !mbar_wait<true>(&sready[stage], phase, abort_flag)) break;
                 const uint64_t da_stage = da0 + static_cast<uint64_t>((stage * stage_bytes) >> 4);
                 for (int sub = 0; sub < a.n_sub; ++sub) {
-                    if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
+                    if (!mbar_wait<true>(&tempty[acc], acc_phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         int stage = 0;
         uint32_t phase = 0;
         for (int64_t j = j0; j < j1; ++j) {
-            if (!mbar_wait(&full[stage], phase, abort_flag)) break;
+            if (!mbar_wait<true>(&full[stage], phase, abort_flag)) break;
             const uint8_t *ss = stg_scales + stage * a.mx_scale_stage;
             for (int m = 0; m < a.mt; ++m) {
                 // pool tiles: block row >> 3 in its own 128-byte slot
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (ngrp > 1 && !split_tiles && static_cast<int>(seq & 1u) != grp) continue;
                 const int acc = static_cast<int>(seq & static_cast<uint32_t>(a.n_acc - 1));
                 const uint32_t par = (seq / static_cast<uint32_t>(a.n_acc)) & 1u;
-                if (!mbar_wait(&tfull[acc], par, abort_flag)) {
+                if (!mbar_wait<true>(&tfull[acc], par, abort_flag)) {
                     ok = false;
                     break;
                 }
