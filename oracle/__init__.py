@@ -92,6 +92,14 @@ def lib():
         L.oracle_project_ikeys.restype = None
         L.oracle_e4m3_round.argtypes = [dbl]
         L.oracle_e4m3_round.restype = ctypes.c_uint8
+        L.oracle_record_bytes.argtypes = [i32, i32, i32]
+        L.oracle_record_bytes.restype = i64
+        L.oracle_bytes_per_token.argtypes = [P, P, i32]
+        L.oracle_bytes_per_token.restype = dbl
+        L.oracle_cache_spill.argtypes = [P, P, P, i32, i64, i32, i32, i32, P, i64, i64, P]
+        L.oracle_cache_spill.restype = None
+        L.oracle_cache_reload.argtypes = [P, P, P, i32, i64, i32, i32, i32, P, P, i64]
+        L.oracle_cache_reload.restype = ctypes.c_int
         for f in (L.oracle_quantize_rows, L.oracle_dequantize_rows, L.oracle_index_score,
                   L.oracle_topk, L.oracle_block_max, L.oracle_attend):
             f.restype = None
@@ -285,6 +293,49 @@ class Cache:
             self.scales[b, l0:l0 + n] = scales[b]
             self.ikeys[b, l0:l0 + n] = ik[b]
             self.lengths[b] = l0 + n
+
+
+# --------------------------------------------------------------------------
+# next: persistent cache records ("G2C Brief", section "FP4 cache entries, and
+# why they're safe", the derivation of the 890 bytes per token)
+# --------------------------------------------------------------------------
+
+def record_bytes(D: int, DI: int, key_format: str = "e4m3") -> int:
+    """Bytes of one cache entry's record: D/2 + D/16 + the indexer entry's bytes."""
+    return int(lib().oracle_record_bytes(D, DI, 1 if key_format == "mxfp4" else 0))
+
+
+def bytes_per_token(records: Sequence[int], ms: Sequence[int]) -> float:
+    """Bytes per token of the caches of several layers, layer i keeping one
+    record of records[i] bytes per ms[i] tokens."""
+    r = np.ascontiguousarray(records, np.int64)
+    m = np.ascontiguousarray(ms, np.int32)
+    return float(lib().oracle_bytes_per_token(_ptr(r), _ptr(m), len(r)))
+
+
+def cache_spill(cache: "Cache", row0: int, n: int) -> np.ndarray:
+    """Records of rows [row0, row0 + n) of every sequence: uint8 [B, n, record]
+    (zeros for rows at or past the sequence's length)."""
+    mx = 1 if cache.key_format == "mxfp4" else 0
+    rb = record_bytes(cache.D, cache.DI, cache.key_format)
+    out = np.zeros((cache.B, n, rb), np.uint8)
+    lengths = np.ascontiguousarray(cache.lengths, np.int64)
+    lib().oracle_cache_spill(_ptr(cache.codes), _ptr(cache.scales), _ptr(cache.ikeys), cache.B, cache.capacity,
+                             cache.D, cache.DI, mx, _ptr(lengths), row0, n, _ptr(out))
+    return out
+
+
+def cache_reload(cache: "Cache", records) -> int:
+    """Appends records [B, n, record] to every sequence (in place); returns the
+    number of sequences left unchanged because they would pass capacity."""
+    mx = 1 if cache.key_format == "mxfp4" else 0
+    rec = _np(records, np.uint8)
+    lengths = np.ascontiguousarray(cache.lengths, np.int64)
+    skipped = lib().oracle_cache_reload(_ptr(cache.codes), _ptr(cache.scales), _ptr(cache.ikeys), cache.B,
+                                        cache.capacity, cache.D, cache.DI, mx, _ptr(lengths), _ptr(rec),
+                                        rec.shape[1])
+    cache.lengths[:] = lengths
+    return int(skipped)
 
 
 def visible_length(length: int, P: int, p: int) -> int:

@@ -572,3 +572,77 @@ void oracle_attend_swa(const uint16_t *q, int H, int D, double scale,
     free(z);
     free(v);
 }
+
+/* ---------------------------------------------------------------------------
+ * Persistent cache records.  "G2C Brief - DeepSeek V4.1-Flash", section "FP4
+ * cache entries, and why they're safe", the derivation of the 890 bytes per
+ * token: a cache entry is its main entry (512 four-bit values and 32 scale
+ * bytes, 288 B) and its indexer entry (128 four-bit values and 4 scale bytes
+ * in MXFP4, 68 B), 356 B; a layer that keeps a cache with compression m stores
+ * one entry per m tokens.  A record keeps the table's order: the main entry's
+ * code bytes, its scale bytes, then the indexer entry's bytes (E4M3: DI value
+ * bytes; MXFP4: DI/2 code bytes, then DI/32 scale bytes).
+ * ------------------------------------------------------------------------- */
+int64_t oracle_record_bytes(int D, int DI, int mx)
+{
+    return (int64_t)(D / 2) + D / 16 + (mx ? DI / 2 + DI / 32 : DI);
+}
+
+/* Bytes per token of the caches of n_layers layers, layer i storing one record
+ * of record_bytes[i] bytes per m[i] tokens. */
+double oracle_bytes_per_token(const int64_t *record_bytes, const int32_t *m, int n_layers)
+{
+    double t = 0.0;
+    for (int i = 0; i < n_layers; ++i)
+        t += (double)record_bytes[i] / (double)m[i];
+    return t;
+}
+
+/* Rows [row0, row0 + n) of each of B sequences as records, out [B][n][record];
+ * a row at or past lengths[b] gives a record of zeros.  keys holds each row's
+ * indexer entry as the record stores it ([B][cap][key bytes]). */
+void oracle_cache_spill(const uint8_t *codes, const uint8_t *scales, const uint8_t *keys, int B, int64_t cap, int D,
+                        int DI, int mx, const int64_t *lengths, int64_t row0, int64_t n, uint8_t *out)
+{
+    const int64_t cb = D / 2, sb = D / 16, kb = oracle_record_bytes(D, DI, mx) - cb - sb;
+    const int64_t rb = cb + sb + kb;
+    for (int b = 0; b < B; ++b)
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t r = row0 + i;
+            uint8_t *rec = out + ((int64_t)b * n + i) * rb;
+            if (r >= lengths[b]) {
+                memset(rec, 0, (size_t)rb);
+                continue;
+            }
+            const int64_t row = (int64_t)b * cap + r;
+            memcpy(rec, codes + row * cb, (size_t)cb);
+            memcpy(rec + cb, scales + row * sb, (size_t)sb);
+            memcpy(rec + cb + sb, keys + row * kb, (size_t)kb);
+        }
+}
+
+/* Appends n records per sequence (in [B][n][record]) at rows lengths[b] ..
+ * lengths[b] + n - 1, then lengths[b] += n; a sequence whose rows would pass
+ * cap is left unchanged.  Returns how many sequences were left unchanged. */
+int oracle_cache_reload(uint8_t *codes, uint8_t *scales, uint8_t *keys, int B, int64_t cap, int D, int DI, int mx,
+                        int64_t *lengths, const uint8_t *in, int64_t n)
+{
+    const int64_t cb = D / 2, sb = D / 16, kb = oracle_record_bytes(D, DI, mx) - cb - sb;
+    const int64_t rb = cb + sb + kb;
+    int skipped = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lengths[b] + n > cap) {
+            ++skipped;
+            continue;
+        }
+        for (int64_t i = 0; i < n; ++i) {
+            const uint8_t *rec = in + ((int64_t)b * n + i) * rb;
+            const int64_t row = (int64_t)b * cap + lengths[b] + i;
+            memcpy(codes + row * cb, rec, (size_t)cb);
+            memcpy(scales + row * sb, rec + cb, (size_t)sb);
+            memcpy(keys + row * kb, rec + cb + sb, (size_t)kb);
+        }
+        lengths[b] += n;
+    }
+    return skipped;
+}
