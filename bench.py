@@ -537,6 +537,226 @@ def bench_reference(args, wl, rank):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------------------
+# Persistent cache records (spill / reload), measured on their own workloads
+# ---------------------------------------------------------------------------
+
+PERSIST_METRIC = "cache entries spilled to records and reloaded per second"
+PERSIST_WORKLOADS = {
+    # one 1M-entry sequence of 512-dim FP4 entries with 128-dim indexer keys
+    "persist_1m_mx": dict(B=1, L=1 << 20, D=512, DI=128, key_format="mxfp4"),
+    "persist_1m": dict(B=1, L=1 << 20, D=512, DI=128, key_format="e4m3"),
+}
+
+
+def persist_workload(name):
+    from fp4_compressed_sparse_append_b300 import workloads as W
+    p = PERSIST_WORKLOADS[name]
+    return W.Workload(name, B=p["B"], L=p["L"], H=64, D=p["D"], HI=64, DI=p["DI"], K=2048,
+                      key_format=p["key_format"])
+
+
+def persist_config(wl, record_bytes):
+    return {"workload": wl.name, "batch": wl.B, "entries_per_sequence": wl.L, "d_latent": wl.D,
+            "indexer_dim": wl.DI, "record_bytes": record_bytes,
+            "kv_format": "E2M1 codes + E4M3 scale per 16 channels; " + (
+                "MXFP4 indexer keys" if wl.key_format == "mxfp4" else "FP8 E4M3 indexer keys"),
+            "step": "spill every entry to records, reload them into a second cache",
+            "l2": "flushed between timed steps (a 256 MiB read outside the timed events)"}
+
+
+def persist_oracle_sample(wl, seed, max_seconds, n_sample=1 << 16):
+    """The oracle's spill and reload of a window of n_sample entries of sequence 0,
+    repeated for about max_seconds.  Returns (entries/s, cores, description, seconds)."""
+    import oracle
+    from fp4_compressed_sparse_append_b300 import workloads as W
+    oracle.build()
+    small = wl.scaled(L=n_sample)
+    lat, ik = W.cache_rows(small, seed, 0, device="cpu")
+    src = oracle.Cache(1, n_sample, wl.D, wl.DI, key_format=wl.key_format)
+    src.append(lat[None].numpy(), ik[None].numpy())
+    done, t0 = 0, time.perf_counter()
+    while True:
+        rec = oracle.cache_spill(src, 0, n_sample)
+        dst = oracle.Cache(1, n_sample, wl.D, wl.DI, key_format=wl.key_format)
+        oracle.cache_reload(dst, rec)
+        done += 1
+        el = time.perf_counter() - t0
+        if el > max_seconds or done >= 1000:
+            break
+    sample = ("oracle (plain C) spill and reload of %d entries of sequence 0, %d time(s), one thread"
+              % (n_sample, done))
+    return done * n_sample / el, 1, sample, el
+
+
+def bench_persist(args, name, rank, world, local_rank):
+    import torch
+    from fp4_compressed_sparse_append_b300 import binding as B
+    from fp4_compressed_sparse_append_b300 import build as BUILD
+    from fp4_compressed_sparse_append_b300 import workloads as W
+
+    if rank == 0 or not os.path.exists(BUILD.LIB):
+        BUILD.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = persist_workload(name)
+    src = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=dev, key_format=wl.key_format)
+    for b in range(wl.B):
+        lat, ik = W.cache_rows(wl, args.seed + rank, b, device=dev)
+        one = B.Cache(1, wl.capacity, wl.D, wl.DI, device=dev, key_format=wl.key_format)
+        B.csa_quantize_append(one, lat[None], ik[None])
+        for t in ("codes", "scales", "ikeys", "iscales"):
+            if getattr(one, t) is not None:
+                getattr(src, t)[b].copy_(getattr(one, t)[0])
+        del one
+    src.lengths.fill_(wl.L)
+    dst = B.Cache(wl.B, wl.capacity, wl.D, wl.DI, device=dev, key_format=wl.key_format)
+    rb = B.csa_cache_record_bytes(src)
+    recs = torch.empty((wl.B, wl.L, rb), dtype=torch.uint8, device=dev)
+    host = torch.empty((wl.B, wl.L, rb), dtype=torch.uint8).pin_memory()
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def spill(out):
+        B.csa_cache_spill(src, 0, wl.L, records=out)
+
+    def reload(inp):
+        dst.lengths.zero_()                     # each step reloads into the same empty cache
+        B.csa_cache_reload(dst, inp)
+
+    for _ in range(max(3, args.warmup)):
+        spill(recs)
+        reload(recs)
+    torch.cuda.synchronize()
+    for t in ("codes", "scales", "ikeys", "iscales", "lengths"):
+        if getattr(src, t) is not None and not torch.equal(getattr(src, t), getattr(dst, t)):
+            raise RuntimeError("reloaded cache differs from the spilled one (%s)" % t)
+    if B.csa_device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    def timed_graph(fn, steps):
+        g = capture(fn)
+        ts = []
+        for i in range(steps + 3):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            if i >= 3:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ts]
+
+    launches0 = B.csa_kernel_launches()
+    step_graph = capture(lambda: (spill(recs), reload(recs)))
+    launches_per_step = B.csa_kernel_launches() - launches0
+    clocks = Clocks(local_rank)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush()
+        ev[i][0].record(stream)
+        step_graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms, value = aggregate_over_ranks(sum(step_ms), wl.B * wl.L, args.steps, world, dev)
+    ms_per_step = total_ms / args.steps
+    # each kernel alone (the roofline's launch time)
+    spill_ms = statistics.mean(timed_graph(lambda: spill(recs), max(3, args.steps)))
+    reload_ms = statistics.mean(timed_graph(lambda: reload(recs), max(3, args.steps)))
+    # end to end: records in pinned host memory (the spill writes them across
+    # the host link, the reload reads them back)
+    e2e_ms = statistics.mean(timed_graph(lambda: (spill(host), reload(host)), max(3, args.steps)))
+    torch.cuda.synchronize()
+    for t in ("codes", "scales", "ikeys", "iscales", "lengths"):
+        if getattr(src, t) is not None and not torch.equal(getattr(src, t), getattr(dst, t)):
+            raise RuntimeError("reloaded cache differs from the spilled one (%s)" % t)
+    if B.csa_device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    rec_bytes = wl.B * wl.L * rb
+    return dict(wl=wl, rb=rb, value=value, ms_per_step=ms_per_step, step_ms=step_ms, clocks=clock_info,
+                launches=launches_per_step * args.steps, spill_ms=spill_ms, reload_ms=reload_ms, e2e_ms=e2e_ms,
+                rec_bytes=rec_bytes)
+
+
+def persist_main(args, rank, world, local_rank):
+    import json as _json
+    r = bench_persist(args, args.workload, rank, world, local_rank)
+    if rank != 0:
+        return
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = _json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured (copy bandwidth, burst)" if peak else "fallback"
+    peak = peak or 6400.0
+    wl, nbytes = r["wl"], r["rec_bytes"]
+    # each kernel reads and writes every record's bytes once: 2 x record bytes per entry
+    kern = {"spill": r["spill_ms"], "reload": r["reload_ms"]}
+    dom = max(kern, key=kern.get)
+    achieved = 2 * nbytes / (kern[dom] / 1e3) / 1e9
+    roof = {"kernel": dom + "_kernel", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_src, "algorithmic_bytes_per_launch": 2 * nbytes,
+            "launch_ms": kern[dom], "traffic": None, "traffic_source": "not captured",
+            "other": {k: {"launch_ms": v, "achieved": 2 * nbytes / (v / 1e3) / 1e9} for k, v in kern.items()}}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, cores, sample, el = persist_oracle_sample(wl, args.seed, 10.0)
+        cpu = {"value": rate, "unit": "entries/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": el}
+    e2e_value = world * wl.B * wl.L / (r["e2e_ms"] / 1e3)
+    line = {
+        "metric": PERSIST_METRIC, "value": r["value"], "unit": "entries/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic (seeded cache rows; no dataset)",
+        "config": persist_config(wl, r["rb"]),
+        "step_algorithmic_bytes": 4 * nbytes, "hbm_gbs": 4 * nbytes / (r["ms_per_step"] / 1e3) / 1e9,
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "entries/s", "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+                "ms_per_step": r["e2e_ms"], "host_link_gbs": 2 * nbytes / (r["e2e_ms"] / 1e3) / 1e9,
+                "how": "spill into pinned host memory and reload from it (the kernels address the host buffer)"},
+        "gpu_launches": r["launches"], "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+def persist_reference(args, rank):
+    if rank != 0:
+        return
+    wl = persist_workload(args.workload)
+    per_step, sample, cores = [], "", 1
+    for i in range(args.warmup + args.steps):
+        rate, cores, sample, el = persist_oracle_sample(wl, args.seed, 0.0)
+        if i >= args.warmup:
+            per_step.append(el)
+    n = 1 << 16
+    ms = 1e3 * statistics.mean(per_step)
+    value = n / (ms / 1e3)
+    from fp4_compressed_sparse_append_b300 import workloads as W  # noqa: F401
+    import oracle
+    line = {"impl": "reference", "metric": PERSIST_METRIC, "value": value, "unit": "entries/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": persist_config(wl, oracle.record_bytes(wl.D, wl.DI, wl.key_format)),
+            "cpu_baseline": {"value": value, "unit": "entries/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: " + sample},
+            "e2e": {"value": value, "unit": "entries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
 def config_of(wl):
     from fp4_compressed_sparse_append_b300 import workloads as W
     return {"workload": wl.name, "batch": wl.B, "context": wl.L, "query_positions": wl.P, "heads": wl.H,
@@ -621,6 +841,17 @@ def main():
     args = parse_args()
     rank, world, local_rank = dist_env()
     from fp4_compressed_sparse_append_b300 import workloads as W
+    if args.workload in PERSIST_WORKLOADS:
+        if args.impl == "reference":
+            persist_reference(args, rank)
+            return
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        persist_main(args, rank, world, local_rank)
+        return
     wl = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         bench_reference(args, wl, rank)

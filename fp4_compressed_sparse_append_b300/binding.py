@@ -25,6 +25,7 @@ EXPORTS = (
     "csa_sparse_attend_noalloc", "csa_sparse_attend_swa", "csa_attend_swa_workspace_size",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
+    "csa_cache_record_bytes", "csa_cache_spill", "csa_cache_reload",
 )
 
 
@@ -90,8 +91,12 @@ def lib() -> ctypes.CDLL:
         L.csa_kernel_launches.restype = ctypes.c_uint64
         L.csa_status_string.argtypes = [ctypes.c_int]
         L.csa_status_string.restype = ctypes.c_char_p
+        L.csa_cache_record_bytes.argtypes = [C]
+        L.csa_cache_record_bytes.restype = SZ
+        L.csa_cache_spill.argtypes = [C, I32, I32, V, V]
+        L.csa_cache_reload.argtypes = [C, V, I32, V]
         for name in EXPORTS:
-            if name not in ("csa_status_string", "csa_kernel_launches"):
+            if name not in ("csa_status_string", "csa_kernel_launches", "csa_cache_record_bytes"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -111,6 +116,15 @@ def _ptr(t: Optional[torch.Tensor]):
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ptr_dev_or_pinned(t: torch.Tensor):
+    """Device tensors, or pinned host tensors (which the device addresses directly)."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("expected a CUDA tensor or pinned host memory")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return ctypes.c_void_p(t.data_ptr())
@@ -176,6 +190,29 @@ def csa_quantize_append_project(cache: Cache, rows: torch.Tensor, w_ik: torch.Te
     n = rows.shape[1]
     _check(lib().csa_quantize_append_project(cache.ref, _ptr(rows), _ptr(w_ik), n, _stream(stream)),
            "csa_quantize_append_project")
+
+
+def csa_cache_record_bytes(cache: Cache) -> int:
+    """Bytes of one persistent record (main entry codes and scales, then the indexer entry)."""
+    return int(lib().csa_cache_record_bytes(cache.ref))
+
+
+def csa_cache_spill(cache: Cache, row0: int, n: int, records: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """Records of rows [row0, row0 + n) of every sequence -> uint8 [B, n, record]
+    (device memory, or the given tensor: device or pinned host memory)."""
+    if records is None:
+        records = torch.empty((cache.batch, n, csa_cache_record_bytes(cache)), dtype=torch.uint8,
+                              device=cache.device)
+    _check(lib().csa_cache_spill(cache.ref, row0, n, _ptr_dev_or_pinned(records), _stream(stream)),
+           "csa_cache_spill")
+    return records
+
+
+def csa_cache_reload(cache: Cache, records: torch.Tensor, stream=None) -> None:
+    """Appends records [B, n, record] (device or pinned host memory) to every sequence."""
+    _check(lib().csa_cache_reload(cache.ref, _ptr_dev_or_pinned(records), records.shape[1], _stream(stream)),
+           "csa_cache_reload")
 
 
 def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optional[torch.Tensor] = None,

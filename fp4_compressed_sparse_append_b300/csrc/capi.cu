@@ -115,6 +115,34 @@ csa_status csa_quantize_append(const csa_cache *cache, const uint16_t *rows, con
     return from_cuda(csa::launch_quantize_append(view(cache), rows, ikeys_new, n_new, st, stream));
 }
 
+size_t csa_cache_record_bytes(const csa_cache *cache)
+{
+    if (check_cache(cache) != CSA_OK) return 0;
+    return csa::record_bytes(view(cache));
+}
+
+csa_status csa_cache_spill(const csa_cache *cache, int32_t row0, int32_t n, uint8_t *records, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (row0 < 0 || n < 0 || static_cast<int64_t>(row0) + n > cache->capacity) return CSA_ERR_INVALID_ARG;
+    if (n == 0) return CSA_OK;
+    if (!records || (reinterpret_cast<uintptr_t>(records) & 3u)) return CSA_ERR_INVALID_ARG;
+    return from_cuda(csa::launch_spill(view(cache), row0, n, records, stream));
+}
+
+csa_status csa_cache_reload(const csa_cache *cache, const uint8_t *records, int32_t n, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (n < 0 || n > cache->capacity) return CSA_ERR_INVALID_ARG;
+    if (n == 0) return CSA_OK;
+    if (!records || (reinterpret_cast<uintptr_t>(records) & 3u)) return CSA_ERR_INVALID_ARG;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_reload(view(cache), records, n, st, stream));
+}
+
 csa_status csa_quantize_append_project(const csa_cache *cache, const uint16_t *rows, const uint16_t *w_ik,
                                        int32_t n_new, csa_stream_t stream)
 {

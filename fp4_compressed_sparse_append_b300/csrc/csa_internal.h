@@ -47,6 +47,11 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
                           int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st,
                           const SwaView *swa = nullptr);
 
+// Persistent records of cache rows (main entry codes, scales, indexer entry).
+size_t record_bytes(const CacheView &c);
+cudaError_t launch_spill(const CacheView &c, int row0, int n, uint8_t *out, cudaStream_t st);
+cudaError_t launch_reload(const CacheView &c, const uint8_t *in, int n, int *status, cudaStream_t st);
+
 // Host-side count of kernel launches issued by the library (csa_kernel_launches).
 void count_launch(int n = 1);
 

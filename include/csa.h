@@ -162,6 +162,43 @@ CSA_API csa_status csa_quantize_append_project(const csa_cache *cache, const uin
                                                int32_t n_new, csa_stream_t stream);
 
 /*
+ * Persistent records of cache entries, to spill a cache out of device memory
+ * (to host memory or storage) and reload it.  ("G2C Brief", section "FP4
+ * cache entries, and why they're safe": an entry is its 288-byte main entry
+ * and its 68-byte MXFP4 indexer entry, 356 B; a cache layer with compression
+ * m keeps one entry per m tokens, which makes the 890 bytes per token of three
+ * m = 2 layers and one m = 1 layer.)
+ * A record is, in this order: the row's d_latent/2 code bytes, its
+ * d_latent/16 scale bytes, then its indexer entry (E4M3 cache: d_index bytes;
+ * MXFP4 cache: d_index/2 code bytes, then d_index/32 scale bytes).
+ * csa_cache_record_bytes returns that size (0 for an invalid cache).
+ */
+CSA_API size_t csa_cache_record_bytes(const csa_cache *cache);
+
+/*
+ * Spill: the records of rows row0 .. row0 + n - 1 of every sequence into
+ *   records : [batch][n][record bytes], device memory or pinned host memory
+ *             the device can address (4-byte aligned; written only)
+ * A row at or past the sequence's length (read on the device) gives a record
+ * of zeros.  The cache is not changed.  row0 + n must not pass capacity
+ * (else CSA_ERR_INVALID_ARG).
+ */
+CSA_API csa_status csa_cache_spill(const csa_cache *cache, int32_t row0, int32_t n, uint8_t *records,
+                                   csa_stream_t stream);
+
+/*
+ * Reload: appends n records per sequence,
+ *   records : [batch][n][record bytes] as csa_cache_spill writes them, device
+ *             memory or device-addressable pinned host memory (4-byte aligned)
+ * at rows lengths[b] .. lengths[b] + n - 1, then lengths[b] += n (the append
+ * rule of csa_quantize_append: a sequence that would pass capacity is left
+ * unchanged and sets CSA_DEV_CAPACITY).  Spilling rows 0 .. L - 1 and
+ * reloading them into an empty cache of the same shape and key format gives
+ * back the same rows.
+ */
+CSA_API csa_status csa_cache_reload(const csa_cache *cache, const uint8_t *records, int32_t n, csa_stream_t stream);
+
+/*
  * a2/a4: indexer scores for B*P queries.
  * ("G2C Brief", sections "The global branch" and "The hierarchical indexer".)
  *   iq     : [batch][P][HI][d_index] E4M3 indexer queries

@@ -170,3 +170,26 @@ def test_mxfp4_cache_checks(lib):
     ]
     for kw, want in bad:
         assert lib.csa_quantize_append(ctypes.byref(fake_cache(**kw)), V(0x50000), None, 0, None) == want, kw
+
+
+def test_persistent_record_checks(lib):
+    V = ctypes.c_void_p
+    lib.csa_cache_record_bytes.restype = ctypes.c_size_t
+    c = fake_cache()                                                        # D 128, d_index 64, E4M3
+    assert lib.csa_cache_record_bytes(ctypes.byref(c)) == 64 + 8 + 64
+    mx = fake_cache(d_index=128, ikey_format=B.CSA_IKEY_MXFP4, iscales=0x60000)
+    assert lib.csa_cache_record_bytes(ctypes.byref(mx)) == 64 + 8 + 64 + 4
+    big = fake_cache(d_latent=512, d_index=128, ikey_format=B.CSA_IKEY_MXFP4, iscales=0x60000)
+    assert lib.csa_cache_record_bytes(ctypes.byref(big)) == 356            # the 288 + 68 B entry
+    assert lib.csa_cache_record_bytes(None) == 0
+    r = ctypes.byref(c)
+    assert lib.csa_cache_spill(r, 0, 0, None, None) == 0                    # nothing to spill
+    assert lib.csa_cache_spill(r, -1, 4, V(0x70000), None) == 1
+    assert lib.csa_cache_spill(r, 60, 5, V(0x70000), None) == 1             # past capacity 64
+    assert lib.csa_cache_spill(r, 0, 4, V(0x70002), None) == 1             # misaligned records
+    assert lib.csa_cache_spill(r, 0, 4, None, None) == 1
+    assert lib.csa_cache_reload(r, V(0x70000), 0, None) == 0
+    assert lib.csa_cache_reload(r, V(0x70000), 65, None) == 1               # more than capacity
+    assert lib.csa_cache_reload(r, V(0x70001), 4, None) == 1
+    assert lib.csa_cache_reload(r, None, 4, None) == 1
+    assert lib.csa_cache_reload(None, V(0x70000), 4, None) == 1
