@@ -1,5 +1,5 @@
 // a2/a4: indexer scores, score(t) = sum_h w_h * ReLU(iq_h . ik_t), with FP8
-// E4M3 indexer queries and keys, on the tcgen05 tensor cores.
+// E4M3 indexer queries and FP8 E4M3 or MXFP4 keys, on the tcgen05 tensor cores.
 // "G2C Brief - DeepSeek V4.1-Flash", section "The global branch: compress,
 // index, select" (item 3: a small side network with its own low-precision
 // queries and keys scores every cached entry), and section "The hierarchical
@@ -48,9 +48,11 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 // bytes and writes them 8 bytes to every 16 (the padded 4-bit operand layout),
 // and the MMA is the block-scaled kind::mxf8f6f4 with an E2M1 A operand and
 // the E4M3 queries as B.  Four scale warps copy each tile's block scales from
-// shared memory to tensor memory (row r at lane r, one 32-bit word holding its
-// four block exponents; the instruction descriptor picks the byte of each
-// 32-channel step), where the MMA applies them.  They take the place of the
+// shared memory to tensor memory, where the MMA applies them: a tile's scales
+// take four columns, the MMA reads row r's 32-bit word (its four block
+// exponents) at lane r of column r / 32, and the instruction descriptor picks
+// the byte of each 32-channel step; each warp writes its 32 rows' words into
+// all four columns of its lane quarter.  They take the place of the
 // second epilogue group, so the CTA keeps 320 threads and two CTAs fit an SM.
 constexpr int kEpiWarpsMx = 4;
 constexpr int kSclWarp0 = 2 + kEpiWarpsMx;
