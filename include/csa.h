@@ -69,7 +69,7 @@ typedef struct CUstream_st *csa_stream_t;
 typedef enum csa_status {
     CSA_OK = 0,
     CSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, bad mode */
-    CSA_ERR_UNSUPPORTED = 2,  /* valid but outside the shapes this build handles */
+    CSA_ERR_UNSUPPORTED = 2,  /* valid but outside the shapes this library handles */
     CSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     CSA_ERR_DEVICE = 4,       /* csa_device_status: a device-side fault bit is set */
     CSA_ERR_WORKSPACE = 5     /* workspace missing or smaller than the size query said */

@@ -263,7 +263,7 @@ void oracle_index_score(const uint8_t *iq, const float *w, int HI, int DI,
  *   scale byte = X + 127 (UE8M0: the value 2^X);
  *   code = sign(x) | E2M1 magnitude nearest to |x| / 2^X (ties to the even
  *   code, 6 beyond), packed two per byte, the even channel in the low nibble.
- * The clamp is this build's addition to the OCP rule: with X in [-8, 6] every
+ * The clamp is this library's addition to the OCP rule: with X in [-8, 6] every
  * stored value 2^X * E2M1 is exactly an E4M3 value (6 * 2^6 = 384 <= 448, and
  * 0.5 * 2^-8 = 2^-9 is E4M3's smallest step), so a key decodes exactly.
  */
