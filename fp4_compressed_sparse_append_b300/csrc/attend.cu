@@ -84,11 +84,6 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col, int rows)
                                  (col & 7) * 2);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi)
-{
-    return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-}
-
 // Two E2M1 codes (one byte, even channel in the low nibble) times an fp16 scale.
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t byte, uint32_t scale_h2)
 {
