@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
     // Below: reads of what earlier kernels on the stream wrote (lengths, indices, cache).
     pdl_wait();
-    len = a.c.lengths[b];
+    len = min(a.c.lengths[b], a.c.cap);
     // The window split's rows: [w_lo, w_hi) of the sequence's local rows, the
     // window of tokens that ends at this position's own row (L - P + p for a
     // sequence of L local rows).  A length outside [P, swa_n] is a caller

@@ -36,6 +36,10 @@ csa_status check_cache(const csa_cache *c)
 {
     if (!c || !c->codes || !c->scales || !c->ikeys || !c->lengths) return CSA_ERR_INVALID_ARG;
     if (c->batch < 1 || c->capacity < 1) return CSA_ERR_INVALID_ARG;
+    // Row coordinates of the TMA tensor maps and the scan's row arithmetic are
+    // 32-bit: batch x capacity rows must stay below 2^31 (far beyond any cache
+    // that fits the device).
+    if (static_cast<int64_t>(c->batch) * c->capacity >= (int64_t(1) << 31)) return CSA_ERR_UNSUPPORTED;
     if (!aligned16(c->codes) || !aligned16(c->scales) || !aligned16(c->ikeys) ||
         (reinterpret_cast<uintptr_t>(c->lengths) & 3u))
         return CSA_ERR_INVALID_ARG;

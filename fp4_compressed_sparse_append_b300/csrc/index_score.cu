@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float *wsrc = a.w + static_cast<int64_t>(it.u) * a.n_real;
                 for (int i = lane; i < a.n_real; i += 32) wcopy[i] = wsrc[i];
                 __syncwarp();
-                len_b = a.pool_mode ? 0 : a.lengths[it.u];
+                len_b = a.pool_mode ? 0 : min(a.lengths[it.u], a.cap);
                 cur = it.u;
             }
             bool ok = true;

@@ -54,7 +54,8 @@ enum SelSource { kRows = 0, kBlocks = 1, kPoolRows = 2, kPairs = 3 };
 struct SelArgs {
     const float *scores;       // kRows/kBlocks/kPoolRows: [rows][ld];  kPairs: [rows][n_pairs]
     int64_t ld;
-    const int32_t *lengths;
+    const int32_t *lengths;    // read as min(lengths[b], cap)
+    int cap;
     int P;
     const int32_t *pool;       // kPoolRows: [rows][pool_blocks]
     int pool_blocks;
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         rv.ids = a.pair_ids + static_cast<int64_t>(row) * a.n_pairs;
     } else {
         const int b = row / a.P, p = row % a.P;
-        const int L = a.lengths[b] - a.P + 1 + p;
+        const int L = min(a.lengths[b], a.cap) - a.P + 1 + p;
         rv.s = a.scores + static_cast<int64_t>(row) * a.ld;
         rv.L = L;
         if (S == kPoolRows) {
@@ -547,6 +548,7 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
     a.scores = scores;
     a.ld = ld;
     a.lengths = c.lengths;
+    a.cap = c.cap;
     a.P = P;
     a.pool = pool;
     a.pool_blocks = pool_blocks;

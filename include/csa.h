@@ -41,7 +41,9 @@
  *    past capacity, a pipeline wait that ran out) do not trap: the kernel
  *    skips the access, ORs a bit into a per-device status word and carries on.
  *    csa_device_status reads (and optionally clears) that word.
- *  - Sequence b holds valid rows [0, lengths[b]).  With P query positions per
+ *  - Sequence b holds valid rows [0, lengths[b]).  Kernels read lengths[b] as
+ *    min(lengths[b], capacity), so no row at or past the capacity is read or
+ *    written whatever the array holds.  With P query positions per
  *    sequence, the last P rows are the step's own positions and position p
  *    (0 <= p < P) sees rows [0, lengths[b] - P + 1 + p).
  *  - Index lists (top-K selections, pools) are written in ascending order
@@ -76,7 +78,7 @@ typedef enum csa_status {
 } csa_status;
 
 /* Bits of the device status word. */
-#define CSA_DEV_BAD_INDEX 0x1   /* a selected row id was >= lengths[b] (row skipped) */
+#define CSA_DEV_BAD_INDEX 0x1   /* a selected row id was >= min(lengths[b], capacity) (row skipped) */
 #define CSA_DEV_CAPACITY  0x2   /* an append would pass capacity (sequence left unchanged) */
 #define CSA_DEV_TIMEOUT   0x4   /* a pipeline wait ran past its limit (kernel returned early) */
 
@@ -95,7 +97,8 @@ typedef enum csa_mode { CSA_FULL = 0, CSA_REINDEX = 1, CSA_REUSE = 2 } csa_mode;
  *   iscales : CSA_IKEY_MXFP4: [batch][capacity][d_index/32] UE8M0 block scales
  *             (2^(byte - 127) per 32 channels); unused (may be NULL) for E4M3
  *   lengths : [batch] int32                  valid rows per sequence
- * d_latent is 128, 256, 384 or 512; d_index is 32, 64 or 128; capacity >= 1.
+ * d_latent is 128, 256, 384 or 512; d_index is 32, 64 or 128; capacity >= 1;
+ * batch x capacity < 2^31 (row ids are 32-bit), else CSA_ERR_UNSUPPORTED.
  * MXFP4 keys ("G2C Brief", section "FP4 cache entries, and why they're safe":
  * 128 values x 4 bits + one 8-bit scale per 32 values = 68 B, the OCP MXFP4
  * format the pages assume) need d_index = 128 and capacity a multiple of 4.

@@ -58,6 +58,9 @@ def test_null_and_bad_cache_rejected_before_launch(lib):
     assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, 1, None) == 1
     c = fake_cache()
     assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, -1, None) == 1
+    big = fake_cache(batch=2, capacity=1 << 30)                       # 2^31 rows: 32-bit row ids overflow
+    assert lib.csa_quantize_append(ctypes.byref(big), ctypes.c_void_p(0x50000), None, 1, None) == 2
+    assert lib.csa_cache_record_bytes(ctypes.byref(big)) == 0
     assert lib.csa_quantize_append(ctypes.byref(c), ctypes.c_void_p(0x50000), None, 0, None) == 0
 
 
