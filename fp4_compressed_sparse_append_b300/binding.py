@@ -121,6 +121,37 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _need(t: Optional[torch.Tensor], nbytes: int, name: str) -> None:
+    """The C ABI sees only a pointer: a tensor smaller than the bytes the call
+    reads or writes would let a kernel run past it, so it is refused here."""
+    if t is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError("%s holds %d bytes; the call touches %d" % (name, t.numel() * t.element_size(), nbytes))
+
+
+def _lead(t: torch.Tensor, name: str, batch: int, last: Optional[int] = None) -> None:
+    """Outputs are allocated from this tensor's shape: its batch (and last) dims
+    must be the cache's."""
+    if t.shape[0] != batch or (last is not None and t.shape[-1] != last):
+        raise ValueError("%s has shape %s; expected [%d, ...%s]" % (name, tuple(t.shape), batch,
+                                                                    "" if last is None else ", %d" % last))
+
+
+def _key_row_bytes(cache: "Cache") -> int:
+    """Bytes of one appended indexer key row (E4M3: DI; MXFP4: DI/2 codes + DI/32 scales)."""
+    return cache.d_index // 2 + cache.d_index // 32 if cache.key_format == "mxfp4" else cache.d_index
+
+
+def _need_attend(cache: "Cache", P: int, H: int, K: int, q, idx, out, lse, swa=None) -> None:
+    Bc, D = cache.batch, cache.d_latent
+    _need(q, Bc * P * H * D * 2, "q")
+    _need(idx, Bc * P * K * 4, "idx")
+    _need(out, Bc * P * H * D * 4, "out")
+    _need(lse, Bc * P * H * 4, "lse")
+    if swa is not None:
+        _need(swa.rows, Bc * swa.rows.shape[1] * D, "swa rows")
+        _need(swa.lengths, Bc * 4, "swa lengths")
+
+
 def _ptr_dev_or_pinned(t: torch.Tensor):
     """Device tensors, or pinned host tensors (which the device addresses directly)."""
     if not t.is_cuda and not t.is_pinned():
@@ -180,6 +211,8 @@ def csa_quantize_append(cache: Cache, rows: torch.Tensor, ikeys_new: Optional[to
                         stream=None) -> None:
     """rows: [B, n, D] bf16 (or its int16 bits); ikeys_new: [B, n, DI] uint8 or None."""
     n = rows.shape[1]
+    _need(rows, cache.batch * n * cache.d_latent * 2, "rows")
+    _need(ikeys_new, cache.batch * n * _key_row_bytes(cache), "ikeys_new")
     _check(lib().csa_quantize_append(cache.ref, _ptr(rows), _ptr(ikeys_new), n, _stream(stream)),
            "csa_quantize_append")
 
@@ -188,6 +221,8 @@ def csa_quantize_append_project(cache: Cache, rows: torch.Tensor, w_ik: torch.Te
     """rows: [B, n, D] bf16 bits; w_ik: [D, DI] bf16 bits.  The appended rows'
     indexer keys are projected from their stored FP4 entries."""
     n = rows.shape[1]
+    _need(rows, cache.batch * n * cache.d_latent * 2, "rows")
+    _need(w_ik, cache.d_latent * cache.d_index * 2, "w_ik")
     _check(lib().csa_quantize_append_project(cache.ref, _ptr(rows), _ptr(w_ik), n, _stream(stream)),
            "csa_quantize_append_project")
 
@@ -204,6 +239,7 @@ def csa_cache_spill(cache: Cache, row0: int, n: int, records: Optional[torch.Ten
     if records is None:
         records = torch.empty((cache.batch, n, csa_cache_record_bytes(cache)), dtype=torch.uint8,
                               device=cache.device)
+    _need(records, cache.batch * n * csa_cache_record_bytes(cache), "records")
     _check(lib().csa_cache_spill(cache.ref, row0, n, _ptr_dev_or_pinned(records), _stream(stream)),
            "csa_cache_spill")
     return records
@@ -211,6 +247,7 @@ def csa_cache_spill(cache: Cache, row0: int, n: int, records: Optional[torch.Ten
 
 def csa_cache_reload(cache: Cache, records: torch.Tensor, stream=None) -> None:
     """Appends records [B, n, record] (device or pinned host memory) to every sequence."""
+    _need(records, cache.batch * records.shape[1] * csa_cache_record_bytes(cache), "records")
     _check(lib().csa_cache_reload(cache.ref, _ptr_dev_or_pinned(records), records.shape[1], _stream(stream)),
            "csa_cache_reload")
 
@@ -220,10 +257,16 @@ def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optio
     """iq [B, P, HI, DI] uint8, w [B, P, HI] fp32, pool [B, P, nblk] int32 or None
     -> scores [B, P, ld] fp32 (ld = capacity rounded up to 4, or 8*nblk)."""
     B, P, HI, _ = iq.shape
+    _lead(iq, "iq", cache.batch, cache.d_index)
     nblk = pool.shape[-1] if pool is not None else 0
     n = nblk * CSA_POOL_BLOCK if pool is not None else cache.capacity
     if scores is None:
         scores = torch.empty((B, P, (n + 3) // 4 * 4), dtype=torch.float32, device=cache.device)
+    Bc = cache.batch
+    _need(iq, Bc * P * HI * cache.d_index, "iq")
+    _need(w, Bc * P * HI * 4, "w")
+    _need(pool, Bc * P * nblk * 4, "pool")
+    _need(scores, Bc * P * scores.shape[-1] * 4, "scores")
     _check(lib().csa_index_score(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, _ptr(scores),
                                  scores.shape[-1], _stream(stream)), "csa_index_score")
     return scores
@@ -241,7 +284,10 @@ def csa_topk(cache: Cache, scores: torch.Tensor, K: int, pool: Optional[torch.Te
              stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """scores [B, P, ld] -> (idx [B, P, K] int32, pool_out [B, P, pool_keep] int32 or None)."""
     B, P, ld = scores.shape
+    _lead(scores, "scores", cache.batch)
     nblk = pool.shape[-1] if pool is not None else 0
+    _need(scores, cache.batch * P * ld * 4, "scores")
+    _need(pool, cache.batch * P * nblk * 4, "pool")
     idx = torch.empty((B, P, K), dtype=torch.int32, device=cache.device)
     pool_out = torch.empty((B, P, pool_keep), dtype=torch.int32, device=cache.device) if pool_keep else None
     if workspace is None:
@@ -263,7 +309,9 @@ def csa_sparse_attend(cache: Cache, q: torch.Tensor, idx: torch.Tensor, scale: f
                       lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """q [B, P, H, D] bf16 bits, idx [B, P, K] int32 -> (out [B, P, H, D] fp32, lse [B, P, H] fp32)."""
     B, P, H, D = q.shape
+    _lead(q, "q", cache.batch, cache.d_latent)
     K = idx.shape[-1]
+    _need_attend(cache, P, H, K, q, idx, out, lse)
     if workspace is None:
         workspace = torch.empty(attend_workspace_size(cache, P, H, K), dtype=torch.uint8, device=cache.device)
     if out is None:
@@ -280,7 +328,9 @@ def csa_sparse_attend_noalloc(cache: Cache, q: torch.Tensor, idx: torch.Tensor, 
     """Sparse attention into caller-provided out/lse, with the library's own
     fixed device scratch (no workspace argument; the call allocates nothing)."""
     B, P, H, D = q.shape
+    _lead(q, "q", cache.batch, cache.d_latent)
     K = idx.shape[-1]
+    _need_attend(cache, P, H, K, q, idx, out, lse)
     _check(lib().csa_sparse_attend_noalloc(cache.ref, P, H, _ptr(q), scale, _ptr(idx), K, _ptr(out), _ptr(lse),
                                            _stream(stream)), "csa_sparse_attend_noalloc")
 
@@ -310,7 +360,9 @@ def csa_sparse_attend_swa(cache: Cache, q: torch.Tensor, idx: torch.Tensor, scal
                           lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Joint softmax over the selected rows and the local window -> (out [B, P, H, D], lse [B, P, H])."""
     B, P, H, D = q.shape
+    _lead(q, "q", cache.batch, cache.d_latent)
     K = idx.shape[-1]
+    _need_attend(cache, P, H, K, q, idx, out, lse, swa)
     if workspace is None:
         workspace = torch.empty(max(attend_swa_workspace_size(cache, P, H, K, swa), 16), dtype=torch.uint8,
                                 device=cache.device)
@@ -331,6 +383,7 @@ class LayerArgs:
                  rows_new=None, ikeys_new=None, pool_in=None, pool_blocks: int = 0, make_pool: bool = False,
                  swa: Optional[Swa] = None, w_ik=None):
         B, P, H, D = q.shape
+        _lead(q, "q", cache.batch, cache.d_latent)
         dev = cache.device
         self.tensors = dict(q=q, iq=iq, w=w, rows_new=rows_new, ikeys_new=ikeys_new, pool_in=pool_in)
         self.idx = idx if idx is not None else torch.empty((B, P, K), dtype=torch.int32, device=dev)
@@ -340,6 +393,14 @@ class LayerArgs:
                          if make_pool else None)
         HI = iq.shape[2] if iq is not None else 0
         n_new = rows_new.shape[1] if rows_new is not None else 0
+        Bc = cache.batch
+        _need_attend(cache, P, H, K, q, idx, None, None, swa)
+        _need(iq, Bc * P * HI * cache.d_index, "iq")
+        _need(w, Bc * P * HI * 4, "w")
+        _need(rows_new, Bc * n_new * cache.d_latent * 2, "rows_new")
+        _need(ikeys_new, Bc * n_new * _key_row_bytes(cache), "ikeys_new")
+        _need(pool_in, Bc * P * pool_blocks * 4, "pool_in")
+        _need(w_ik, cache.d_latent * cache.d_index * 2, "w_ik")
         self.struct = csa_layer_args(mode, P, H, HI, K, scale, _ptr(q), _ptr(iq), _ptr(w), _ptr(rows_new),
                                      _ptr(ikeys_new), n_new, pool_blocks, _ptr(pool_in), _ptr(self.pool_out),
                                      _ptr(self.idx), _ptr(self.out), _ptr(self.lse), None, 0,
