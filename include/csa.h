@@ -252,8 +252,8 @@ CSA_API csa_status csa_topk_workspace_size(const csa_cache *cache, int32_t P, in
  * ("G2C Brief", "The global branch": the query attends to only the selected
  *  entries; "Pushing the Limits", "The Paper": one W_KV, so K and V are equal.)
  *   q     : [batch][P][H][d_latent] bf16 bits
- *   idx   : [batch][P][K] row ids (-1 = skip; >= lengths[b] sets CSA_DEV_BAD_INDEX
- *           and is skipped)
+ *   idx   : [batch][P][K] row ids (-1 = skip; an id >= min(lengths[b], capacity)
+ *           sets CSA_DEV_BAD_INDEX and is skipped)
  *   out   : [batch][P][H][d_latent] fp32 = sum_j softmax_j(scale * q.v_j) v_j
  *   lse   : [batch][P][H] fp32 log-sum-exp of the logits, or NULL
  *   workspace : device scratch of csa_attend_workspace_size bytes
