@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int k = 0; k < 16; ++k) {
                         const int jb = it.job * 16 + k;
                         blk[k] = jb < a.pool_blocks ? prow[jb] : -1;
-                        if (blk[k] >= 0 && blk[k] * kPoolBlock < a.cap)
+                        if (blk[k] >= 0 && blk[k] < (a.cap + kPoolBlock - 1) / kPoolBlock)  // no overflow
                             ++nv;
                         else
                             blk[k] = -1;
