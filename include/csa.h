@@ -179,7 +179,9 @@ CSA_API csa_status csa_quantize_append_project(const csa_cache *cache, const uin
 CSA_API size_t csa_cache_record_bytes(const csa_cache *cache);
 
 /*
- * Spill: the records of rows row0 .. row0 + n - 1 of every sequence into
+ * Spill (persistent records, "G2C Brief", section "FP4 cache entries, and why
+ * they're safe", as above): the records of rows row0 .. row0 + n - 1 of every
+ * sequence into
  *   records : [batch][n][record bytes], device memory or pinned host memory
  *             the device can address (4-byte aligned; written only)
  * A row at or past the sequence's length (read on the device) gives a record
@@ -190,7 +192,8 @@ CSA_API csa_status csa_cache_spill(const csa_cache *cache, int32_t row0, int32_t
                                    csa_stream_t stream);
 
 /*
- * Reload: appends n records per sequence,
+ * Reload (persistent records, "G2C Brief", section "FP4 cache entries, and why
+ * they're safe", as above): appends n records per sequence,
  *   records : [batch][n][record bytes] as csa_cache_spill writes them, device
  *             memory or device-addressable pinned host memory (4-byte aligned)
  * at rows lengths[b] .. lengths[b] + n - 1, then lengths[b] += n (the append
@@ -242,8 +245,10 @@ CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scor
                     int32_t pool_keep, int32_t *pool_out, void *workspace, size_t workspace_bytes,
                     csa_stream_t stream);
 
-/* pool_blocks > 0: the scores are over a pool of that many blocks; pool_keep > 0:
- * a pool of that many blocks is also built. */
+/* Workspace query of csa_topk.  No counterpart on the pages: the library
+ * allocates nothing, so the caller supplies the scratch of the two-stage
+ * select of long rows.  pool_blocks > 0: the scores are over a pool of that
+ * many blocks; pool_keep > 0: a pool of that many blocks is also built. */
 CSA_API csa_status csa_topk_workspace_size(const csa_cache *cache, int32_t P, int32_t pool_blocks, int32_t K,
                                            int32_t pool_keep, size_t *bytes);
 
@@ -263,6 +268,9 @@ CSA_API csa_status csa_sparse_attend(const csa_cache *cache, int32_t P, int32_t 
                              float scale, const int32_t *idx, int32_t K, float *out, float *lse,
                              void *workspace, size_t workspace_bytes, csa_stream_t stream);
 
+/* Workspace query of csa_sparse_attend.  No counterpart on the pages: the bytes
+ * of split partials the call keeps in the caller's workspace (0 when every
+ * query's splits merge on chip). */
 CSA_API csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K,
                                      size_t *bytes);
 
@@ -294,7 +302,9 @@ typedef struct csa_swa {
 } csa_swa;
 
 /*
- * csa_sparse_attend with the local window: out and lse are those of the joint
+ * csa_sparse_attend with the local window ("G2C Brief", "Two attention paths
+ * in every layer"; "Pushing the Limits", "The Paper"; the reading above): out
+ * and lse are those of the joint
  * softmax over the selected rows of idx and the window rows of swa (NULL swa:
  * exactly csa_sparse_attend).  workspace: csa_attend_swa_workspace_size bytes.
  */
@@ -302,6 +312,8 @@ CSA_API csa_status csa_sparse_attend_swa(const csa_cache *cache, int32_t P, int3
                                          float scale, const int32_t *idx, int32_t K, const csa_swa *swa, float *out,
                                          float *lse, void *workspace, size_t workspace_bytes, csa_stream_t stream);
 
+/* Workspace query of csa_sparse_attend_swa (no counterpart on the pages; the
+ * window adds one split to each query). */
 CSA_API csa_status csa_attend_swa_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K,
                                                  const csa_swa *swa, size_t *bytes);
 
@@ -339,7 +351,12 @@ CSA_API csa_status csa_sparse_attend_noalloc(const csa_cache *cache, int32_t P, 
                                              csa_stream_t stream);
 
 /*
- * a7: one CSA2 layer for B*P queries.
+ * a7: one CSA2 layer for B*P queries.  ("G2C Brief", section "CSA2: most
+ * layers don't keep their own cache": Full layers own the KV, the indexer keys
+ * and the selection, Reindex layers borrow the KV and keys and select afresh
+ * with their own indexer query, Reuse layers borrow the last selection; every
+ * layer has its own query.  Section "The hierarchical indexer": the first Full
+ * layer's pool, which later Reindex layers search.)
  *   FULL    : [append rows_new/ikeys_new if n_new > 0] -> scores over every
  *             visible row -> idx (top K) [-> pool_out] -> attention
  *   REINDEX : scores over every visible row, or over pool_in's rows when
@@ -378,20 +395,24 @@ typedef struct csa_layer_args {
 
 CSA_API csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *args, csa_stream_t stream);
 
+/* Workspace query of csa_layer_step (no counterpart on the pages): scores,
+ * selection scratch and attention partials of one layer. */
 CSA_API csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args *args, size_t *bytes);
 
 /*
+ * No counterpart on the pages (error reporting of this library).
  * Waits for `stream`, then copies the device status word of the current
  * device into *bits (0 = no fault) and, if clear != 0, resets it.
  * Returns CSA_ERR_DEVICE when a bit is set, else CSA_OK.
  */
 CSA_API csa_status csa_device_status(int32_t *bits, int32_t clear, csa_stream_t stream);
 
-/* Number of kernels this library has launched in the calling process (a host
- * counter, for accounting in benchmarks; no device work). */
+/* No counterpart on the pages.  Number of kernels this library has launched in
+ * the calling process (a host counter, for accounting in benchmarks; no device
+ * work). */
 CSA_API uint64_t csa_kernel_launches(void);
 
-/* Static description of a status code. */
+/* No counterpart on the pages.  Static description of a status code. */
 CSA_API const char *csa_status_string(csa_status status);
 
 #ifdef __cplusplus

@@ -34,6 +34,21 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(B.EXPORTS)
 
 
+def test_every_declaration_cites_its_passage():
+    """Each entry point's comment cites the page passage it follows, or says the
+    pages have no counterpart (workspace queries, status and accounting)."""
+    text = open(os.path.join(ROOT, "include", "csa.h")).read()
+    decls = list(re.finditer(r"CSA_API\s+[\w\s\*]+?\b(csa_\w+)\s*\(", text))
+    assert len(decls) == len(B.EXPORTS)
+    for m in decls:
+        before = text[:m.start()]
+        comment = before[before.rfind("/*"):before.rfind("*/") + 2]
+        assert "CSA_API" not in before[before.rfind("*/"):], (m.group(1), "no comment of its own")
+        squashed = " ".join(comment.replace("*", " ").split())
+        assert any(k in squashed for k in ("G2C Brief", "Pushing the Limits", "no counterpart", "No counterpart",
+                                           "describe no counterpart")), m.group(1)
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert B.status_string(s)
