@@ -393,6 +393,8 @@ typedef struct csa_layer_args {
                                     instead of copying ikeys_new (which must then be NULL); or NULL */
 } csa_layer_args;
 
+/* One layer of the CSA2 mode chain ("G2C Brief", section "CSA2: most layers
+ * don't keep their own cache"), as described above csa_layer_args. */
 CSA_API csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *args, csa_stream_t stream);
 
 /* Workspace query of csa_layer_step (no counterpart on the pages): scores,
