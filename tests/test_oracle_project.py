@@ -9,7 +9,6 @@ product, and closed-form properties (identity and one-entry projections,
 linearity, sign symmetry, saturation).
 """
 import numpy as np
-import pytest
 import torch
 
 import oracle

@@ -8,7 +8,6 @@ and must refuse a problem whose partials do not fit the fixed array.  This file
 is collected last so that a run stopping at its first failure has already run
 every other test.
 """
-import ctypes
 
 import numpy as np
 import pytest
