@@ -1,11 +1,14 @@
 #!/usr/bin/env python3
 """Benchmark of the CSA2 decode step over an FP4 global KV cache.
 
-One step = one pass of the whole hot path over one batch: for the default
-workload (full_64k: 8 sequences x 65,536 cached FP4 rows, 64 query heads,
-D=512, a 64x128 FP8 indexer, top-2048) that is one Full-mode CSA2 layer:
-indexer scores over every cached row, top-K selection, sparse attention over
-the selected FP4 rows.  Chain workloads run every layer of the chain per step.
+One step = one pass of the whole hot path over one batch.  The default
+workload is hier_1m: one sequence of 1,048,576 cached FP4 rows (D = 512, 64
+query heads, a 64x128 FP8 indexer, top-2048), a Full layer that scores every
+row, selects its top 2048 and keeps the hierarchical pool of 2048 blocks of 8
+rows, then 7 Reindex layers that rescore only the pool's 16,384 rows and
+select afresh; every layer attends over its selected FP4 rows.  Layers run in
+order, as in a model where each layer's query depends on the layer before.
+Other workloads (--workload full_64k, chain_128k, ...) run their own chains.
 
 Prints one JSON line.  --impl reference times the CPU oracle instead (on a
 bounded sample of the same workload).  Under torchrun each rank runs its own
@@ -34,7 +37,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="full_64k")
+    ap.add_argument("--workload", default="hier_1m")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -349,33 +352,45 @@ def capture(fn):
     return g
 
 
+def layer_kinds(wl):
+    """The distinct layer kinds of the chain, in order, with how many layers of
+    each kind one step runs: [(kind, first layer index, count)].  A kind is the
+    mode plus whether it builds or reads the hierarchical pool."""
+    from fp4_compressed_sparse_append_b300 import workloads as W
+    kinds, seen = [], {}
+    pool_built = False
+    for li, mode in enumerate(wl.layers):
+        if mode == W.FULL:
+            kind = "full+pool" if (wl.pool_blocks and not pool_built) else "full"
+            pool_built = pool_built or bool(wl.pool_blocks)
+        elif mode == W.REINDEX:
+            kind = "reindex.pool" if (wl.pool_blocks and pool_built) else "reindex"
+        else:
+            kind = "reuse"
+        if kind in seen:
+            kinds[seen[kind]][2] += 1
+        else:
+            seen[kind] = len(kinds)
+            kinds.append([kind, li, 1])
+    return [tuple(k) for k in kinds]
+
+
 def stage_times(cache, layers, wl, flush, steps, stream):
-    """Times the first layer's stages one at a time: each captured as a CUDA
-    graph, replayed with the L2 flushed before every replay."""
+    """Times the stages of the first layer of each layer kind one at a time,
+    each through its own public call, captured as a CUDA graph and replayed
+    with the L2 flushed before every replay (CUDA events on the launching
+    stream).  Returns {stage: {"ms", "launches", "kind", "stage"}} where
+    launches counts the stage's launches per step."""
     import torch
     from fp4_compressed_sparse_append_b300 import binding as B
     from fp4_compressed_sparse_append_b300 import workloads as W
 
-    la = layers[0]
-    q, iq, w = la.tensors["q"], la.tensors["iq"], la.tensors["w"]
-    out = {}
-    if la.struct.mode == W.REUSE:
-        return out
     dev = cache.device
-    scores = B.csa_index_score(cache, iq, w)
-    ws_sel = torch.empty(max(16, B.topk_workspace_size(cache, wl.P, wl.K)), dtype=torch.uint8, device=dev)
-    idx, _ = B.csa_topk(cache, scores, wl.K, workspace=ws_sel)
-    swa = la.swa
-    ws_att = torch.empty(max(16, B.attend_swa_workspace_size(cache, wl.P, wl.H, wl.K, swa)), dtype=torch.uint8,
-                         device=dev)
-    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    torch.cuda.synchronize()
 
     def timed(fn):
         g = capture(fn)
         ts = []
-        for i in range(max(3, steps) + 3):
+        for i in range(max(3, min(steps, 100)) + 3):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -386,10 +401,40 @@ def stage_times(cache, layers, wl, flush, steps, stream):
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in ts)
 
-    out["index_score"] = timed(lambda: B.csa_index_score(cache, iq, w, scores=scores))
-    out["topk"] = timed(lambda: B.csa_topk(cache, scores, wl.K, workspace=ws_sel))
-    out["sparse_attend"] = timed(lambda: B.csa_sparse_attend_swa(cache, q, idx, wl.scale, swa, workspace=ws_att,
-                                                                 out=o, lse=lse))
+    out = {}
+    for kind, li, count in layer_kinds(wl):
+        la = layers[li]
+        q, iq, w = la.tensors["q"], la.tensors["iq"], la.tensors["w"]
+        pool_in = la.tensors["pool_in"]
+        make_pool = la.pool_out is not None
+        if la.struct.mode != W.REUSE:
+            nblk = pool_in.shape[-1] if pool_in is not None else 0
+            scores = B.csa_index_score(cache, iq, w, pool=pool_in)
+            ws_sel = torch.empty(max(16, B.topk_workspace_size(cache, wl.P, wl.K, nblk,
+                                                               wl.pool_blocks if make_pool else 0)),
+                                 dtype=torch.uint8, device=dev)
+            idx, _ = B.csa_topk(cache, scores, wl.K, pool=pool_in, pool_keep=wl.pool_blocks if make_pool else 0,
+                                workspace=ws_sel)
+            torch.cuda.synchronize()
+            out[kind + ".index_score"] = dict(
+                ms=timed(lambda: B.csa_index_score(cache, iq, w, pool=pool_in, scores=scores)),
+                launches=count, kind=kind, stage="index_score")
+            out[kind + ".topk"] = dict(
+                ms=timed(lambda: B.csa_topk(cache, scores, wl.K, pool=pool_in,
+                                            pool_keep=wl.pool_blocks if make_pool else 0, workspace=ws_sel)),
+                launches=count, kind=kind, stage="topk")
+        else:
+            idx = la.idx
+        swa = la.swa
+        ws_att = torch.empty(max(16, B.attend_swa_workspace_size(cache, wl.P, wl.H, wl.K, swa)), dtype=torch.uint8,
+                             device=dev)
+        o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        out[kind + ".sparse_attend"] = dict(
+            ms=timed(lambda: B.csa_sparse_attend_swa(cache, q, idx, wl.scale, swa, workspace=ws_att, out=o,
+                                                     lse=lse)),
+            launches=count, kind=kind, stage="sparse_attend")
     return out
 
 
@@ -769,21 +814,31 @@ def config_of(wl):
             "l2": "flushed between timed steps (a 256 MiB read outside the timed events)"}
 
 
-def index_traffic_from_profile(workload):
-    """DRAM bytes per index_score launch from the committed ncu summary of this
-    workload's step (profiles/index_score_<workload>.md), or None where there
-    is none, or when the kernel's sources have changed since that capture (the
-    summary records the sha256 of the sources it was taken with)."""
+# Sources whose hash a profile summary records, per stage: the summary's DRAM
+# traffic applies only while these files are unchanged.
+STAGE_SOURCES = {
+    "index_score": ("index_score.cu", "common.cuh"),
+    "topk": ("topk.cu", "common.cuh"),
+    "sparse_attend": ("attend.cu", "common.cuh"),
+}
+
+
+def traffic_from_profile(stage, kind, workload):
+    """DRAM bytes per launch of a stage's kernel from the committed ncu summary
+    profiles/<stage>_<kind>_<workload>.md, or None where there is none, or when
+    the kernel's sources have changed since that capture (the summary records
+    the sha256 of the sources it was taken with)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "index_score_%s.md" % workload)
+    name = "%s_%s_%s.md" % (stage, kind.replace("+", "_").replace(".", "_"), workload)
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
-        return None, "no ncu capture of this workload"
+        return None, "no ncu capture of this stage on this workload"
     csrc = os.path.join(ROOT, "fp4_compressed_sparse_append_b300", "csrc")
     try:
         text = open(path).read()
         h = hashlib.sha256()
-        for name in ("index_score.cu", "common.cuh"):
-            with open(os.path.join(csrc, name), "rb") as f:
+        for src in STAGE_SOURCES[stage]:
+            with open(os.path.join(csrc, src), "rb") as f:
                 h.update(f.read())
     except OSError:
         return None, "no ncu summary"
@@ -793,47 +848,70 @@ def index_traffic_from_profile(workload):
         return None, "no ncu summary"
     if want.group(1) != h.hexdigest():
         return None, "kernel changed since the ncu capture"
-    return int(val.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/%s)" % os.path.basename(path)
+    return int(val.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/%s)" % name
 
 
-def stage_rooflines(wl, stages, index_bytes, peak_hbm, peak_src, peak_tf, peak_tf_src, traffic, traffic_src):
-    """Roofline of each stage of the first layer, each timed alone (stage_times):
-    index_score is bound by HBM (indexer keys scanned + queries and weights);
-    sparse_attend (the attention kernel and its split merge) by the tensor
-    cores: S = Q.V^T and O = P.V, 2*H*D flops each per selected row and query
-    (fp16 operands, the dense bf16 rate); topk is reported against HBM for the
-    scores it reads and the ids it writes."""
+def stage_bytes(wl, kind, stage):
+    """Algorithmic bytes (bytes that must move) of one launch of a stage:
+    index_score: the indexer keys scanned, the indexer queries and weights;
+    topk: the scores read (and the pool's block ids) and the ids written;
+    sparse_attend: the selected FP4 rows, the bf16 queries, the fp32 outputs
+    and log-sum-exps (and the local window's FP8 rows)."""
+    from fp4_compressed_sparse_append_b300 import workloads as W
     units = wl.B * wl.P
     L = wl.length_after_append
+    kb = W.key_bytes(wl)
+    pool_rows = wl.pool_blocks * 8
+    q_index = units * wl.HI * (wl.DI + 4)
+    if stage == "index_score":
+        keys = units * pool_rows * kb if kind == "reindex.pool" else wl.B * L * kb
+        return keys + q_index
+    if stage == "topk":
+        n = pool_rows if kind == "reindex.pool" else L
+        b = units * n * 4 + units * wl.K * 4
+        if kind == "reindex.pool":
+            b += units * wl.pool_blocks * 4
+        if kind == "full+pool":
+            b += units * wl.pool_blocks * 4
+        return b
+    row = wl.D // 2 + wl.D // 16
+    b = units * (min(wl.K, L) * row + wl.H * wl.D * (2 + 4) + wl.H * 4)
+    if wl.window:
+        b += wl.B * (wl.window + wl.P - 1) * wl.D
+    return b
+
+
+KERNELS = {"index_score": "index_score_kernel", "topk": "select_kernel",
+           "sparse_attend": "attend_kernel (+ attend_merge_kernel)"}
+
+
+def stage_rooflines(wl, stages, peak_hbm, peak_src, peak_tf, peak_tf_src):
+    """Roofline of every timed stage against HBM (the bound of every workload
+    but the multi-position verify ones, whose attention is reported against the
+    tensor cores: S = Q.V^T and O = P.V, 2*H*D flops each per selected row and
+    query, fp16 operands at the dense bf16 rate)."""
     out = {}
-    ms = stages.get("index_score")
-    if ms:
-        ach = index_bytes / (ms / 1e3) / 1e9
-        out["index_score"] = {
-            "kernel": "index_score_kernel", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
-            "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
-            "algorithmic_bytes_per_launch": index_bytes, "launch_ms": ms, "traffic": traffic,
-            "traffic_source": traffic_src}
-    ms = stages.get("topk")
-    if ms:
-        nbytes = units * min(L, wl.capacity) * 4 + units * wl.K * 4
-        ach = nbytes / (ms / 1e3) / 1e9
-        out["topk"] = {
-            "kernel": "select_kernel", "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
-            "frac": ach / peak_hbm, "peak_source": peak_src + " (copy bandwidth, burst)",
-            "algorithmic_bytes_per_launch": nbytes, "launch_ms": ms, "traffic": None,
-            "traffic_source": "not captured"}
-    ms = stages.get("sparse_attend")
-    if ms:
-        kk = min(wl.K, L)
-        flops = units * 4.0 * wl.H * kk * wl.D
-        ach = flops / (ms / 1e3) / 1e12
-        out["sparse_attend"] = {
-            "kernel": "attend_kernel + attend_merge_kernel", "bound": "tensor", "achieved": ach, "peak": peak_tf,
-            "unit": "TFLOP/s", "frac": ach / peak_tf, "peak_source": peak_tf_src + " (bf16 dense, burst)",
-            "algorithmic_flops_per_launch": flops,
-            "algorithmic_bytes_per_launch": units * (kk * (wl.D // 2 + wl.D // 16) + wl.H * wl.D * (2 + 4)),
-            "launch_ms": ms, "traffic": None, "traffic_source": "not captured"}
+    for name, st in stages.items():
+        ms = st["ms"]
+        stage = st["stage"]
+        nbytes = stage_bytes(wl, st["kind"], stage)
+        traffic, traffic_src = traffic_from_profile(stage, st["kind"], wl.name)
+        r = {"kernel": KERNELS[stage], "launches_per_step": st["launches"], "launch_ms": ms,
+             "share_of_stage_time": None, "algorithmic_bytes_per_launch": nbytes,
+             "traffic": traffic, "traffic_source": traffic_src}
+        if stage == "sparse_attend" and wl.P > 1:
+            flops = wl.B * wl.P * 4.0 * wl.H * min(wl.K, wl.length_after_append) * wl.D
+            ach = flops / (ms / 1e3) / 1e12
+            r.update(bound="tensor", achieved=ach, peak=peak_tf, unit="TFLOP/s", frac=ach / peak_tf,
+                     peak_source=peak_tf_src + " (bf16 dense, burst)", algorithmic_flops_per_launch=flops)
+        else:
+            ach = nbytes / (ms / 1e3) / 1e9
+            r.update(bound="hbm", achieved=ach, peak=peak_hbm, unit="GB/s", frac=ach / peak_hbm,
+                     peak_source=peak_src + " (copy bandwidth, burst)")
+        out[name] = r
+    total = sum(st["ms"] * st["launches"] for st in stages.values())
+    for name, st in stages.items():
+        out[name]["share_of_stage_time"] = st["ms"] * st["launches"] / total if total else None
     return out
 
 
@@ -877,10 +955,11 @@ def main():
     peak_tf = peaks.get("bf16_tflops")
     peak_tf_src = "measured" if peak_tf else "fallback"
     peak_tf = peak_tf or 1800.0
-    traffic, traffic_src = index_traffic_from_profile(wl.name)
-    dominant = max(r["stages"], key=r["stages"].get) if r["stages"] else None
-    rooflines = stage_rooflines(wl, r["stages"], r["index_bytes"], peak_hbm, peak_src, peak_tf, peak_tf_src,
-                                traffic, traffic_src)
+    # The dominant kernel: the stage with the largest time per step (its time
+    # alone times its launches per step).
+    stages = r["stages"]
+    dominant = max(stages, key=lambda k: stages[k]["ms"] * stages[k]["launches"]) if stages else None
+    rooflines = stage_rooflines(wl, stages, peak_hbm, peak_src, peak_tf, peak_tf_src)
     roof = rooflines.get(dominant)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -895,7 +974,7 @@ def main():
         "config": config_of(wl),
         "hbm_gbs": r["gbs"], "frac_of_8tbs": r["gbs"] / NOMINAL_HBM_GBS, "frac_of_measured_hbm": r["gbs"] / peak_hbm,
         "step_algorithmic_bytes": r["step_bytes"],
-        "stages_ms": r["stages"], "dominant_stage": dominant,
+        "stages_ms": {k: v["ms"] for k, v in stages.items()}, "dominant_stage": dominant,
         "layers_ms": {"modes": [W.MODE_NAMES[m] for m in wl.layers], "ms": r["layer_ms"],
                       "how": "each layer alone as a graph, L2 flushed before each replay"},
         "roofline": roof, "roofline_stages": rooflines, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],

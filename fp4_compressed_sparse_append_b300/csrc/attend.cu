@@ -723,7 +723,7 @@ Plan plan(const CacheView &c, int P, int K, const SwaView *swa)
     const int units = c.B * P;
     const int extra = swa ? 1 : 0;
     const int tiles = (K + kRows - 1) / kRows;
-    int want = 148 / units - extra;  // splits x queries within one wave of CTAs (one per SM)
+    int want = sm_count() / units - extra;  // splits x queries within one wave of CTAs (one per SM)
     if (want > tiles) want = tiles;
     if (want > kMaxSplit - extra) want = kMaxSplit - extra;
     if (want < 1) want = 1;

@@ -441,6 +441,27 @@ std::atomic<uint64_t> &launch_counter()
 
 void count_launch(int n) { launch_counter() += static_cast<uint64_t>(n); }
 
+int sm_count()
+{
+    static int counts[kMaxDevices];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();  // no device here: clear the error and plan for a B300
+        return 148;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 148;
+        }
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 namespace {
 
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,

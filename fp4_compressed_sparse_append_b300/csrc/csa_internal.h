@@ -55,6 +55,11 @@ cudaError_t launch_reload(const CacheView &c, const uint8_t *in, int n, int *sta
 // Host-side count of kernel launches issued by the library (csa_kernel_launches).
 void count_launch(int n = 1);
 
+// Streaming multiprocessors of the current device (queried once per device;
+// 148, a B300's count, when no device can be queried).  Grid and split plans
+// size themselves by it.
+int sm_count();
+
 // Launches `kernel` with programmatic stream serialization (it may begin while
 // the previous kernel on the stream finishes; the kernel calls pdl_wait()
 // before reading anything earlier work wrote) and, if cluster_x > 0, with

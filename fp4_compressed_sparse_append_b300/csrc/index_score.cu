@@ -624,8 +624,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-int g_num_sms = 0;
-
 }  // namespace
 
 cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
@@ -733,17 +731,11 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
         s8 = k8;
     }
 
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 148;
-    }
     auto kernel = a.mx ? index_score_kernel<true> : index_score_kernel<false>;
     const cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_kernel(kernel, dim3(g_num_sms * per_sm), dim3(kThreads), smem, st, 0, k128, k8, qm, s128, s8, a);
+    return launch_kernel(kernel, dim3(sm_count() * per_sm), dim3(kThreads), smem, st, 0, k128, k8, qm, s128, s8, a);
 }
 
 }  // namespace csa

@@ -276,7 +276,7 @@ cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, con
     if (n_new <= 0) return cudaSuccess;
     const int64_t work = static_cast<int64_t>(n_new) * (c.D / 8);
     int64_t blocks_x = (work + 255) / 256;
-    const int64_t want = (4 * 148 + c.B - 1) / c.B;  // enough CTAs to cover the GPU for tiny appends too
+    const int64_t want = (4 * static_cast<int64_t>(sm_count()) + c.B - 1) / c.B;  // cover the GPU for tiny appends too
     if (blocks_x > want * 8) blocks_x = want * 8;
     if (blocks_x < 1) blocks_x = 1;
     dim3 grid(static_cast<unsigned>(blocks_x), c.B);

@@ -482,7 +482,7 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
     int C = 1;
     while (C < kMaxCluster &&
            ((n_per_cluster + C - 1) / C > kSelCacheMax ||
-            (static_cast<int64_t>(grid_rows) * C < 148 && (n_per_cluster + 2 * C - 1) / (2 * C) >= min_chunk)))
+            (static_cast<int64_t>(grid_rows) * C < sm_count() && (n_per_cluster + 2 * C - 1) / (2 * C) >= min_chunk)))
         C *= 2;
     const int64_t chunk = (n_per_cluster + C - 1) / C;
     if (chunk > kSelCacheMax) return cudaErrorInvalidValue;

@@ -78,3 +78,99 @@ def ascending_then_padding(idx_row):
     n = int((v >= 0).sum())
     assert np.all(v[n:] == -1)
     assert np.all(np.diff(v[:n]) > 0)
+
+
+# ---------------------------------------------------------------------------
+# Whole chains
+# ---------------------------------------------------------------------------
+
+def oracle_inputs(wl: W.Workload, seed: int, lat, ik, seqs, threads: int):
+    """Oracle cache of the listed sequences (host copies of the same draws, the
+    step's appended rows included) and each layer's inputs for them."""
+    cache = oracle.Cache(len(seqs), wl.capacity, wl.D, wl.DI, key_format=wl.key_format)
+    w_ik = W.ikey_projection(wl, seed, device="cuda").cpu().numpy() if wl.project else None
+    project = oracle.project_ikeys_mx if wl.key_format == "mxfp4" else oracle.project_ikeys
+
+    def keys(rows_bits, given):
+        # projected workloads: the oracle projects the keys itself, from its own quantisation
+        if not wl.project:
+            return given
+        return np.stack([project(*oracle.quantize_rows(r), w_ik) for r in rows_bits])
+
+    lat_s = lat[seqs].cpu().numpy()
+    cache.append(lat_s, keys(lat_s, None if ik is None else ik[seqs].cpu().numpy()), threads=threads)
+    if wl.n_append:
+        app = W.append_rows(wl, seed, device="cuda")
+        rows_s = app["rows"][seqs].cpu().numpy()
+        cache.append(rows_s, keys(rows_s, app["ikeys"][seqs].cpu().numpy()))
+    inputs = []
+    for li in range(len(wl.layers)):
+        inp = W.layer_inputs(wl, seed, li, device="cuda")
+        inputs.append({k: v[seqs].cpu().numpy() for k, v in inp.items()})
+    swa = (W.local_rows(wl, seed, device="cuda")[seqs].cpu().numpy(), wl.window) if wl.window else None
+    return cache, inputs, swa
+
+
+def oracle_attend_unit(cache, j: int, p: int, q_bits, idx, wl: W.Workload, swa=None):
+    """The oracle's attention (joint with the local window when swa is given)
+    of oracle sequence j, position p over the selection idx."""
+    if swa is None:
+        return oracle.attend(q_bits, cache.codes[j], cache.scales[j], idx, wl.scale)
+    rows_b, window = swa[0][j], swa[1]
+    lo, hi = oracle.swa_window(rows_b.shape[0], wl.P, p, window)
+    return oracle.attend_swa(q_bits, cache.codes[j], cache.scales[j], idx, rows_b, lo, hi, wl.scale)
+
+
+def check_chain(wl: W.Workload, seed: int, gpu_layers, lat, ik, seqs, threads: int = 1) -> int:
+    """Checks every layer of a chain the GPU ran, on the listed sequences, at
+    every query position.
+
+    Several selections can be correct where scores tie to within the top-K
+    tolerance, so the GPU's choices are first checked against the oracle's
+    (check_topk), and the oracle then continues from the GPU's validated
+    choices: Reindex layers rescore the GPU's pool, Reuse layers attend over
+    the GPU's previous selection, and every attention output is compared with
+    the oracle's attention over the very rows the GPU selected.  Returns the
+    number of (layer, query) units whose selection differed by a near tie."""
+    cache, inputs, swa = oracle_inputs(wl, seed, lat, ik, seqs, threads)
+    units = [(j, p) for j in range(len(seqs)) for p in range(wl.P)]
+    prev, pool, near_ties = None, None, 0
+    for li, mode in enumerate(wl.layers):
+        g = gpu_layers[li]
+        gi = g.idx.cpu().numpy()
+        go = g.out.cpu().numpy()
+        r = oracle.run_layer(cache, mode, inputs[li], wl.K, wl.scale, wl.P,
+                             prev_idx=prev if mode == W.REUSE else None,
+                             pool_in=pool if mode == W.REINDEX else None,
+                             pool_keep=wl.pool_blocks if (mode == W.FULL and pool is None) else 0,
+                             units=units, threads=min(threads, len(units)), score_threads=threads, swa=swa)
+        for (j, p) in units:
+            b = seqs[j]
+            ru = r[(j, p)]
+            what = (wl.name, li, b, p)
+            ascending_then_padding(gi[b, p])
+            equal = True
+            if mode != W.REUSE:
+                if "rows" in ru:
+                    ok = ru["valid"] > 0
+                    by_row = dict(zip(ru["rows"][ok].tolist(), ru["scores"][ok].tolist()))
+                    scores_of = lambda rows, m=by_row: np.array([m[int(x)] for x in rows], np.float32)
+                else:
+                    scores_of = lambda rows, s=ru["scores"]: s[rows]
+                equal = check_topk(gi[b, p], ru["idx"], scores_of, wl.K, what)
+            if "pool" in ru:
+                bm = oracle.block_max(ru["scores"])
+                check_topk(g.pool_out.cpu().numpy()[b, p], ru["pool"], lambda blocks, s=bm: s[blocks],
+                           wl.pool_blocks, what + ("pool",))
+            if equal:
+                ref = ru["out"]
+            else:
+                near_ties += 1
+                ref, _ = oracle_attend_unit(cache, j, p, inputs[li]["q"][j, p], gi[b, p], wl, swa)
+            check_attention(go[b, p], ref, what)
+        if mode != W.REUSE:
+            prev = {(j, p): gi[seqs[j], p].astype(np.int64) for (j, p) in units}
+        if mode == W.FULL and wl.pool_blocks and pool is None:
+            gp = gpu_layers[li].pool_out.cpu().numpy()
+            pool = {(j, p): gp[seqs[j], p].astype(np.int64) for (j, p) in units}
+    return near_ties

@@ -144,7 +144,9 @@ def test_layer_step_with_window(mode):
                                         ik[b].cpu().numpy(), rows)
                 sel = oracle.topk(s, wl.K)
                 if not check_topk(la.idx[b, p].cpu().numpy(), sel, lambda r, s=s: s[r], wl.K, (b, p)):
-                    continue                    # a near-tie swap: the attended sets differ
+                    # a near-tie swap, which is a correct selection too: the
+                    # reference is the attention over the rows the GPU chose
+                    sel = la.idx[b, p].cpu().numpy().astype(np.int64)
             else:
                 sel = given[b, p].numpy()
             lo, hi = oracle.swa_window(local.shape[1], wl.P, p, wl.window)
