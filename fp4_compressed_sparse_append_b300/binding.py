@@ -21,7 +21,8 @@ CSA_POOL_BLOCK = 8
 CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
-    "csa_quantize_append", "csa_quantize_append_project", "csa_index_score", "csa_topk", "csa_topk_workspace_size", "csa_sparse_attend",
+    "csa_quantize_append", "csa_quantize_append_project", "csa_index_score", "csa_topk", "csa_topk_workspace_size",
+    "csa_pool_topk", "csa_sparse_attend",
     "csa_sparse_attend_noalloc", "csa_sparse_attend_swa", "csa_attend_swa_workspace_size",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
         L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, SZ, V]
         L.csa_topk_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
+        L.csa_pool_topk.argtypes = [C, I32, I32, V, V, V, I32, I32, V, V]
         L.csa_sparse_attend.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V, SZ, V]
         L.csa_sparse_attend_noalloc.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V]
         L.csa_attend_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
@@ -296,6 +298,26 @@ def csa_topk(cache: Cache, scores: torch.Tensor, K: int, pool: Optional[torch.Te
     _check(lib().csa_topk(cache.ref, P, _ptr(scores), ld, _ptr(pool), nblk, K, _ptr(idx), pool_keep,
                           _ptr(pool_out), _ptr(workspace), workspace.numel(), _stream(stream)), "csa_topk")
     return idx, pool_out
+
+
+def csa_pool_topk(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: torch.Tensor, K: int,
+                  idx: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Reindex over a pool in one call: iq [B, P, HI, DI] uint8, w [B, P, HI]
+    fp32, pool [B, P, nblk] int32 -> idx [B, P, K] int32 (the top K of the
+    pool's rows, ascending, -1 padded)."""
+    B, P, HI, _ = iq.shape
+    _lead(iq, "iq", cache.batch, cache.d_index)
+    nblk = pool.shape[-1]
+    Bc = cache.batch
+    _need(iq, Bc * P * HI * cache.d_index, "iq")
+    _need(w, Bc * P * HI * 4, "w")
+    _need(pool, Bc * P * nblk * 4, "pool")
+    if idx is None:
+        idx = torch.empty((B, P, K), dtype=torch.int32, device=cache.device)
+    _need(idx, Bc * P * K * 4, "idx")
+    _check(lib().csa_pool_topk(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, K, _ptr(idx),
+                               _stream(stream)), "csa_pool_topk")
+    return idx
 
 
 def attend_workspace_size(cache: Cache, P: int, H: int, K: int) -> int:

@@ -13,8 +13,11 @@
 //                  dequantises it to fp16 (E2M1 x E4M3 is exact in fp16) into a
 //                  K-major 128B-swizzled tile V[64 rows][D] (two buffers);
 //   MMA thread     S = Q . V^T (M = 64 heads, N = 64 rows, K = D; Q staged once
-//                  per CTA as fp16 scaled per head by a power of two, exact for
-//                  bf16 and safe from fp16 overflow), and O^T += V^T . P^T with
+//                  per CTA as fp16 scaled per head by a power of two, safe from
+//                  fp16 overflow and exact for every entry that lands in fp16's
+//                  normal range, i.e. for heads whose entries span fewer than
+//                  about 28 binades; smaller entries round to fp16 subnormals),
+//                  and O^T += V^T . P^T with
 //                  P split into fp16 high and low parts (two MMAs into one fp32
 //                  accumulator keep P's precision near fp32); V^T is read from
 //                  the same tile through an MN-major descriptor.  S of tile t+1
@@ -194,7 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         for (int kb = 0; kb < D / 64; ++kb)
             tma_load_2d(q_stage + kb * kMaxHeads * 128, &qmap, &sm.qbar, kb * 128, unit * H);
     }
-    // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15, before the
+    // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15 (exact while
+    // an entry stays within fp16's normal range, about 28 binades below the
+    // head's largest; smaller ones round to fp16 subnormals), before the
     // wait on the previous kernel (q is an input of the step): thread (head
     // qh, quarter qq) of the first 256 threads converts dims [qq*D/4, (qq+1)*D/4)
     // from the bf16 block in shared memory.
@@ -755,6 +760,7 @@ size_t smem_bytes(int D, int NH)
 
 size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K, const SwaView *swa)
 {
+    if (!swa && decode_supported(c, P, H, K)) return decode_workspace_bytes(c, P, H, K);
     const Plan p = plan(c, P, K, swa);
     if (p.nsplit == 1 || p.cluster) return 0;
     const size_t units = static_cast<size_t>(c.B) * P;
@@ -770,6 +776,8 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     const int units = c.B * P;
     if (units == 0) return cudaSuccess;
     if (H > kMaxHeads || c.D % 128 || c.D > 512) return cudaErrorInvalidValue;
+    if (!swa && decode_supported(c, P, H, K))
+        return launch_attend_decode(c, P, H, q, scale, idx, K, out, lse, ws, ws_bytes, status, st);
     if (swa && (!swa->rows || swa->n < P || swa->window < 1)) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(c.D, (H + 15) / 16 * 16);
     const Plan p = plan(c, P, K, swa);

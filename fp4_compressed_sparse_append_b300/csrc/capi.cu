@@ -231,12 +231,32 @@ csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int6
     const size_t need = topk_ws(cache, P, pool_blocks, pool != nullptr, K, pool_keep, pool_out != nullptr);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CSA_ERR_WORKSPACE;
     const csa::CacheView v = view(cache);
+    if (pool_out && csa::pool_rows_supported(pool_keep, K)) {
+        // the pool first; the top K rows then lie in the pool's blocks
+        cudaError_t e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out,
+                                           workspace, workspace_bytes, stream);
+        if (e == cudaSuccess) e = csa::launch_pool_rows(v, P, scores, ld, pool_out, pool_keep, K, idx, stream);
+        return from_cuda(e);
+    }
     cudaError_t e =
         csa::launch_select(v, P, scores, ld, pool, pool ? pool_blocks : 0, 1, K, idx, workspace, workspace_bytes, stream);
     if (e == cudaSuccess && pool_out)
         e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out, workspace,
                                workspace_bytes, stream);
     return from_cuda(e);
+}
+
+csa_status csa_pool_topk(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
+                         const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx, csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (P < 1 || HI < 1 || K < 1 || K > 16384 || !iq || !w || !pool || !idx || pool_blocks < 1) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(iq) || !aligned16(w) || !aligned16(pool) || !aligned16(idx)) return CSA_ERR_INVALID_ARG;
+    if (!csa::pool_select_supported(view(cache), P, HI, pool_blocks, K)) return CSA_ERR_UNSUPPORTED;
+    int *st = status_word();
+    if (!st) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_pool_select(view(cache), P, HI, iq, w, pool, pool_blocks, K, idx, st, stream));
 }
 
 csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K, size_t *bytes)
@@ -314,6 +334,14 @@ csa_status csa_sparse_attend_swa(const csa_cache *cache, int32_t P, int32_t H, c
         csa::launch_attend(v, P, H, q, scale, idx, K, out, lse, workspace, workspace_bytes, st, stream, svp));
 }
 
+// A Reindex layer over a pool whose scoring and selection run as one kernel
+// (no scores in the workspace).
+static bool layer_pool_fused(const csa_cache *cache, const csa_layer_args *a)
+{
+    return a->mode == CSA_REINDEX && a->pool_in &&
+           csa::pool_select_supported(view(cache), a->P, a->HI, a->pool_blocks, a->K);
+}
+
 static size_t layer_scores_ld(const csa_cache *cache, const csa_layer_args *a)
 {
     if (a->mode == CSA_REINDEX && a->pool_in) return round_up(static_cast<size_t>(a->pool_blocks) * CSA_POOL_BLOCK, 4);
@@ -364,7 +392,7 @@ csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args
     if (!bytes) return CSA_ERR_INVALID_ARG;
     const csa::CacheView v = view(cache);
     size_t total = 0;
-    if (a->mode != CSA_REUSE) {
+    if (a->mode != CSA_REUSE && !layer_pool_fused(cache, a)) {
         total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_scores_ld(cache, a) * sizeof(float), 256);
         total += round_up(layer_select_ws(cache, a), 256);
     }
@@ -386,7 +414,10 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
     const csa::CacheView v = view(cache);
     uint8_t *ws = static_cast<uint8_t *>(a->workspace);
     cudaError_t e = cudaSuccess;
-    if (a->mode != CSA_REUSE) {
+    if (layer_pool_fused(cache, a)) {
+        e = csa::launch_pool_select(v, a->P, a->HI, a->iq, a->w, a->pool_in, a->pool_blocks, a->K, a->idx, st, stream);
+        if (e != cudaSuccess) return CSA_ERR_CUDA;
+    } else if (a->mode != CSA_REUSE) {
         const int64_t ld = static_cast<int64_t>(layer_scores_ld(cache, a));
         float *scores = reinterpret_cast<float *>(ws);
         ws += round_up(static_cast<size_t>(cache->batch) * a->P * ld * sizeof(float), 256);
@@ -400,11 +431,22 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         const int32_t *pool = a->mode == CSA_REINDEX ? a->pool_in : nullptr;
         const int pool_blocks = pool ? a->pool_blocks : 0;
         e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);
-        if (e == cudaSuccess)
-            e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, sel_ws, sel_bytes, stream);
-        if (e == cudaSuccess && a->mode == CSA_FULL && a->pool_out)
-            e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out, sel_ws,
-                                   sel_bytes, stream);
+        const bool make_pool = a->mode == CSA_FULL && a->pool_out;
+        if (make_pool && csa::pool_rows_supported(a->pool_blocks, a->K)) {
+            // the pool first; the top K rows then lie in the pool's blocks
+            if (e == cudaSuccess)
+                e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out,
+                                       sel_ws, sel_bytes, stream);
+            if (e == cudaSuccess)
+                e = csa::launch_pool_rows(v, a->P, scores, ld, a->pool_out, a->pool_blocks, a->K, a->idx, stream);
+        } else {
+            if (e == cudaSuccess)
+                e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, sel_ws, sel_bytes,
+                                       stream);
+            if (e == cudaSuccess && make_pool)
+                e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out,
+                                       sel_ws, sel_bytes, stream);
+        }
         if (e != cudaSuccess) return CSA_ERR_CUDA;
     }
     const csa::SwaView sv = a->swa ? swa_view(a->swa) : csa::SwaView{};
@@ -496,6 +538,20 @@ CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t in
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tensor_map_2d_f32(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                                  uint32_t box_cols, uint32_t box_rows)
+{
+    const EncodeFn fn = encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 

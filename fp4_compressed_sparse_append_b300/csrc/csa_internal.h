@@ -36,6 +36,19 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
                           int pool_blocks, int block, int K, int32_t *out, void *ws, size_t ws_bytes,
                           cudaStream_t st);
 
+// a4 over a pool in one kernel (scores stay on chip; E4M3 keys, HI <= 64,
+// pools of up to 2,048 blocks).
+int pool_select_supported(const CacheView &c, int P, int HI, int pool_blocks, int K);
+cudaError_t launch_pool_select(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
+                               const int32_t *pool, int pool_blocks, int K, int32_t *idx, int *status,
+                               cudaStream_t st);
+
+// Full layer with a pool of pool_keep >= K blocks: the top K rows from the
+// pool's rows (exact, see pool_select.cu), given the scan's scores.
+int pool_rows_supported(int pool_keep, int K);
+cudaError_t launch_pool_rows(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
+                             int pool_blocks, int K, int32_t *idx, cudaStream_t st);
+
 // a5/a6, and the local window of the joint softmax (rows [B][n][D] FP8 E4M3).
 struct SwaView {
     const uint8_t *rows;
@@ -46,6 +59,14 @@ size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K, const Swa
 cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, float scale, const int32_t *idx,
                           int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st,
                           const SwaView *swa = nullptr);
+
+// a5/a6 for few queries (every query's splits within one wave of CTAs): one
+// cluster per query, split partials merged through the workspace.
+int decode_supported(const CacheView &c, int P, int H, int K);
+size_t decode_workspace_bytes(const CacheView &c, int P, int H, int K);
+cudaError_t launch_attend_decode(const CacheView &c, int P, int H, const uint16_t *q, float scale,
+                                 const int32_t *idx, int K, float *out, float *lse, void *ws, size_t ws_bytes,
+                                 int *status, cudaStream_t st);
 
 // Persistent records of cache rows (main entry codes, scales, indexer entry).
 size_t record_bytes(const CacheView &c);
@@ -95,6 +116,10 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
                                  uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// fp32 matrix [rows][cols] (row stride cols * 4 bytes), boxes of box_cols x
+// box_rows elements landing in shared memory row after row, no swizzle.
+CUresult encode_tensor_map_2d_f32(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                                  uint32_t box_cols, uint32_t box_rows);
 // Rows of 128 packed 4-bit values (64 bytes): a box of box_rows rows lands in
 // shared memory as 128-byte rows, each 16-byte chunk holding 8 code bytes then
 // 8 untouched bytes, with the 128-byte swizzle; the copy completes 64 bytes a

@@ -1,0 +1,661 @@
+// a4: a Reindex layer over the hierarchical pool, scoring and selection in one
+// kernel.  "G2C Brief - DeepSeek V4.1-Flash", section "The hierarchical
+// indexer: making later indexers context-independent": the first Full layer
+// keeps a pool of 2,048 blocks of 8 positions, and later Reindex layers score
+// only the pool's 16,384 rows with their own indexer query and keep the best
+// K; section "CSA2: most layers don't keep their own cache" (Reindex borrows
+// the keys and selects afresh).  Score: sum_h w_h * ReLU(iq_h . ik), FP8 E4M3
+// queries and keys, fp32 accumulation.
+//
+// One thread-block cluster per (sequence, position): CTA r of C takes a
+// contiguous share of the pool's blocks (at most 128 blocks, 1,024 rows).
+//   1. Each of its first 128 threads reads one block id and starts the TMA
+//      copy of that block's 8 key rows into the CTA's tile of 16 blocks; the
+//      indexer query arrives by TMA too.
+//   2. One thread issues, per 128-row tile, the kind::f8f6f4 MMA
+//      D[128 rows x HI] = K_tile . Q^T into its own tensor-memory columns.
+//   3. Four warps (one per lane quarter) turn each row's HI accumulators into
+//      sum_h w_h ReLU(.) and store the row's order-preserving score key (0 for
+//      an empty pool slot or a row past the visible length) straight into the
+//      shared memory of CTA 0, with the block ids.
+//   4. After one cluster barrier CTA 0 alone selects the K largest keys of the
+//      whole pool (ties: the earlier pool slot, which is the lower row id for
+//      an ascending pool) by a radix select over the keys' actual range: the
+//      first pass histograms the top 11 bits of (key - min key), so the bins
+//      spread over the scores present; later passes resolve the threshold bin.
+//      Selected rows are written in pool order, then -1 padding.
+// Every wait is bounded; a wait that runs out raises CSA_DEV_TIMEOUT.
+#include "common.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kTileRows = 128;
+constexpr int kMaxTiles = 8;                   // 1,024 rows per CTA
+constexpr int kBlocksPerCta = kMaxTiles * kTileRows / kPoolBlock;  // 128
+constexpr int kMaxCluster = 16;
+constexpr int kMaxCand = kMaxCluster * kMaxTiles * kTileRows;     // 16,384
+constexpr int kDigitBits = 13;                // radix digit: 8,192 bins
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kU = 4;                          // keys in flight per thread in each pass
+
+struct PoolArgs {
+    int P, HI, cap, DI;
+    const int32_t *lengths;
+    const int32_t *pool;    // [units][pool_blocks], ascending, -1 padded
+    int pool_blocks;
+    int bpc;                // blocks per CTA (<= 128)
+    const float *w;         // [units][HI]
+    int K;
+    int32_t *idx;           // [units][K]
+    int *status;
+};
+
+struct PoolSmem {
+    uint64_t tbar[kMaxTiles];   // key tile copied
+    uint64_t mbar[kMaxTiles];   // tile's MMA done
+    uint64_t qbar, done;
+    float w[64];
+    int32_t blk[kBlocksPerCta];
+    uint32_t warp_a[kThreads / 32], warp_b[kThreads / 32];
+    uint32_t jw[kMaxCand / 32];   // per (round, warp) taken-key counts, then their exclusive prefix
+    uint32_t res_bin, res_above;
+    uint32_t tmem_slot;
+    int abort;
+};
+
+__device__ __forceinline__ uint32_t swizzle_mode(int di)
+{
+    return di == 128 ? 2u : (di == 64 ? 4u : 6u);  // 128B, 64B, 32B
+}
+
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Block-wide sums of two per-thread values; every thread gets both totals.
+__device__ __forceinline__ void block_sum2(uint32_t &a, uint32_t &b, PoolSmem &sm)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+        b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    }
+    __syncthreads();
+    if (lane == 0) {
+        sm.warp_a[warp] = a;
+        sm.warp_b[warp] = b;
+    }
+    __syncthreads();
+    a = 0;
+    b = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) {
+        a += sm.warp_a[i];
+        b += sm.warp_b[i];
+    }
+}
+
+// Block-wide exclusive scan of one value per thread; *total gets the sum.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, PoolSmem &sm, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) sm.warp_a[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, t = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) {
+        if (i < warp) before += sm.warp_a[i];
+        t += sm.warp_a[i];
+    }
+    *total = t;
+    return before + x - v;
+}
+
+// The K largest of n order-preserving keys in shared memory (0 = no
+// candidate), ties to the earlier candidate, written in candidate order as
+// row ids (candidate c is row blk[c / 8] * 8 + c % 8), then -1 padding.  All
+// threads of the CTA call it.  A radix select over the keys' actual range:
+// pass 0 finds the count, minimum and maximum; each further pass histograms
+// the next 11 bits of (key - minimum) among the keys that share the bits
+// fixed so far, until the threshold bin is taken whole or one value is left.
+// Every pass keeps kU keys per thread in flight: one CTA does all the work,
+// so its loops are bound by latency, not by issue.
+__device__ __forceinline__ void select_from_keys(const uint32_t *allk, const int32_t *allb, int n, int Kin, int32_t *out,
+                                              uint32_t *hist, PoolSmem &sm)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t K = static_cast<uint32_t>(Kin);
+    // Pass 0: count, minimum and maximum of the candidate keys (0 = none).
+    uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0;
+    for (int i0 = tid; i0 < n; i0 += kU * kThreads) {
+        uint32_t kk[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) kk[u] = i0 + u * kThreads < n ? allk[i0 + u * kThreads] : 0u;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (kk[u]) {
+                ++cnt;
+                kmin = min(kmin, kk[u]);
+                kmax = max(kmax, kk[u]);
+            }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+    }
+    __syncthreads();
+    if (lane == 0) {
+        sm.warp_a[warp] = kmin;
+        sm.warp_b[warp] = kmax;
+    }
+    __syncthreads();
+    kmin = 0xFFFFFFFFu;
+    kmax = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) {
+        kmin = min(kmin, sm.warp_a[i]);
+        kmax = max(kmax, sm.warp_b[i]);
+    }
+    uint32_t total = cnt, unused = 0;
+    block_sum2(total, unused, sm);
+
+    // Threshold: keys > thr_gt are taken, and the first `need` keys equal to
+    // thr_eq (in pool order).
+    uint32_t thr_gt = 0, thr_eq = 0, need = 0;
+    if (total > K) {
+        const uint32_t range = kmax - kmin;
+        int hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
+        uint32_t prefix = 0, above = 0;
+        while (true) {
+            if (hi == 0) {
+                // a single key value remains: ties
+                thr_gt = kmin + prefix;
+                thr_eq = thr_gt;
+                need = K - above;
+                break;
+            }
+            const int lo = hi > kDigitBits ? hi - kDigitBits : 0;
+            const int nb = 1 << (hi - lo);
+            __syncthreads();
+            for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+            __syncthreads();
+            for (int i0 = tid; i0 < n; i0 += kU * kThreads) {
+                uint32_t kk[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) kk[u] = i0 + u * kThreads < n ? allk[i0 + u * kThreads] : 0u;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const uint64_t v = kk[u] - kmin;
+                    if (kk[u] && (v >> hi) == prefix) atomicAdd(&hist[(v >> lo) & (nb - 1)], 1u);
+                }
+            }
+            __syncthreads();
+            // the bin holding the (K - above)-th largest key: thread t scans
+            // bins [nb - (t+1)*per, nb - t*per) from the top
+            const uint32_t want = K - above;
+            const int per = nb >= kThreads ? nb / kThreads : 1;
+            const int bhi = nb - tid * per, blo = bhi - per;
+            uint32_t ssum = 0;
+            if (blo >= 0)
+                for (int bb = blo; bb < bhi; ++bb) ssum += hist[bb];
+            uint32_t tot;
+            const uint32_t excl = block_exclusive_scan(ssum, sm, &tot);
+            if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
+                uint32_t cum = excl;
+                for (int bb = bhi - 1; bb >= blo; --bb) {
+                    if (cum + hist[bb] >= want) {
+                        sm.res_bin = static_cast<uint32_t>(bb);
+                        sm.res_above = cum;
+                        break;
+                    }
+                    cum += hist[bb];
+                }
+            }
+            __syncthreads();
+            const uint32_t bin = sm.res_bin;
+            above += sm.res_above;
+            const uint32_t in_bin = hist[bin];
+            prefix = (prefix << (hi - lo)) | bin;
+            hi = lo;
+            if (above + in_bin == K) {
+                // the threshold bin is taken whole
+                thr_gt = kmin + (prefix << lo) - 1u;
+                need = 0;
+                break;
+            }
+        }
+    }
+
+    // Output in candidate order.  Round j covers candidates [j*T, (j+1)*T)
+    // (T threads, consecutive candidates in consecutive lanes); per (round,
+    // warp) counts of taken keys come from warp ballots, and one block scan of
+    // those counts gives every taken key its position.
+    const int J = (n + kThreads - 1) / kThreads;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int j0 = 0; j0 < J; j0 += kU) {
+        uint32_t kk[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int c = (j0 + u) * kThreads + tid;
+            kk[u] = (j0 + u < J && c < n) ? allk[c] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const unsigned ba = __ballot_sync(0xFFFFFFFFu, kk[u] && kk[u] > thr_gt);
+            const unsigned be = __ballot_sync(0xFFFFFFFFu, need && kk[u] == thr_eq);
+            if (lane == 0 && j0 + u < J)
+                sm.jw[(j0 + u) * (kThreads / 32) + warp] = (static_cast<uint32_t>(__popc(ba)) << 16) | __popc(be);
+        }
+    }
+    __syncthreads();
+    {
+        // each thread scans a few consecutive (round, warp) counts
+        const int nw = J * (kThreads / 32);
+        const int per = (nw + kThreads - 1) / kThreads;
+        const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
+        uint32_t sum = 0;
+        for (int w = w0; w < w1; ++w) sum += sm.jw[w];
+        uint32_t tot;
+        uint32_t run = block_exclusive_scan(sum, sm, &tot);
+        for (int w = w0; w < w1; ++w) {
+            const uint32_t v = sm.jw[w];
+            sm.jw[w] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int j0 = 0; j0 < J; j0 += kU) {
+        uint32_t kk[kU], base[kU];
+        int32_t blk[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int c = (j0 + u) * kThreads + tid;
+            const bool in = j0 + u < J && c < n;
+            kk[u] = in ? allk[c] : 0u;
+            blk[u] = in ? allb[c >> 3] : -1;
+            base[u] = j0 + u < J ? sm.jw[(j0 + u) * (kThreads / 32) + warp] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int c = (j0 + u) * kThreads + tid;
+            const bool is_above = kk[u] && kk[u] > thr_gt;
+            const bool is_tie = need && kk[u] == thr_eq;
+            const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
+            const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
+            const uint32_t a_before = (base[u] >> 16) + __popc(ba & lt);
+            const uint32_t t_before = (base[u] & 0xFFFFu) + __popc(be & lt);
+            int64_t pos = -1;
+            if (is_above) pos = a_before + min(t_before, need);
+            else if (is_tie && t_before < need) pos = a_before + t_before;
+            if (pos >= 0) out[pos] = blk[u] * kPoolBlock + (c & 7);
+        }
+    }
+    const uint32_t selected = total > K ? K : total;
+    for (uint32_t j = selected + tid; j < K; j += kThreads) out[j] = -1;
+}
+
+template <int HT>
+__global__ void __launch_bounds__(kThreads, 1)
+    pool_select_kernel(const __grid_constant__ CUtensorMap keys8, const __grid_constant__ CUtensorMap qmap, PoolArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    const int DI = a.DI;
+    uint8_t *k_s = base;                                       // [8 tiles][128 rows][DI] key tiles
+    uint8_t *q_s = k_s + kMaxTiles * kTileRows * DI;           // [HT rows][DI] indexer query
+    uint32_t *allk = reinterpret_cast<uint32_t *>(q_s + ((HT * DI + 1023) & ~1023));  // CTA 0: [candidates] keys
+    int32_t *allb = reinterpret_cast<int32_t *>(allk + kMaxCand);                    // CTA 0: [blocks] ids
+    PoolSmem &sm = *reinterpret_cast<PoolSmem *>(allb + kMaxCluster * kBlocksPerCta);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(k_s);      // CTA 0, select phase: over the dead key tiles
+    volatile int *abort_flag = &sm.abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.y;
+    const uint32_t rank = blockIdx.x;   // cluster rank (the cluster spans x)
+    const int C = gridDim.x;
+    const int n_tiles = (a.bpc * kPoolBlock + kTileRows - 1) / kTileRows;
+
+    if (tid == 0) {
+        for (int t = 0; t < kMaxTiles; ++t) {
+            mbar_init(&sm.tbar[t], 16);
+            mbar_init(&sm.mbar[t], 1);
+        }
+        mbar_init(&sm.qbar, 1);
+        mbar_init(&sm.done, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&keys8);
+        prefetch_tensormap(&qmap);
+    }
+    if (warp == 4) {
+        tmem_alloc(&sm.tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // Every CTA of the cluster has started before any stores into CTA 0.
+    if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    const uint32_t tmem = sm.tmem_slot;
+
+    // Below: reads of what earlier work on the stream wrote.
+    pdl_wait();
+    pdl_trigger();
+    const int b = unit / a.P, p = unit % a.P;
+    const int Lp = min(a.lengths[b], a.cap) - a.P + 1 + p;
+    const int cap_blocks = (a.cap + kPoolBlock - 1) / kPoolBlock;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(HT * DI));
+        tma_load_2d(q_s, &qmap, &sm.qbar, 0, unit * a.HI);
+    }
+    if (tid < HT) sm.w[tid] = tid < a.HI ? a.w[static_cast<int64_t>(unit) * a.HI + tid] : 0.f;
+    if (tid < n_tiles * 16) {
+        // one pool block per thread: its id, and the copy of its 8 key rows
+        const int j = rank * a.bpc + tid;
+        int32_t blk = (tid < a.bpc && j < a.pool_blocks) ? a.pool[static_cast<int64_t>(unit) * a.pool_blocks + j] : -1;
+        if (blk >= cap_blocks) blk = -1;
+        sm.blk[tid] = blk;
+        uint64_t *bar = &sm.tbar[tid >> 4];
+        if (blk >= 0) {
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kPoolBlock * DI));
+            tma_load_2d(k_s + tid * kPoolBlock * DI, &keys8, bar, 0, b * a.cap + blk * kPoolBlock);
+        } else {
+            mbar_arrive(bar);
+        }
+    }
+    __syncthreads();  // block ids and weights in shared memory
+    if (C > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sw = swizzle_mode(DI), sbo = 8 * DI;
+            const uint64_t da0 = smem_desc(smem_u32(k_s), 16, sbo, sw);
+            const uint64_t db = smem_desc(smem_u32(q_s), 16, sbo, sw);
+            const uint32_t idesc = instr_desc(128, HT, 0, 0, 0, 0);
+            bool ok = mbar_wait<true>(&sm.qbar, 0, abort_flag);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                if (!mbar_wait<true>(&sm.tbar[t], 0, abort_flag)) break;
+                tc_fence_after();
+                const uint64_t da = da0 + static_cast<uint64_t>((t * kTileRows * DI) >> 4);
+                for (int k = 0; k < DI / 32; ++k) mma_f8f6f4(tmem + t * HT, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
+                mma_commit(&sm.mbar[t]);
+            }
+            // Before tensor memory is released and the key tiles are reused:
+            // every issued MMA has completed and every key copy has landed.
+            mma_commit(&sm.done);
+            unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(&sm.done, 0) && global_ns() - t0 < kWaitLimitNs) {
+            }
+            for (int t = 0; t < n_tiles; ++t) {
+                t0 = global_ns();
+                while (!mbar_try_wait(&sm.tbar[t], 0) && global_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ scores
+        const int row = warp * 32 + lane;                                  // row within a tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t dst0 = cluster_map(smem_u32(allk), 0) + rank * a.bpc * kPoolBlock * 4;
+        const uint32_t dstb = cluster_map(smem_u32(allb), 0) + rank * a.bpc * 4;
+        if (row < a.bpc) st_cluster_u32(dstb + row * 4, static_cast<uint32_t>(sm.blk[row]));
+        for (int t = 0; t < n_tiles; ++t) {
+            if (!mbar_wait<true>(&sm.mbar[t], 0, abort_flag)) break;
+            tc_fence_after();
+            float s = 0.f;
+            {
+                // 32 heads' accumulators at a time (registers are few at 1,024 threads)
+                constexpr int HC = HT < 32 ? HT : 32;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < HT; c0 += HC) {
+                    uint32_t r[HC];
+#pragma unroll
+                    for (int c = 0; c < HC; c += 16)
+                        tmem_ld16(tmem + lane_off + t * HT + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(&r[c]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < HC; h += 4) {
+                        s0 = fmaf(sm.w[c0 + h], fmaxf(__uint_as_float(r[h]), 0.f), s0);
+                        s1 = fmaf(sm.w[c0 + h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
+                        s2 = fmaf(sm.w[c0 + h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
+                        s3 = fmaf(sm.w[c0 + h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+                    }
+                }
+                s = (s0 + s1) + (s2 + s3);
+            }
+            const int local = t * kTileRows + row;      // candidate within this CTA
+            if (local < a.bpc * kPoolBlock) {
+                const int32_t blk = sm.blk[local >> 3];
+                const bool valid = blk >= 0 && blk * kPoolBlock + (local & 7) < Lp;
+                st_cluster_u32(dst0 + local * 4, valid ? score_key(s) : 0u);
+            }
+        }
+    }
+
+    // Every CTA's keys are in CTA 0 after this barrier.
+    tc_fence_before();
+    __syncthreads();
+    if (C > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (*abort_flag && tid == 0) raise_status(a.status, CSA_DEV_TIMEOUT);
+    if (rank != 0) return;
+
+    select_from_keys(allk, allb, C * a.bpc * kPoolBlock, a.K, a.idx + static_cast<int64_t>(unit) * a.K, hist, sm);
+}
+
+// A Full layer that also keeps a pool of at least K blocks selects its top K
+// rows among the pool's rows, from the scores the scan wrote.  This is exact:
+// a block outside the pool has at least pool_keep >= K blocks ranked above it
+// (best member score, then lower block id), and each of those holds a visible
+// row that outranks every row of that block (a higher score, or an equal
+// score at a lower row id), so none of its rows is among the top K.  One CTA
+// per (sequence, position) reads the pool's rows' scores and selects.
+struct RowsArgs {
+    const float *scores;    // [units][ld]
+    int64_t ld;
+    const int32_t *lengths;
+    int cap, P;
+    const int32_t *pool;    // [units][pool_blocks], ascending, -1 padded
+    int pool_blocks;
+    int K;
+    int32_t *idx;           // [units][K]
+};
+
+__global__ void __launch_bounds__(kThreads, 1) pool_rows_kernel(RowsArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint32_t *allk = reinterpret_cast<uint32_t *>(smem_raw);       // [pool rows] keys
+    int32_t *allb = reinterpret_cast<int32_t *>(allk + kMaxCand);   // [pool blocks] ids
+    uint32_t *hist = reinterpret_cast<uint32_t *>(allb + kMaxCluster * kBlocksPerCta);
+    PoolSmem &sm = *reinterpret_cast<PoolSmem *>(hist + kBins);
+    const int tid = threadIdx.x;
+    const int unit = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int b = unit / a.P, p = unit % a.P;
+    const int Lp = min(a.lengths[b], a.cap) - a.P + 1 + p;
+    const int cap_blocks = (a.cap + kPoolBlock - 1) / kPoolBlock;
+    const int32_t *prow = a.pool + static_cast<int64_t>(unit) * a.pool_blocks;
+    for (int j = tid; j < a.pool_blocks; j += kThreads) {
+        int32_t blk = prow[j];
+        if (blk >= cap_blocks) blk = -1;
+        allb[j] = blk;
+    }
+    __syncthreads();
+    const float *srow = a.scores + static_cast<int64_t>(unit) * a.ld;
+    const int n = a.pool_blocks * kPoolBlock;
+    // Each block's 8 scores are two 16-byte loads (row ids are multiples of 8
+    // and ld a multiple of 4); four blocks per thread are in flight at once.
+    for (int j0 = tid; j0 < a.pool_blocks; j0 += kU * kThreads) {
+        float4 v[kU][2];
+        int32_t blk[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = j0 + u * kThreads;
+            blk[u] = j < a.pool_blocks ? allb[j] : -1;
+            const int64_t r0 = static_cast<int64_t>(blk[u] >= 0 ? blk[u] : 0) * kPoolBlock;
+            if (blk[u] >= 0 && r0 + kPoolBlock <= a.ld) {
+                const float4 *sp = reinterpret_cast<const float4 *>(srow + r0);
+                v[u][0] = __ldg(sp);
+                v[u][1] = __ldg(sp + 1);
+            } else {
+                // a block that reaches past the row's end (capacity not a
+                // multiple of 8): its rows one by one, within the row
+                float t[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) t[m] = (blk[u] >= 0 && r0 + m < a.ld) ? __ldg(srow + r0 + m) : 0.f;
+                v[u][0] = make_float4(t[0], t[1], t[2], t[3]);
+                v[u][1] = make_float4(t[4], t[5], t[6], t[7]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j >= a.pool_blocks) continue;
+            const float f[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+            uint32_t kq[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) kq[m] = (blk[u] >= 0 && blk[u] * kPoolBlock + m < Lp) ? score_key(f[m]) : 0u;
+            uint4 *dst = reinterpret_cast<uint4 *>(allk + j * kPoolBlock);
+            dst[0] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+            dst[1] = make_uint4(kq[4], kq[5], kq[6], kq[7]);
+        }
+    }
+    __syncthreads();
+    select_from_keys(allk, allb, n, a.K, a.idx + static_cast<int64_t>(unit) * a.K, hist, sm);
+}
+
+size_t pool_smem_bytes(int DI, int HT)
+{
+    return 1024 + static_cast<size_t>(kMaxTiles) * kTileRows * DI + ((static_cast<size_t>(HT) * DI + 1023) & ~size_t(1023)) +
+           static_cast<size_t>(kMaxCand) * 4 + kMaxCluster * kBlocksPerCta * 4 + sizeof(PoolSmem);
+}
+
+int heads_tile(int HI) { return HI <= 16 ? 16 : (HI <= 32 ? 32 : 64); }
+
+// The kernel's shared-memory limit is set once, to the largest request any
+// call can make (128-byte keys).
+template <int HT>
+cudaError_t configure()
+{
+    static bool done = false;
+    if (done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(pool_select_kernel<HT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(pool_smem_bytes(128, HT)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(pool_select_kernel<HT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    done = e == cudaSuccess;
+    return e;
+}
+
+}  // namespace
+
+int pool_select_supported(const CacheView &c, int P, int HI, int pool_blocks, int K)
+{
+    // E4M3 keys, HI <= 64 heads (a multiple of 16 or 8 padded up), pools of
+    // up to 2,048 blocks (16 CTAs of 128 blocks), K <= 16,384.
+    return !c.mx && HI >= 1 && HI <= 64 && (c.DI == 32 || c.DI == 64 || c.DI == 128) && pool_blocks >= 1 &&
+           pool_blocks <= kMaxCluster * kBlocksPerCta && K >= 1 && K <= kMaxCand && c.B * P >= 1;
+}
+
+int pool_rows_supported(int pool_keep, int K)
+{
+    return pool_keep >= K && pool_keep <= kMaxCluster * kBlocksPerCta;
+}
+
+cudaError_t launch_pool_rows(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
+                             int pool_blocks, int K, int32_t *idx, cudaStream_t st)
+{
+    if (!pool_rows_supported(pool_blocks, K)) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(kMaxCand) * 4 + kMaxCluster * kBlocksPerCta * 4 + kBins * 4 + sizeof(PoolSmem);
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(pool_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    RowsArgs a{};
+    a.scores = scores;
+    a.ld = ld;
+    a.lengths = c.lengths;
+    a.cap = c.cap;
+    a.P = P;
+    a.pool = pool;
+    a.pool_blocks = pool_blocks;
+    a.K = K;
+    a.idx = idx;
+    return launch_kernel(pool_rows_kernel, dim3(c.B * P), dim3(kThreads), smem, st, 0, a);
+}
+
+cudaError_t launch_pool_select(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
+                               const int32_t *pool, int pool_blocks, int K, int32_t *idx, int *status,
+                               cudaStream_t st)
+{
+    if (!pool_select_supported(c, P, HI, pool_blocks, K)) return cudaErrorInvalidValue;
+    const int units = c.B * P;
+    const int HT = heads_tile(HI);
+    // Cluster size: the smallest power of two whose CTAs hold at most 128 blocks each.
+    int C = 1;
+    while (C * kBlocksPerCta < pool_blocks) C *= 2;
+    PoolArgs a{};
+    a.P = P;
+    a.HI = HI;
+    a.cap = c.cap;
+    a.DI = c.DI;
+    a.lengths = c.lengths;
+    a.pool = pool;
+    a.pool_blocks = pool_blocks;
+    a.bpc = (pool_blocks + C - 1) / C;
+    a.w = w;
+    a.K = K;
+    a.idx = idx;
+    a.status = status;
+    const size_t smem = pool_smem_bytes(c.DI, HT);
+    cudaError_t e = HT == 16 ? configure<16>() : (HT == 32 ? configure<32>() : configure<64>());
+    if (e != cudaSuccess) return e;
+    const CUtensorMapSwizzle sw = c.DI == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : c.DI == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUtensorMap k8, qm;
+    if (encode_tensor_map_2d_u8(&k8, c.ikeys, c.DI, static_cast<uint64_t>(c.B) * c.cap, c.DI, kPoolBlock, sw) !=
+            CUDA_SUCCESS ||
+        encode_tensor_map_2d_u8(&qm, iq, c.DI, static_cast<uint64_t>(units) * HI, c.DI, HT, sw) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int cl = C > 1 ? C : 0;
+    if (HT == 16) return launch_kernel(pool_select_kernel<16>, dim3(C, units), dim3(kThreads), smem, st, cl, k8, qm, a);
+    if (HT == 32) return launch_kernel(pool_select_kernel<32>, dim3(C, units), dim3(kThreads), smem, st, cl, k8, qm, a);
+    return launch_kernel(pool_select_kernel<64>, dim3(C, units), dim3(kThreads), smem, st, cl, k8, qm, a);
+}
+
+}  // namespace csa

@@ -245,6 +245,28 @@ CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scor
                     int32_t pool_keep, int32_t *pool_out, void *workspace, size_t workspace_bytes,
                     csa_stream_t stream);
 
+/*
+ * a4 over the hierarchical pool in one call: csa_index_score of the pool's
+ * rows followed by csa_topk of those scores, with the scores kept on chip.
+ * ("G2C Brief", section "The hierarchical indexer": later Reindex layers
+ * score only the pool's rows with their own indexer query and keep the best;
+ * section "CSA2: most layers don't keep their own cache": Reindex borrows the
+ * keys and selects afresh.)
+ *   iq, w          : as csa_index_score
+ *   pool           : [batch][P][pool_blocks] block ids, ascending, -1 padded
+ *   idx            : [batch][P][K] ids of the K best-scoring pool rows among
+ *                    rows < L_p (ties: the earlier pool slot), ascending, then
+ *                    -1 padding
+ * The same result as csa_index_score + csa_topk (up to the fp32 summation
+ * order of the scores).  Supported: E4M3 keys, HI <= 64, pool_blocks <= 2048,
+ * K <= 16384; otherwise CSA_ERR_UNSUPPORTED (use the two calls instead).
+ * csa_layer_step takes this path for Reindex layers over a pool that it
+ * supports.
+ */
+CSA_API csa_status csa_pool_topk(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
+                                 const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx,
+                                 csa_stream_t stream);
+
 /* Workspace query of csa_topk.  No counterpart on the pages: the library
  * allocates nothing, so the caller supplies the scratch of the two-stage
  * select of long rows.  pool_blocks > 0: the scores are over a pool of that

@@ -97,10 +97,18 @@ def test_argument_checks_of_each_call(lib):
     # attention: too many heads, missing workspace
     assert lib.csa_sparse_attend(c, 1, 65, V(0x1000), 1.0, V(0x2000), 8, V(0x3000), None, V(0x4000), 1 << 20,
                                  None) == 2
-    # (K=2048 over 2 queries is split over several CTAs, so it needs a workspace)
+    # K=2048 over 2 queries is split over several CTAs whose partials meet in
+    # the workspace: a call without one is refused before any launch
     assert lib.csa_sparse_attend(c, 1, 16, V(0x1000), 1.0, V(0x2000), 2048, V(0x3000), None, None, 0, None) == 5
     n = ctypes.c_size_t(0)
     assert lib.csa_attend_workspace_size(c, 1, 16, 2048, ctypes.byref(n)) == 0 and n.value > 0
+    # with a local window (K=2048 over 2 queries), the splits' partials go through
+    # the workspace, and a call without one is refused before any launch
+    win = B.csa_swa(rows=0x7000, lengths=None, n=128, window=128)
+    assert lib.csa_attend_swa_workspace_size(c, 1, 16, 2048, ctypes.byref(win), ctypes.byref(n)) == 0
+    assert n.value > 0
+    assert lib.csa_sparse_attend_swa(c, 1, 16, V(0x1000), 1.0, V(0x2000), 2048, ctypes.byref(win), V(0x3000), None,
+                                     None, 0, None) == 5
 
 
 def test_layer_args_checks(lib):

@@ -15,32 +15,43 @@ def host_cache(cache):
     return cache.codes.cpu().numpy(), cache.scales.cpu().numpy()
 
 
-# Split plans covered: a cluster of 4 splits (1 query, 4 tiles), 32 splits
-# merged by the merge kernel (2 queries), a cluster of 2 (6 queries), one
-# split, a cluster of 7 (odd size: ragged dim slices; 20 queries), 11 splits
-# merged by the merge kernel with 48 heads and D = 384 (12 queries), 16 splits
-# (8 queries, the 64K decode shape), and clusters of 5 at D = 384 and of 7 at
-# D = 256, whose last dim slice is shorter than the others.
-@pytest.mark.parametrize("H,D,K,Bn,P", [(16, 128, 256, 1, 1), (64, 512, 2048, 2, 1), (7, 256, 100, 2, 3),
-                                        (64, 512, 1, 1, 1), (64, 512, 2048, 20, 1), (48, 384, 700, 12, 1),
-                                        (64, 512, 2048, 8, 1), (8, 384, 320, 29, 1), (8, 256, 448, 21, 1)])
-def test_attention_matches_oracle(H, D, K, Bn, P):
+# Queries whose splits fit one wave of CTAs (at most one per SM) run one
+# cluster per query, 128 selected rows per tile, merged on chip: 1 query over
+# 2, 4 and 16 splits; 6 queries of 7 heads (16-column tiles) in one split;
+# 12 queries of 48 heads at D = 384 over 4 splits of 2 tiles; 29 and 21
+# queries of 8 heads at D = 384 and 256 over 2 and 4 splits (uneven tile
+# counts); 8 queries, the 64K decode shape.  Two cases use a logit scale of 1,
+# where a later tile's maximum exceeds the running one by more than 2^8 and the
+# accumulated output is rescaled; one of them has two tiles per split and the
+# split merge at D = 128 (8 dims per split).  More queries than SMs go to the
+# split-K kernel (160 queries).
+CASES = [(16, 128, 256, 1, 1, None), (64, 512, 2048, 2, 1, None), (7, 256, 100, 2, 3, None),
+         (64, 512, 1, 1, 1, None), (64, 512, 2048, 20, 1, None), (48, 384, 700, 12, 1, None),
+         (64, 512, 2048, 8, 1, None), (8, 384, 320, 29, 1, None), (8, 256, 448, 21, 1, None),
+         (32, 512, 4096, 1, 1, 1.0), (64, 128, 4096, 1, 1, 1.0), (64, 512, 512, 1, 1, None),
+         (16, 128, 200, 160, 1, None)]
+
+
+@pytest.mark.parametrize("H,D,K,Bn,P,scale", CASES)
+def test_attention_matches_oracle(H, D, K, Bn, P, scale):
     need_gpu()
     wl = W.Workload("t", B=Bn, L=5000, H=H, D=D, HI=4, DI=64, K=K, P=P, outlier_channels=5)
+    sc = wl.scale if scale is None else scale
     cache, lat, _ = device_cache(wl, seed=21)
     q = W.layer_inputs(wl, 21, 0, device="cuda")["q"]
     idx = W.random_ints((Bn, P, K), 0, wl.L, seed=22).to(torch.int32)
     idx[..., ::5] = -1                                 # padding entries are skipped
     if K > 2:
         idx[..., 1] = idx[..., 2]                      # a duplicated row counts twice
-    out, lse = B.csa_sparse_attend(cache, q, idx.cuda(), wl.scale)
+    out, lse = B.csa_sparse_attend(cache, q, idx.cuda(), sc)
     torch.cuda.synchronize()
+    assert B.csa_device_status() == 0
     # the oracle quantises the same bf16 rows itself
     codes, scales = oracle.quantize_rows(lat.cpu().numpy())
     qh, ih = q.cpu().numpy(), idx.numpy()
     for b in range(Bn):
         for p in range(P):
-            o, l = oracle.attend(qh[b, p], codes[b], scales[b], ih[b, p], wl.scale)
+            o, l = oracle.attend(qh[b, p], codes[b], scales[b], ih[b, p], sc)
             check_attention(out[b, p].cpu().numpy(), o, (b, p))
             assert np.allclose(lse[b, p].cpu().numpy(), l, rtol=1e-5, atol=1e-5)
 
