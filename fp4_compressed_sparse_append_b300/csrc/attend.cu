@@ -760,7 +760,6 @@ size_t smem_bytes(int D, int NH)
 
 size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K, const SwaView *swa)
 {
-    if (!swa && decode_supported(c, P, H, K)) return decode_workspace_bytes(c, P, H, K);
     const Plan p = plan(c, P, K, swa);
     if (p.nsplit == 1 || p.cluster) return 0;
     const size_t units = static_cast<size_t>(c.B) * P;
@@ -776,8 +775,6 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     const int units = c.B * P;
     if (units == 0) return cudaSuccess;
     if (H > kMaxHeads || c.D % 128 || c.D > 512) return cudaErrorInvalidValue;
-    if (!swa && decode_supported(c, P, H, K))
-        return launch_attend_decode(c, P, H, q, scale, idx, K, out, lse, ws, ws_bytes, status, st);
     if (swa && (!swa->rows || swa->n < P || swa->window < 1)) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(c.D, (H + 15) / 16 * 16);
     const Plan p = plan(c, P, K, swa);

@@ -334,14 +334,6 @@ csa_status csa_sparse_attend_swa(const csa_cache *cache, int32_t P, int32_t H, c
         csa::launch_attend(v, P, H, q, scale, idx, K, out, lse, workspace, workspace_bytes, st, stream, svp));
 }
 
-// A Reindex layer over a pool whose scoring and selection run as one kernel
-// (no scores in the workspace).
-static bool layer_pool_fused(const csa_cache *cache, const csa_layer_args *a)
-{
-    return a->mode == CSA_REINDEX && a->pool_in &&
-           csa::pool_select_supported(view(cache), a->P, a->HI, a->pool_blocks, a->K);
-}
-
 static size_t layer_scores_ld(const csa_cache *cache, const csa_layer_args *a)
 {
     if (a->mode == CSA_REINDEX && a->pool_in) return round_up(static_cast<size_t>(a->pool_blocks) * CSA_POOL_BLOCK, 4);
@@ -392,7 +384,7 @@ csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args
     if (!bytes) return CSA_ERR_INVALID_ARG;
     const csa::CacheView v = view(cache);
     size_t total = 0;
-    if (a->mode != CSA_REUSE && !layer_pool_fused(cache, a)) {
+    if (a->mode != CSA_REUSE) {
         total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_scores_ld(cache, a) * sizeof(float), 256);
         total += round_up(layer_select_ws(cache, a), 256);
     }
@@ -414,10 +406,7 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
     const csa::CacheView v = view(cache);
     uint8_t *ws = static_cast<uint8_t *>(a->workspace);
     cudaError_t e = cudaSuccess;
-    if (layer_pool_fused(cache, a)) {
-        e = csa::launch_pool_select(v, a->P, a->HI, a->iq, a->w, a->pool_in, a->pool_blocks, a->K, a->idx, st, stream);
-        if (e != cudaSuccess) return CSA_ERR_CUDA;
-    } else if (a->mode != CSA_REUSE) {
+    if (a->mode != CSA_REUSE) {
         const int64_t ld = static_cast<int64_t>(layer_scores_ld(cache, a));
         float *scores = reinterpret_cast<float *>(ws);
         ws += round_up(static_cast<size_t>(cache->batch) * a->P * ld * sizeof(float), 256);
@@ -538,20 +527,6 @@ CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t in
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
-CUresult encode_tensor_map_2d_f32(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
-                                  uint32_t box_cols, uint32_t box_rows)
-{
-    const EncodeFn fn = encode_fn();
-    if (!fn) return CUDA_ERROR_NOT_FOUND;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 4};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 

@@ -60,14 +60,6 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
                           int K, float *out, float *lse, void *ws, size_t ws_bytes, int *status, cudaStream_t st,
                           const SwaView *swa = nullptr);
 
-// a5/a6 for few queries (every query's splits within one wave of CTAs): one
-// cluster per query, split partials merged through the workspace.
-int decode_supported(const CacheView &c, int P, int H, int K);
-size_t decode_workspace_bytes(const CacheView &c, int P, int H, int K);
-cudaError_t launch_attend_decode(const CacheView &c, int P, int H, const uint16_t *q, float scale,
-                                 const int32_t *idx, int K, float *out, float *lse, void *ws, size_t ws_bytes,
-                                 int *status, cudaStream_t st);
-
 // Persistent records of cache rows (main entry codes, scales, indexer entry).
 size_t record_bytes(const CacheView &c);
 cudaError_t launch_spill(const CacheView &c, int row0, int n, uint8_t *out, cudaStream_t st);
@@ -116,10 +108,6 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 CUresult encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
                                  uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
-// fp32 matrix [rows][cols] (row stride cols * 4 bytes), boxes of box_cols x
-// box_rows elements landing in shared memory row after row, no swizzle.
-CUresult encode_tensor_map_2d_f32(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
-                                  uint32_t box_cols, uint32_t box_rows);
 // Rows of 128 packed 4-bit values (64 bytes): a box of box_rows rows lands in
 // shared memory as 128-byte rows, each 16-byte chunk holding 8 code bytes then
 // 8 untouched bytes, with the 128-byte swizzle; the copy completes 64 bytes a

@@ -39,7 +39,7 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxCand = kMaxCluster * kMaxTiles * kTileRows;     // 16,384
 constexpr int kDigitBits = 13;                // radix digit: 8,192 bins
 constexpr int kBins = 1 << kDigitBits;
-constexpr int kU = 4;                          // keys in flight per thread in each pass
+constexpr int kU = 4;                          // loads in flight per thread (score gathers)
 
 struct PoolArgs {
     int P, HI, cap, DI;
@@ -59,8 +59,7 @@ struct PoolSmem {
     uint64_t qbar, done;
     float w[64];
     int32_t blk[kBlocksPerCta];
-    uint32_t warp_a[kThreads / 32], warp_b[kThreads / 32];
-    uint32_t jw[kMaxCand / 32];   // per (round, warp) taken-key counts, then their exclusive prefix
+    uint32_t warp_a[kThreads / 32], warp_b[kThreads / 32], warp_c[kThreads / 32];
     uint32_t res_bin, res_above;
     uint32_t tmem_slot;
     int abort;
@@ -81,30 +80,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank)
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Block-wide sums of two per-thread values; every thread gets both totals.
-__device__ __forceinline__ void block_sum2(uint32_t &a, uint32_t &b, PoolSmem &sm)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-        b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
-    }
-    __syncthreads();
-    if (lane == 0) {
-        sm.warp_a[warp] = a;
-        sm.warp_b[warp] = b;
-    }
-    __syncthreads();
-    a = 0;
-    b = 0;
-#pragma unroll
-    for (int i = 0; i < kThreads / 32; ++i) {
-        a += sm.warp_a[i];
-        b += sm.warp_b[i];
-    }
 }
 
 // Block-wide exclusive scan of one value per thread; *total gets the sum.
@@ -130,57 +105,63 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, PoolSmem &s
     return before + x - v;
 }
 
-// The K largest of n order-preserving keys in shared memory (0 = no
-// candidate), ties to the earlier candidate, written in candidate order as
+// The K largest of n <= kMaxCand order-preserving keys in shared memory (0 =
+// no candidate), ties to the earlier candidate, written in candidate order as
 // row ids (candidate c is row blk[c / 8] * 8 + c % 8), then -1 padding.  All
-// threads of the CTA call it.  A radix select over the keys' actual range:
-// pass 0 finds the count, minimum and maximum; each further pass histograms
-// the next 11 bits of (key - minimum) among the keys that share the bits
-// fixed so far, until the threshold bin is taken whole or one value is left.
-// Every pass keeps kU keys per thread in flight: one CTA does all the work,
-// so its loops are bound by latency, not by issue.
+// threads of the CTA call it.  Each thread first loads its kNk keys into
+// registers (warp w holds candidates [w*32*kNk, (w+1)*32*kNk), 32 consecutive
+// ones per register), and every pass then runs on registers: one CTA does all
+// the work, so each pass must be a few independent instructions per key, not
+// a chain of shared-memory round trips.  A radix select over the keys' actual
+// range: pass 0 finds the count, minimum and maximum; each further pass
+// histograms the next kDigitBits bits of (key - minimum) among the keys that
+// share the bits fixed so far, until the threshold bin is taken whole or one
+// value is left.
+constexpr int kNk = kMaxCand / kThreads;  // keys per thread
+
 __device__ __forceinline__ void select_from_keys(const uint32_t *allk, const int32_t *allb, int n, int Kin, int32_t *out,
-                                              uint32_t *hist, PoolSmem &sm)
+                                                 uint32_t *hist, PoolSmem &sm)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t K = static_cast<uint32_t>(Kin);
+    const int c_beg = warp * 32 * kNk;
+    uint32_t kk[kNk];
+#pragma unroll
+    for (int j = 0; j < kNk; ++j) {
+        const int c = c_beg + 32 * j + lane;
+        kk[j] = c < n ? allk[c] : 0u;
+    }
     // Pass 0: count, minimum and maximum of the candidate keys (0 = none).
     uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0;
-    for (int i0 = tid; i0 < n; i0 += kU * kThreads) {
-        uint32_t kk[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) kk[u] = i0 + u * kThreads < n ? allk[i0 + u * kThreads] : 0u;
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            if (kk[u]) {
-                ++cnt;
-                kmin = min(kmin, kk[u]);
-                kmax = max(kmax, kk[u]);
-            }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
-    }
+    for (int j = 0; j < kNk; ++j)
+        if (kk[j]) {
+            ++cnt;
+            kmin = min(kmin, kk[j]);
+            kmax = max(kmax, kk[j]);
+        }
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
     __syncthreads();
     if (lane == 0) {
         sm.warp_a[warp] = kmin;
         sm.warp_b[warp] = kmax;
+        sm.warp_c[warp] = cnt;
     }
     __syncthreads();
     kmin = 0xFFFFFFFFu;
     kmax = 0;
+    uint32_t total = 0;
 #pragma unroll
     for (int i = 0; i < kThreads / 32; ++i) {
         kmin = min(kmin, sm.warp_a[i]);
         kmax = max(kmax, sm.warp_b[i]);
+        total += sm.warp_c[i];
     }
-    uint32_t total = cnt, unused = 0;
-    block_sum2(total, unused, sm);
 
     // Threshold: keys > thr_gt are taken, and the first `need` keys equal to
-    // thr_eq (in pool order).
+    // thr_eq (in candidate order).
     uint32_t thr_gt = 0, thr_eq = 0, need = 0;
     if (total > K) {
         const uint32_t range = kmax - kmin;
@@ -199,15 +180,10 @@ __device__ __forceinline__ void select_from_keys(const uint32_t *allk, const int
             __syncthreads();
             for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
             __syncthreads();
-            for (int i0 = tid; i0 < n; i0 += kU * kThreads) {
-                uint32_t kk[kU];
 #pragma unroll
-                for (int u = 0; u < kU; ++u) kk[u] = i0 + u * kThreads < n ? allk[i0 + u * kThreads] : 0u;
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const uint64_t v = kk[u] - kmin;
-                    if (kk[u] && (v >> hi) == prefix) atomicAdd(&hist[(v >> lo) & (nb - 1)], 1u);
-                }
+            for (int j = 0; j < kNk; ++j) {
+                const uint64_t v = kk[j] - kmin;
+                if (kk[j] && (v >> hi) == prefix) atomicAdd(&hist[(v >> lo) & (nb - 1)], 1u);
             }
             __syncthreads();
             // the bin holding the (K - above)-th largest key: thread t scans
@@ -216,8 +192,10 @@ __device__ __forceinline__ void select_from_keys(const uint32_t *allk, const int
             const int per = nb >= kThreads ? nb / kThreads : 1;
             const int bhi = nb - tid * per, blo = bhi - per;
             uint32_t ssum = 0;
+            // each thread's bins are read in an order rotated by the thread's
+            // index, so the lanes of a warp hit different banks
             if (blo >= 0)
-                for (int bb = blo; bb < bhi; ++bb) ssum += hist[bb];
+                for (int j = 0; j < per; ++j) ssum += hist[blo + ((j + tid) & (per - 1))];
             uint32_t tot;
             const uint32_t excl = block_exclusive_scan(ssum, sm, &tot);
             if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
@@ -246,69 +224,40 @@ __device__ __forceinline__ void select_from_keys(const uint32_t *allk, const int
         }
     }
 
-    // Output in candidate order.  Round j covers candidates [j*T, (j+1)*T)
-    // (T threads, consecutive candidates in consecutive lanes); per (round,
-    // warp) counts of taken keys come from warp ballots, and one block scan of
-    // those counts gives every taken key its position.
-    const int J = (n + kThreads - 1) / kThreads;
+    // Output in candidate order: per register j, warp ballots of the taken
+    // keys; one prefix over the warps gives each warp its first position.
     const unsigned lt = (1u << lane) - 1u;
-    for (int j0 = 0; j0 < J; j0 += kU) {
-        uint32_t kk[kU];
+    uint32_t na = 0, ne = 0;
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int c = (j0 + u) * kThreads + tid;
-            kk[u] = (j0 + u < J && c < n) ? allk[c] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const unsigned ba = __ballot_sync(0xFFFFFFFFu, kk[u] && kk[u] > thr_gt);
-            const unsigned be = __ballot_sync(0xFFFFFFFFu, need && kk[u] == thr_eq);
-            if (lane == 0 && j0 + u < J)
-                sm.jw[(j0 + u) * (kThreads / 32) + warp] = (static_cast<uint32_t>(__popc(ba)) << 16) | __popc(be);
-        }
+    for (int j = 0; j < kNk; ++j) {
+        na += __popc(__ballot_sync(0xFFFFFFFFu, kk[j] && kk[j] > thr_gt));
+        ne += __popc(__ballot_sync(0xFFFFFFFFu, need && kk[j] == thr_eq));
     }
     __syncthreads();
-    {
-        // each thread scans a few consecutive (round, warp) counts
-        const int nw = J * (kThreads / 32);
-        const int per = (nw + kThreads - 1) / kThreads;
-        const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
-        uint32_t sum = 0;
-        for (int w = w0; w < w1; ++w) sum += sm.jw[w];
-        uint32_t tot;
-        uint32_t run = block_exclusive_scan(sum, sm, &tot);
-        for (int w = w0; w < w1; ++w) {
-            const uint32_t v = sm.jw[w];
-            sm.jw[w] = run;
-            run += v;
-        }
+    if (lane == 0) {
+        sm.warp_a[warp] = na;
+        sm.warp_b[warp] = ne;
     }
     __syncthreads();
-    for (int j0 = 0; j0 < J; j0 += kU) {
-        uint32_t kk[kU], base[kU];
-        int32_t blk[kU];
+    uint32_t a_before = 0, t_before = 0;
+    for (int w = 0; w < warp; ++w) {
+        a_before += sm.warp_a[w];
+        t_before += sm.warp_b[w];
+    }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int c = (j0 + u) * kThreads + tid;
-            const bool in = j0 + u < J && c < n;
-            kk[u] = in ? allk[c] : 0u;
-            blk[u] = in ? allb[c >> 3] : -1;
-            base[u] = j0 + u < J ? sm.jw[(j0 + u) * (kThreads / 32) + warp] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int c = (j0 + u) * kThreads + tid;
-            const bool is_above = kk[u] && kk[u] > thr_gt;
-            const bool is_tie = need && kk[u] == thr_eq;
-            const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
-            const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
-            const uint32_t a_before = (base[u] >> 16) + __popc(ba & lt);
-            const uint32_t t_before = (base[u] & 0xFFFFu) + __popc(be & lt);
-            int64_t pos = -1;
-            if (is_above) pos = a_before + min(t_before, need);
-            else if (is_tie && t_before < need) pos = a_before + t_before;
-            if (pos >= 0) out[pos] = blk[u] * kPoolBlock + (c & 7);
-        }
+    for (int j = 0; j < kNk; ++j) {
+        const int c = c_beg + 32 * j + lane;
+        const bool is_above = kk[j] && kk[j] > thr_gt;
+        const bool is_tie = need && kk[j] == thr_eq;
+        const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
+        const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
+        const uint32_t ab = a_before + __popc(ba & lt), tb = t_before + __popc(be & lt);
+        int64_t pos = -1;
+        if (is_above) pos = ab + min(tb, need);
+        else if (is_tie && tb < need) pos = ab + tb;
+        if (pos >= 0) out[pos] = allb[c >> 3] * kPoolBlock + (c & 7);
+        a_before += __popc(ba);
+        t_before += __popc(be);
     }
     const uint32_t selected = total > K ? K : total;
     for (uint32_t j = selected + tid; j < K; j += kThreads) out[j] = -1;

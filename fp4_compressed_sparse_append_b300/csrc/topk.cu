@@ -248,8 +248,10 @@ __device__ __forceinline__ uint32_t find_bin(const uint32_t *h, int nb, uint32_t
     const int hi = nb - tid * per;
     const int lo = hi - per;
     uint32_t s = 0;
+    // each thread's bins are read in an order rotated by the thread's index
+    // (per is a power of two), so the lanes of a warp hit different banks
     if (lo >= 0)
-        for (int b = lo; b < hi; ++b) s += h[b];
+        for (int j = 0; j < per; ++j) s += h[lo + ((j + tid) & (per - 1))];
     uint32_t total;
     const uint32_t excl = block_exclusive_scan(s, sh.warp_tot, &total);
     if (lo >= 0 && s && excl < need && excl + s >= need) {

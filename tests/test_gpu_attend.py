@@ -15,16 +15,15 @@ def host_cache(cache):
     return cache.codes.cpu().numpy(), cache.scales.cpu().numpy()
 
 
-# Queries whose splits fit one wave of CTAs (at most one per SM) run one
-# cluster per query, 128 selected rows per tile, merged on chip: 1 query over
-# 2, 4 and 16 splits; 6 queries of 7 heads (16-column tiles) in one split;
-# 12 queries of 48 heads at D = 384 over 4 splits of 2 tiles; 29 and 21
-# queries of 8 heads at D = 384 and 256 over 2 and 4 splits (uneven tile
-# counts); 8 queries, the 64K decode shape.  Two cases use a logit scale of 1,
-# where a later tile's maximum exceeds the running one by more than 2^8 and the
-# accumulated output is rescaled; one of them has two tiles per split and the
-# split merge at D = 128 (8 dims per split).  More queries than SMs go to the
-# split-K kernel (160 queries).
+# Split plans covered: a cluster of 2 and of 4 splits merged on chip (one
+# query), 32 splits merged by the merge kernel (2 queries), one split (6 queries
+# of 7 heads, 3 positions), clusters of 7 (20 queries) and of odd sizes whose
+# last dim slice is shorter (29 and 21 queries at D = 384 and 256), 11 splits
+# merged by the merge kernel with 48 heads at D = 384 (12 queries), 16 splits
+# (8 queries, the 64K decode shape), and one split per query (160 queries, more
+# queries than SMs).  Two cases use a logit scale of 1, where a later tile's
+# maximum exceeds the running one by more than 2^8 and the accumulated output
+# is rescaled.
 CASES = [(16, 128, 256, 1, 1, None), (64, 512, 2048, 2, 1, None), (7, 256, 100, 2, 3, None),
          (64, 512, 1, 1, 1, None), (64, 512, 2048, 20, 1, None), (48, 384, 700, 12, 1, None),
          (64, 512, 2048, 8, 1, None), (8, 384, 320, 29, 1, None), (8, 256, 448, 21, 1, None),
