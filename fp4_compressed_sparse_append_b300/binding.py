@@ -22,7 +22,7 @@ CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
     "csa_quantize_append", "csa_quantize_append_project", "csa_index_score", "csa_topk", "csa_topk_workspace_size",
-    "csa_pool_topk", "csa_sparse_attend",
+    "csa_pool_topk", "csa_select_pairs", "csa_topk_pairs", "csa_ids_window", "csa_lse_merge", "csa_sparse_attend",
     "csa_sparse_attend_noalloc", "csa_sparse_attend_swa", "csa_attend_swa_workspace_size",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
@@ -80,6 +80,10 @@ def lib() -> ctypes.CDLL:
         L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, SZ, V]
         L.csa_topk_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
         L.csa_pool_topk.argtypes = [C, I32, I32, V, V, V, I32, I32, V, V]
+        L.csa_select_pairs.argtypes = [C, V, I64, V, I32, I32, I32, V, V, V]
+        L.csa_topk_pairs.argtypes = [I32, I32, V, V, I32, V, V]
+        L.csa_ids_window.argtypes = [V, I64, I32, I32, V, V]
+        L.csa_lse_merge.argtypes = [I32, I32, I32, I32, V, V, V, V, V]
         L.csa_sparse_attend.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V, SZ, V]
         L.csa_sparse_attend_noalloc.argtypes = [C, I32, I32, V, ctypes.c_float, V, I32, V, V, V]
         L.csa_attend_workspace_size.argtypes = [C, I32, I32, I32, ctypes.POINTER(SZ)]
@@ -318,6 +322,52 @@ def csa_pool_topk(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: torch.T
     _check(lib().csa_pool_topk(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, K, _ptr(idx),
                                _stream(stream)), "csa_pool_topk")
     return idx
+
+
+def csa_select_pairs(cache: Cache, scores: torch.Tensor, idx: torch.Tensor, block: int, id_offset: int,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """scores [B, 1, ld] fp32 of the cache's rows, idx [B, 1, n] int32 local ids
+    (rows, or blocks of 8 rows with block=8) -> (pair_scores [B, 1, n] fp32,
+    pair_ids [B, 1, n] int32 = id + id_offset, -1 for empty slots)."""
+    Bc, n = cache.batch, idx.shape[-1]
+    _need(scores, Bc * scores.shape[-1] * 4, "scores")
+    _need(idx, Bc * n * 4, "idx")
+    ps = torch.empty((Bc, 1, n), dtype=torch.float32, device=cache.device)
+    pi = torch.empty((Bc, 1, n), dtype=torch.int32, device=cache.device)
+    _check(lib().csa_select_pairs(cache.ref, _ptr(scores), scores.shape[-1], _ptr(idx), n, block, id_offset,
+                                  _ptr(ps), _ptr(pi), _stream(stream)), "csa_select_pairs")
+    return ps, pi
+
+
+def csa_topk_pairs(pair_scores: torch.Tensor, pair_ids: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+    """pair_scores / pair_ids [rows, n] -> idx [rows, K] int32 (the ids of the K
+    best pairs, in pair order, -1 padded)."""
+    rows, n = pair_scores.shape[0], pair_scores.shape[-1]
+    ps, pi = pair_scores.reshape(rows, n).contiguous(), pair_ids.reshape(rows, n).contiguous()
+    idx = torch.empty((rows, K), dtype=torch.int32, device=ps.device)
+    _check(lib().csa_topk_pairs(rows, n, _ptr(ps), _ptr(pi), K, _ptr(idx), _stream(stream)), "csa_topk_pairs")
+    return idx
+
+
+def csa_ids_window(ids: torch.Tensor, lo: int, hi: int, stream=None) -> torch.Tensor:
+    """ids - lo where lo <= ids < hi, else -1 (same shape, int32)."""
+    ids = ids.contiguous()
+    out = torch.empty_like(ids)
+    _check(lib().csa_ids_window(_ptr(ids), ids.numel(), lo, hi, _ptr(out), _stream(stream)), "csa_ids_window")
+    return out
+
+
+def csa_lse_merge(outs: torch.Tensor, lses: torch.Tensor, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """outs [parts, units..., H, D] fp32, lses [parts, units..., H] fp32 ->
+    (out [units..., H, D], lse [units..., H]): the log-sum-exp merge."""
+    parts, H, D = outs.shape[0], outs.shape[-2], outs.shape[-1]
+    units = outs[0].numel() // (H * D)
+    o, l = outs.contiguous(), lses.contiguous()
+    out = torch.empty(outs.shape[1:], dtype=torch.float32, device=outs.device)
+    lse = torch.empty(lses.shape[1:], dtype=torch.float32, device=outs.device)
+    _check(lib().csa_lse_merge(parts, units, H, D, _ptr(o), _ptr(l), _ptr(out), _ptr(lse), _stream(stream)),
+           "csa_lse_merge")
+    return out, lse
 
 
 def attend_workspace_size(cache: Cache, P: int, H: int, K: int) -> int:

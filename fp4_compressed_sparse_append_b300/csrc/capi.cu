@@ -259,6 +259,43 @@ csa_status csa_pool_topk(const csa_cache *cache, int32_t P, int32_t HI, const ui
     return from_cuda(csa::launch_pool_select(view(cache), P, HI, iq, w, pool, pool_blocks, K, idx, st, stream));
 }
 
+csa_status csa_select_pairs(const csa_cache *cache, const float *scores, int64_t ld, const int32_t *idx, int32_t n,
+                            int32_t block, int32_t id_offset, float *pair_scores, int32_t *pair_ids,
+                            csa_stream_t stream)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (!scores || !idx || !pair_scores || !pair_ids || n < 1 || (block != 1 && block != CSA_POOL_BLOCK))
+        return CSA_ERR_INVALID_ARG;
+    if (ld < cache->capacity || ld % 4) return CSA_ERR_INVALID_ARG;
+    return from_cuda(csa::launch_pairs_from_idx(view(cache), scores, ld, idx, n, block, id_offset, pair_scores, pair_ids,
+                                                stream));
+}
+
+csa_status csa_topk_pairs(int32_t rows, int32_t n, const float *pair_scores, const int32_t *pair_ids, int32_t K,
+                          int32_t *idx, csa_stream_t stream)
+{
+    if (rows < 1 || n < 1 || K < 1 || K > 16384 || !pair_scores || !pair_ids || !idx) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(pair_scores) || !aligned16(pair_ids) || !aligned16(idx)) return CSA_ERR_INVALID_ARG;
+    if (!csa::select_pairs_supported(n, K)) return CSA_ERR_UNSUPPORTED;
+    return from_cuda(csa::launch_select_pairs(rows, n, pair_scores, pair_ids, K, idx, stream));
+}
+
+csa_status csa_ids_window(const int32_t *ids, int64_t count, int32_t lo, int32_t hi, int32_t *out, csa_stream_t stream)
+{
+    if (count < 0 || !ids || !out || hi < lo) return CSA_ERR_INVALID_ARG;
+    return from_cuda(csa::launch_ids_window(ids, count, lo, hi, out, stream));
+}
+
+csa_status csa_lse_merge(int32_t parts, int32_t units, int32_t H, int32_t D, const float *outs, const float *lses,
+                         float *out, float *lse, csa_stream_t stream)
+{
+    if (parts < 1 || units < 1 || H < 1 || D < 4 || D % 4 || !outs || !lses || !out) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(outs) || !aligned16(out) || (lse && !aligned16(lse))) return CSA_ERR_INVALID_ARG;
+    if (H > 65535 || units > 65535) return CSA_ERR_UNSUPPORTED;
+    return from_cuda(csa::launch_lse_merge(parts, units, H, D, outs, lses, out, lse, stream));
+}
+
 csa_status csa_attend_workspace_size(const csa_cache *cache, int32_t P, int32_t H, int32_t K, size_t *bytes)
 {
     csa_status s = check_cache(cache);

@@ -49,6 +49,19 @@ int pool_rows_supported(int pool_keep, int K);
 cudaError_t launch_pool_rows(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
                              int pool_blocks, int K, int32_t *idx, cudaStream_t st);
 
+// a3 over candidate pairs: the K best of n (score, id) pairs per row (id -1 =
+// empty; ties to the earlier pair), ids written in pair order, -1 padded.
+int select_pairs_supported(int n, int K);
+cudaError_t launch_select_pairs(int rows, int n, const float *scores, const int32_t *ids, int K, int32_t *out,
+                                cudaStream_t st);
+
+// The context split of one sequence's rows over several devices (split.cu).
+cudaError_t launch_pairs_from_idx(const CacheView &c, const float *scores, int64_t ld, const int32_t *idx, int n,
+                                  int block, int32_t id_offset, float *pair_scores, int32_t *pair_ids, cudaStream_t st);
+cudaError_t launch_ids_window(const int32_t *ids, int64_t count, int32_t lo, int32_t hi, int32_t *out, cudaStream_t st);
+cudaError_t launch_lse_merge(int parts, int units, int H, int D, const float *outs, const float *lses, float *out,
+                             float *lse, cudaStream_t st);
+
 // a5/a6, and the local window of the joint softmax (rows [B][n][D] FP8 E4M3).
 struct SwaView {
     const uint8_t *rows;

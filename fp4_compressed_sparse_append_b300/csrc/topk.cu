@@ -586,4 +586,26 @@ cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_
     return launch(kPairs, b, rows, b.n_pairs, st);
 }
 
+int select_pairs_supported(int n, int K)
+{
+    return n >= 1 && K >= 1 && static_cast<int64_t>(n) <= static_cast<int64_t>(kMaxCluster) * kSelCacheMax;
+}
+
+cudaError_t launch_select_pairs(int rows, int n, const float *scores, const int32_t *ids, int K, int32_t *out,
+                                cudaStream_t st)
+{
+    if (rows == 0) return cudaSuccess;
+    if (!select_pairs_supported(n, K)) return cudaErrorInvalidValue;
+    SelArgs b{};
+    b.scores = scores;
+    b.pair_ids = ids;
+    b.n_pairs = n;
+    b.P = 1;
+    b.segments = 1;
+    b.seg_len = n;
+    b.K = K;
+    b.out_ids = out;
+    return launch(kPairs, b, rows, n, st);
+}
+
 }  // namespace csa

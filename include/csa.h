@@ -425,6 +425,55 @@ CSA_API csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *
 CSA_API csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args *args, size_t *bytes);
 
 /*
+ * The context split: one sequence's cached rows split into contiguous slices
+ * over G devices (each slice a csa_cache of its own, one query position per
+ * sequence).  ("G2C Brief", section "The global branch: compress, index,
+ * select": every entry is scored, the best are kept and attended to; section
+ * "The hierarchical indexer": blocks of 8 scored by their best member.)  Each
+ * device selects its slice's top K, turns it into (score, global id) pairs
+ * (csa_select_pairs), the pairs of every device are gathered (by the caller's
+ * collective), the global top K is taken among them (csa_topk_pairs; exact,
+ * since a member of the global top K is in its own slice's top K), each
+ * device attends over the selected ids in its slice (csa_ids_window, then
+ * csa_sparse_attend), and the partial outputs are merged (csa_lse_merge).
+ *
+ * csa_select_pairs: for each sequence b of the slice's cache,
+ *   idx         : [batch][n] local ids selected from scores (-1 = empty),
+ *                 rows (block = 1) or blocks of 8 rows (block = 8)
+ *   pair_scores : [batch][n] the score of each id (for a block: its best
+ *                 member among the visible rows), -inf for an empty slot
+ *   pair_ids    : [batch][n] id + id_offset (the slice's first global row, or
+ *                 block), -1 for an empty slot
+ */
+CSA_API csa_status csa_select_pairs(const csa_cache *cache, const float *scores, int64_t ld, const int32_t *idx,
+                                    int32_t n, int32_t block, int32_t id_offset, float *pair_scores,
+                                    int32_t *pair_ids, csa_stream_t stream);
+
+/* The context split's global selection ("G2C Brief", "The global branch"):
+ * for each of `rows` rows, the ids of the K best of n (score, id) pairs
+ * (ties: the earlier pair; id -1 = empty), in pair order then -1 padding;
+ * pairs given in ascending id order (the devices' lists in slice order) give
+ * ascending ids.  n <= 262144, 1 <= K <= 16384. */
+CSA_API csa_status csa_topk_pairs(int32_t rows, int32_t n, const float *pair_scores, const int32_t *pair_ids,
+                                  int32_t K, int32_t *idx, csa_stream_t stream);
+
+/* No counterpart on the pages (the context split's bookkeeping): out[i] =
+ * ids[i] - lo for lo <= ids[i] < hi, else -1 (the global ids a device owns, as
+ * its local ids). */
+CSA_API csa_status csa_ids_window(const int32_t *ids, int64_t count, int32_t lo, int32_t hi, int32_t *out,
+                                  csa_stream_t stream);
+
+/* The context split's merge ("G2C Brief", "The global branch": one softmax
+ * over all the selected entries): parts partial results of the same queries,
+ *   outs : [parts][units][H][D] fp32, each normalised over its own rows
+ *   lses : [parts][units][H] fp32 (natural log; -inf = no rows)
+ * -> out [units][H][D] = sum_g e^(lse_g - L) outs_g with L = ln sum_g e^lse_g,
+ *    lse [units][H] = L (or NULL).  D a multiple of 4, all pointers 16-byte
+ *    aligned. */
+CSA_API csa_status csa_lse_merge(int32_t parts, int32_t units, int32_t H, int32_t D, const float *outs,
+                                 const float *lses, float *out, float *lse, csa_stream_t stream);
+
+/*
  * No counterpart on the pages (error reporting of this library).
  * Waits for `stream`, then copies the device status word of the current
  * device into *bits (0 = no fault) and, if clear != 0, resets it.
