@@ -28,6 +28,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode tokens/s and achieved HBM GB/s (% of ~8 TB/s) per CSA2 layer step"
 NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 126 * 1000 * 1000     # B300 L2
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -214,7 +215,10 @@ class L2Flush:
 
 def build_state(wl, seed, device):
     """Untimed setup: the cache (built through csa_quantize_append) and the
-    per-layer arguments with their workspaces."""
+    per-layer arguments with their workspaces.  Returns (cache, layers,
+    base_len, more_layers); more_layers() builds another set of layer
+    arguments over the same cache, with tensors of its own (the e2e leg
+    double-buffers its inputs and outputs across steps)."""
     import torch
     from fp4_compressed_sparse_append_b300 import binding as B
     from fp4_compressed_sparse_append_b300 import workloads as W
@@ -233,23 +237,28 @@ def build_state(wl, seed, device):
     torch.cuda.synchronize()
     app = W.append_rows(wl, seed, device=device) if wl.n_append else None
     swa = B.Swa(W.local_rows(wl, seed, device=device), wl.window) if wl.window else None
-    layers, prev, pool = [], None, None
-    for li, mode in enumerate(wl.layers):
-        inp = W.layer_inputs(wl, seed, li, device=device)
-        la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
-                         idx=prev if mode == W.REUSE else None,
-                         rows_new=app["rows"] if (app and li == 0) else None,
-                         ikeys_new=app["ikeys"] if (app and li == 0 and not wl.project) else None,
-                         w_ik=w_ik if (app and li == 0) else None,
-                         pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
-                         make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None), swa=swa)
-        if mode != W.REUSE:
-            prev = la.idx
-        if la.pool_out is not None:
-            pool = la.pool_out
-        layers.append(la)
+
+    def more_layers():
+        layers, prev, pool = [], None, None
+        for li, mode in enumerate(wl.layers):
+            inp = W.layer_inputs(wl, seed, li, device=device)
+            la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
+                             idx=prev if mode == W.REUSE else None,
+                             rows_new=app["rows"] if (app and li == 0) else None,
+                             ikeys_new=app["ikeys"] if (app and li == 0 and not wl.project) else None,
+                             w_ik=w_ik if (app and li == 0) else None,
+                             pool_in=pool if mode == W.REINDEX else None, pool_blocks=wl.pool_blocks,
+                             make_pool=(mode == W.FULL and wl.pool_blocks > 0 and pool is None), swa=swa)
+            if mode != W.REUSE:
+                prev = la.idx
+            if la.pool_out is not None:
+                pool = la.pool_out
+            layers.append(la)
+        return layers
+
+    layers = more_layers()
     base_len = cache.lengths.clone()
-    return cache, layers, base_len
+    return cache, layers, base_len, more_layers
 
 
 def run_step(cache, layers, base_len, wl):
@@ -270,7 +279,7 @@ def bench_ours(args, wl, rank, world, local_rank):
         dist.barrier()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cache, layers, base_len = build_state(wl, args.seed, dev)
+    cache, layers, base_len, more_layers = build_state(wl, args.seed, dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
@@ -322,7 +331,7 @@ def bench_ours(args, wl, rank, world, local_rank):
     stages = stage_times(cache, layers, wl, flush, args.steps, stream)
     layer_ms = layer_times(cache, layers, base_len, wl, flush, args.steps, stream)
     # e2e through the public API with host buffers
-    e2e = e2e_run(cache, layers, base_len, wl, args, stream, flush)
+    e2e = e2e_run(cache, [layers, more_layers()], base_len, wl, args, stream, flush)
     if B.csa_device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
     return dict(value=value, ms_per_step=ms_per_step, gbs=gbs, step_bytes=sbytes, index_bytes=ibytes, layer_ms=layer_ms,
@@ -465,15 +474,25 @@ def layer_times(cache, layers, base_len, wl, flush, steps, stream):
     return out
 
 
-def e2e_run(cache, layers, base_len, wl, args, stream, flush):
-    """Same step through the public API with pinned host inputs and outputs:
-    per step, copy every layer's q/iq/w host->device, run the layers through
-    csa_layer_step, copy every layer's output device->host.  The copies and the
-    calls are captured once as a CUDA graph (as a serving loop would run them),
-    so the timing holds no Python launch overhead; each replay is one step."""
+def e2e_run(cache, layer_sets, base_len, wl, args, stream, flush):
+    """Same steps through the public API with pinned host inputs and outputs:
+    each step copies every layer's q/iq/w host->device, runs the layers through
+    csa_layer_step and copies every layer's output device->host.
+
+    Two sets of layer arguments (device inputs and outputs) alternate between
+    steps, and the copies run on two copy streams, ordered by events: the
+    inputs of step s+1 go up while step s computes, and the outputs of step s
+    come down while step s+1 computes.  The layer calls of each set are
+    captured once as a CUDA graph (as a serving loop would run them).  The
+    time is that of the whole run, from the first input copy to the end of
+    the last output copy, over the steps.  When a step moves more bytes than
+    the L2 holds, nothing is flushed between steps (the step's own scan
+    evicts it); otherwise the L2 flush runs before each step's layer calls,
+    inside the timed run."""
     import torch
-    hin, hout, h2d, d2h = [], [], 0, 0
-    for la in layers:
+    h2d, d2h = 0, 0
+    hin, hout = [], []
+    for la in layer_sets[0]:
         row = {}
         for k in ("q", "iq", "w"):
             t = la.tensors[k]
@@ -481,38 +500,71 @@ def e2e_run(cache, layers, base_len, wl, args, stream, flush):
                 row[k] = t.cpu().pin_memory()
                 h2d += t.numel() * t.element_size()
         hin.append(row)
-        hout.append(torch.empty(la.out.shape, dtype=la.out.dtype).pin_memory())
         d2h += la.out.numel() * la.out.element_size()
+    hout = [[torch.empty(la.out.shape, dtype=la.out.dtype).pin_memory() for la in ls] for ls in layer_sets]
+    sbytes, _ = step_bytes(wl)
+    flush_between = sbytes <= L2_BYTES
 
-    def step():
-        for la, row in zip(layers, hin):
-            for k, h in row.items():
-                la.tensors[k].copy_(h, non_blocking=True)
-        run_step(cache, layers, base_len, wl)
-        for la, h in zip(layers, hout):
-            h.copy_(la.out, non_blocking=True)
-
-    if wl.n_append:
-        cache.lengths.copy_(base_len)
-    step()
-    torch.cuda.synchronize()
-    graph = capture(step)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps + 2):
+    def compute(ls):
         if wl.n_append:
             cache.lengths.copy_(base_len)
-        flush()
-        if i >= 2:
-            ev[i - 2][0].record(stream)
-        graph.replay()
-        if i >= 2:
-            ev[i - 2][1].record(stream)
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        if flush_between:
+            flush()
+        run_step(cache, ls, base_len, wl)
+
+    graphs = []
+    for ls in layer_sets:
+        compute(ls)
+        torch.cuda.synchronize()
+        graphs.append(capture(lambda ls=ls: run_step(cache, ls, base_len, wl)))
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in layer_sets]      # inputs of the set are on the device
+    done = [torch.cuda.Event() for _ in layer_sets]       # the set's layer calls are done
+    drained = [torch.cuda.Event() for _ in layer_sets]    # the set's outputs are on the host
+
+    def run(n, t0=None, t1=None):
+        for s in range(n):
+            p = s % 2
+            with torch.cuda.stream(up):
+                if s >= 2:
+                    up.wait_event(done[p])                 # step s-2 no longer reads these inputs
+                if s == 0 and t0 is not None:
+                    t0.record(up)
+                for la, row in zip(layer_sets[p], hin):
+                    for k, h in row.items():
+                        la.tensors[k].copy_(h, non_blocking=True)
+                ready[p].record(up)
+            stream.wait_event(ready[p])
+            if s >= 2:
+                stream.wait_event(drained[p])              # step s-2's outputs have left these buffers
+            if wl.n_append:
+                cache.lengths.copy_(base_len)
+            if flush_between:
+                flush()
+            graphs[p].replay()
+            done[p].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(done[p])
+                for la, h in zip(layer_sets[p], hout[p]):
+                    h.copy_(la.out, non_blocking=True)
+                drained[p].record(down)
+        if t1 is not None:
+            down.wait_stream(up)
+            t1.record(down)
+        torch.cuda.synchronize()
+
+    run(4)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(args.steps, t0, t1)
+    ms = t0.elapsed_time(t1) / args.steps
     return {"value": wl.B * wl.P / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "pinned host->device copies of every layer's q/iq/w, the layer calls, device->host copy of "
-                   "every layer's output; captured once as a CUDA graph and replayed per step"}
+            "l2": ("flushed before each step's layer calls, inside the timed run" if flush_between else
+                   "not flushed: a step moves more bytes than the L2 holds"),
+            "how": "pinned host->device copies of every layer's q/iq/w, the layer calls (one CUDA graph per "
+                   "buffer set), device->host copies of every layer's output; two buffer sets alternate "
+                   "between steps and the copies run on two copy streams under the neighbouring steps' "
+                   "layer calls; whole run from the first input copy to the last output copy, per step"}
 
 
 # ---------------------------------------------------------------------------

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
 CSA_FULL, CSA_REINDEX, CSA_REUSE = 0, 1, 2
 CSA_POOL_BLOCK = 8
+CSA_NOALLOC_SCRATCH_BYTES = 17 << 20
 CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (

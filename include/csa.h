@@ -363,9 +363,15 @@ CSA_API csa_status csa_attend_swa_workspace_size(const csa_cache *cache, int32_t
  *    each other's partials: order them on one stream or with events.
  *  - The array keeps whatever the last call left in it; nothing in it has to
  *    start at zero, because each call writes every partial it later reads.
- *  - Only calls with few queries (at most 9) split a query over more CTAs than
- *    a thread-block cluster holds and need partials in memory at all; 17 MiB
- *    holds them for up to 8 queries of 64 heads x 512 dims.
+ *  - A call needs partials in memory only when its plan splits each query
+ *    over more CTAs than a thread-block cluster holds (more than 8): at most
+ *    16 queries (batch x P) on a 148-SM GPU, and K above 512.  Whether they
+ *    fit depends on batch x P, H, d_latent and K together, and not
+ *    monotonically on the number of queries: at 64 heads x 512 dims and
+ *    K = 2048, 1 to 8 and 10 to 12 queries fit, 9 and 13 do not.  The exact
+ *    test is csa_attend_workspace_size(cache, P, H, K, &n) with
+ *    n <= CSA_NOALLOC_SCRATCH_BYTES: a call that passes it is never refused
+ *    for size.
  */
 #define CSA_NOALLOC_SCRATCH_BYTES (17u << 20)
 

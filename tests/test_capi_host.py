@@ -219,3 +219,16 @@ def test_persistent_record_checks(lib):
     assert lib.csa_cache_reload(r, V(0x70001), 4, None) == 1
     assert lib.csa_cache_reload(r, None, 4, None) == 1
     assert lib.csa_cache_reload(None, V(0x70000), 4, None) == 1
+
+
+def test_binding_constants_match_the_header():
+    """Every constant the binding mirrors has the header's value (the no-alloc
+    scratch size, the pool block, the device status bits, the key formats)."""
+    text = open(os.path.join(ROOT, "include", "csa.h")).read()
+    defines = dict(re.findall(r"#define\s+(CSA_[A-Z0-9_]+)\s+([0-9xXa-fA-Fu<>() ]+?)\s*(?:/\*|\n)", text))
+    mirrored = ["CSA_NOALLOC_SCRATCH_BYTES", "CSA_POOL_BLOCK", "CSA_DEV_BAD_INDEX", "CSA_DEV_CAPACITY",
+                "CSA_DEV_TIMEOUT", "CSA_IKEY_E4M3", "CSA_IKEY_MXFP4"]
+    for name in mirrored:
+        expr = defines[name].replace("u", "")
+        assert re.fullmatch(r"[0-9xXa-fA-F<>() ]+", expr), (name, expr)
+        assert eval(expr) == getattr(B, name), (name, expr, getattr(B, name))
