@@ -384,6 +384,13 @@ def layer_kinds(wl):
     return [tuple(k) for k in kinds]
 
 
+def fused_pool_select(wl, pool_in):
+    """Whether csa_layer_step scores and selects a Reindex layer over the
+    pool in one kernel (the condition csa_pool_topk supports)."""
+    return (pool_in is not None and wl.key_format == "e4m3" and wl.HI <= 64 and wl.DI in (32, 64, 128)
+            and pool_in.shape[-1] <= 2048 and wl.K <= 16384)
+
+
 def stage_times(cache, layers, wl, flush, steps, stream):
     """Times the stages of the first layer of each layer kind one at a time,
     each through its own public call, captured as a CUDA graph and replayed
@@ -416,7 +423,14 @@ def stage_times(cache, layers, wl, flush, steps, stream):
         q, iq, w = la.tensors["q"], la.tensors["iq"], la.tensors["w"]
         pool_in = la.tensors["pool_in"]
         make_pool = la.pool_out is not None
-        if la.struct.mode != W.REUSE:
+        if la.struct.mode != W.REUSE and fused_pool_select(wl, pool_in):
+            # a Reindex layer over the pool: scores and selection in one kernel
+            idx = B.csa_pool_topk(cache, iq, w, pool_in, wl.K)
+            torch.cuda.synchronize()
+            out[kind + ".pool_topk"] = dict(
+                ms=timed(lambda: B.csa_pool_topk(cache, iq, w, pool_in, wl.K, idx=idx)),
+                launches=count, kind=kind, stage="pool_topk")
+        elif la.struct.mode != W.REUSE:
             nblk = pool_in.shape[-1] if pool_in is not None else 0
             scores = B.csa_index_score(cache, iq, w, pool=pool_in)
             ws_sel = torch.empty(max(16, B.topk_workspace_size(cache, wl.P, wl.K, nblk,
@@ -870,7 +884,8 @@ def config_of(wl):
 # traffic applies only while these files are unchanged.
 STAGE_SOURCES = {
     "index_score": ("index_score.cu", "common.cuh"),
-    "topk": ("topk.cu", "common.cuh"),
+    "topk": ("topk.cu", "pool_select.cu", "select_cta.cuh", "common.cuh"),
+    "pool_topk": ("pool_select.cu", "select_cta.cuh", "common.cuh"),
     "sparse_attend": ("attend.cu", "common.cuh"),
 }
 
@@ -907,6 +922,8 @@ def stage_bytes(wl, kind, stage):
     """Algorithmic bytes (bytes that must move) of one launch of a stage:
     index_score: the indexer keys scanned, the indexer queries and weights;
     topk: the scores read (and the pool's block ids) and the ids written;
+    pool_topk (index_score and topk of a Reindex layer in one kernel): the
+    pool's block ids and keys, the indexer queries and weights, the ids;
     sparse_attend: the selected FP4 rows, the bf16 queries, the fp32 outputs
     and log-sum-exps (and the local window's FP8 rows)."""
     from fp4_compressed_sparse_append_b300 import workloads as W
@@ -918,6 +935,9 @@ def stage_bytes(wl, kind, stage):
     if stage == "index_score":
         keys = units * pool_rows * kb if kind == "reindex.pool" else wl.B * L * kb
         return keys + q_index
+    if stage == "pool_topk":
+        # the pool's block ids and its rows' keys read, the ids written
+        return units * (wl.pool_blocks * 4 + pool_rows * kb + wl.K * 4) + q_index
     if stage == "topk":
         n = pool_rows if kind == "reindex.pool" else L
         b = units * n * 4 + units * wl.K * 4
@@ -933,8 +953,8 @@ def stage_bytes(wl, kind, stage):
     return b
 
 
-KERNELS = {"index_score": "index_score_kernel", "topk": "select_kernel",
-           "sparse_attend": "attend_kernel (+ attend_merge_kernel)"}
+KERNELS = {"index_score": "index_score_kernel", "topk": "select_kernel (+ select_one_kernel, pool_rows_kernel)",
+           "pool_topk": "pool_select_kernel", "sparse_attend": "attend_kernel (+ attend_merge_kernel)"}
 
 
 def stage_rooflines(wl, stages, peak_hbm, peak_src, peak_tf, peak_tf_src):

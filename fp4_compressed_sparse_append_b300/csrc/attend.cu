@@ -659,55 +659,53 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
 }
 
-// Combines the split partials: block = (512 dims, head, query); each thread
-// loads its 4 dims (one 16-byte load) from every split at once.
+// Combines the split partials: block = one warp over (128 dims, head, query),
+// so that even one query's merge spreads over more CTAs than there are SMs
+// (each SM's share of the partials is what bounds it); each lane loads its 4
+// dims (one 16-byte load) from every split at once.
 // out = sum_s 2^(m_s - M) O_s / L, L = sum_s 2^(m_s - M) l_s,
 // lse = ln 2 * (M + log2 L).
 constexpr int kMaxSplit = 32;  // one warp holds every split's (m, l) in the merge
+constexpr int kMergeDims = 128;
 
 template <int MS>
-__global__ void __launch_bounds__(128) attend_merge_kernel(int D, int H, int nsplit, const float *__restrict__ part_o,
-                                                          const float2 *__restrict__ part_ml, float *__restrict__ out,
-                                                          float *__restrict__ lse)
+__global__ void __launch_bounds__(32) attend_merge_kernel(int D, int H, int nsplit, const float *__restrict__ part_o,
+                                                         const float2 *__restrict__ part_ml, float *__restrict__ out,
+                                                         float *__restrict__ lse)
 {
     pdl_wait();
     __shared__ float wsh[MS];
-    __shared__ float inv_l;
-    const int d = (blockIdx.x * 128 + threadIdx.x) * 4, h = blockIdx.y, unit = blockIdx.z;
+    const int lane = threadIdx.x;
+    const int d = blockIdx.x * kMergeDims + lane * 4, h = blockIdx.y, unit = blockIdx.z;
     float4 pv[MS];
 #pragma unroll
     for (int s = 0; s < MS; ++s)
         pv[s] = (s < nsplit && d < D) ? *reinterpret_cast<const float4 *>(
                                             part_o + ((static_cast<int64_t>(unit) * nsplit + s) * H + h) * D + d)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (threadIdx.x < 32) {
-        const int s = threadIdx.x;
-        float2 ml = make_float2(-INFINITY, 0.f);
-        if (s < nsplit) ml = part_ml[(static_cast<int64_t>(unit) * nsplit + s) * H + h];
-        float M = ml.y > 0.f ? ml.x : -INFINITY;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < nsplit) ml = part_ml[(static_cast<int64_t>(unit) * nsplit + lane) * H + h];
+    float M = ml.y > 0.f ? ml.x : -INFINITY;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
-        float L = w * ml.y;
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+    float L = w * ml.y;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
-        if (s < MS) wsh[s] = w;
-        if (s == 0) {
-            inv_l = L > 0.f ? 1.f / L : 0.f;
-            if (lse && blockIdx.x == 0) lse[static_cast<int64_t>(unit) * H + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-        }
-    }
-    __syncthreads();
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+    if (lane < MS) wsh[lane] = w;
+    if (lse && blockIdx.x == 0 && lane == 0)
+        lse[static_cast<int64_t>(unit) * H + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    __syncwarp();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < MS; ++s) {
-        const float w = wsh[s];
-        acc.x = fmaf(w, pv[s].x, acc.x);
-        acc.y = fmaf(w, pv[s].y, acc.y);
-        acc.z = fmaf(w, pv[s].z, acc.z);
-        acc.w = fmaf(w, pv[s].w, acc.w);
+        const float ws = wsh[s];
+        acc.x = fmaf(ws, pv[s].x, acc.x);
+        acc.y = fmaf(ws, pv[s].y, acc.y);
+        acc.z = fmaf(ws, pv[s].z, acc.z);
+        acc.w = fmaf(ws, pv[s].w, acc.w);
     }
-    const float il = inv_l;
+    const float il = L > 0.f ? 1.f / L : 0.f;
     if (d < D)
         *reinterpret_cast<float4 *>(out + (static_cast<int64_t>(unit) * H + h) * D + d) =
             make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
@@ -820,7 +818,7 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
     // The merge loads every split's value at once: 16 or 32 registers.
     auto merge = p.nsplit <= 16 ? attend_merge_kernel<16> : attend_merge_kernel<kMaxSplit>;
-    return launch_kernel(merge, dim3((c.D + 511) / 512, H, units), dim3(128), 0, st, 0, c.D, H, p.nsplit,
+    return launch_kernel(merge, dim3((c.D + kMergeDims - 1) / kMergeDims, H, units), dim3(32), 0, st, 0, c.D, H, p.nsplit,
                          static_cast<const float *>(a.part_o), static_cast<const float2 *>(a.part_ml), out, lse);
 }
 

@@ -456,22 +456,27 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         }
         const int32_t *pool = a->mode == CSA_REINDEX ? a->pool_in : nullptr;
         const int pool_blocks = pool ? a->pool_blocks : 0;
-        e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);
         const bool make_pool = a->mode == CSA_FULL && a->pool_out;
-        if (make_pool && csa::pool_rows_supported(a->pool_blocks, a->K)) {
-            // the pool first; the top K rows then lie in the pool's blocks
-            if (e == cudaSuccess)
-                e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out,
-                                       sel_ws, sel_bytes, stream);
-            if (e == cudaSuccess)
-                e = csa::launch_pool_rows(v, a->P, scores, ld, a->pool_out, a->pool_blocks, a->K, a->idx, stream);
+        if (pool && csa::pool_select_supported(v, a->P, a->HI, pool_blocks, a->K)) {
+            // a Reindex layer over the pool: scores and selection in one kernel
+            e = csa::launch_pool_select(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, a->K, a->idx, st, stream);
         } else {
-            if (e == cudaSuccess)
-                e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, sel_ws, sel_bytes,
-                                       stream);
-            if (e == cudaSuccess && make_pool)
-                e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks, a->pool_out,
-                                       sel_ws, sel_bytes, stream);
+            e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);
+            if (make_pool && csa::pool_rows_supported(a->pool_blocks, a->K)) {
+                // the pool first; the top K rows then lie in the pool's blocks
+                if (e == cudaSuccess)
+                    e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks,
+                                           a->pool_out, sel_ws, sel_bytes, stream);
+                if (e == cudaSuccess)
+                    e = csa::launch_pool_rows(v, a->P, scores, ld, a->pool_out, a->pool_blocks, a->K, a->idx, stream);
+            } else {
+                if (e == cudaSuccess)
+                    e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, sel_ws, sel_bytes,
+                                           stream);
+                if (e == cudaSuccess && make_pool)
+                    e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks,
+                                           a->pool_out, sel_ws, sel_bytes, stream);
+            }
         }
         if (e != cudaSuccess) return CSA_ERR_CUDA;
     }

@@ -20,13 +20,12 @@
 //      shared memory of CTA 0, with the block ids.
 //   4. After one cluster barrier CTA 0 alone selects the K largest keys of the
 //      whole pool (ties: the earlier pool slot, which is the lower row id for
-//      an ascending pool) by a radix select over the keys' actual range: the
-//      first pass histograms the top 11 bits of (key - min key), so the bins
-//      spread over the scores present; later passes resolve the threshold bin.
-//      Selected rows are written in pool order, then -1 padding.
+//      an ascending pool) with cta_select::select_keys (select_cta.cuh) and
+//      writes the selected rows in pool order, then -1 padding.
 // Every wait is bounded; a wait that runs out raises CSA_DEV_TIMEOUT.
 #include "common.cuh"
 #include "csa_internal.h"
+#include "select_cta.cuh"
 
 namespace csa {
 namespace {
@@ -37,8 +36,6 @@ constexpr int kMaxTiles = 8;                   // 1,024 rows per CTA
 constexpr int kBlocksPerCta = kMaxTiles * kTileRows / kPoolBlock;  // 128
 constexpr int kMaxCluster = 16;
 constexpr int kMaxCand = kMaxCluster * kMaxTiles * kTileRows;     // 16,384
-constexpr int kDigitBits = 13;                // radix digit: 8,192 bins
-constexpr int kBins = 1 << kDigitBits;
 constexpr int kU = 4;                          // loads in flight per thread (score gathers)
 
 struct PoolArgs {
@@ -59,8 +56,6 @@ struct PoolSmem {
     uint64_t qbar, done;
     float w[64];
     int32_t blk[kBlocksPerCta];
-    uint32_t warp_a[kThreads / 32], warp_b[kThreads / 32], warp_c[kThreads / 32];
-    uint32_t res_bin, res_above;
     uint32_t tmem_slot;
     int abort;
 };
@@ -82,185 +77,20 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Block-wide exclusive scan of one value per thread; *total gets the sum.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, PoolSmem &sm, uint32_t *total)
+static_assert(kThreads == cta_select::kThreads && kMaxCand == cta_select::kMaxKeys, "one selection CTA shape");
+
+// The K best of the n pool rows whose keys are in allk (at their key_slot),
+// written to out as row ids in pool order (candidate c is row
+// allb[c / 8] * 8 + c % 8), then -1 padding.  All threads of the CTA call it.
+__device__ __forceinline__ void write_selection(uint32_t *allk, const int32_t *allb, int n, int K, int32_t *out,
+                                                cta_select::Scratch &sc)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
+    int32_t *kept_c = reinterpret_cast<int32_t *>(allk);
+    const int kept = cta_select::select_keys(allk, n, static_cast<uint32_t>(K), kept_c, sc);
+    for (int j = threadIdx.x; j < K; j += kThreads) {
+        const int c = j < kept ? kept_c[j] : -1;
+        out[j] = c >= 0 ? allb[c >> 3] * kPoolBlock + (c & 7) : -1;
     }
-    __syncthreads();
-    if (lane == 31) sm.warp_a[warp] = x;
-    __syncthreads();
-    uint32_t before = 0, t = 0;
-#pragma unroll
-    for (int i = 0; i < kThreads / 32; ++i) {
-        if (i < warp) before += sm.warp_a[i];
-        t += sm.warp_a[i];
-    }
-    *total = t;
-    return before + x - v;
-}
-
-// The K largest of n <= kMaxCand order-preserving keys in shared memory (0 =
-// no candidate), ties to the earlier candidate, written in candidate order as
-// row ids (candidate c is row blk[c / 8] * 8 + c % 8), then -1 padding.  All
-// threads of the CTA call it.  Each thread first loads its kNk keys into
-// registers (warp w holds candidates [w*32*kNk, (w+1)*32*kNk), 32 consecutive
-// ones per register), and every pass then runs on registers: one CTA does all
-// the work, so each pass must be a few independent instructions per key, not
-// a chain of shared-memory round trips.  A radix select over the keys' actual
-// range: pass 0 finds the count, minimum and maximum; each further pass
-// histograms the next kDigitBits bits of (key - minimum) among the keys that
-// share the bits fixed so far, until the threshold bin is taken whole or one
-// value is left.
-constexpr int kNk = kMaxCand / kThreads;  // keys per thread
-
-__device__ __forceinline__ void select_from_keys(const uint32_t *allk, const int32_t *allb, int n, int Kin, int32_t *out,
-                                                 uint32_t *hist, PoolSmem &sm)
-{
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t K = static_cast<uint32_t>(Kin);
-    const int c_beg = warp * 32 * kNk;
-    uint32_t kk[kNk];
-#pragma unroll
-    for (int j = 0; j < kNk; ++j) {
-        const int c = c_beg + 32 * j + lane;
-        kk[j] = c < n ? allk[c] : 0u;
-    }
-    // Pass 0: count, minimum and maximum of the candidate keys (0 = none).
-    uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0;
-#pragma unroll
-    for (int j = 0; j < kNk; ++j)
-        if (kk[j]) {
-            ++cnt;
-            kmin = min(kmin, kk[j]);
-            kmax = max(kmax, kk[j]);
-        }
-    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
-    __syncthreads();
-    if (lane == 0) {
-        sm.warp_a[warp] = kmin;
-        sm.warp_b[warp] = kmax;
-        sm.warp_c[warp] = cnt;
-    }
-    __syncthreads();
-    kmin = 0xFFFFFFFFu;
-    kmax = 0;
-    uint32_t total = 0;
-#pragma unroll
-    for (int i = 0; i < kThreads / 32; ++i) {
-        kmin = min(kmin, sm.warp_a[i]);
-        kmax = max(kmax, sm.warp_b[i]);
-        total += sm.warp_c[i];
-    }
-
-    // Threshold: keys > thr_gt are taken, and the first `need` keys equal to
-    // thr_eq (in candidate order).
-    uint32_t thr_gt = 0, thr_eq = 0, need = 0;
-    if (total > K) {
-        const uint32_t range = kmax - kmin;
-        int hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
-        uint32_t prefix = 0, above = 0;
-        while (true) {
-            if (hi == 0) {
-                // a single key value remains: ties
-                thr_gt = kmin + prefix;
-                thr_eq = thr_gt;
-                need = K - above;
-                break;
-            }
-            const int lo = hi > kDigitBits ? hi - kDigitBits : 0;
-            const int nb = 1 << (hi - lo);
-            __syncthreads();
-            for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
-            __syncthreads();
-#pragma unroll
-            for (int j = 0; j < kNk; ++j) {
-                const uint64_t v = kk[j] - kmin;
-                if (kk[j] && (v >> hi) == prefix) atomicAdd(&hist[(v >> lo) & (nb - 1)], 1u);
-            }
-            __syncthreads();
-            // the bin holding the (K - above)-th largest key: thread t scans
-            // bins [nb - (t+1)*per, nb - t*per) from the top
-            const uint32_t want = K - above;
-            const int per = nb >= kThreads ? nb / kThreads : 1;
-            const int bhi = nb - tid * per, blo = bhi - per;
-            uint32_t ssum = 0;
-            // each thread's bins are read in an order rotated by the thread's
-            // index, so the lanes of a warp hit different banks
-            if (blo >= 0)
-                for (int j = 0; j < per; ++j) ssum += hist[blo + ((j + tid) & (per - 1))];
-            uint32_t tot;
-            const uint32_t excl = block_exclusive_scan(ssum, sm, &tot);
-            if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
-                uint32_t cum = excl;
-                for (int bb = bhi - 1; bb >= blo; --bb) {
-                    if (cum + hist[bb] >= want) {
-                        sm.res_bin = static_cast<uint32_t>(bb);
-                        sm.res_above = cum;
-                        break;
-                    }
-                    cum += hist[bb];
-                }
-            }
-            __syncthreads();
-            const uint32_t bin = sm.res_bin;
-            above += sm.res_above;
-            const uint32_t in_bin = hist[bin];
-            prefix = (prefix << (hi - lo)) | bin;
-            hi = lo;
-            if (above + in_bin == K) {
-                // the threshold bin is taken whole
-                thr_gt = kmin + (prefix << lo) - 1u;
-                need = 0;
-                break;
-            }
-        }
-    }
-
-    // Output in candidate order: per register j, warp ballots of the taken
-    // keys; one prefix over the warps gives each warp its first position.
-    const unsigned lt = (1u << lane) - 1u;
-    uint32_t na = 0, ne = 0;
-#pragma unroll
-    for (int j = 0; j < kNk; ++j) {
-        na += __popc(__ballot_sync(0xFFFFFFFFu, kk[j] && kk[j] > thr_gt));
-        ne += __popc(__ballot_sync(0xFFFFFFFFu, need && kk[j] == thr_eq));
-    }
-    __syncthreads();
-    if (lane == 0) {
-        sm.warp_a[warp] = na;
-        sm.warp_b[warp] = ne;
-    }
-    __syncthreads();
-    uint32_t a_before = 0, t_before = 0;
-    for (int w = 0; w < warp; ++w) {
-        a_before += sm.warp_a[w];
-        t_before += sm.warp_b[w];
-    }
-#pragma unroll
-    for (int j = 0; j < kNk; ++j) {
-        const int c = c_beg + 32 * j + lane;
-        const bool is_above = kk[j] && kk[j] > thr_gt;
-        const bool is_tie = need && kk[j] == thr_eq;
-        const unsigned ba = __ballot_sync(0xFFFFFFFFu, is_above);
-        const unsigned be = __ballot_sync(0xFFFFFFFFu, is_tie);
-        const uint32_t ab = a_before + __popc(ba & lt), tb = t_before + __popc(be & lt);
-        int64_t pos = -1;
-        if (is_above) pos = ab + min(tb, need);
-        else if (is_tie && tb < need) pos = ab + tb;
-        if (pos >= 0) out[pos] = allb[c >> 3] * kPoolBlock + (c & 7);
-        a_before += __popc(ba);
-        t_before += __popc(be);
-    }
-    const uint32_t selected = total > K ? K : total;
-    for (uint32_t j = selected + tid; j < K; j += kThreads) out[j] = -1;
 }
 
 template <int HT>
@@ -276,7 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *allk = reinterpret_cast<uint32_t *>(q_s + ((HT * DI + 1023) & ~1023));  // CTA 0: [candidates] keys
     int32_t *allb = reinterpret_cast<int32_t *>(allk + kMaxCand);                    // CTA 0: [blocks] ids
     PoolSmem &sm = *reinterpret_cast<PoolSmem *>(allb + kMaxCluster * kBlocksPerCta);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(k_s);      // CTA 0, select phase: over the dead key tiles
+    // CTA 0, select phase: the selection's scratch over the dead key tiles
+    // (at least 32 KB: 8 tiles of 128 rows of >= 32 bytes)
+    cta_select::Scratch &sc = *reinterpret_cast<cta_select::Scratch *>(k_s);
     volatile int *abort_flag = &sm.abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -368,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ scores
         const int row = warp * 32 + lane;                                  // row within a tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t dst0 = cluster_map(smem_u32(allk), 0) + rank * a.bpc * kPoolBlock * 4;
+        const uint32_t dst0 = cluster_map(smem_u32(allk), 0);
         const uint32_t dstb = cluster_map(smem_u32(allb), 0) + rank * a.bpc * 4;
         if (row < a.bpc) st_cluster_u32(dstb + row * 4, static_cast<uint32_t>(sm.blk[row]));
         for (int t = 0; t < n_tiles; ++t) {
@@ -400,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (local < a.bpc * kPoolBlock) {
                 const int32_t blk = sm.blk[local >> 3];
                 const bool valid = blk >= 0 && blk * kPoolBlock + (local & 7) < Lp;
-                st_cluster_u32(dst0 + local * 4, valid ? score_key(s) : 0u);
+                const int cand = static_cast<int>(rank) * a.bpc * kPoolBlock + local;
+                st_cluster_u32(dst0 + cta_select::key_slot(cand) * 4, valid ? score_key(s) : 0u);
             }
         }
     }
@@ -419,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag && tid == 0) raise_status(a.status, CSA_DEV_TIMEOUT);
     if (rank != 0) return;
 
-    select_from_keys(allk, allb, C * a.bpc * kPoolBlock, a.K, a.idx + static_cast<int64_t>(unit) * a.K, hist, sm);
+    write_selection(allk, allb, C * a.bpc * kPoolBlock, a.K, a.idx + static_cast<int64_t>(unit) * a.K, sc);
 }
 
 // A Full layer that also keeps a pool of at least K blocks selects its top K
@@ -445,8 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) pool_rows_kernel(RowsArgs a)
     extern __shared__ uint8_t smem_raw[];
     uint32_t *allk = reinterpret_cast<uint32_t *>(smem_raw);       // [pool rows] keys
     int32_t *allb = reinterpret_cast<int32_t *>(allk + kMaxCand);   // [pool blocks] ids
-    uint32_t *hist = reinterpret_cast<uint32_t *>(allb + kMaxCluster * kBlocksPerCta);
-    PoolSmem &sm = *reinterpret_cast<PoolSmem *>(hist + kBins);
+    cta_select::Scratch &sc = *reinterpret_cast<cta_select::Scratch *>(allb + kMaxCluster * kBlocksPerCta);
     const int tid = threadIdx.x;
     const int unit = blockIdx.x;
     pdl_wait();
@@ -495,13 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1) pool_rows_kernel(RowsArgs a)
             uint32_t kq[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m) kq[m] = (blk[u] >= 0 && blk[u] * kPoolBlock + m < Lp) ? score_key(f[m]) : 0u;
-            uint4 *dst = reinterpret_cast<uint4 *>(allk + j * kPoolBlock);
-            dst[0] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-            dst[1] = make_uint4(kq[4], kq[5], kq[6], kq[7]);
+            // candidates 8j .. 8j+7 at their swizzled slots (cta_select::key_slot)
+            uint4 *dst = reinterpret_cast<uint4 *>(allk);
+            const int sw = (j >> 2) & 7;
+            dst[(2 * j) ^ sw] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+            dst[(2 * j + 1) ^ sw] = make_uint4(kq[4], kq[5], kq[6], kq[7]);
         }
     }
     __syncthreads();
-    select_from_keys(allk, allb, n, a.K, a.idx + static_cast<int64_t>(unit) * a.K, hist, sm);
+    write_selection(allk, allb, n, a.K, a.idx + static_cast<int64_t>(unit) * a.K, sc);
 }
 
 size_t pool_smem_bytes(int DI, int HT)
@@ -546,7 +380,7 @@ cudaError_t launch_pool_rows(const CacheView &c, int P, const float *scores, int
                              int pool_blocks, int K, int32_t *idx, cudaStream_t st)
 {
     if (!pool_rows_supported(pool_blocks, K)) return cudaErrorInvalidValue;
-    const size_t smem = static_cast<size_t>(kMaxCand) * 4 + kMaxCluster * kBlocksPerCta * 4 + kBins * 4 + sizeof(PoolSmem);
+    const size_t smem = static_cast<size_t>(kMaxCand) * 4 + kMaxCluster * kBlocksPerCta * 4 + sizeof(cta_select::Scratch);
     static bool configured = false;
     if (!configured) {
         const cudaError_t e =

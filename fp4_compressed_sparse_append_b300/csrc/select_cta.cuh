@@ -1,0 +1,362 @@
+// Top-K selection inside one CTA, for up to 16,384 candidates: the K largest
+// order-preserving 32-bit keys (0 = no candidate), ties to the lower candidate
+// index, returned as candidate indices in ascending order.  "DeepSeek V4.1
+// Flash: Pushing the Limits" (talk write-up), section "The Paper": the query
+// keeps only the top indices; "G2C Brief - DeepSeek V4.1-Flash", section "The
+// hierarchical indexer": a Reindex layer keeps the best K of the pool's rows.
+//
+// One CTA of 512 threads does all the work, so the cost is the instructions
+// issued per key (16 warps share four schedulers: one instruction per key is
+// about 0.07 us), and the design keeps that count small:
+//   - thread t owns the 32 consecutive candidates [32t, 32t + 32), held in
+//     registers: what a thread keeps is counted without warp votes (a vote
+//     costs tens of cycles per warp here) and output positions come from one
+//     block scan of per-thread counts;
+//   - one histogram pass over all keys: (key - minimum) over 4,096 bins that
+//     span the keys' actual range (indexer scores of exactly 0, where every
+//     head's product is negative, stretch that range, so the bin holding the
+//     K-th largest key can hold hundreds of keys);
+//   - the keys of that bin are gathered, in candidate order, into a list of at
+//     most 1,024 (another pass over all keys first if the bin is larger), and
+//     further passes over the next lower bits run on the list only;
+//   - a list of at most 32 keys is ranked exactly by one warp;
+//   - every outcome is one rule: keep the keys above thr_gt, and the first
+//     `need` keys equal to thr_eq in candidate order.
+// The keys live in shared memory at key_slot(c): 16-byte chunks of each
+// 32-key row XOR-swizzled by the row index, so that both a warp's coalesced
+// writes (32 consecutive candidates, or 8 lanes of 4) and its per-thread
+// 16-byte reads (one thread's 32 candidates) are free of bank conflicts.
+#pragma once
+
+#include "common.cuh"
+
+namespace csa {
+namespace cta_select {
+
+constexpr int kThreads = 512;
+constexpr int kPerThread = 32;
+constexpr int kMaxKeys = kThreads * kPerThread;  // 16,384
+constexpr int kBinBits = 12;
+constexpr int kBins = 1 << kBinBits;
+constexpr int kListMax = 1024;                   // keys of a threshold bin gathered into a list
+constexpr int kRankMax = 32;                     // list length ranked exactly by one warp
+constexpr int kWarps = kThreads / 32;
+static_assert(kListMax == 2 * kThreads, "list passes give each thread two entries");
+
+struct Scratch {
+    uint32_t hist[kBins];
+    uint32_t lk[kListMax];  // gathered keys, in candidate order
+    int32_t lc[kListMax];   // and their candidates
+    uint32_t wa[kWarps], wb[kWarps], wc[kWarps];
+    uint32_t res_bin, res_above;
+    uint32_t thr_gt, thr_eq, need;
+};
+
+// Shared-memory index of candidate c's key.
+__device__ __forceinline__ int key_slot(int c) { return c ^ (((c >> 5) & 7) << 2); }
+
+// Exclusive block scan of one value per thread (all kThreads threads); *total
+// gets the sum.  Its first CTA barrier orders it after the previous scan's
+// reads of the per-warp sums; its second makes them visible.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, Scratch &sc, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) sc.wa[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, t = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+        const uint32_t w = sc.wa[i];
+        before += i < warp ? w : 0u;
+        t += w;
+    }
+    *total = t;
+    return before + x - v;
+}
+
+__device__ __forceinline__ void zero_bins(Scratch &sc, int nb)
+{
+    uint4 *z = reinterpret_cast<uint4 *>(sc.hist);
+    for (int i = threadIdx.x; i < (nb + 3) / 4; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {  // overwritten by find_bin's owner of the bin
+        sc.res_bin = 0;
+        sc.res_above = 0;
+    }
+}
+
+// With sc.hist holding nb bins: the bin b holding the want-th largest key
+// (fewer than `want` keys in the bins above b, at least `want` in b and
+// above).  Thread t sums bins [nb - (t+1)*per, nb - t*per), read in an order
+// rotated by t so that a warp's lanes hit different banks.  Sets *bin and
+// *above (the count in the bins above it), the same in every thread.
+__device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uint32_t *bin, uint32_t *above)
+{
+    const int tid = threadIdx.x;
+    const int per = nb >= kThreads ? nb / kThreads : 1;
+    const int bhi = nb - tid * per, blo = bhi - per;
+    uint32_t ssum = 0;
+    if (blo >= 0)
+        for (int j = 0; j < per; ++j) ssum += sc.hist[blo + ((j + tid) & (per - 1))];
+    uint32_t tot;
+    const uint32_t excl = block_scan(ssum, sc, &tot);
+    if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
+        uint32_t cum = excl;
+        for (int bb = bhi - 1; bb >= blo; --bb) {
+            const uint32_t h = sc.hist[bb];
+            if (cum + h >= want) {
+                sc.res_bin = static_cast<uint32_t>(bb);
+                sc.res_above = cum;
+                break;
+            }
+            cum += h;
+        }
+    }
+    __syncthreads();
+    *bin = sc.res_bin;
+    *above = sc.res_above;
+}
+
+// The K largest of the keys of candidates [0, n), n <= kMaxKeys, read from
+// keys[key_slot(c)].  Writes the kept candidates' indices in ascending order
+// to obuf[0, kept) and returns kept = min(K, number of non-zero keys).  obuf
+// may be the key array itself (every key is in registers before the first
+// write).  Called by all kThreads threads; ends with a CTA barrier (obuf is
+// then complete).
+__device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t K, int32_t *obuf, Scratch &sc)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c0 = tid * kPerThread;
+    uint32_t kk[kPerThread];
+    {
+        const uint4 *kv = reinterpret_cast<const uint4 *>(keys + c0);
+#pragma unroll
+        for (int m = 0; m < kPerThread / 4; ++m) {
+            const uint4 v = kv[m ^ (tid & 7)];
+            kk[4 * m] = c0 + 4 * m < n ? v.x : 0u;
+            kk[4 * m + 1] = c0 + 4 * m + 1 < n ? v.y : 0u;
+            kk[4 * m + 2] = c0 + 4 * m + 2 < n ? v.z : 0u;
+            kk[4 * m + 3] = c0 + 4 * m + 3 < n ? v.w : 0u;
+        }
+    }
+    uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const uint32_t k = kk[j];
+        cnt += k ? 1u : 0u;
+        kmin = min(kmin, k ? k : 0xFFFFFFFFu);
+        kmax = max(kmax, k);
+    }
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    __syncthreads();  // the caller's last use of the scratch words is over
+    if (lane == 0) {
+        sc.wa[warp] = kmin;
+        sc.wb[warp] = kmax;
+        sc.wc[warp] = cnt;
+    }
+    __syncthreads();
+    kmin = 0xFFFFFFFFu;
+    kmax = 0;
+    uint32_t total = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+        kmin = min(kmin, sc.wa[i]);
+        kmax = max(kmax, sc.wb[i]);
+        total += sc.wc[i];
+    }
+
+    // The rule: keep keys > thr_gt, and the first `need` keys == thr_eq.
+    uint32_t thr_gt = 0, thr_eq = 0, need = 0;
+    if (total > K) {
+        // v = key - kmin; the bits of v above `hi` are fixed to `prefix`, and
+        // `above` keys lie above them (all of them kept).
+        const uint32_t range = kmax - kmin;
+        int hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
+        uint32_t prefix = 0, above = 0;
+        bool done = false;
+        int passes = 0;
+        // A. passes over all keys until the threshold bin holds <= kListMax keys
+        while (true) {
+            if (hi == 0) {  // one key value left
+                thr_gt = thr_eq = kmin + prefix;
+                need = K - above;
+                done = true;
+                break;
+            }
+            const int d = hi < kBinBits ? hi : kBinBits, lo = hi - d, nb = 1 << d;
+            if (passes++) __syncthreads();  // every thread has read the last pass's bins
+            zero_bins(sc, nb);
+            __syncthreads();
+            const uint32_t mask = hi >= 32 ? 0u : (0xFFFFFFFFu << hi);
+            const uint32_t pfx = hi >= 32 ? 0u : (prefix << hi);
+#pragma unroll
+            for (int j = 0; j < kPerThread; ++j) {
+                const uint32_t v = kk[j] - kmin;
+                if (kk[j] && (v & mask) == pfx) atomicAdd(&sc.hist[(v >> lo) & (nb - 1)], 1u);
+            }
+            __syncthreads();
+            uint32_t bin, ab;
+            find_bin(nb, K - above, sc, &bin, &ab);
+            above += ab;
+            const uint32_t in_bin = sc.hist[bin];
+            const uint32_t P = (prefix << d) | bin;
+            if (in_bin == K - above) {  // the bin is taken whole
+                thr_gt = kmin + (P << lo) - 1u;
+                done = true;
+                break;
+            }
+            if (lo == 0) {  // the bin is one key value
+                thr_gt = thr_eq = kmin + P;
+                need = K - above;
+                done = true;
+                break;
+            }
+            prefix = P;
+            hi = lo;
+            if (in_bin <= kListMax) break;
+        }
+        if (!done) {
+            // B. gather the bin's keys ((v >> hi) == prefix, 1 <= hi < 32) into
+            // the list, in candidate order
+            uint32_t mine = 0;
+#pragma unroll
+            for (int j = 0; j < kPerThread; ++j)
+                mine += (kk[j] && ((kk[j] - kmin) >> hi) == prefix) ? 1u : 0u;
+            uint32_t m;
+            uint32_t off = block_scan(mine, sc, &m);
+#pragma unroll
+            for (int j = 0; j < kPerThread; ++j)
+                if (kk[j] && ((kk[j] - kmin) >> hi) == prefix) {
+                    sc.lk[off] = kk[j];
+                    sc.lc[off] = c0 + j;
+                    ++off;
+                }
+            __syncthreads();
+            // C. passes over the list; thread t holds entries 2t and 2t + 1
+            uint32_t nd = K - above;  // keys still to keep, all in the list
+            while (static_cast<int>(m) > kRankMax) {
+                if (hi == 0) {  // one key value left
+                    thr_gt = thr_eq = kmin + prefix;
+                    need = nd;
+                    done = true;
+                    break;
+                }
+                const int d = hi < kBinBits ? hi : kBinBits, lo = hi - d, nb = 1 << d;
+                const int i0 = 2 * tid, i1 = 2 * tid + 1;
+                const bool h0 = i0 < static_cast<int>(m), h1 = i1 < static_cast<int>(m);
+                const uint32_t e0 = h0 ? sc.lk[i0] : 0u, e1 = h1 ? sc.lk[i1] : 0u;
+                const int32_t ec0 = h0 ? sc.lc[i0] : 0, ec1 = h1 ? sc.lc[i1] : 0;
+                zero_bins(sc, nb);
+                __syncthreads();
+                const uint32_t b0 = ((e0 - kmin) >> lo) & (nb - 1), b1 = ((e1 - kmin) >> lo) & (nb - 1);
+                if (h0) atomicAdd(&sc.hist[b0], 1u);
+                if (h1) atomicAdd(&sc.hist[b1], 1u);
+                __syncthreads();
+                uint32_t bin, ab;
+                find_bin(nb, nd, sc, &bin, &ab);
+                nd -= ab;
+                const uint32_t in_bin = sc.hist[bin];
+                const uint32_t P = (prefix << d) | bin;
+                if (in_bin == nd) {
+                    thr_gt = kmin + (P << lo) - 1u;
+                    need = 0;
+                    done = true;
+                    break;
+                }
+                if (lo == 0) {
+                    thr_gt = thr_eq = kmin + P;
+                    need = nd;
+                    done = true;
+                    break;
+                }
+                // keep the bin's entries, in order (each thread's entries were
+                // read before the scan's first barrier)
+                const bool k0 = h0 && b0 == bin, k1 = h1 && b1 == bin;
+                uint32_t o = block_scan((k0 ? 1u : 0u) + (k1 ? 1u : 0u), sc, &m);
+                if (k0) {
+                    sc.lk[o] = e0;
+                    sc.lc[o] = ec0;
+                    ++o;
+                }
+                if (k1) {
+                    sc.lk[o] = e1;
+                    sc.lc[o] = ec1;
+                }
+                __syncthreads();
+                prefix = P;
+                hi = lo;
+            }
+            if (!done) {
+                // D. rank the m <= 32 listed keys in one warp; the nd-th
+                // largest, V, sets the rule: keys > V, and the first
+                // nd - (listed keys > V) keys equal to V (every key equal to V
+                // is listed)
+                if (warp == 0) {
+                    const bool has = lane < static_cast<int>(m);
+                    const uint32_t key = has ? sc.lk[lane] : 0u;
+                    const int32_t cand = has ? sc.lc[lane] : 0;
+                    uint32_t r = 0;
+                    for (int i = 0; i < static_cast<int>(m); ++i) {
+                        const uint32_t o = __shfl_sync(0xFFFFFFFFu, key, i);
+                        const int32_t oc = __shfl_sync(0xFFFFFFFFu, cand, i);
+                        r += (o > key || (o == key && oc < cand)) ? 1u : 0u;
+                    }
+                    const unsigned at = __ballot_sync(0xFFFFFFFFu, has && r == nd - 1u);
+                    const uint32_t V = __shfl_sync(0xFFFFFFFFu, key, __ffs(static_cast<int>(at)) - 1);
+                    const uint32_t gt = __reduce_add_sync(0xFFFFFFFFu, (has && key > V) ? 1u : 0u);
+                    if (lane == 0) {
+                        sc.thr_gt = V;
+                        sc.thr_eq = V;
+                        sc.need = nd - gt;
+                    }
+                }
+                __syncthreads();
+                thr_gt = sc.thr_gt;
+                thr_eq = sc.thr_eq;
+                need = sc.need;
+            }
+        }
+    }
+
+    // Output: this thread's kept candidates (bit j = candidate c0 + j), the
+    // positions from one scan of (kept, ties) counts.
+    uint32_t sel = 0, tie = 0;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        sel |= (kk[j] > thr_gt ? 1u : 0u) << j;
+        tie |= (need && kk[j] == thr_eq ? 1u : 0u) << j;
+    }
+    uint32_t tot2;
+    const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(sel)) << 16) | static_cast<uint32_t>(__popc(tie)), sc,
+                                   &tot2);
+    const uint32_t a_before = ex >> 16, t_before = ex & 0xFFFFu;
+    if (need) {
+        // the first `need` ties in candidate order are kept
+        uint32_t take = need > t_before ? need - t_before : 0u;
+        uint32_t tb = tie;
+        while (take && tb) {
+            sel |= tb & (~tb + 1u);
+            tb &= tb - 1u;
+            --take;
+        }
+    }
+    uint32_t pos = a_before + min(t_before, need);
+    while (sel) {
+        const int j = __ffs(static_cast<int>(sel)) - 1;
+        obuf[pos++] = c0 + j;
+        sel &= sel - 1u;
+    }
+    __syncthreads();
+    return static_cast<int>(total > K ? K : total);
+}
+
+}  // namespace cta_select
+}  // namespace csa

@@ -23,6 +23,10 @@
 // order: per (iteration, warp) counts from warp ballots, one block scan, and
 // one exchange of per-CTA counts give every selected key its position.
 //
+// A row of at most 16,384 candidates goes to one CTA instead
+// (select_one_kernel, with the selection of select_cta.cuh): no cluster
+// barrier, no warp votes.
+//
 // Rows longer than one cluster holds are split into segments: stage 1 keeps
 // each segment's own top K (with scores) in the workspace; stage 2 selects the
 // row's top K among those, which is exact because every member of the row's
@@ -31,6 +35,7 @@
 
 #include "common.cuh"
 #include "csa_internal.h"
+#include "select_cta.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -45,7 +50,6 @@ constexpr int kDigit2Bins = 256;     // key bits 7..0
 constexpr int kSelCacheMax = 16384;  // keys held per CTA at most (64 KB): two CTAs fit one SM
 constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
-constexpr int kMinChunk = 4096;      // a row of up to 2x this stays whole in one CTA (no cluster barrier)
 constexpr int kMinChunkLong = 1024;  // a longer row is not spread thinner than this per CTA
 constexpr int64_t kSegmentLen = static_cast<int64_t>(kMaxCluster) * 8192;
 
@@ -110,6 +114,34 @@ struct RowView {
         const int32_t id = __ldg(ids + i);
         const float v = __ldg(s + i);
         return id >= 0 ? score_key(v) : 0u;
+    }
+    // Keys of candidates 4q .. 4q+3 (4q < n) from one 16-byte score load (and
+    // one block id or four pair ids): rows, pool rows and pairs whose row
+    // start is 16-byte aligned (a row of scores always is: the C ABI takes
+    // them 16-byte aligned with a stride that is a multiple of 4, at least the
+    // row's length).  Candidates >= n get 0.
+    __device__ __forceinline__ uint4 key4(int q, int n) const
+    {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(s) + q);
+        const int i = 4 * q;
+        bool ok[4];
+        if (S == kPoolRows) {
+            const int32_t blk = __ldg(prow + (q >> 1));
+            const int64_t r0 = static_cast<int64_t>(blk) * kPoolBlock + (i & 7);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) ok[r] = blk >= 0 && r0 + r < L;
+        } else if (S == kPairs) {
+            const int4 id4 = __ldg(reinterpret_cast<const int4 *>(ids) + q);
+            ok[0] = id4.x >= 0 && i < n;
+            ok[1] = id4.y >= 0 && i + 1 < n;
+            ok[2] = id4.z >= 0 && i + 2 < n;
+            ok[3] = id4.w >= 0 && i + 3 < n;
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) ok[r] = i + r < n;
+        }
+        return make_uint4(ok[0] ? score_key(v.x) : 0u, ok[1] ? score_key(v.y) : 0u, ok[2] ? score_key(v.z) : 0u,
+                          ok[3] ? score_key(v.w) : 0u);
     }
     __device__ __forceinline__ int32_t id(int64_t i) const
     {
@@ -457,6 +489,78 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
         }
 }
 
+// A row of at most cta_select::kMaxKeys candidates: one CTA, no cluster.  The
+// keys are gathered with eight loads in flight per thread, selected by
+// cta_select::select_keys, and the kept candidates' ids written in order with
+// -1 padding.
+template <int S>
+__global__ void __launch_bounds__(cta_select::kThreads, 1) select_one_kernel(SelArgs a)
+{
+    namespace cs = cta_select;
+    extern __shared__ __align__(16) uint8_t dyn_smem[];
+    uint32_t *keys = reinterpret_cast<uint32_t *>(dyn_smem);  // then the kept candidates
+    cs::Scratch &sc = *reinterpret_cast<cs::Scratch *>(keys + cs::kMaxKeys);
+    const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int row = blockIdx.y;
+    int n;
+    RowView<S> rv{nullptr, nullptr, nullptr, 0};
+    if (S == kPairs) {
+        n = a.n_pairs;
+        rv.s = a.scores + static_cast<int64_t>(row) * a.n_pairs;
+        rv.ids = a.pair_ids + static_cast<int64_t>(row) * a.n_pairs;
+    } else {
+        const int b = row / a.P, p = row % a.P;
+        const int L = min(a.lengths[b], a.cap) - a.P + 1 + p;
+        rv.s = a.scores + static_cast<int64_t>(row) * a.ld;
+        rv.L = L;
+        if (S == kPoolRows) {
+            n = a.pool_blocks * kPoolBlock;
+            rv.prow = a.pool + static_cast<int64_t>(row) * a.pool_blocks;
+        } else {
+            n = L <= 0 ? 0 : (S == kRows ? L : (L + kPoolBlock - 1) / kPoolBlock);
+        }
+    }
+    n = min(n, cs::kMaxKeys);  // the host sends longer rows to the cluster kernel
+    const bool vec = S != kBlocks && (S != kPairs || (a.n_pairs & 3) == 0);
+    if (vec) {
+        // 16-byte loads, all of a thread's in flight at once (n <= 16,384 is
+        // at most 8 quads per thread)
+        const int nq = (n + 3) / 4;
+        uint4 k[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int q = u * cs::kThreads + tid;
+            k[u] = q < nq ? rv.key4(q, n) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int q = u * cs::kThreads + tid;
+            if (q < nq) *reinterpret_cast<uint4 *>(keys + cs::key_slot(4 * q)) = k[u];
+        }
+    }
+    constexpr int U = S == kBlocks ? 2 : 8;
+    for (int base = 0; !vec && base < n; base += U * cs::kThreads) {
+        uint32_t k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * cs::kThreads + tid;
+            k[u] = i < n ? rv.key(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * cs::kThreads + tid;
+            if (i < n) keys[cs::key_slot(i)] = k[u];
+        }
+    }
+    __syncthreads();
+    int32_t *kept_c = reinterpret_cast<int32_t *>(keys);
+    const int kept = cs::select_keys(keys, n, static_cast<uint32_t>(a.K), kept_c, sc);
+    int32_t *out = a.out_ids + static_cast<int64_t>(row) * a.K;
+    for (int j = tid; j < a.K; j += cs::kThreads) out[j] = j < kept ? rv.id(kept_c[j]) : -1;
+}
+
 size_t select_smem(int64_t chunk)
 {
     return sizeof(SelShared) + static_cast<size_t>((chunk + 3) / 4 * 4) * sizeof(uint32_t);
@@ -477,10 +581,9 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
     // Smallest cluster whose chunks fit shared memory, widened (down to
     // kMinChunkLong keys per CTA) while the grid is under one CTA per SM: spreading
     // a row's keys over more CTAs also spreads the contention of its shared-
-    // memory histogram, which crowded indexer scores make high.
-    // Rows of at most 2 * kMinChunk keys stay in one CTA: there the cluster
-    // barriers cost more than the spread saves.
-    const int64_t min_chunk = n_per_cluster <= 2 * kMinChunk ? kMinChunk : kMinChunkLong;
+    // memory histogram, which crowded indexer scores make high.  (Rows short
+    // enough for one CTA mostly go to select_one_kernel.)
+    const int64_t min_chunk = kMinChunkLong;
     int C = 1;
     while (C < kMaxCluster &&
            ((n_per_cluster + C - 1) / C > kSelCacheMax ||
@@ -491,13 +594,31 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
     return launch_kernel(select_kernel<S>, dim3(C, grid_rows), dim3(kSelThreads), select_smem(chunk), st, C, args);
 }
 
+// Rows of at most cta_select::kMaxKeys candidates without per-candidate score
+// outputs go to one CTA each (select_one_kernel), longer ones to the clusters.
+template <int S>
+cudaError_t launch_one_or_cluster(const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)
+{
+    if (n_per_cluster > cta_select::kMaxKeys || args.segments != 1 || args.out_scores)
+        return launch_source<S>(args, grid_rows, n_per_cluster, st);
+    constexpr size_t smem = cta_select::kMaxKeys * 4 + sizeof(cta_select::Scratch);
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(select_one_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_kernel(select_one_kernel<S>, dim3(1, grid_rows), dim3(cta_select::kThreads), smem, st, 0, args);
+}
+
 cudaError_t launch(int source, const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)
 {
     switch (source) {
-    case kRows: return launch_source<kRows>(args, grid_rows, n_per_cluster, st);
-    case kBlocks: return launch_source<kBlocks>(args, grid_rows, n_per_cluster, st);
-    case kPoolRows: return launch_source<kPoolRows>(args, grid_rows, n_per_cluster, st);
-    default: return launch_source<kPairs>(args, grid_rows, n_per_cluster, st);
+    case kRows: return launch_one_or_cluster<kRows>(args, grid_rows, n_per_cluster, st);
+    case kBlocks: return launch_one_or_cluster<kBlocks>(args, grid_rows, n_per_cluster, st);
+    case kPoolRows: return launch_one_or_cluster<kPoolRows>(args, grid_rows, n_per_cluster, st);
+    default: return launch_one_or_cluster<kPairs>(args, grid_rows, n_per_cluster, st);
     }
 }
 

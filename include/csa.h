@@ -260,9 +260,8 @@ CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scor
  * The same result as csa_index_score + csa_topk (up to the fp32 summation
  * order of the scores), in one launch and without a scores buffer.
  * Supported: E4M3 keys, HI <= 64, pool_blocks <= 2048, K <= 16384; otherwise
- * CSA_ERR_UNSUPPORTED (use the two calls instead).  csa_layer_step keeps the
- * two calls for Reindex layers: on B300 they measure faster within a layer,
- * because the one-CTA selection here is latency-bound.
+ * CSA_ERR_UNSUPPORTED (use the two calls instead).  csa_layer_step takes this
+ * path for Reindex layers over a pool whenever it is supported.
  */
 CSA_API csa_status csa_pool_topk(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
                                  const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx,
