@@ -57,7 +57,8 @@ constexpr int kMaxClusterSplit = 8;  // portable cluster size
 
 struct AttArgs {
     CacheView c;
-    int P, H, K;
+    int P, H, K;      // H: heads per CTA (one head group)
+    int G;            // head groups per query: CTA row y is query y / G, heads (y % G) * H ..
     int NH;           // heads rounded up to 16 (MMA N of O^T)
     const uint16_t *q;
     float scale;
@@ -156,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     volatile int *abort_flag = &sm.abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.y, split = blockIdx.x;
+    // vunit: a query's head group (its q, out, lse and partials); unit: the
+    // query (its selection, sequence and window)
+    const int vunit = blockIdx.y, unit = vunit / a.G, split = blockIdx.x;
     const int b = unit / a.P;
     int len = 0;
     const bool win = split == a.swa_split;
@@ -193,9 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     // kernels, so it is fetched before waiting on the previous kernel.
     uint8_t *q_stage = v_s + kRows * D * 2;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(kMaxHeads * D * 2));
+        mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(NH * D * 2));
         for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_2d(q_stage + kb * kMaxHeads * 128, &qmap, &sm.qbar, kb * 128, unit * H);
+            tma_load_2d(q_stage + kb * kMaxHeads * 128, &qmap, &sm.qbar, kb * 128, vunit * H);
     }
     // Q staged once as fp16 * 2^e per head, max|q| * 2^e < 2^15 (exact while
     // an entry stays within fp16's normal range, about 28 binades below the
@@ -545,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
         if (lane < 16 && active && !a.cluster) {
             if (a.nsplit == 1) {
                 if (a.lse)
-                    a.lse[static_cast<int64_t>(unit) * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                    a.lse[static_cast<int64_t>(vunit) * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
             } else {
-                a.part_ml[(static_cast<int64_t>(unit) * a.nsplit + split) * H + h] = make_float2(m_run, l_run);
+                a.part_ml[(static_cast<int64_t>(vunit) * a.nsplit + split) * H + h] = make_float2(m_run, l_run);
             }
         }
     }
@@ -567,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             const int nc16 = NH / 16, items = (D / 128) * nc16;
             const bool final_out = a.nsplit == 1 && !a.cluster;
             float *obuf = reinterpret_cast<float *>(v_s);
-            float *obase = final_out ? a.out + static_cast<int64_t>(unit) * H * D
-                                     : a.part_o + (static_cast<int64_t>(unit) * a.nsplit + split) * H * D;
+            float *obase = final_out ? a.out + static_cast<int64_t>(vunit) * H * D
+                                     : a.part_o + (static_cast<int64_t>(vunit) * a.nsplit + split) * H * D;
             for (int it = grp; it < items; it += ngrp) {
                 const int mt = it / nc16, c0 = (it - mt * nc16) * 16;
                 const int d = mt * 128 + q4 * 32 + lane;
@@ -623,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             const float inv = L > 0.f ? 1.f / L : 0.f;
             for (int q = 0; q < C; ++q) wq[q * kMaxHeads + tid] = mq[q] * inv;
             if (rank == 0 && a.lse)
-                a.lse[static_cast<int64_t>(unit) * H + tid] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+                a.lse[static_cast<int64_t>(vunit) * H + tid] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
         __syncthreads();
         const int nd4 = (d1 - d0) / 4;
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 acc.z = fmaf(wgt, v[q].z, acc.z);
                 acc.w = fmaf(wgt, v[q].w, acc.w);
             }
-            *reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(unit) * H + hh) * D + d) = acc;
+            *reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(vunit) * H + hh) * D + d) = acc;
         }
         cluster.sync();  // no CTA leaves while another still reads its shared memory
     }
@@ -714,6 +717,7 @@ __global__ void __launch_bounds__(32) attend_merge_kernel(int D, int H, int nspl
 struct Plan {
     int nsplit, tiles_per_split, tiles_total, cluster;
     int swa_split;  // index of the local-window split, or -1
+    int G;          // head groups per query
 };
 
 // Splits of one query's selection: at most one wave of CTAs.  Up to
@@ -721,7 +725,13 @@ struct Plan {
 // very few queries) merge through global memory, which measures faster than a
 // cluster of 16 for them.  With a local window, one more split per query
 // attends to the window and is merged like the others.
-Plan plan(const CacheView &c, int P, int K, const SwaView *swa)
+// When a query's splits still leave SMs idle, its heads are split into G
+// groups of at least 16 (the heads' softmaxes are independent), each group a
+// CTA row of its own over the same selection: a CTA then converts only its
+// group's query rows and writes only its group's share of the output or
+// partial (a quarter of the 128 KB partial for one query of 64 heads split 4
+// ways).  The partials and the workspace keep their total size.
+Plan plan(const CacheView &c, int P, int H, int K, const SwaView *swa)
 {
     const int units = c.B * P;
     const int extra = swa ? 1 : 0;
@@ -737,6 +747,7 @@ Plan plan(const CacheView &c, int P, int K, const SwaView *swa)
         p.nsplit = 1 + extra;
         p.swa_split = swa ? 1 : -1;
         p.cluster = p.nsplit > 1;
+        p.G = 1;
         return p;
     }
     p.tiles_total = tiles;
@@ -745,6 +756,10 @@ Plan plan(const CacheView &c, int P, int K, const SwaView *swa)
     p.nsplit = main_splits + extra;
     p.swa_split = swa ? main_splits : -1;
     p.cluster = p.nsplit > 1 && p.nsplit <= kMaxClusterSplit;
+    p.G = 1;
+    while (H % (2 * p.G) == 0 && H / (2 * p.G) >= 16 &&
+           static_cast<int64_t>(units) * p.nsplit * 2 * p.G <= sm_count())
+        p.G *= 2;
     return p;
 }
 
@@ -758,7 +773,7 @@ size_t smem_bytes(int D, int NH)
 
 size_t attend_workspace_bytes(const CacheView &c, int P, int H, int K, const SwaView *swa)
 {
-    const Plan p = plan(c, P, K, swa);
+    const Plan p = plan(c, P, H, K, swa);
     if (p.nsplit == 1 || p.cluster) return 0;
     const size_t units = static_cast<size_t>(c.B) * P;
     size_t o = units * p.nsplit * H * c.D * sizeof(float);
@@ -774,8 +789,9 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     if (units == 0) return cudaSuccess;
     if (H > kMaxHeads || c.D % 128 || c.D > 512) return cudaErrorInvalidValue;
     if (swa && (!swa->rows || swa->n < P || swa->window < 1)) return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes(c.D, (H + 15) / 16 * 16);
-    const Plan p = plan(c, P, K, swa);
+    const Plan p = plan(c, P, H, K, swa);
+    const int Hg = H / p.G;  // heads per CTA
+    const size_t smem = smem_bytes(c.D, (Hg + 15) / 16 * 16);
     cudaError_t e =
         cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -783,9 +799,10 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     AttArgs a{};
     a.c = c;
     a.P = P;
-    a.H = H;
+    a.H = Hg;
+    a.G = p.G;
     a.K = K;
-    a.NH = (H + 15) / 16 * 16;
+    a.NH = (Hg + 15) / 16 * 16;
     a.q = q;
     a.scale = scale;
     a.idx = idx;
@@ -808,17 +825,19 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     while (cols < static_cast<uint32_t>(2 * kRows + (c.D / 128) * a.NH)) cols *= 2;
     a.tmem_cols = cols;
     a.status = status;
-    // Query rows [units*H][D] bf16 as bytes: 64-dim (128-byte) boxes of 64 rows.
+    // Query rows [units*H][D] bf16 as bytes: 64-dim (128-byte) boxes of NH rows
+    // (one head group, rounded up to 16).
     CUtensorMap qm;
     if (encode_tensor_map_2d_u8(&qm, q, static_cast<uint64_t>(c.D) * 2, static_cast<uint64_t>(units) * H, 128,
-                                kMaxHeads, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+                                a.NH, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    e = launch_kernel(attend_kernel, dim3(p.nsplit, units), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0, qm,
-                      a);
+    e = launch_kernel(attend_kernel, dim3(p.nsplit, units * p.G), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0,
+                      qm, a);
     if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
     // The merge loads every split's value at once: 16 or 32 registers.
     auto merge = p.nsplit <= 16 ? attend_merge_kernel<16> : attend_merge_kernel<kMaxSplit>;
-    return launch_kernel(merge, dim3((c.D + kMergeDims - 1) / kMergeDims, H, units), dim3(32), 0, st, 0, c.D, H, p.nsplit,
+    return launch_kernel(merge, dim3((c.D + kMergeDims - 1) / kMergeDims, Hg, units * p.G), dim3(32), 0, st, 0, c.D, Hg,
+                         p.nsplit,
                          static_cast<const float *>(a.part_o), static_cast<const float2 *>(a.part_ml), out, lse);
 }
 
