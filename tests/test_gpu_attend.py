@@ -23,12 +23,16 @@ def host_cache(cache):
 # (8 queries, the 64K decode shape), and one split per query (160 queries, more
 # queries than SMs).  Two cases use a logit scale of 1, where a later tile's
 # maximum exceeds the running one by more than 2^8 and the accumulated output
-# is rescaled.
+# is rescaled.  Few queries split their heads into groups: 2 groups of 32
+# heads (2 queries), 4 of 16 (one query, with 32 splits and with a cluster of
+# 8), 2 of 16 (32 heads), and groups that are not a multiple of 16: 2 of 24
+# (48 heads) and 2 of 20 (40 heads, 2 queries), whose query boxes reach into
+# the next group's rows and past the last query.
 CASES = [(16, 128, 256, 1, 1, None), (64, 512, 2048, 2, 1, None), (7, 256, 100, 2, 3, None),
          (64, 512, 1, 1, 1, None), (64, 512, 2048, 20, 1, None), (48, 384, 700, 12, 1, None),
          (64, 512, 2048, 8, 1, None), (8, 384, 320, 29, 1, None), (8, 256, 448, 21, 1, None),
          (32, 512, 4096, 1, 1, 1.0), (64, 128, 4096, 1, 1, 1.0), (64, 512, 512, 1, 1, None),
-         (16, 128, 200, 160, 1, None)]
+         (16, 128, 200, 160, 1, None), (48, 512, 2048, 1, 1, None), (40, 256, 1500, 2, 1, None)]
 
 
 @pytest.mark.parametrize("H,D,K,Bn,P,scale", CASES)

@@ -82,3 +82,51 @@ def test_select_over_pool_candidates():
         ref = rows[sel[sel >= 0]]
         assert sorted(gi[0, p][gi[0, p] >= 0].tolist()) == sorted(ref.tolist())
         ascending_then_padding(gi[0, p])
+
+
+def shaped_scores(n, kind, seed):
+    """Score rows that drive each branch of the one-CTA selection: a few huge
+    scores that stretch the key range so that the threshold bin of the first
+    pass holds thousands of keys (another pass over all keys), a narrow band of
+    distinct scores (several passes over the gathered list), and a band of
+    exact ties at the K-th value (the tie rule)."""
+    rng = np.random.default_rng(seed)
+    if kind == "stretched":
+        s = (1.0 + rng.random(n) * 1e-3).astype(np.float32)
+        s[rng.choice(n, 384, replace=False)] = 1e30
+    elif kind == "band":
+        # 384 huge scores; 600 scores on 256 consecutive floats above 1 (two or
+        # three copies each: the gathered list needs two passes, the second
+        # down to single values); the rest near 0.5
+        s = (0.5 + rng.random(n) * 1e-3).astype(np.float32)
+        pick = rng.choice(n, 984, replace=False)
+        s[pick[:384]] = 1e30
+        s[pick[384:]] = np.float32(1.0) + (np.arange(600) % 256).astype(np.float32) * np.float32(2.0 ** -23)
+    else:  # "tie_cut": 1500 above, 1000 tied, the rest below
+        s = rng.random(n).astype(np.float32)
+        order = rng.permutation(n)
+        s[order[:1500]] += 10.0
+        s[order[1500:2500]] = 5.0
+    return s
+
+
+@pytest.mark.parametrize("n,K,kind", [(16384, 2048, "plain"), (16385, 2048, "plain"), (16384, 16384, "plain"),
+                                      (16384, 1, "plain"), (16384, 2048, "stretched"), (9000, 700, "band"),
+                                      (16384, 2048, "tie_cut"), (4097, 3000, "tie_cut")])
+def test_one_cta_select_branches(n, K, kind):
+    """Rows of at most 16,384 candidates are selected by one CTA
+    (select_one_kernel), longer ones by a cluster; both equal the oracle."""
+    need_gpu()
+    cap = (n + 3) // 4 * 4
+    if kind == "plain":
+        s = scores_with_ties((1, 1, cap), n, "plain")[0, 0]
+    else:
+        s = np.zeros(cap, np.float32)
+        s[:n] = shaped_scores(n, kind, n + K)
+    cache = lengths_cache(1, cap, [n])
+    idx, _ = B.csa_topk(cache, torch.from_numpy(s.reshape(1, 1, cap)).cuda(), K)
+    got = idx.cpu().numpy()[0, 0]
+    ref = oracle.topk(s[:n], K)
+    assert got[got >= 0].tolist() == sorted(ref[ref >= 0].tolist())
+    assert (got >= 0).sum() == min(n, K)
+    ascending_then_padding(got)
