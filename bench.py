@@ -238,11 +238,36 @@ def build_state(wl, seed, device):
     app = W.append_rows(wl, seed, device=device) if wl.n_append else None
     swa = B.Swa(W.local_rows(wl, seed, device=device), wl.window) if wl.window else None
 
-    def more_layers():
+    def more_layers(arena: bool = False):
+        """Another set of layer arguments.  arena=True: every layer's q, iq and
+        w are views into one device buffer and every layer's output into
+        another, so that a step's inputs and outputs move in one copy each;
+        returns (layers, inputs buffer, outputs buffer)."""
+        inputs = [W.layer_inputs(wl, seed, li, device=device) for li in range(len(wl.layers))]
+        outs = [None] * len(wl.layers)
+        if arena:
+            def carve(tensors):
+                sizes = [(t.numel() * t.element_size() + 255) // 256 * 256 for t in tensors]
+                buf = torch.empty(sum(sizes), dtype=torch.uint8, device=device)
+                views, off = [], 0
+                for t, n in zip(tensors, sizes):
+                    nb = t.numel() * t.element_size()
+                    views.append(buf[off:off + nb].view(t.dtype).view(t.shape))
+                    off += n
+                return buf, views
+            flat = [t for inp in inputs for t in (inp["q"], inp["iq"], inp["w"])]
+            in_buf, in_views = carve(flat)
+            for v, t in zip(in_views, flat):
+                v.copy_(t)
+            inputs = [dict(q=in_views[3 * li], iq=in_views[3 * li + 1], w=in_views[3 * li + 2])
+                      for li in range(len(wl.layers))]
+            out_shape = (wl.B, wl.P, wl.H, wl.D)
+            out_buf, outs = carve([torch.empty(out_shape, dtype=torch.float32, device=device)
+                                   for _ in wl.layers])
         layers, prev, pool = [], None, None
         for li, mode in enumerate(wl.layers):
-            inp = W.layer_inputs(wl, seed, li, device=device)
-            la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"],
+            inp = inputs[li]
+            la = B.LayerArgs(cache, mode, inp["q"], wl.K, wl.scale, iq=inp["iq"], w=inp["w"], out=outs[li],
                              idx=prev if mode == W.REUSE else None,
                              rows_new=app["rows"] if (app and li == 0) else None,
                              ikeys_new=app["ikeys"] if (app and li == 0 and not wl.project) else None,
@@ -254,7 +279,7 @@ def build_state(wl, seed, device):
             if la.pool_out is not None:
                 pool = la.pool_out
             layers.append(la)
-        return layers
+        return (layers, in_buf, out_buf) if arena else layers
 
     layers = more_layers()
     base_len = cache.lengths.clone()
@@ -331,7 +356,7 @@ def bench_ours(args, wl, rank, world, local_rank):
     stages = stage_times(cache, layers, wl, flush, args.steps, stream)
     layer_ms = layer_times(cache, layers, base_len, wl, flush, args.steps, stream)
     # e2e through the public API with host buffers
-    e2e = e2e_run(cache, [layers, more_layers()], base_len, wl, args, stream, flush)
+    e2e = e2e_run(cache, [more_layers(arena=True), more_layers(arena=True)], base_len, wl, args, stream, flush)
     if B.csa_device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
     return dict(value=value, ms_per_step=ms_per_step, gbs=gbs, step_bytes=sbytes, index_bytes=ibytes, layer_ms=layer_ms,
@@ -488,34 +513,30 @@ def layer_times(cache, layers, base_len, wl, flush, steps, stream):
     return out
 
 
-def e2e_run(cache, layer_sets, base_len, wl, args, stream, flush):
+def e2e_run(cache, sets, base_len, wl, args, stream, flush):
     """Same steps through the public API with pinned host inputs and outputs:
     each step copies every layer's q/iq/w host->device, runs the layers through
     csa_layer_step and copies every layer's output device->host.
 
-    Two sets of layer arguments (device inputs and outputs) alternate between
-    steps, and the copies run on two copy streams, ordered by events: the
-    inputs of step s+1 go up while step s computes, and the outputs of step s
-    come down while step s+1 computes.  The layer calls of each set are
-    captured once as a CUDA graph (as a serving loop would run them).  The
-    time is that of the whole run, from the first input copy to the end of
-    the last output copy, over the steps.  When a step moves more bytes than
-    the L2 holds, nothing is flushed between steps (the step's own scan
-    evicts it); otherwise the L2 flush runs before each step's layer calls,
-    inside the timed run."""
+    Two sets of layer arguments alternate between steps; each set's inputs
+    are views into one device buffer and its outputs into another, so a
+    step's inputs go up in one copy and its outputs come down in one.  The
+    copies run on two copy streams, ordered by events: the inputs of step s+1
+    go up while step s computes, and the outputs of step s come down while
+    step s+1 computes.  The layer calls of each set are captured once as a
+    CUDA graph (as a serving loop would run them).  The time is that of the
+    whole run, from the first input copy to the end of the last output copy,
+    over the steps.  When a step moves more bytes than the L2 holds, nothing
+    is flushed between steps (the step's own scan evicts it); otherwise the L2
+    flush runs before each step's layer calls, inside the timed run."""
     import torch
-    h2d, d2h = 0, 0
-    hin, hout = [], []
-    for la in layer_sets[0]:
-        row = {}
-        for k in ("q", "iq", "w"):
-            t = la.tensors[k]
-            if t is not None:
-                row[k] = t.cpu().pin_memory()
-                h2d += t.numel() * t.element_size()
-        hin.append(row)
-        d2h += la.out.numel() * la.out.element_size()
-    hout = [[torch.empty(la.out.shape, dtype=la.out.dtype).pin_memory() for la in ls] for ls in layer_sets]
+    layer_sets = [st[0] for st in sets]
+    dev_in = [st[1] for st in sets]
+    dev_out = [st[2] for st in sets]
+    host_in = dev_in[0].cpu().pin_memory()  # both sets hold the same inputs
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dev_out]
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = dev_out[0].numel() * dev_out[0].element_size()
     sbytes, _ = step_bytes(wl)
     flush_between = sbytes <= L2_BYTES
 
@@ -544,9 +565,7 @@ def e2e_run(cache, layer_sets, base_len, wl, args, stream, flush):
                     up.wait_event(done[p])                 # step s-2 no longer reads these inputs
                 if s == 0 and t0 is not None:
                     t0.record(up)
-                for la, row in zip(layer_sets[p], hin):
-                    for k, h in row.items():
-                        la.tensors[k].copy_(h, non_blocking=True)
+                dev_in[p].copy_(host_in, non_blocking=True)
                 ready[p].record(up)
             stream.wait_event(ready[p])
             if s >= 2:
@@ -559,8 +578,7 @@ def e2e_run(cache, layer_sets, base_len, wl, args, stream, flush):
             done[p].record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(done[p])
-                for la, h in zip(layer_sets[p], hout[p]):
-                    h.copy_(la.out, non_blocking=True)
+                hout[p].copy_(dev_out[p], non_blocking=True)
                 drained[p].record(down)
         if t1 is not None:
             down.wait_stream(up)
@@ -575,8 +593,8 @@ def e2e_run(cache, layer_sets, base_len, wl, args, stream, flush):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "l2": ("flushed before each step's layer calls, inside the timed run" if flush_between else
                    "not flushed: a step moves more bytes than the L2 holds"),
-            "how": "pinned host->device copies of every layer's q/iq/w, the layer calls (one CUDA graph per "
-                   "buffer set), device->host copies of every layer's output; two buffer sets alternate "
+            "how": "one pinned host->device copy of every layer's q/iq/w, the layer calls (one CUDA graph per "
+                   "buffer set), one device->host copy of every layer's output; two buffer sets alternate "
                    "between steps and the copies run on two copy streams under the neighbouring steps' "
                    "layer calls; whole run from the first input copy to the last output copy, per step"}
 

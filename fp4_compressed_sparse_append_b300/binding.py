@@ -454,14 +454,16 @@ class LayerArgs:
 
     def __init__(self, cache: Cache, mode: int, q, K: int, scale: float, iq=None, w=None, idx=None,
                  rows_new=None, ikeys_new=None, pool_in=None, pool_blocks: int = 0, make_pool: bool = False,
-                 swa: Optional[Swa] = None, w_ik=None):
+                 swa: Optional[Swa] = None, w_ik=None, out=None, lse=None):
         B, P, H, D = q.shape
         _lead(q, "q", cache.batch, cache.d_latent)
         dev = cache.device
         self.tensors = dict(q=q, iq=iq, w=w, rows_new=rows_new, ikeys_new=ikeys_new, pool_in=pool_in)
         self.idx = idx if idx is not None else torch.empty((B, P, K), dtype=torch.int32, device=dev)
-        self.out = torch.empty((B, P, H, D), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((B, P, H), dtype=torch.float32, device=dev)
+        self.out = out if out is not None else torch.empty((B, P, H, D), dtype=torch.float32, device=dev)
+        self.lse = lse if lse is not None else torch.empty((B, P, H), dtype=torch.float32, device=dev)
+        _need(self.out, B * P * H * D * 4, "out")
+        _need(self.lse, B * P * H * 4, "lse")
         self.pool_out = (torch.empty((B, P, pool_blocks), dtype=torch.int32, device=dev)
                          if make_pool else None)
         HI = iq.shape[2] if iq is not None else 0
