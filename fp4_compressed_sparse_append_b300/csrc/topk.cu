@@ -23,9 +23,10 @@
 // order: per (iteration, warp) counts from warp ballots, one block scan, and
 // one exchange of per-CTA counts give every selected key its position.
 //
-// A row of at most 16,384 candidates goes to one CTA instead
+// A row of 8,193 to 16,384 candidates goes to one CTA instead
 // (select_one_kernel, with the selection of select_cta.cuh): no cluster
-// barrier, no warp votes.
+// barrier, no warp votes.  A row of at most 8,192 stays in one CTA of this
+// kernel.
 //
 // Rows longer than one cluster holds are split into segments: stage 1 keeps
 // each segment's own top K (with scores) in the workspace; stage 2 selects the
@@ -50,6 +51,7 @@ constexpr int kDigit2Bins = 256;     // key bits 7..0
 constexpr int kSelCacheMax = 16384;  // keys held per CTA at most (64 KB): two CTAs fit one SM
 constexpr int kMaxIters = kSelCacheMax / kSelThreads;
 constexpr int kMaxCluster = 16;
+constexpr int kMinChunk = 4096;      // a row of up to 2x this stays whole in one CTA (no cluster barrier)
 constexpr int kMinChunkLong = 1024;  // a longer row is not spread thinner than this per CTA
 constexpr int64_t kSegmentLen = static_cast<int64_t>(kMaxCluster) * 8192;
 
@@ -581,9 +583,10 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
     // Smallest cluster whose chunks fit shared memory, widened (down to
     // kMinChunkLong keys per CTA) while the grid is under one CTA per SM: spreading
     // a row's keys over more CTAs also spreads the contention of its shared-
-    // memory histogram, which crowded indexer scores make high.  (Rows short
-    // enough for one CTA mostly go to select_one_kernel.)
-    const int64_t min_chunk = kMinChunkLong;
+    // memory histogram, which crowded indexer scores make high.
+    // Rows of at most 2 * kMinChunk keys stay in one CTA: there the cluster
+    // barriers cost more than the spread saves.
+    const int64_t min_chunk = n_per_cluster <= 2 * kMinChunk ? kMinChunk : kMinChunkLong;
     int C = 1;
     while (C < kMaxCluster &&
            ((n_per_cluster + C - 1) / C > kSelCacheMax ||
@@ -594,12 +597,16 @@ cudaError_t launch_source(const SelArgs &args, int grid_rows, int64_t n_per_clus
     return launch_kernel(select_kernel<S>, dim3(C, grid_rows), dim3(kSelThreads), select_smem(chunk), st, C, args);
 }
 
-// Rows of at most cta_select::kMaxKeys candidates without per-candidate score
-// outputs go to one CTA each (select_one_kernel), longer ones to the clusters.
+// Rows of 2 * kMinChunk + 1 to cta_select::kMaxKeys candidates without
+// per-candidate score outputs go to one CTA each (select_one_kernel); longer
+// ones to the clusters; shorter ones to select_kernel alone in one CTA, whose
+// loops cover only the row's keys (select_one_kernel's cover 16,384 slots,
+// which measures slower for 4,096 keys and faster for 16,384).
 template <int S>
 cudaError_t launch_one_or_cluster(const SelArgs &args, int grid_rows, int64_t n_per_cluster, cudaStream_t st)
 {
-    if (n_per_cluster > cta_select::kMaxKeys || args.segments != 1 || args.out_scores)
+    if (n_per_cluster <= 2 * kMinChunk || n_per_cluster > cta_select::kMaxKeys || args.segments != 1 ||
+        args.out_scores)
         return launch_source<S>(args, grid_rows, n_per_cluster, st);
     constexpr size_t smem = cta_select::kMaxKeys * 4 + sizeof(cta_select::Scratch);
     static bool configured = false;

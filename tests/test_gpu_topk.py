@@ -114,8 +114,9 @@ def shaped_scores(n, kind, seed):
                                       (16384, 1, "plain"), (16384, 2048, "stretched"), (9000, 700, "band"),
                                       (16384, 2048, "tie_cut"), (4097, 3000, "tie_cut")])
 def test_one_cta_select_branches(n, K, kind):
-    """Rows of at most 16,384 candidates are selected by one CTA
-    (select_one_kernel), longer ones by a cluster; both equal the oracle."""
+    """Rows of 8,193 to 16,384 candidates are selected by select_one_kernel,
+    longer ones by a cluster, shorter ones by select_kernel in one CTA; all
+    equal the oracle."""
     need_gpu()
     cap = (n + 3) // 4 * 4
     if kind == "plain":
