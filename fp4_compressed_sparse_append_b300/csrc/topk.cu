@@ -100,6 +100,13 @@ struct RowView {
         if (S == kRows) return score_key(__ldg(s + i));
         if (S == kBlocks) {
             const int64_t r0 = i * kPoolBlock;
+            if (r0 + kPoolBlock <= L) {
+                // a whole block: two 16-byte loads (a row of scores starts 16-byte
+                // aligned and a block at a multiple of 8 scores)
+                const float4 a = __ldg(reinterpret_cast<const float4 *>(s + r0));
+                const float4 b = __ldg(reinterpret_cast<const float4 *>(s + r0) + 1);
+                return score_key(fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w))));
+            }
             float best = __ldg(s + r0);
 #pragma unroll
             for (int m = 1; m < kPoolBlock; ++m)
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
 
     // Pass 0: keys into shared memory and the digit-0 histogram.  Loads are
     // issued U at a time so that their latencies overlap.
-    constexpr int U = S == kBlocks ? 2 : 8;
+    constexpr int U = 8;
     for (int base = 0; base < m; base += U * kSelThreads) {
         uint32_t k[U];
 #pragma unroll
