@@ -450,10 +450,13 @@ def stage_times(cache, layers, wl, flush, steps, stream):
         make_pool = la.pool_out is not None
         if la.struct.mode != W.REUSE and fused_pool_select(wl, pool_in):
             # a Reindex layer over the pool: scores and selection in one kernel
-            idx = B.csa_pool_topk(cache, iq, w, pool_in, wl.K)
+            # (the spread form, as csa_layer_step runs it)
+            ws_pool = torch.empty(B.pool_topk_workspace_size(cache, wl.P, pool_in.shape[-1]), dtype=torch.uint8,
+                                  device=dev)
+            idx = B.csa_pool_topk(cache, iq, w, pool_in, wl.K, workspace=ws_pool)
             torch.cuda.synchronize()
             out[kind + ".pool_topk"] = dict(
-                ms=timed(lambda: B.csa_pool_topk(cache, iq, w, pool_in, wl.K, idx=idx)),
+                ms=timed(lambda: B.csa_pool_topk(cache, iq, w, pool_in, wl.K, idx=idx, workspace=ws_pool)),
                 launches=count, kind=kind, stage="pool_topk")
         elif la.struct.mode != W.REUSE:
             nblk = pool_in.shape[-1] if pool_in is not None else 0
@@ -972,7 +975,7 @@ def stage_bytes(wl, kind, stage):
 
 
 KERNELS = {"index_score": "index_score_kernel", "topk": "select_kernel (+ select_one_kernel, pool_rows_kernel)",
-           "pool_topk": "pool_select_kernel", "sparse_attend": "attend_kernel (+ attend_merge_kernel)"}
+           "pool_topk": "pool_spread_kernel", "sparse_attend": "attend_kernel (+ attend_merge_kernel)"}
 
 
 def stage_rooflines(wl, stages, peak_hbm, peak_src, peak_tf, peak_tf_src):

@@ -23,7 +23,7 @@ CSA_DEV_BAD_INDEX, CSA_DEV_CAPACITY, CSA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = (
     "csa_quantize_append", "csa_quantize_append_project", "csa_index_score", "csa_topk", "csa_topk_workspace_size",
-    "csa_pool_topk", "csa_select_pairs", "csa_topk_pairs", "csa_ids_window", "csa_lse_merge", "csa_sparse_attend",
+    "csa_pool_topk", "csa_pool_topk_workspace_size", "csa_select_pairs", "csa_topk_pairs", "csa_ids_window", "csa_lse_merge", "csa_sparse_attend",
     "csa_sparse_attend_noalloc", "csa_sparse_attend_swa", "csa_attend_swa_workspace_size",
     "csa_attend_workspace_size", "csa_layer_step", "csa_layer_workspace_size",
     "csa_device_status", "csa_kernel_launches", "csa_status_string",
@@ -80,7 +80,8 @@ def lib() -> ctypes.CDLL:
         L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
         L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, SZ, V]
         L.csa_topk_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
-        L.csa_pool_topk.argtypes = [C, I32, I32, V, V, V, I32, I32, V, V]
+        L.csa_pool_topk.argtypes = [C, I32, I32, V, V, V, I32, I32, V, V, SZ, V]
+        L.csa_pool_topk_workspace_size.argtypes = [C, I32, I32, ctypes.POINTER(SZ)]
         L.csa_select_pairs.argtypes = [C, V, I64, V, I32, I32, I32, V, V, V]
         L.csa_topk_pairs.argtypes = [I32, I32, V, V, I32, V, V]
         L.csa_ids_window.argtypes = [V, I64, I32, I32, V, V]
@@ -305,11 +306,20 @@ def csa_topk(cache: Cache, scores: torch.Tensor, K: int, pool: Optional[torch.Te
     return idx, pool_out
 
 
+def pool_topk_workspace_size(cache: Cache, P: int, pool_blocks: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().csa_pool_topk_workspace_size(cache.ref, P, pool_blocks, ctypes.byref(n)),
+           "csa_pool_topk_workspace_size")
+    return n.value
+
+
 def csa_pool_topk(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: torch.Tensor, K: int,
-                  idx: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                  idx: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
     """Reindex over a pool in one call: iq [B, P, HI, DI] uint8, w [B, P, HI]
     fp32, pool [B, P, nblk] int32 -> idx [B, P, K] int32 (the top K of the
-    pool's rows, ascending, -1 padded)."""
+    pool's rows, ascending, -1 padded).  workspace (pool_topk_workspace_size
+    bytes) selects the spread form, None the cluster form."""
     B, P, HI, _ = iq.shape
     _lead(iq, "iq", cache.batch, cache.d_index)
     nblk = pool.shape[-1]
@@ -320,7 +330,10 @@ def csa_pool_topk(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: torch.T
     if idx is None:
         idx = torch.empty((B, P, K), dtype=torch.int32, device=cache.device)
     _need(idx, Bc * P * K * 4, "idx")
-    _check(lib().csa_pool_topk(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, K, _ptr(idx),
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _check(lib().csa_pool_topk(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, K, _ptr(idx), ws_ptr, ws_bytes,
                                _stream(stream)), "csa_pool_topk")
     return idx
 

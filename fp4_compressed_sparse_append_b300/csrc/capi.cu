@@ -247,16 +247,34 @@ csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int6
 }
 
 csa_status csa_pool_topk(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
-                         const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx, csa_stream_t stream)
+                         const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx, void *workspace,
+                         size_t workspace_bytes, csa_stream_t stream)
 {
     csa_status s = check_cache(cache);
     if (s != CSA_OK) return s;
     if (P < 1 || HI < 1 || K < 1 || K > 16384 || !iq || !w || !pool || !idx || pool_blocks < 1) return CSA_ERR_INVALID_ARG;
     if (!aligned16(iq) || !aligned16(w) || !aligned16(pool) || !aligned16(idx)) return CSA_ERR_INVALID_ARG;
-    if (!csa::pool_select_supported(view(cache), P, HI, pool_blocks, K)) return CSA_ERR_UNSUPPORTED;
+    const csa::CacheView v = view(cache);
+    if (!csa::pool_select_supported(v, P, HI, pool_blocks, K)) return CSA_ERR_UNSUPPORTED;
+    if (workspace) {
+        if (!csa::pool_spread_supported(v, P, HI, pool_blocks, K)) return CSA_ERR_UNSUPPORTED;
+        if (!aligned16(workspace) || workspace_bytes < csa::pool_spread_keys_bytes(v, P, pool_blocks))
+            return CSA_ERR_WORKSPACE;
+    }
     int *st = status_word();
     if (!st) return CSA_ERR_CUDA;
-    return from_cuda(csa::launch_pool_select(view(cache), P, HI, iq, w, pool, pool_blocks, K, idx, st, stream));
+    if (!workspace) return from_cuda(csa::launch_pool_select(v, P, HI, iq, w, pool, pool_blocks, K, idx, st, stream));
+    return from_cuda(csa::launch_pool_spread(v, P, HI, iq, w, pool, pool_blocks, K, idx,
+                                             static_cast<uint32_t *>(workspace), st, stream));
+}
+
+csa_status csa_pool_topk_workspace_size(const csa_cache *cache, int32_t P, int32_t pool_blocks, size_t *bytes)
+{
+    csa_status s = check_cache(cache);
+    if (s != CSA_OK) return s;
+    if (!bytes || P < 1 || pool_blocks < 1) return CSA_ERR_INVALID_ARG;
+    *bytes = csa::pool_spread_keys_bytes(view(cache), P, pool_blocks);
+    return CSA_OK;
 }
 
 csa_status csa_select_pairs(const csa_cache *cache, const float *scores, int64_t ld, const int32_t *idx, int32_t n,
@@ -457,8 +475,12 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         const int32_t *pool = a->mode == CSA_REINDEX ? a->pool_in : nullptr;
         const int pool_blocks = pool ? a->pool_blocks : 0;
         const bool make_pool = a->mode == CSA_FULL && a->pool_out;
-        if (pool && csa::pool_select_supported(v, a->P, a->HI, pool_blocks, a->K)) {
-            // a Reindex layer over the pool: scores and selection in one kernel
+        if (pool && csa::pool_spread_supported(v, a->P, a->HI, pool_blocks, a->K)) {
+            // a Reindex layer over the pool: scores and selection in one kernel,
+            // the keys through the scores' workspace
+            e = csa::launch_pool_spread(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, a->K, a->idx,
+                                        reinterpret_cast<uint32_t *>(scores), st, stream);
+        } else if (pool && csa::pool_select_supported(v, a->P, a->HI, pool_blocks, a->K)) {
             e = csa::launch_pool_select(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, a->K, a->idx, st, stream);
         } else {
             e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);

@@ -42,6 +42,14 @@ int pool_select_supported(const CacheView &c, int P, int HI, int pool_blocks, in
 cudaError_t launch_pool_select(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
                                const int32_t *pool, int pool_blocks, int K, int32_t *idx, int *status,
                                cudaStream_t st);
+// A Reindex layer over the pool spread over one CTA per 128-row tile, the last
+// CTA of each query selecting; keys: [B*P][pool_blocks * 8] words of scratch
+// (pool_spread_keys_bytes).  Uses library-owned arrival counters.
+int pool_spread_supported(const CacheView &c, int P, int HI, int pool_blocks, int K);
+size_t pool_spread_keys_bytes(const CacheView &c, int P, int pool_blocks);
+cudaError_t launch_pool_spread(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
+                               const int32_t *pool, int pool_blocks, int K, int32_t *idx, uint32_t *keys,
+                               int *status, cudaStream_t st);
 
 // Full layer with a pool of pool_keep >= K blocks: the top K rows from the
 // pool's rows (exact, see pool_select.cu), given the scan's scores.

@@ -23,6 +23,9 @@
 //      an ascending pool) with cta_select::select_keys (select_cta.cuh) and
 //      writes the selected rows in pool order, then -1 padding.
 // Every wait is bounded; a wait that runs out raises CSA_DEV_TIMEOUT.
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "csa_internal.h"
 #include "select_cta.cuh"
@@ -255,6 +258,209 @@ __global__ void __launch_bounds__(kThreads, 1)
     write_selection(allk, allb, C * a.bpc * kPoolBlock, a.K, a.idx + static_cast<int64_t>(unit) * a.K, sc);
 }
 
+// Arrival counters of pool_spread_kernel: a library-owned array, zero when the
+// library is loaded; each launch leaves its counters at 0 again (the last
+// arrival wraps them).  Launches take consecutive ranges in turn, one counter
+// per query, so only launches kSpreadCounters queries apart in issue order
+// share a counter.  In host code this name is only a stand-in for the device
+// array: the kernel gets the device address looked up below.
+constexpr int kSpreadCounters = 1 << 16;
+static __device__ unsigned int g_spread_counters[kSpreadCounters];
+
+// The same Reindex layer spread over one CTA per 128-row tile of the pool
+// (16 blocks), with no cluster: a cluster holds at most 16 CTAs, each of which
+// must then copy 128 KB of keys at one SM's share of the L2's bandwidth.  Each
+// CTA scores its tile and stores its rows' order-preserving keys to global
+// memory (the caller's workspace); every thread fences its stores, and one
+// thread counts the CTA's arrival with atomicInc on the query's counter.  The
+// CTA that arrives last (the counter then wraps back to 0 by itself) reads
+// every key of the pool from the L2 and selects, as CTA 0 of the cluster
+// kernel does.  No CTA waits for another.
+struct SpreadArgs {
+    int P, HI, cap, DI;
+    const int32_t *lengths;
+    const int32_t *pool;        // [units][pool_blocks], ascending, -1 padded
+    int pool_blocks;
+    const float *w;             // [units][HI]
+    int K;
+    int32_t *idx;               // [units][K]
+    uint32_t *keys;             // [units][pool_blocks * 8] (workspace)
+    unsigned int *counters;     // [units] arrival counters, 0 between launches
+    int *status;
+};
+
+struct SpreadSmem {
+    uint64_t tbar, mbar, qbar, done;
+    float w[64];
+    int32_t blk[16];
+    uint32_t tmem_slot;
+    int abort;
+    int last;
+};
+
+constexpr int kSpreadBlocks = kTileRows / kPoolBlock;  // 16 pool blocks per CTA
+constexpr size_t kSpreadSmemBytes = (sizeof(SpreadSmem) + 1023) & ~size_t(1023);  // keeps the keys 1024-aligned
+
+template <int HT>
+__global__ void __launch_bounds__(kThreads, 1)
+    pool_spread_kernel(const __grid_constant__ CUtensorMap keys8, const __grid_constant__ CUtensorMap qmap,
+                       SpreadArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    const int DI = a.DI;
+    uint8_t *k_s = base;                                       // [128 rows][DI] key tile
+    uint8_t *q_s = k_s + kTileRows * DI;                       // [HT rows][DI] indexer query
+    // the barriers first (8-byte aligned at a 1024-byte offset), then the last
+    // CTA's keys, block ids and selection scratch
+    SpreadSmem &sm = *reinterpret_cast<SpreadSmem *>(q_s + ((HT * DI + 1023) & ~1023));
+    uint32_t *allk = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(&sm) + kSpreadSmemBytes);
+    int32_t *allb = reinterpret_cast<int32_t *>(allk + kMaxCand);                    // last CTA: [blocks]
+    cta_select::Scratch &sc = *reinterpret_cast<cta_select::Scratch *>(allb + kMaxCluster * kBlocksPerCta);
+    volatile int *abort_flag = &sm.abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.y, cta = blockIdx.x, ctas = gridDim.x;
+    const int n = a.pool_blocks * kPoolBlock;
+    constexpr uint32_t kCols = HT < 32 ? 32 : HT;
+
+    if (tid == 0) {
+        mbar_init(&sm.tbar, kSpreadBlocks);
+        mbar_init(&sm.mbar, 1);
+        mbar_init(&sm.qbar, 1);
+        mbar_init(&sm.done, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&keys8);
+        prefetch_tensormap(&qmap);
+    }
+    if (warp == 4) {
+        tmem_alloc(&sm.tmem_slot, kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_slot;
+
+    // Below: reads of what earlier work on the stream wrote.
+    pdl_wait();
+    pdl_trigger();
+    const int b = unit / a.P, p = unit % a.P;
+    const int Lp = min(a.lengths[b], a.cap) - a.P + 1 + p;
+    const int cap_blocks = (a.cap + kPoolBlock - 1) / kPoolBlock;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(HT * DI));
+        tma_load_2d(q_s, &qmap, &sm.qbar, 0, unit * a.HI);
+    }
+    if (tid < HT) sm.w[tid] = tid < a.HI ? a.w[static_cast<int64_t>(unit) * a.HI + tid] : 0.f;
+    if (tid < kSpreadBlocks) {
+        // one pool block per thread: its id, and the copy of its 8 key rows
+        const int j = cta * kSpreadBlocks + tid;
+        int32_t blk = j < a.pool_blocks ? a.pool[static_cast<int64_t>(unit) * a.pool_blocks + j] : -1;
+        if (blk >= cap_blocks) blk = -1;
+        sm.blk[tid] = blk;
+        if (blk >= 0) {
+            mbar_arrive_expect_tx(&sm.tbar, static_cast<uint32_t>(kPoolBlock * DI));
+            tma_load_2d(k_s + tid * kPoolBlock * DI, &keys8, &sm.tbar, 0, b * a.cap + blk * kPoolBlock);
+        } else {
+            mbar_arrive(&sm.tbar);
+        }
+    }
+    __syncthreads();  // block ids and weights in shared memory
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sw = swizzle_mode(DI), sbo = 8 * DI;
+            const uint64_t da = smem_desc(smem_u32(k_s), 16, sbo, sw);
+            const uint64_t db = smem_desc(smem_u32(q_s), 16, sbo, sw);
+            const uint32_t idesc = instr_desc(128, HT, 0, 0, 0, 0);
+            if (mbar_wait<true>(&sm.qbar, 0, abort_flag) && mbar_wait<true>(&sm.tbar, 0, abort_flag)) {
+                tc_fence_after();
+                for (int k = 0; k < DI / 32; ++k) mma_f8f6f4(tmem, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
+                mma_commit(&sm.mbar);
+            }
+            // Before tensor memory is released: every issued MMA has completed
+            // and every key copy has landed.
+            mma_commit(&sm.done);
+            unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(&sm.done, 0) && global_ns() - t0 < kWaitLimitNs) {
+            }
+            t0 = global_ns();
+            while (!mbar_try_wait(&sm.tbar, 0) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ scores
+        const int row = warp * 32 + lane;  // row within the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int cand = cta * kTileRows + row;
+        if (mbar_wait<true>(&sm.mbar, 0, abort_flag)) {
+            tc_fence_after();
+            constexpr int HC = HT < 32 ? HT : 32;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < HT; c0 += HC) {
+                uint32_t r[HC];
+#pragma unroll
+                for (int c = 0; c < HC; c += 16)
+                    tmem_ld16(tmem + lane_off + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(&r[c]));
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < HC; h += 4) {
+                    s0 = fmaf(sm.w[c0 + h], fmaxf(__uint_as_float(r[h]), 0.f), s0);
+                    s1 = fmaf(sm.w[c0 + h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
+                    s2 = fmaf(sm.w[c0 + h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
+                    s3 = fmaf(sm.w[c0 + h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+                }
+            }
+            const float sc_row = (s0 + s1) + (s2 + s3);
+            if (cand < n) {
+                const int32_t blk = sm.blk[row >> 3];
+                const bool valid = blk >= 0 && blk * kPoolBlock + (row & 7) < Lp;
+                a.keys[static_cast<int64_t>(unit) * n + cand] = valid ? score_key(sc_row) : 0u;
+            }
+        } else if (cand < n) {
+            a.keys[static_cast<int64_t>(unit) * n + cand] = 0u;  // timed out: no candidate
+        }
+        __threadfence();  // this thread's key, before the CTA's arrival is counted
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kCols);
+    }
+    if (tid == 0) {
+        // Every CTA arrives exactly once; the last arrival wraps the counter to 0.
+        const unsigned int old = atomicInc(a.counters + unit, static_cast<unsigned int>(ctas - 1));
+        sm.last = old == static_cast<unsigned int>(ctas - 1);
+        if (*abort_flag) raise_status(a.status, CSA_DEV_TIMEOUT);
+    }
+    __syncthreads();
+    if (!sm.last) return;
+
+    // ---- the last CTA of this query: every key and block id of its pool
+    __threadfence();  // the other CTAs' keys, counted before this arrival
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.keys + static_cast<int64_t>(unit) * n);
+    const int nq = n / 4;
+#pragma unroll
+    for (int u = 0; u < kMaxCand / 4 / kThreads; ++u) {
+        const int q = u * kThreads + tid;
+        if (q < nq) *reinterpret_cast<uint4 *>(allk + cta_select::key_slot(4 * q)) = __ldcg(src + q);
+    }
+    for (int j = tid; j < a.pool_blocks; j += kThreads) {
+        int32_t blk = a.pool[static_cast<int64_t>(unit) * a.pool_blocks + j];
+        allb[j] = blk >= cap_blocks ? -1 : blk;
+    }
+    __syncthreads();
+    write_selection(allk, allb, n, a.K, a.idx + static_cast<int64_t>(unit) * a.K, sc);
+}
+
 // A Full layer that also keeps a pool of at least K blocks selects its top K
 // rows among the pool's rows, from the scores the scan wrote.  This is exact:
 // a block outside the pool has at least pool_keep >= K blocks ranked above it
@@ -342,6 +548,13 @@ size_t pool_smem_bytes(int DI, int HT)
 {
     return 1024 + static_cast<size_t>(kMaxTiles) * kTileRows * DI + ((static_cast<size_t>(HT) * DI + 1023) & ~size_t(1023)) +
            static_cast<size_t>(kMaxCand) * 4 + kMaxCluster * kBlocksPerCta * 4 + sizeof(PoolSmem);
+}
+
+size_t spread_smem_bytes(int DI, int HT)
+{
+    return 1024 + static_cast<size_t>(kTileRows) * DI + ((static_cast<size_t>(HT) * DI + 1023) & ~size_t(1023)) +
+           kSpreadSmemBytes + static_cast<size_t>(kMaxCand) * 4 + kMaxCluster * kBlocksPerCta * 4 +
+           sizeof(cta_select::Scratch);
 }
 
 int heads_tile(int HI) { return HI <= 16 ? 16 : (HI <= 32 ? 32 : 64); }
@@ -439,6 +652,99 @@ cudaError_t launch_pool_select(const CacheView &c, int P, int HI, const uint8_t 
     if (HT == 16) return launch_kernel(pool_select_kernel<16>, dim3(C, units), dim3(kThreads), smem, st, cl, k8, qm, a);
     if (HT == 32) return launch_kernel(pool_select_kernel<32>, dim3(C, units), dim3(kThreads), smem, st, cl, k8, qm, a);
     return launch_kernel(pool_select_kernel<64>, dim3(C, units), dim3(kThreads), smem, st, cl, k8, qm, a);
+}
+
+int pool_spread_supported(const CacheView &c, int P, int HI, int pool_blocks, int K)
+{
+    return pool_select_supported(c, P, HI, pool_blocks, K) && c.B * P <= kSpreadCounters &&
+           c.B * P <= 65535;
+}
+
+size_t pool_spread_keys_bytes(const CacheView &c, int P, int pool_blocks)
+{
+    return static_cast<size_t>(c.B) * P * pool_blocks * kPoolBlock * sizeof(uint32_t);
+}
+
+namespace {
+
+constexpr int kMaxDevicesSpread = 64;
+unsigned int *g_counters_ptr[kMaxDevicesSpread];
+std::mutex g_counters_mu;
+std::atomic<uint32_t> g_counter_next{0};
+
+// Device address of the counters on the current device (looked up once per
+// device, with that device current), and the first of `units` consecutive
+// counters for this launch.
+unsigned int *spread_counters(int units)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesSpread) return nullptr;
+    unsigned int *base;
+    {
+        std::lock_guard<std::mutex> lk(g_counters_mu);
+        if (!g_counters_ptr[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_spread_counters) != cudaSuccess) return nullptr;
+            g_counters_ptr[dev] = static_cast<unsigned int *>(p);
+        }
+        base = g_counters_ptr[dev];
+    }
+    uint32_t first = g_counter_next.fetch_add(static_cast<uint32_t>(units)) % kSpreadCounters;
+    if (first + units > static_cast<uint32_t>(kSpreadCounters)) first = 0;
+    return base + first;
+}
+
+template <int HT>
+cudaError_t configure_spread()
+{
+    static bool done = false;
+    if (done) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(pool_spread_kernel<HT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(spread_smem_bytes(128, HT)));
+    done = e == cudaSuccess;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_pool_spread(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
+                               const int32_t *pool, int pool_blocks, int K, int32_t *idx, uint32_t *keys,
+                               int *status, cudaStream_t st)
+{
+    if (!pool_spread_supported(c, P, HI, pool_blocks, K) || !keys) return cudaErrorInvalidValue;
+    const int units = c.B * P;
+    unsigned int *counters = spread_counters(units);
+    if (!counters) return cudaErrorInvalidValue;
+    const int HT = heads_tile(HI);
+    SpreadArgs a{};
+    a.P = P;
+    a.HI = HI;
+    a.cap = c.cap;
+    a.DI = c.DI;
+    a.lengths = c.lengths;
+    a.pool = pool;
+    a.pool_blocks = pool_blocks;
+    a.w = w;
+    a.K = K;
+    a.idx = idx;
+    a.keys = keys;
+    a.counters = counters;
+    a.status = status;
+    cudaError_t e = HT == 16 ? configure_spread<16>() : (HT == 32 ? configure_spread<32>() : configure_spread<64>());
+    if (e != cudaSuccess) return e;
+    const CUtensorMapSwizzle sw = c.DI == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : c.DI == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUtensorMap k8, qm;
+    if (encode_tensor_map_2d_u8(&k8, c.ikeys, c.DI, static_cast<uint64_t>(c.B) * c.cap, c.DI, kPoolBlock, sw) !=
+            CUDA_SUCCESS ||
+        encode_tensor_map_2d_u8(&qm, iq, c.DI, static_cast<uint64_t>(units) * HI, c.DI, HT, sw) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const size_t smem = spread_smem_bytes(c.DI, HT);
+    const dim3 grid((pool_blocks + kSpreadBlocks - 1) / kSpreadBlocks, units);
+    if (HT == 16) return launch_kernel(pool_spread_kernel<16>, grid, dim3(kThreads), smem, st, 0, k8, qm, a);
+    if (HT == 32) return launch_kernel(pool_spread_kernel<32>, grid, dim3(kThreads), smem, st, 0, k8, qm, a);
+    return launch_kernel(pool_spread_kernel<64>, grid, dim3(kThreads), smem, st, 0, k8, qm, a);
 }
 
 }  // namespace csa

@@ -43,7 +43,7 @@ constexpr int kRankMax = 32;                     // list length ranked exactly b
 constexpr int kWarps = kThreads / 32;
 static_assert(kListMax == 2 * kThreads, "list passes give each thread two entries");
 
-struct Scratch {
+struct alignas(16) Scratch {
     uint32_t hist[kBins];
     uint32_t lk[kListMax];  // gathered keys, in candidate order
     int32_t lc[kListMax];   // and their candidates
@@ -51,6 +51,8 @@ struct Scratch {
     uint32_t res_bin, res_above;
     uint32_t thr_gt, thr_eq, need;
 };
+// Whatever a kernel places after the scratch starts 16-byte aligned.
+static_assert(sizeof(Scratch) % 16 == 0, "the scratch's size keeps what follows it aligned");
 
 // Shared-memory index of candidate c's key.
 __device__ __forceinline__ int key_slot(int c) { return c ^ (((c >> 5) & 7) << 2); }

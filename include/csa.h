@@ -257,15 +257,28 @@ CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scor
  *   idx            : [batch][P][K] ids of the K best-scoring pool rows among
  *                    rows < L_p (ties: the earlier pool slot), ascending, then
  *                    -1 padding
+ *   workspace      : NULL, or csa_pool_topk_workspace_size bytes of device
+ *                    scratch (16-byte aligned)
  * The same result as csa_index_score + csa_topk (up to the fp32 summation
- * order of the scores), in one launch and without a scores buffer.
+ * order of the scores), in one launch.  Without a workspace, one cluster of up
+ * to 16 CTAs scores the pool and selects on chip.  With one, one CTA per 128
+ * pool rows scores its rows into the workspace and the last CTA of each query
+ * to finish selects (faster: the key copies spread over more SMs); its
+ * arrival counters come from a library-owned array of 65,536, taken in turn,
+ * so calls whose counters coincide (65,536 query units of such calls apart in
+ * issue order) must not run at the same time.  csa_layer_step takes the
+ * workspace form for Reindex layers over a pool.
  * Supported: E4M3 keys, HI <= 64, pool_blocks <= 2048, K <= 16384; otherwise
- * CSA_ERR_UNSUPPORTED (use the two calls instead).  csa_layer_step takes this
- * path for Reindex layers over a pool whenever it is supported.
+ * CSA_ERR_UNSUPPORTED (use the two calls instead).
  */
 CSA_API csa_status csa_pool_topk(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
-                                 const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx,
-                                 csa_stream_t stream);
+                                 const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx, void *workspace,
+                                 size_t workspace_bytes, csa_stream_t stream);
+
+/* Workspace query of csa_pool_topk's spread form.  No counterpart on the
+ * pages: B * P * pool_blocks * 8 four-byte keys. */
+CSA_API csa_status csa_pool_topk_workspace_size(const csa_cache *cache, int32_t P, int32_t pool_blocks,
+                                                size_t *bytes);
 
 /* Workspace query of csa_topk.  No counterpart on the pages: the library
  * allocates nothing, so the caller supplies the scratch of the two-stage

@@ -109,6 +109,14 @@ def test_argument_checks_of_each_call(lib):
     assert n.value > 0
     assert lib.csa_sparse_attend_swa(c, 1, 16, V(0x1000), 1.0, V(0x2000), 2048, ctypes.byref(win), V(0x3000), None,
                                      None, 0, None) == 5
+    # the spread form of the pool's one-call top-K: its keys need pool_blocks * 8
+    # words per query; a shorter workspace is refused before any launch
+    c128 = ctypes.byref(fake_cache(d_index=128))
+    assert lib.csa_pool_topk_workspace_size(c128, 1, 300, ctypes.byref(n)) == 0 and n.value == 2 * 300 * 8 * 4
+    assert lib.csa_pool_topk(c128, 1, 64, V(0x1000), V(0x2000), V(0x3000), 300, 700, V(0x4000), V(0x5000),
+                             n.value - 16, None) == 5
+    assert lib.csa_pool_topk(c128, 1, 64, V(0x1000), V(0x2000), V(0x3000), 300, 700, V(0x4000), V(0x5008),
+                             n.value, None) == 5
 
 
 def test_layer_args_checks(lib):

@@ -1,6 +1,7 @@
 """a4 on the GPU: a Reindex layer over the hierarchical pool in one call
-(csa_pool_topk, the path csa_layer_step takes for it), against the oracle's
-scoring of the pool's rows and its top-K.
+(csa_pool_topk, in both forms: one cluster that selects on chip, and one CTA
+per 128 rows whose last CTA selects, the form csa_layer_step takes), against
+the oracle's scoring of the pool's rows and its top-K.
 
 The GPU scores in fp32 and the oracle in double, so the selected sets must be
 equal except for members whose oracle score is within 1e-5 relative of the
@@ -31,6 +32,7 @@ def make_pool(rng, P, nblk, cap_blocks, n_valid):
     return pool
 
 
+@pytest.mark.parametrize("form", ["cluster", "spread"])
 @pytest.mark.parametrize("HI,DI,nblk,n_valid,K,P,L", [
     (64, 128, 2048, 2048, 2048, 1, 1048576 // 16),
     (64, 128, 2048, 1900, 2048, 2, 40000),
@@ -39,7 +41,7 @@ def make_pool(rng, P, nblk, cap_blocks, n_valid):
     (48, 128, 512, 500, 4000, 3, 9000),
     (64, 64, 1000, 1000, 1, 1, 30000),
 ])
-def test_pool_topk_matches_oracle(HI, DI, nblk, n_valid, K, P, L):
+def test_pool_topk_matches_oracle(HI, DI, nblk, n_valid, K, P, L, form):
     need_gpu()
     seed = 61
     rng = np.random.default_rng(seed)
@@ -57,7 +59,10 @@ def test_pool_topk_matches_oracle(HI, DI, nblk, n_valid, K, P, L):
     pool = np.stack([make_pool(rng, P, nblk, cap_blocks, n_valid) for _ in range(wl.B)])
     pool[0, 0, 3] = -1 if n_valid > 3 else pool[0, 0, 3]      # a hole inside the pool
     pool_t = torch.tensor(pool, dtype=torch.int32, device="cuda")
-    idx = B.csa_pool_topk(cache, inp["iq"], inp["w"], pool_t, K)
+    ws = None
+    if form == "spread":
+        ws = torch.empty(B.pool_topk_workspace_size(cache, P, nblk), dtype=torch.uint8, device="cuda")
+    idx = B.csa_pool_topk(cache, inp["iq"], inp["w"], pool_t, K, workspace=ws)
     torch.cuda.synchronize()
     assert B.csa_device_status() == 0
     gi = idx.cpu().numpy()
@@ -76,8 +81,10 @@ def test_pool_topk_matches_oracle(HI, DI, nblk, n_valid, K, P, L):
 
 
 def test_pool_topk_agrees_with_two_calls():
-    """The fused call and csa_index_score + csa_topk over the same pool select
-    the same rows (their fp32 scores differ only in summation order)."""
+    """Both forms of the fused call and csa_index_score + csa_topk over the
+    same pool select the same rows (their fp32 scores differ only in summation
+    order); the two fused forms score identically, so they select identically,
+    and calling the spread form again (its counters back at 0) repeats it."""
     need_gpu()
     wl = W.Workload("pool2", B=1, L=100000, H=16, D=128, HI=64, DI=128, K=2048)
     cache = B.Cache(wl.B, wl.capacity, wl.D, wl.DI)
@@ -88,6 +95,8 @@ def test_pool_topk_agrees_with_two_calls():
     rng = np.random.default_rng(7)
     pool = torch.tensor(make_pool(rng, 1, 2048, (wl.L + 7) // 8, 2048)[None], dtype=torch.int32, device="cuda")
     fused = B.csa_pool_topk(cache, inp["iq"], inp["w"], pool, wl.K)
+    ws = torch.empty(B.pool_topk_workspace_size(cache, 1, 2048), dtype=torch.uint8, device="cuda")
+    spread = [B.csa_pool_topk(cache, inp["iq"], inp["w"], pool, wl.K, workspace=ws) for _ in range(3)]
     scores = B.csa_index_score(cache, inp["iq"], inp["w"], pool=pool)
     two, _ = B.csa_topk(cache, scores, wl.K, pool=pool)
     torch.cuda.synchronize()
@@ -96,3 +105,6 @@ def test_pool_topk_agrees_with_two_calls():
     by_row = dict(zip(rows.tolist(), s.tolist()))
     check_topk(fused[0, 0].cpu().numpy(), two[0, 0].cpu().numpy(),
                lambda r: np.array([by_row[int(x)] for x in r], np.float32), wl.K)
+    for sp in spread:
+        assert torch.equal(sp, fused)
+    assert B.csa_device_status() == 0
