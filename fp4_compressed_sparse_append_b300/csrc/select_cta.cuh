@@ -48,6 +48,7 @@ struct alignas(16) Scratch {
     uint32_t lk[kListMax];  // gathered keys, in candidate order
     int32_t lc[kListMax];   // and their candidates
     uint32_t wa[kWarps], wb[kWarps], wc[kWarps];
+    uint32_t scan_buf[2][kWarps];  // per-warp sums of block_scan, used in turn
     uint32_t res_bin, res_above;
     uint32_t thr_gt, thr_eq, need;
 };
@@ -57,10 +58,12 @@ static_assert(sizeof(Scratch) % 16 == 0, "the scratch's size keeps what follows 
 // Shared-memory index of candidate c's key.
 __device__ __forceinline__ int key_slot(int c) { return c ^ (((c >> 5) & 7) << 2); }
 
-// Exclusive block scan of one value per thread (all kThreads threads); *total
-// gets the sum.  Its first CTA barrier orders it after the previous scan's
-// reads of the per-warp sums; its second makes them visible.
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, Scratch &sc, uint32_t *total)
+// Exclusive block scan of one value per thread (all kThreads threads, in the
+// same sequence of calls); *total gets the sum.  One CTA barrier: the per-warp
+// sums alternate between two buffers (sb, the caller's index, flips), and a
+// thread passes scan k+1's barrier only after its reads of scan k's buffer, so
+// scan k+2 may rewrite it.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, Scratch &sc, uint32_t *total, int &sb)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
@@ -69,13 +72,14 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, Scratch &sc, uint32_t
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
         if (lane >= o) x += y;
     }
-    __syncthreads();
-    if (lane == 31) sc.wa[warp] = x;
+    uint32_t *buf = sc.scan_buf[sb];
+    sb ^= 1;
+    if (lane == 31) buf[warp] = x;
     __syncthreads();
     uint32_t before = 0, t = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) {
-        const uint32_t w = sc.wa[i];
+        const uint32_t w = buf[i];
         before += i < warp ? w : 0u;
         t += w;
     }
@@ -98,7 +102,7 @@ __device__ __forceinline__ void zero_bins(Scratch &sc, int nb)
 // above).  Thread t sums bins [nb - (t+1)*per, nb - t*per), read in an order
 // rotated by t so that a warp's lanes hit different banks.  Sets *bin and
 // *above (the count in the bins above it), the same in every thread.
-__device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uint32_t *bin, uint32_t *above)
+__device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uint32_t *bin, uint32_t *above, int &sb)
 {
     const int tid = threadIdx.x;
     const int per = nb >= kThreads ? nb / kThreads : 1;
@@ -107,7 +111,7 @@ __device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uin
     if (blo >= 0)
         for (int j = 0; j < per; ++j) ssum += sc.hist[blo + ((j + tid) & (per - 1))];
     uint32_t tot;
-    const uint32_t excl = block_scan(ssum, sc, &tot);
+    const uint32_t excl = block_scan(ssum, sc, &tot, sb);
     if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
         uint32_t cum = excl;
         for (int bb = bhi - 1; bb >= blo; --bb) {
@@ -129,8 +133,9 @@ __device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uin
 // keys[key_slot(c)].  Writes the kept candidates' indices in ascending order
 // to obuf[0, kept) and returns kept = min(K, number of non-zero keys).  obuf
 // may be the key array itself (every key is in registers before the first
-// write).  Called by all kThreads threads; ends with a CTA barrier (obuf is
-// then complete).
+// write).  Called by all kThreads threads, after a CTA barrier that follows
+// the keys' stores (and any earlier use of the scratch); ends with a CTA
+// barrier (obuf is then complete).
 __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t K, int32_t *obuf, Scratch &sc)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -158,12 +163,12 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
     kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
     kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
     cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
-    __syncthreads();  // the caller's last use of the scratch words is over
     if (lane == 0) {
         sc.wa[warp] = kmin;
         sc.wb[warp] = kmax;
         sc.wc[warp] = cnt;
     }
+    zero_bins(sc, kBins);  // the first pass's bins, ordered before it by the barrier below
     __syncthreads();
     kmin = 0xFFFFFFFFu;
     kmax = 0;
@@ -177,6 +182,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
 
     // The rule: keep keys > thr_gt, and the first `need` keys == thr_eq.
     uint32_t thr_gt = 0, thr_eq = 0, need = 0;
+    int sb = 0;  // block_scan's buffer
     if (total > K) {
         // v = key - kmin; the bits of v above `hi` are fixed to `prefix`, and
         // `above` keys lie above them (all of them kept).
@@ -194,9 +200,11 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                 break;
             }
             const int d = hi < kBinBits ? hi : kBinBits, lo = hi - d, nb = 1 << d;
-            if (passes++) __syncthreads();  // every thread has read the last pass's bins
-            zero_bins(sc, nb);
-            __syncthreads();
+            if (passes++) {
+                __syncthreads();  // every thread has read the last pass's bins
+                zero_bins(sc, nb);
+                __syncthreads();
+            }
             const uint32_t mask = hi >= 32 ? 0u : (0xFFFFFFFFu << hi);
             const uint32_t pfx = hi >= 32 ? 0u : (prefix << hi);
 #pragma unroll
@@ -206,7 +214,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             }
             __syncthreads();
             uint32_t bin, ab;
-            find_bin(nb, K - above, sc, &bin, &ab);
+            find_bin(nb, K - above, sc, &bin, &ab, sb);
             above += ab;
             const uint32_t in_bin = sc.hist[bin];
             const uint32_t P = (prefix << d) | bin;
@@ -233,7 +241,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             for (int j = 0; j < kPerThread; ++j)
                 mine += (kk[j] && ((kk[j] - kmin) >> hi) == prefix) ? 1u : 0u;
             uint32_t m;
-            uint32_t off = block_scan(mine, sc, &m);
+            uint32_t off = block_scan(mine, sc, &m, sb);
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j)
                 if (kk[j] && ((kk[j] - kmin) >> hi) == prefix) {
@@ -263,7 +271,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                 if (h1) atomicAdd(&sc.hist[b1], 1u);
                 __syncthreads();
                 uint32_t bin, ab;
-                find_bin(nb, nd, sc, &bin, &ab);
+                find_bin(nb, nd, sc, &bin, &ab, sb);
                 nd -= ab;
                 const uint32_t in_bin = sc.hist[bin];
                 const uint32_t P = (prefix << d) | bin;
@@ -282,7 +290,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                 // keep the bin's entries, in order (each thread's entries were
                 // read before the scan's first barrier)
                 const bool k0 = h0 && b0 == bin, k1 = h1 && b1 == bin;
-                uint32_t o = block_scan((k0 ? 1u : 0u) + (k1 ? 1u : 0u), sc, &m);
+                uint32_t o = block_scan((k0 ? 1u : 0u) + (k1 ? 1u : 0u), sc, &m, sb);
                 if (k0) {
                     sc.lk[o] = e0;
                     sc.lc[o] = ec0;
@@ -338,7 +346,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
     }
     uint32_t tot2;
     const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(sel)) << 16) | static_cast<uint32_t>(__popc(tie)), sc,
-                                   &tot2);
+                                   &tot2, sb);
     const uint32_t a_before = ex >> 16, t_before = ex & 0xFFFFu;
     if (need) {
         // the first `need` ties in candidate order are kept
