@@ -249,6 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
     // Below: reads of what earlier kernels on the stream wrote (lengths, indices, cache).
     pdl_wait();
+    // A gather thread's row id in the first tile of a selection split, loaded
+    // beside the sequence length (the two loads are independent).
+    int32_t first_id = -1;
+    {
+        const int j0 = (split * a.tiles_per_split) * kRows + ((tid - 32 * kSoftWarps) & (kRows - 1));
+        if (!win && warp >= kSoftWarps && warp < mma_warp && split * a.tiles_per_split < a.tiles_total && j0 < a.K)
+            first_id = irow[j0];
+    }
     len = min(a.c.lengths[b], a.c.cap);
     // The window split's rows: [w_lo, w_hi) of the sequence's local rows, the
     // window of tokens that ends at this position's own row (L - P + p for a
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             return;
         }
         const int j = tile * kRows + gr;
-        int32_t row = j < a.K ? irow[j] : -1;
+        int32_t row = tile == t_first ? first_id : (j < a.K ? irow[j] : -1);
         if (row >= len) {
             if (gp == 0) raise_status(a.status, CSA_DEV_BAD_INDEX);
             row = -1;

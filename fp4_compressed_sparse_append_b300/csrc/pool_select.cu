@@ -348,8 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     pdl_trigger();
     const int b = unit / a.P, p = unit % a.P;
-    const int Lp = min(a.lengths[b], a.cap) - a.P + 1 + p;
     const int cap_blocks = (a.cap + kPoolBlock - 1) / kPoolBlock;
+    // the block ids first: the key copies wait on them, the length only on the epilogue
+    const int jb = cta * kSpreadBlocks + tid;
+    int32_t blk = (tid < kSpreadBlocks && jb < a.pool_blocks) ? a.pool[static_cast<int64_t>(unit) * a.pool_blocks + jb] : -1;
+    const int Lp = min(a.lengths[b], a.cap) - a.P + 1 + p;
     if (tid == 0) {
         mbar_arrive_expect_tx(&sm.qbar, static_cast<uint32_t>(HT * DI));
         tma_load_2d(q_s, &qmap, &sm.qbar, 0, unit * a.HI);
@@ -357,8 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < HT) sm.w[tid] = tid < a.HI ? a.w[static_cast<int64_t>(unit) * a.HI + tid] : 0.f;
     if (tid < kSpreadBlocks) {
         // one pool block per thread: its id, and the copy of its 8 key rows
-        const int j = cta * kSpreadBlocks + tid;
-        int32_t blk = j < a.pool_blocks ? a.pool[static_cast<int64_t>(unit) * a.pool_blocks + j] : -1;
         if (blk >= cap_blocks) blk = -1;
         sm.blk[tid] = blk;
         if (blk >= 0) {
