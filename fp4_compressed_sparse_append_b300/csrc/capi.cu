@@ -395,6 +395,14 @@ static size_t layer_scores_ld(const csa_cache *cache, const csa_layer_args *a)
     return round_up(static_cast<size_t>(cache->capacity), 4);
 }
 
+// A Full layer that builds the pool: the scan also writes each 8-row block's
+// best visible score, [B*P][ld] with ld = ceil(capacity / 8) rounded up to 4.
+static size_t layer_bmax_ld(const csa_cache *cache, const csa_layer_args *a)
+{
+    if (a->mode != CSA_FULL || !a->pool_out) return 0;
+    return round_up((static_cast<size_t>(cache->capacity) + CSA_POOL_BLOCK - 1) / CSA_POOL_BLOCK, 4);
+}
+
 static csa_status check_layer(const csa_cache *cache, const csa_layer_args *a)
 {
     csa_status s = check_cache(cache);
@@ -442,6 +450,7 @@ csa_status csa_layer_workspace_size(const csa_cache *cache, const csa_layer_args
     if (a->mode != CSA_REUSE) {
         total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_scores_ld(cache, a) * sizeof(float), 256);
         total += round_up(layer_select_ws(cache, a), 256);
+        total += round_up(static_cast<size_t>(cache->batch) * a->P * layer_bmax_ld(cache, a) * sizeof(float), 256);
     }
     const csa::SwaView sv = a->swa ? swa_view(a->swa) : csa::SwaView{};
     total += round_up(csa::attend_workspace_bytes(v, a->P, a->H, a->K, a->swa ? &sv : nullptr), 256);
@@ -468,6 +477,9 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         void *sel_ws = ws;
         const size_t sel_bytes = layer_select_ws(cache, a);
         ws += round_up(sel_bytes, 256);
+        const int64_t ldb = static_cast<int64_t>(layer_bmax_ld(cache, a));
+        float *bmax = ldb ? reinterpret_cast<float *>(ws) : nullptr;
+        ws += round_up(static_cast<size_t>(cache->batch) * a->P * ldb * sizeof(float), 256);
         if (a->n_new > 0) {
             e = csa::launch_quantize_append(v, a->rows_new, a->ikeys_new, a->n_new, st, stream, a->w_ik);
             if (e != cudaSuccess) return CSA_ERR_CUDA;
@@ -483,12 +495,14 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
         } else if (pool && csa::pool_select_supported(v, a->P, a->HI, pool_blocks, a->K)) {
             e = csa::launch_pool_select(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, a->K, a->idx, st, stream);
         } else {
-            e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream);
+            e = csa::launch_index_score(v, a->P, a->HI, a->iq, a->w, pool, pool_blocks, scores, ld, st, stream, bmax,
+                                        ldb);
             if (make_pool && csa::pool_rows_supported(a->pool_blocks, a->K)) {
-                // the pool first; the top K rows then lie in the pool's blocks
+                // the pool first (from the blocks' best scores the scan wrote); the
+                // top K rows then lie in the pool's blocks
                 if (e == cudaSuccess)
-                    e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks,
-                                           a->pool_out, sel_ws, sel_bytes, stream);
+                    e = csa::launch_select(v, a->P, bmax, ldb, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks,
+                                           a->pool_out, sel_ws, sel_bytes, stream, true);
                 if (e == cudaSuccess)
                     e = csa::launch_pool_rows(v, a->P, scores, ld, a->pool_out, a->pool_blocks, a->K, a->idx, stream);
             } else {
@@ -496,8 +510,8 @@ csa_status csa_layer_step(const csa_cache *cache, const csa_layer_args *a, csa_s
                     e = csa::launch_select(v, a->P, scores, ld, pool, pool_blocks, 1, a->K, a->idx, sel_ws, sel_bytes,
                                            stream);
                 if (e == cudaSuccess && make_pool)
-                    e = csa::launch_select(v, a->P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks,
-                                           a->pool_out, sel_ws, sel_bytes, stream);
+                    e = csa::launch_select(v, a->P, bmax, ldb, nullptr, 0, CSA_POOL_BLOCK, a->pool_blocks,
+                                           a->pool_out, sel_ws, sel_bytes, stream, true);
             }
         }
         if (e != cudaSuccess) return CSA_ERR_CUDA;

@@ -25,16 +25,20 @@ cudaError_t launch_quantize_append(const CacheView &c, const uint16_t *rows, con
                                    int *status, cudaStream_t st, const uint16_t *w_ik = nullptr);
 
 // a2/a4
+// bmax (full scan only, or null): each 8-row block's best visible score,
+// [B*P][ldb], beside the row scores.
 cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
                                const int32_t *pool, int pool_blocks, float *scores, int64_t ld, int *status,
-                               cudaStream_t st);
+                               cudaStream_t st, float *bmax = nullptr, int64_t ldb = 0);
 
 // a3 (and the pool): `block` = 1 selects rows, 8 selects blocks of 8 rows by their best member.
 size_t select_workspace_bytes(const CacheView &c, int P, const int32_t *pool, int pool_blocks, int block, int K);
 int select_supported(const CacheView &c, const int32_t *pool, int pool_blocks, int block, int K);
+// block_max (with block = 8): scores holds each block's best visible score
+// ([B*P][ld], from launch_index_score's bmax) instead of the rows' scores.
 cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
                           int pool_blocks, int block, int K, int32_t *out, void *ws, size_t ws_bytes,
-                          cudaStream_t st);
+                          cudaStream_t st, bool block_max = false);
 
 // a4 over a pool in one kernel (scores stay on chip; E4M3 keys, HI <= 64,
 // pools of up to 2,048 blocks).

@@ -94,6 +94,8 @@ struct IdxArgs {
     const float *w;
     float *scores;
     int64_t ld;
+    float *bmax;     // full scan, or null: each 8-row block's best visible score, [units*P][ldb]
+    int64_t ldb;
     int *status;
 };
 
@@ -603,6 +605,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (!a.pool_mode) {
                             const int Lp = len_b - a.P + 1 + g;
                             if (r < Lp) a.scores[(static_cast<int64_t>(it.u) * a.P + g) * a.ld + r] = s;
+                            if (a.bmax) {
+                                // a block's 8 rows are 8 consecutive lanes of this warp
+                                float v = r < Lp ? s : -INFINITY;
+                                v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+                                v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+                                v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+                                if ((r & 7) == 0 && r < Lp)
+                                    a.bmax[(static_cast<int64_t>(it.u) * a.P + g) * a.ldb + (r >> 3)] = v;
+                            }
                         } else {
                             if (r < a.pool_blocks * kPoolBlock) a.scores[static_cast<int64_t>(it.u) * a.ld + r] = s;
                         }
@@ -628,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t *iq, const float *w,
                                const int32_t *pool, int pool_blocks, float *scores, int64_t ld, int *status,
-                               cudaStream_t st)
+                               cudaStream_t st, float *bmax, int64_t ldb)
 {
     if (c.B * P == 0) return cudaSuccess;
     IdxArgs a{};
@@ -680,6 +691,8 @@ cudaError_t launch_index_score(const CacheView &c, int P, int HI, const uint8_t 
     a.w = w;
     a.scores = scores;
     a.ld = ld;
+    a.bmax = pool ? nullptr : bmax;
+    a.ldb = ldb;
     a.status = status;
 
     const size_t stage_bytes = static_cast<size_t>(a.mt) * kTileRows * c.DI;

@@ -55,7 +55,9 @@ constexpr int kMinChunk = 4096;      // a row of up to 2x this stays whole in on
 constexpr int kMinChunkLong = 1024;  // a longer row is not spread thinner than this per CTA
 constexpr int64_t kSegmentLen = static_cast<int64_t>(kMaxCluster) * 8192;
 
-enum SelSource { kRows = 0, kBlocks = 1, kPoolRows = 2, kPairs = 3 };
+// kBlockMax: blocks of 8 rows whose best visible scores the scan already
+// wrote (one score per block), instead of kBlocks' maximum over row scores.
+enum SelSource { kRows = 0, kBlocks = 1, kPoolRows = 2, kPairs = 3, kBlockMax = 4 };
 
 struct SelArgs {
     const float *scores;       // kRows/kBlocks/kPoolRows: [rows][ld];  kPairs: [rows][n_pairs]
@@ -97,7 +99,7 @@ struct RowView {
     int L;
     __device__ __forceinline__ uint32_t key(int64_t i) const
     {
-        if (S == kRows) return score_key(__ldg(s + i));
+        if (S == kRows || S == kBlockMax) return score_key(__ldg(s + i));
         if (S == kBlocks) {
             const int64_t r0 = i * kPoolBlock;
             if (r0 + kPoolBlock <= L) {
@@ -632,6 +634,7 @@ cudaError_t launch(int source, const SelArgs &args, int grid_rows, int64_t n_per
     case kRows: return launch_one_or_cluster<kRows>(args, grid_rows, n_per_cluster, st);
     case kBlocks: return launch_one_or_cluster<kBlocks>(args, grid_rows, n_per_cluster, st);
     case kPoolRows: return launch_one_or_cluster<kPoolRows>(args, grid_rows, n_per_cluster, st);
+    case kBlockMax: return launch_one_or_cluster<kBlockMax>(args, grid_rows, n_per_cluster, st);
     default: return launch_one_or_cluster<kPairs>(args, grid_rows, n_per_cluster, st);
     }
 }
@@ -675,12 +678,12 @@ int select_supported(const CacheView &c, const int32_t *pool, int pool_blocks, i
 
 cudaError_t launch_select(const CacheView &c, int P, const float *scores, int64_t ld, const int32_t *pool,
                           int pool_blocks, int block, int K, int32_t *out, void *ws, size_t ws_bytes,
-                          cudaStream_t st)
+                          cudaStream_t st, bool block_max)
 {
     const int rows = c.B * P;
     if (rows == 0) return cudaSuccess;
     const SelPlan p = sel_plan(c, pool, pool_blocks, block, K);
-    const int source = pool ? kPoolRows : (block == 1 ? kRows : kBlocks);
+    const int source = pool ? kPoolRows : (block == 1 ? kRows : (block_max ? kBlockMax : kBlocks));
     SelArgs a{};
     a.scores = scores;
     a.ld = ld;
