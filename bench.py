@@ -460,19 +460,23 @@ def stage_times(cache, layers, wl, flush, steps, stream):
                 launches=count, kind=kind, stage="pool_topk")
         elif la.struct.mode != W.REUSE:
             nblk = pool_in.shape[-1] if pool_in is not None else 0
-            scores = B.csa_index_score(cache, iq, w, pool=pool_in)
+            # a Full layer that builds the pool has its scan write the block
+            # maxima, from which the pool is selected (as csa_layer_step does)
+            bm = B.block_max_buffer(cache, wl.P) if make_pool else None
+            scores = B.csa_index_score(cache, iq, w, pool=pool_in, block_max=bm)
             ws_sel = torch.empty(max(16, B.topk_workspace_size(cache, wl.P, wl.K, nblk,
                                                                wl.pool_blocks if make_pool else 0)),
                                  dtype=torch.uint8, device=dev)
             idx, _ = B.csa_topk(cache, scores, wl.K, pool=pool_in, pool_keep=wl.pool_blocks if make_pool else 0,
-                                workspace=ws_sel)
+                                block_max=bm, workspace=ws_sel)
             torch.cuda.synchronize()
             out[kind + ".index_score"] = dict(
-                ms=timed(lambda: B.csa_index_score(cache, iq, w, pool=pool_in, scores=scores)),
+                ms=timed(lambda: B.csa_index_score(cache, iq, w, pool=pool_in, scores=scores, block_max=bm)),
                 launches=count, kind=kind, stage="index_score")
             out[kind + ".topk"] = dict(
                 ms=timed(lambda: B.csa_topk(cache, scores, wl.K, pool=pool_in,
-                                            pool_keep=wl.pool_blocks if make_pool else 0, workspace=ws_sel)),
+                                            pool_keep=wl.pool_blocks if make_pool else 0, block_max=bm,
+                                            workspace=ws_sel)),
                 launches=count, kind=kind, stage="topk")
         else:
             idx = la.idx
@@ -942,7 +946,9 @@ def traffic_from_profile(stage, kind, workload):
 def stage_bytes(wl, kind, stage):
     """Algorithmic bytes (bytes that must move) of one launch of a stage:
     index_score: the indexer keys scanned, the indexer queries and weights;
-    topk: the scores read (and the pool's block ids) and the ids written;
+    topk: the scores read (and the pool's block ids) and the ids written; a
+    Full layer that builds the pool reads its blocks' maxima (L/8) and the
+    pool's rows' scores instead of all L scores;
     pool_topk (index_score and topk of a Reindex layer in one kernel): the
     pool's block ids and keys, the indexer queries and weights, the ids;
     sparse_attend: the selected FP4 rows, the bf16 queries, the fp32 outputs
@@ -960,11 +966,12 @@ def stage_bytes(wl, kind, stage):
         # the pool's block ids and its rows' keys read, the ids written
         return units * (wl.pool_blocks * 4 + pool_rows * kb + wl.K * 4) + q_index
     if stage == "topk":
+        if kind == "full+pool":
+            # the block maxima, the pool's rows' scores, the pool written, the ids
+            return units * (((L + 7) // 8) * 4 + pool_rows * 4 + wl.pool_blocks * 4 + wl.K * 4)
         n = pool_rows if kind == "reindex.pool" else L
         b = units * n * 4 + units * wl.K * 4
         if kind == "reindex.pool":
-            b += units * wl.pool_blocks * 4
-        if kind == "full+pool":
             b += units * wl.pool_blocks * 4
         return b
     row = wl.D // 2 + wl.D // 16

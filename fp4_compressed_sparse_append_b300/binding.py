@@ -77,8 +77,8 @@ def lib() -> ctypes.CDLL:
         C = ctypes.POINTER(csa_cache)
         L.csa_quantize_append.argtypes = [C, V, V, I32, V]
         L.csa_quantize_append_project.argtypes = [C, V, V, I32, V]
-        L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V]
-        L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, SZ, V]
+        L.csa_index_score.argtypes = [C, I32, I32, V, V, V, I32, V, I64, V, I64, V]
+        L.csa_topk.argtypes = [C, I32, V, I64, V, I32, I32, V, I32, V, V, I64, V, SZ, V]
         L.csa_topk_workspace_size.argtypes = [C, I32, I32, I32, I32, ctypes.POINTER(SZ)]
         L.csa_pool_topk.argtypes = [C, I32, I32, V, V, V, I32, I32, V, V, SZ, V]
         L.csa_pool_topk_workspace_size.argtypes = [C, I32, I32, ctypes.POINTER(SZ)]
@@ -260,10 +260,20 @@ def csa_cache_reload(cache: Cache, records: torch.Tensor, stream=None) -> None:
            "csa_cache_reload")
 
 
+def block_max_buffer(cache: Cache, P: int) -> torch.Tensor:
+    """An empty [B, P, ldb] fp32 buffer for csa_index_score's block maxima
+    (ldb = ceil(capacity / 8) rounded up to 4)."""
+    ldb = ((cache.capacity + CSA_POOL_BLOCK - 1) // CSA_POOL_BLOCK + 3) // 4 * 4
+    return torch.empty((cache.batch, P, ldb), dtype=torch.float32, device=cache.device)
+
+
 def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optional[torch.Tensor] = None,
-                    scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                    scores: Optional[torch.Tensor] = None, block_max: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
     """iq [B, P, HI, DI] uint8, w [B, P, HI] fp32, pool [B, P, nblk] int32 or None
-    -> scores [B, P, ld] fp32 (ld = capacity rounded up to 4, or 8*nblk)."""
+    -> scores [B, P, ld] fp32 (ld = capacity rounded up to 4, or 8*nblk).
+    block_max [B, P, ldb] fp32 (block_max_buffer; full scans only) also
+    receives each 8-row block's best visible score."""
     B, P, HI, _ = iq.shape
     _lead(iq, "iq", cache.batch, cache.d_index)
     nblk = pool.shape[-1] if pool is not None else 0
@@ -275,8 +285,10 @@ def csa_index_score(cache: Cache, iq: torch.Tensor, w: torch.Tensor, pool: Optio
     _need(w, Bc * P * HI * 4, "w")
     _need(pool, Bc * P * nblk * 4, "pool")
     _need(scores, Bc * P * scores.shape[-1] * 4, "scores")
+    ldb = block_max.shape[-1] if block_max is not None else 0
+    _need(block_max, Bc * P * ldb * 4, "block_max")
     _check(lib().csa_index_score(cache.ref, P, HI, _ptr(iq), _ptr(w), _ptr(pool), nblk, _ptr(scores),
-                                 scores.shape[-1], _stream(stream)), "csa_index_score")
+                                 scores.shape[-1], _ptr(block_max), ldb, _stream(stream)), "csa_index_score")
     return scores
 
 
@@ -288,21 +300,26 @@ def topk_workspace_size(cache: Cache, P: int, K: int, pool_blocks: int = 0, pool
 
 
 def csa_topk(cache: Cache, scores: torch.Tensor, K: int, pool: Optional[torch.Tensor] = None,
-             pool_keep: int = 0, workspace: Optional[torch.Tensor] = None,
+             pool_keep: int = 0, block_max: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
              stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """scores [B, P, ld] -> (idx [B, P, K] int32, pool_out [B, P, pool_keep] int32 or None)."""
+    """scores [B, P, ld] -> (idx [B, P, K] int32, pool_out [B, P, pool_keep] int32 or None).
+    block_max: the block maxima csa_index_score wrote beside these scores
+    (with pool_keep > 0), from which the pool is then selected."""
     B, P, ld = scores.shape
     _lead(scores, "scores", cache.batch)
     nblk = pool.shape[-1] if pool is not None else 0
     _need(scores, cache.batch * P * ld * 4, "scores")
     _need(pool, cache.batch * P * nblk * 4, "pool")
+    ldb = block_max.shape[-1] if block_max is not None else 0
+    _need(block_max, cache.batch * P * ldb * 4, "block_max")
     idx = torch.empty((B, P, K), dtype=torch.int32, device=cache.device)
     pool_out = torch.empty((B, P, pool_keep), dtype=torch.int32, device=cache.device) if pool_keep else None
     if workspace is None:
         n = topk_workspace_size(cache, P, K, nblk, pool_keep)
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
     _check(lib().csa_topk(cache.ref, P, _ptr(scores), ld, _ptr(pool), nblk, K, _ptr(idx), pool_keep,
-                          _ptr(pool_out), _ptr(workspace), workspace.numel(), _stream(stream)), "csa_topk")
+                          _ptr(pool_out), _ptr(block_max), ldb, _ptr(workspace), workspace.numel(),
+                          _stream(stream)), "csa_topk")
     return idx, pool_out
 
 

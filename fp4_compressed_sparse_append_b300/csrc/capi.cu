@@ -162,17 +162,26 @@ csa_status csa_quantize_append_project(const csa_cache *cache, const uint16_t *r
     return from_cuda(csa::launch_quantize_append(view(cache), rows, nullptr, n_new, st, stream, w_ik));
 }
 
+// Block maxima beside a full scan's scores: one fp32 per 8 rows of capacity.
+static bool block_max_ok(const csa_cache *c, const float *block_max, int64_t ldb)
+{
+    const int64_t blocks = (static_cast<int64_t>(c->capacity) + CSA_POOL_BLOCK - 1) / CSA_POOL_BLOCK;
+    return block_max && aligned16(block_max) && ldb >= blocks && ldb % 4 == 0;
+}
+
 csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI, const uint8_t *iq, const float *w,
-                           const int32_t *pool, int32_t pool_blocks, float *scores, int64_t ld, csa_stream_t stream)
+                           const int32_t *pool, int32_t pool_blocks, float *scores, int64_t ld, float *block_max,
+                           int64_t ldb, csa_stream_t stream)
 {
     csa_status s = check_cache(cache);
     if (s != CSA_OK) return s;
     s = check_index_args(cache, P, HI, iq, w, pool, pool_blocks, scores, ld);
     if (s != CSA_OK) return s;
+    if (block_max && (pool || !block_max_ok(cache, block_max, ldb))) return CSA_ERR_INVALID_ARG;
     int *st = status_word();
     if (!st) return CSA_ERR_CUDA;
     return from_cuda(csa::launch_index_score(view(cache), P, HI, iq, w, pool, pool ? pool_blocks : 0, scores, ld, st,
-                                             stream));
+                                             stream, block_max, block_max ? ldb : 0));
 }
 
 static csa_status check_topk(const csa_cache *cache, int32_t P, int32_t pool_blocks, int has_pool, int32_t K,
@@ -216,7 +225,8 @@ csa_status csa_topk_workspace_size(const csa_cache *cache, int32_t P, int32_t po
 
 csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld, const int32_t *pool,
                     int32_t pool_blocks, int32_t K, int32_t *idx, int32_t pool_keep, int32_t *pool_out,
-                    void *workspace, size_t workspace_bytes, csa_stream_t stream)
+                    const float *block_max, int64_t ldb, void *workspace, size_t workspace_bytes,
+                    csa_stream_t stream)
 {
     csa_status s = check_cache(cache);
     if (s != CSA_OK) return s;
@@ -224,6 +234,7 @@ csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int6
     if (!aligned16(scores) || !aligned16(idx) || ld % 4) return CSA_ERR_INVALID_ARG;
     if (pool && !aligned16(pool)) return CSA_ERR_INVALID_ARG;
     if (pool_out && !aligned16(pool_out)) return CSA_ERR_INVALID_ARG;
+    if (block_max && (!pool_out || !block_max_ok(cache, block_max, ldb))) return CSA_ERR_INVALID_ARG;
     s = check_topk(cache, P, pool_blocks, pool != nullptr, K, pool_keep, pool_out != nullptr);
     if (s != CSA_OK) return s;
     if (pool ? ld < static_cast<int64_t>(pool_blocks) * CSA_POOL_BLOCK : ld < cache->capacity)
@@ -231,18 +242,21 @@ csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int6
     const size_t need = topk_ws(cache, P, pool_blocks, pool != nullptr, K, pool_keep, pool_out != nullptr);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return CSA_ERR_WORKSPACE;
     const csa::CacheView v = view(cache);
+    // the pool's blocks, from the block maxima when the scan wrote them
+    const float *bsrc = block_max ? block_max : scores;
+    const int64_t bld = block_max ? ldb : ld;
     if (pool_out && csa::pool_rows_supported(pool_keep, K)) {
         // the pool first; the top K rows then lie in the pool's blocks
-        cudaError_t e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out,
-                                           workspace, workspace_bytes, stream);
+        cudaError_t e = csa::launch_select(v, P, bsrc, bld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out,
+                                           workspace, workspace_bytes, stream, block_max != nullptr);
         if (e == cudaSuccess) e = csa::launch_pool_rows(v, P, scores, ld, pool_out, pool_keep, K, idx, stream);
         return from_cuda(e);
     }
     cudaError_t e =
         csa::launch_select(v, P, scores, ld, pool, pool ? pool_blocks : 0, 1, K, idx, workspace, workspace_bytes, stream);
     if (e == cudaSuccess && pool_out)
-        e = csa::launch_select(v, P, scores, ld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out, workspace,
-                               workspace_bytes, stream);
+        e = csa::launch_select(v, P, bsrc, bld, nullptr, 0, CSA_POOL_BLOCK, pool_keep, pool_out, workspace,
+                               workspace_bytes, stream, block_max != nullptr);
     return from_cuda(e);
 }
 

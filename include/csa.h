@@ -215,14 +215,22 @@ CSA_API csa_status csa_cache_reload(const csa_cache *cache, const uint8_t *recor
  *                   -> score candidate c = 8*j + m, row pool[j]*8 + m;
  *                      scores[(b*P+p)*ld + c]
  *   scores : fp32, row stride ld (>= capacity, or >= 8*pool_blocks with a pool)
+ *   block_max : NULL, or (only with pool == NULL) fp32 with row stride ldb
+ *            (>= ceil(capacity / 8), a multiple of 4; 16-byte aligned):
+ *            block_max[(b*P+p)*ldb + j] = the largest score of rows
+ *            8j .. 8j+7 below L_p, for j < ceil(L_p / 8) ("The hierarchical
+ *            indexer": a block of 8 is ranked by its best member); csa_topk
+ *            builds its pool from these instead of the row scores
  * score = sum_h w[h] * ReLU(sum_d iq[h][d] * ik[row][d]), fp32.  Entries for
- * rows past L_p or empty pool slots are left unspecified.
+ * rows past L_p or empty pool slots, and block maxima past ceil(L_p / 8), are
+ * left unspecified.
  * Supported: HI*P <= 512, HI % 16 == 0 (or HI*P % 16 == 0).
  */
 CSA_API csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI,
                            const uint8_t *iq, const float *w,
                            const int32_t *pool, int32_t pool_blocks,
-                           float *scores, int64_t ld, csa_stream_t stream);
+                           float *scores, int64_t ld, float *block_max, int64_t ldb,
+                           csa_stream_t stream);
 
 /*
  * a3: top-K selection (and the hierarchical block pool) from scores.
@@ -236,14 +244,18 @@ CSA_API csa_status csa_index_score(const csa_cache *cache, int32_t P, int32_t HI
  *              the pool_keep blocks of 8 rows (block j = rows 8j..8j+7 < L_p)
  *              with the largest best-member score (ties: lower id), ascending,
  *              then -1 padding
+ *   block_max, ldb : NULL, or (only with pool_out) the block maxima that
+ *              csa_index_score wrote beside these scores; the pool is then
+ *              selected from them (ceil(L_p / 8) reads instead of L_p), with
+ *              the same result
  *   workspace: csa_topk_workspace_size bytes (zero for rows of at most 196,608
  *              candidates; longer rows are selected in two stages through it)
  * 1 <= K <= 16384; pool_keep <= 16384.
  */
 CSA_API csa_status csa_topk(const csa_cache *cache, int32_t P, const float *scores, int64_t ld,
                     const int32_t *pool, int32_t pool_blocks, int32_t K, int32_t *idx,
-                    int32_t pool_keep, int32_t *pool_out, void *workspace, size_t workspace_bytes,
-                    csa_stream_t stream);
+                    int32_t pool_keep, int32_t *pool_out, const float *block_max, int64_t ldb,
+                    void *workspace, size_t workspace_bytes, csa_stream_t stream);
 
 /*
  * a4 over the hierarchical pool in one call: csa_index_score of the pool's

@@ -83,16 +83,25 @@ def test_argument_checks_of_each_call(lib):
     c = ctypes.byref(fake_cache())
     V = ctypes.c_void_p
     # index score: ld below capacity, HI*P too large
-    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), None, 0, V(0x3000), 32, None) == 1
-    assert lib.csa_index_score(c, 8, 128, V(0x1000), V(0x2000), None, 0, V(0x3000), 64, None) == 2
+    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), None, 0, V(0x3000), 32, None, 0, None) == 1
+    assert lib.csa_index_score(c, 8, 128, V(0x1000), V(0x2000), None, 0, V(0x3000), 64, None, 0, None) == 2
+    # block maxima (capacity 64: 8 blocks): with a pool, a stride below 8 or not a
+    # multiple of 4, a misaligned buffer
+    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), V(0x4000), 4, V(0x3000), 64, V(0x5000), 8, None) == 1
+    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), None, 0, V(0x3000), 64, V(0x5000), 4, None) == 1
+    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), None, 0, V(0x3000), 64, V(0x5000), 10, None) == 1
+    assert lib.csa_index_score(c, 1, 4, V(0x1000), V(0x2000), None, 0, V(0x3000), 64, V(0x5008), 8, None) == 1
     # top-K: K out of range; pool_out together with a pool
-    assert lib.csa_topk(c, 1, V(0x1000), 64, None, 0, 0, V(0x2000), 0, None, None, 0, None) == 1
-    assert lib.csa_topk(c, 1, V(0x1000), 64, V(0x4000), 8, 4, V(0x2000), 8, V(0x5000), None, 0, None) == 1
+    assert lib.csa_topk(c, 1, V(0x1000), 64, None, 0, 0, V(0x2000), 0, None, None, 0, None, 0, None) == 1
+    assert lib.csa_topk(c, 1, V(0x1000), 64, V(0x4000), 8, 4, V(0x2000), 8, V(0x5000), None, 0, None, 0, None) == 1
+    # block maxima without a pool to build, or with a stride below 8
+    assert lib.csa_topk(c, 1, V(0x1000), 64, None, 0, 4, V(0x2000), 0, None, V(0x6000), 8, None, 0, None) == 1
+    assert lib.csa_topk(c, 1, V(0x1000), 64, None, 0, 4, V(0x2000), 4, V(0x5000), V(0x6000), 4, None, 0, None) == 1
     # a row longer than one cluster holds is selected in two stages through the workspace
     n = ctypes.c_size_t(0)
     big = ctypes.byref(fake_cache(capacity=1 << 20))
     assert lib.csa_topk_workspace_size(big, 1, 0, 2048, 0, ctypes.byref(n)) == 0 and n.value > 0
-    assert lib.csa_topk(big, 1, V(0x1000), 1 << 20, None, 0, 2048, V(0x2000), 0, None, None, 0, None) == 5
+    assert lib.csa_topk(big, 1, V(0x1000), 1 << 20, None, 0, 2048, V(0x2000), 0, None, None, 0, None, 0, None) == 5
     assert lib.csa_topk_workspace_size(c, 1, 0, 2048, 0, ctypes.byref(n)) == 0 and n.value == 0
     # attention: too many heads, missing workspace
     assert lib.csa_sparse_attend(c, 1, 65, V(0x1000), 1.0, V(0x2000), 8, V(0x3000), None, V(0x4000), 1 << 20,

@@ -62,3 +62,34 @@ def test_pool_scores_with_ragged_tail():
         ora = oracle.index_scores(iqh[b, 0], wh[b, 0], ikh[b], rows)
         v = valid.astype(bool)
         compare(s[b, 0, :320][v], ora[v], abs_bound(iqh[b, 0], wh[b, 0], ikh[b, rows[v]]), b)
+
+
+@pytest.mark.parametrize("L,P", [(3001, 3), (4096, 1), (17, 2)])
+def test_block_maxima(L, P):
+    """The scan's block maxima ("G2C Brief", "The hierarchical indexer": a block
+    of 8 rows is ranked by its best member): each block's entry equals the
+    largest of the same call's row scores below L_p bit for bit, and the
+    oracle's block maximum within the scores' bound; the row scores are those
+    of the call without block maxima."""
+    need_gpu()
+    wl = W.Workload("t", B=2, L=L, H=4, D=128, HI=16, DI=128, K=8, P=P)
+    cache, _, ik = device_cache(wl, seed=13)
+    inp = W.layer_inputs(wl, 13, 0, device="cuda")
+    bm = B.block_max_buffer(cache, P)
+    bm.fill_(float("nan"))
+    scores = B.csa_index_score(cache, inp["iq"], inp["w"], block_max=bm)
+    plain = B.csa_index_score(cache, inp["iq"], inp["w"])
+    torch.cuda.synchronize()
+    s, g, s0 = scores.cpu().numpy(), bm.cpu().numpy(), plain.cpu().numpy()
+    ikh, iqh, wh = ik.cpu().numpy(), inp["iq"].cpu().numpy(), inp["w"].cpu().numpy()
+    for b in range(wl.B):
+        for p in range(P):
+            Lp = wl.L - P + 1 + p
+            nb = (Lp + 7) // 8
+            assert np.array_equal(s[b, p, :Lp], s0[b, p, :Lp]), (b, p)
+            assert np.array_equal(g[b, p, :nb], oracle.block_max(s[b, p, :Lp])), (b, p)
+            ora = oracle.index_scores(iqh[b, p], wh[b, p], ikh[b], np.arange(Lp))
+            bound = abs_bound(iqh[b, p], wh[b, p], ikh[b, :Lp])
+            bb = np.zeros(nb * 8)
+            bb[:Lp] = bound
+            compare(g[b, p, :nb], oracle.block_max(ora.astype(np.float32)), bb.reshape(nb, 8).max(1), (b, p))

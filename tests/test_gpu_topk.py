@@ -131,3 +131,37 @@ def test_one_cta_select_branches(n, K, kind):
     assert got[got >= 0].tolist() == sorted(ref[ref >= 0].tolist())
     assert (got >= 0).sum() == min(n, K)
     ascending_then_padding(got)
+
+
+@pytest.mark.parametrize("P,cap,lengths,keep,kind", [
+    (6, 4000, [3990, 17], 100, "ties"),          # causal positions, a sequence shorter than the pool
+    (1, 1 << 20, [1 << 20, 1000003], 2048, "zeros"),   # 131,072 blocks: the cluster path
+    (1, 100000, [100000, 99999], 2048, "plain"),  # 12,500 blocks: the one-CTA path
+    (1, 1 << 21, [1 << 21], 2048, "plain"),       # 262,144 blocks: two stages through the workspace
+])
+def test_pool_from_block_maxima(P, cap, lengths, keep, kind):
+    """csa_topk given block maxima (here the oracle's, from the same scores)
+    keeps the same pool as the oracle's build_pool, and the same top K rows."""
+    need_gpu()
+    Bn = len(lengths)
+    s = scores_with_ties((Bn, P, cap), cap + keep, kind)
+    cache = lengths_cache(Bn, cap, lengths)
+    bm = B.block_max_buffer(cache, P)
+    bmh = np.full(tuple(bm.shape), np.nan, np.float32)
+    for b in range(Bn):
+        for p in range(P):
+            L = max(lengths[b] - P + 1 + p, 0)
+            bmh[b, p, :(L + 7) // 8] = oracle.block_max(s[b, p, :L])
+    bm.copy_(torch.from_numpy(bmh))
+    K = 64 if cap < 10000 else 2048
+    ws = torch.empty(max(16, B.topk_workspace_size(cache, P, K, 0, keep)), dtype=torch.uint8, device="cuda")
+    idx, pool = B.csa_topk(cache, torch.from_numpy(s).cuda(), K, pool_keep=keep, block_max=bm, workspace=ws)
+    gi, gp = idx.cpu().numpy(), pool.cpu().numpy()
+    for b in range(Bn):
+        for p in range(P):
+            L = max(lengths[b] - P + 1 + p, 0)
+            refp = oracle.build_pool(s[b, p, :L], keep) if L else -np.ones(keep, np.int64)
+            assert gp[b, p].tolist() == refp.tolist(), (b, p)
+            ref = oracle.topk(s[b, p, :L], K)
+            assert sorted(gi[b, p][gi[b, p] >= 0].tolist()) == sorted(ref[ref >= 0].tolist()), (b, p)
+            ascending_then_padding(gi[b, p])
