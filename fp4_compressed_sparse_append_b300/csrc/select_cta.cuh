@@ -12,10 +12,15 @@
 //     registers: what a thread keeps is counted without warp votes (a vote
 //     costs tens of cycles per warp here) and output positions come from one
 //     block scan of per-thread counts;
-//   - one histogram pass over all keys: (key - minimum) over 4,096 bins that
-//     span the keys' actual range (indexer scores of exactly 0, where every
-//     head's product is negative, stretch that range, so the bin holding the
-//     K-th largest key can hold hundreds of keys);
+//   - one histogram pass over all keys: (key - base) over 4,096 bins that
+//     span [base, maximum].  For K <= 2,048, base is a lower bound on the
+//     K-th largest key: the smallest of the largest keys of the 2,048 groups
+//     of 8 consecutive candidates.  When at least K groups hold a key, those
+//     are at least K distinct keys, and of any K keys one is no larger than
+//     the K-th largest, so no key below base is kept (otherwise base is the
+//     smallest key).  Without the bound, indexer scores of exactly 0 (every
+//     head's product negative) stretch the range, and the bin holding the
+//     K-th largest key can hold hundreds of keys;
 //   - the keys of that bin are gathered, in candidate order, into a list of at
 //     most 1,024 (another pass over all keys first if the bin is larger), and
 //     further passes over the next lower bits run on the list only;
@@ -40,6 +45,7 @@ constexpr int kBinBits = 12;
 constexpr int kBins = 1 << kBinBits;
 constexpr int kListMax = 1024;                   // keys of a threshold bin gathered into a list
 constexpr int kRankMax = 32;                     // list length ranked exactly by one warp
+constexpr int kGroup = 8;                        // keys per group of the lower bound
 constexpr int kWarps = kThreads / 32;
 static_assert(kListMax == 2 * kThreads, "list passes give each thread two entries");
 
@@ -47,7 +53,7 @@ struct alignas(16) Scratch {
     uint32_t hist[kBins];
     uint32_t lk[kListMax];  // gathered keys, in candidate order
     int32_t lc[kListMax];   // and their candidates
-    uint32_t wa[kWarps], wb[kWarps], wc[kWarps];
+    uint32_t wa[kWarps], wb[kWarps], wc[kWarps], wd[kWarps], we[kWarps];
     uint32_t scan_buf[2][kWarps];  // per-warp sums of block_scan, used in turn
     uint32_t res_bin, res_above;
     uint32_t thr_gt, thr_eq, need;
@@ -152,41 +158,59 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             kk[4 * m + 3] = c0 + 4 * m + 3 < n ? v.w : 0u;
         }
     }
-    uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0;
+    uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0, gmin = 0xFFFFFFFFu, gcnt = 0;
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        const uint32_t k = kk[j];
-        cnt += k ? 1u : 0u;
-        kmin = min(kmin, k ? k : 0xFFFFFFFFu);
-        kmax = max(kmax, k);
+    for (int g = 0; g < kPerThread / kGroup; ++g) {
+        uint32_t gm = 0;  // the group's largest key (0: an empty group)
+#pragma unroll
+        for (int j = g * kGroup; j < (g + 1) * kGroup; ++j) {
+            const uint32_t k = kk[j];
+            cnt += k ? 1u : 0u;
+            kmin = min(kmin, k ? k : 0xFFFFFFFFu);
+            gm = max(gm, k);
+        }
+        kmax = max(kmax, gm);
+        gmin = min(gmin, gm ? gm : 0xFFFFFFFFu);
+        gcnt += gm ? 1u : 0u;
     }
     kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
     kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
     cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    gmin = __reduce_min_sync(0xFFFFFFFFu, gmin);
+    gcnt = __reduce_add_sync(0xFFFFFFFFu, gcnt);
     if (lane == 0) {
         sc.wa[warp] = kmin;
         sc.wb[warp] = kmax;
         sc.wc[warp] = cnt;
+        sc.wd[warp] = gmin;
+        sc.we[warp] = gcnt;
     }
     zero_bins(sc, kBins);  // the first pass's bins, ordered before it by the barrier below
     __syncthreads();
     kmin = 0xFFFFFFFFu;
     kmax = 0;
+    gmin = 0xFFFFFFFFu;
     uint32_t total = 0;
+    gcnt = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) {
         kmin = min(kmin, sc.wa[i]);
         kmax = max(kmax, sc.wb[i]);
         total += sc.wc[i];
+        gmin = min(gmin, sc.wd[i]);
+        gcnt += sc.we[i];
     }
+    // Keys below base are never kept; every non-zero key is >= kmin >= 1, so
+    // "key >= base" also excludes the empty candidates.
+    const uint32_t base = gcnt >= K ? gmin : kmin;
 
     // The rule: keep keys > thr_gt, and the first `need` keys == thr_eq.
     uint32_t thr_gt = 0, thr_eq = 0, need = 0;
     int sb = 0;  // block_scan's buffer
     if (total > K) {
-        // v = key - kmin; the bits of v above `hi` are fixed to `prefix`, and
+        // v = key - base; the bits of v above `hi` are fixed to `prefix`, and
         // `above` keys lie above them (all of them kept).
-        const uint32_t range = kmax - kmin;
+        const uint32_t range = kmax - base;
         int hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
         uint32_t prefix = 0, above = 0;
         bool done = false;
@@ -194,7 +218,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
         // A. passes over all keys until the threshold bin holds <= kListMax keys
         while (true) {
             if (hi == 0) {  // one key value left
-                thr_gt = thr_eq = kmin + prefix;
+                thr_gt = thr_eq = base + prefix;
                 need = K - above;
                 done = true;
                 break;
@@ -209,8 +233,8 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             const uint32_t pfx = hi >= 32 ? 0u : (prefix << hi);
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j) {
-                const uint32_t v = kk[j] - kmin;
-                if (kk[j] && (v & mask) == pfx) atomicAdd(&sc.hist[(v >> lo) & (nb - 1)], 1u);
+                const uint32_t v = kk[j] - base;
+                if (kk[j] >= base && (v & mask) == pfx) atomicAdd(&sc.hist[(v >> lo) & (nb - 1)], 1u);
             }
             __syncthreads();
             uint32_t bin, ab;
@@ -219,12 +243,12 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             const uint32_t in_bin = sc.hist[bin];
             const uint32_t P = (prefix << d) | bin;
             if (in_bin == K - above) {  // the bin is taken whole
-                thr_gt = kmin + (P << lo) - 1u;
+                thr_gt = base + (P << lo) - 1u;
                 done = true;
                 break;
             }
             if (lo == 0) {  // the bin is one key value
-                thr_gt = thr_eq = kmin + P;
+                thr_gt = thr_eq = base + P;
                 need = K - above;
                 done = true;
                 break;
@@ -239,12 +263,12 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             uint32_t mine = 0;
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j)
-                mine += (kk[j] && ((kk[j] - kmin) >> hi) == prefix) ? 1u : 0u;
+                mine += (kk[j] >= base && ((kk[j] - base) >> hi) == prefix) ? 1u : 0u;
             uint32_t m;
             uint32_t off = block_scan(mine, sc, &m, sb);
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j)
-                if (kk[j] && ((kk[j] - kmin) >> hi) == prefix) {
+                if (kk[j] >= base && ((kk[j] - base) >> hi) == prefix) {
                     sc.lk[off] = kk[j];
                     sc.lc[off] = c0 + j;
                     ++off;
@@ -254,7 +278,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
             uint32_t nd = K - above;  // keys still to keep, all in the list
             while (static_cast<int>(m) > kRankMax) {
                 if (hi == 0) {  // one key value left
-                    thr_gt = thr_eq = kmin + prefix;
+                    thr_gt = thr_eq = base + prefix;
                     need = nd;
                     done = true;
                     break;
@@ -266,7 +290,7 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                 const int32_t ec0 = h0 ? sc.lc[i0] : 0, ec1 = h1 ? sc.lc[i1] : 0;
                 zero_bins(sc, nb);
                 __syncthreads();
-                const uint32_t b0 = ((e0 - kmin) >> lo) & (nb - 1), b1 = ((e1 - kmin) >> lo) & (nb - 1);
+                const uint32_t b0 = ((e0 - base) >> lo) & (nb - 1), b1 = ((e1 - base) >> lo) & (nb - 1);
                 if (h0) atomicAdd(&sc.hist[b0], 1u);
                 if (h1) atomicAdd(&sc.hist[b1], 1u);
                 __syncthreads();
@@ -276,13 +300,13 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                 const uint32_t in_bin = sc.hist[bin];
                 const uint32_t P = (prefix << d) | bin;
                 if (in_bin == nd) {
-                    thr_gt = kmin + (P << lo) - 1u;
+                    thr_gt = base + (P << lo) - 1u;
                     need = 0;
                     done = true;
                     break;
                 }
                 if (lo == 0) {
-                    thr_gt = thr_eq = kmin + P;
+                    thr_gt = thr_eq = base + P;
                     need = nd;
                     done = true;
                     break;

@@ -89,7 +89,9 @@ def shaped_scores(n, kind, seed):
     scores that stretch the key range so that the threshold bin of the first
     pass holds thousands of keys (another pass over all keys), a narrow band of
     distinct scores (several passes over the gathered list), and a band of
-    exact ties at the K-th value (the tie rule)."""
+    exact ties at the K-th value (the tie rule); rows whose K-th largest score
+    equals the selection's lower bound (the least of the largest of each run of
+    8), and rows with exact zeros."""
     rng = np.random.default_rng(seed)
     if kind == "stretched":
         s = (1.0 + rng.random(n) * 1e-3).astype(np.float32)
@@ -102,6 +104,18 @@ def shaped_scores(n, kind, seed):
         pick = rng.choice(n, 984, replace=False)
         s[pick[:384]] = 1e30
         s[pick[384:]] = np.float32(1.0) + (np.arange(600) % 256).astype(np.float32) * np.float32(2.0 ** -23)
+    elif kind in ("group_max", "group_max_ties"):
+        # every run of 8 candidates has its largest score 3.0 (the selection's
+        # lower bound is then the K-th largest itself at K = n / 8); with
+        # "group_max_ties" 100 more candidates tie at 3.0
+        s = rng.random(n).astype(np.float32)
+        s[np.arange(0, n - 7, 8) + rng.integers(0, 8, size=n // 8)] = 3.0
+        if kind == "group_max_ties":
+            s[rng.choice(np.flatnonzero(s < 3.0), 100, replace=False)] = 3.0
+    elif kind == "relu_zeros":
+        # 40 % exact zeros (every head's product negative), the rest positive
+        s = rng.random(n).astype(np.float32) * 4.0
+        s[rng.random(n) < 0.4] = 0.0
     else:  # "tie_cut": 1500 above, 1000 tied, the rest below
         s = rng.random(n).astype(np.float32)
         order = rng.permutation(n)
@@ -112,7 +126,10 @@ def shaped_scores(n, kind, seed):
 
 @pytest.mark.parametrize("n,K,kind", [(16384, 2048, "plain"), (16385, 2048, "plain"), (16384, 16384, "plain"),
                                       (16384, 1, "plain"), (16384, 2048, "stretched"), (9000, 700, "band"),
-                                      (16384, 2048, "tie_cut"), (4097, 3000, "tie_cut")])
+                                      (16384, 2048, "tie_cut"), (4097, 3000, "tie_cut"),
+                                      (16384, 2048, "group_max"), (16384, 2048, "group_max_ties"),
+                                      (16384, 2048, "relu_zeros"), (16384, 8000, "relu_zeros"),
+                                      (9000, 2048, "relu_zeros"), (16384, 1000, "group_max")])
 def test_one_cta_select_branches(n, K, kind):
     """Rows of 8,193 to 16,384 candidates are selected by select_one_kernel,
     longer ones by a cluster, shorter ones by select_kernel in one CTA; all
