@@ -454,9 +454,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = u * kThreads + tid;
         if (q < nq) *reinterpret_cast<uint4 *>(allk + cta_select::key_slot(4 * q)) = __ldcg(src + q);
     }
-    for (int j = tid; j < a.pool_blocks; j += kThreads) {
-        int32_t blk = a.pool[static_cast<int64_t>(unit) * a.pool_blocks + j];
-        allb[j] = blk >= cap_blocks ? -1 : blk;
+    {
+        // the block ids (at most kMaxCluster * kBlocksPerCta): every load in
+        // flight at once, beside the keys'
+        constexpr int kIdLoads = kMaxCluster * kBlocksPerCta / kThreads;
+        int32_t bl[kIdLoads];
+#pragma unroll
+        for (int u = 0; u < kIdLoads; ++u) {
+            const int j = u * kThreads + tid;
+            bl[u] = j < a.pool_blocks ? a.pool[static_cast<int64_t>(unit) * a.pool_blocks + j] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kIdLoads; ++u) {
+            const int j = u * kThreads + tid;
+            if (j < a.pool_blocks) allb[j] = bl[u] >= cap_blocks ? -1 : bl[u];
+        }
     }
     __syncthreads();
     write_selection(allk, allb, n, a.K, a.idx + static_cast<int64_t>(unit) * a.K, sc);
@@ -494,23 +506,25 @@ __global__ void __launch_bounds__(kThreads, 1) pool_rows_kernel(RowsArgs a)
     const int Lp = min(a.lengths[b], a.cap) - a.P + 1 + p;
     const int cap_blocks = (a.cap + kPoolBlock - 1) / kPoolBlock;
     const int32_t *prow = a.pool + static_cast<int64_t>(unit) * a.pool_blocks;
-    for (int j = tid; j < a.pool_blocks; j += kThreads) {
-        int32_t blk = prow[j];
-        if (blk >= cap_blocks) blk = -1;
-        allb[j] = blk;
-    }
-    __syncthreads();
     const float *srow = a.scores + static_cast<int64_t>(unit) * a.ld;
     const int n = a.pool_blocks * kPoolBlock;
     // Each block's 8 scores are two 16-byte loads (row ids are multiples of 8
     // and ld a multiple of 4); four blocks per thread are in flight at once.
+    // A thread reads its blocks' ids itself (all four loads in flight), so its
+    // score loads wait on those alone.
     for (int j0 = tid; j0 < a.pool_blocks; j0 += kU * kThreads) {
         float4 v[kU][2];
         int32_t blk[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int j = j0 + u * kThreads;
-            blk[u] = j < a.pool_blocks ? allb[j] : -1;
+            const int32_t x = j < a.pool_blocks ? prow[j] : -1;
+            blk[u] = x >= cap_blocks ? -1 : x;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < a.pool_blocks) allb[j] = blk[u];
             const int64_t r0 = static_cast<int64_t>(blk[u] >= 0 ? blk[u] : 0) * kPoolBlock;
             if (blk[u] >= 0 && r0 + kPoolBlock <= a.ld) {
                 const float4 *sp = reinterpret_cast<const float4 *>(srow + r0);

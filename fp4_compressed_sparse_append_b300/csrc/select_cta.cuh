@@ -20,10 +20,16 @@
 //     the K-th largest, so no key below base is kept (otherwise base is the
 //     smallest key).  Without the bound, indexer scores of exactly 0 (every
 //     head's product negative) stretch the range, and the bin holding the
-//     K-th largest key can hold hundreds of keys;
-//   - the keys of that bin are gathered, in candidate order, into a list of at
-//     most 1,024 (another pass over all keys first if the bin is larger), and
-//     further passes over the next lower bits run on the list only;
+//     K-th largest key can hold hundreds of keys.
+//     When at most 4,096 keys lie at or above base (the usual case: the
+//     bound is tight), they are first moved, in candidate order, into one
+//     list over the key array, 8 entries a thread, and the passes and the
+//     output run over those: a shared-memory atomic costs about as much with
+//     one lane active as with 32, and most of a thread's 32 keys lie below
+//     base;
+//   - the keys of the threshold bin are gathered, in candidate order, into a
+//     list of at most 1,024 (another pass first if the bin is larger), and
+//     further passes over the next lower bits run on that list only;
 //   - a list of at most 32 keys is ranked exactly by one warp;
 //   - every outcome is one rule: keep the keys above thr_gt, and the first
 //     `need` keys equal to thr_eq in candidate order.
@@ -46,7 +52,12 @@ constexpr int kBins = 1 << kBinBits;
 constexpr int kListMax = 1024;                   // keys of a threshold bin gathered into a list
 constexpr int kRankMax = 32;                     // list length ranked exactly by one warp
 constexpr int kGroup = 8;                        // keys per group of the lower bound
+constexpr int kBigList = 4096;                   // keys >= the bound moved into one list, at most
+constexpr int kBigPer = kBigList / kThreads;     // its entries a thread
+static_assert(2 * kBigList <= kMaxKeys, "the big list's keys and candidates fit the key array");
+static_assert(kBigPer % 4 == 0, "a thread's list entries load as 16-byte pieces");
 constexpr int kWarps = kThreads / 32;
+static_assert(kWarps <= 32, "one lane per warp in the cross-warp reductions");
 static_assert(kListMax == 2 * kThreads, "list passes give each thread two entries");
 
 struct alignas(16) Scratch {
@@ -82,15 +93,11 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, Scratch &sc, uint32_t
     sb ^= 1;
     if (lane == 31) buf[warp] = x;
     __syncthreads();
-    uint32_t before = 0, t = 0;
-#pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
-        const uint32_t w = buf[i];
-        before += i < warp ? w : 0u;
-        t += w;
-    }
-    *total = t;
-    return before + x - v;
+    // lane i reads warp i's sum: one load and two warp reductions, not a
+    // loop of kWarps dependent loads
+    const uint32_t w = lane < kWarps ? buf[lane] : 0u;
+    *total = __reduce_add_sync(0xFFFFFFFFu, w);
+    return __reduce_add_sync(0xFFFFFFFFu, lane < warp ? w : 0u) + x - v;
 }
 
 __device__ __forceinline__ void zero_bins(Scratch &sc, int nb)
@@ -105,29 +112,51 @@ __device__ __forceinline__ void zero_bins(Scratch &sc, int nb)
 
 // With sc.hist holding nb bins: the bin b holding the want-th largest key
 // (fewer than `want` keys in the bins above b, at least `want` in b and
-// above).  Thread t sums bins [nb - (t+1)*per, nb - t*per), read in an order
-// rotated by t so that a warp's lanes hit different banks.  Sets *bin and
-// *above (the count in the bins above it), the same in every thread.
+// above).  Thread t sums bins [nb - (t+1)*per, nb - t*per): with 4,096 bins,
+// its 8 bins in two 16-byte loads, kept in registers for the owner's search;
+// otherwise one by one, in an order rotated by t so that a warp's lanes hit
+// different banks.  Sets *bin and *above (the count in the bins above it),
+// the same in every thread.
 __device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uint32_t *bin, uint32_t *above, int &sb)
 {
     const int tid = threadIdx.x;
     const int per = nb >= kThreads ? nb / kThreads : 1;
     const int bhi = nb - tid * per, blo = bhi - per;
+    uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     uint32_t ssum = 0;
-    if (blo >= 0)
+    if (per == 8) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(&sc.hist[blo]);
+        const uint4 b = *reinterpret_cast<const uint4 *>(&sc.hist[blo + 4]);
+        h[0] = a.x, h[1] = a.y, h[2] = a.z, h[3] = a.w, h[4] = b.x, h[5] = b.y, h[6] = b.z, h[7] = b.w;
+        ssum = ((h[0] + h[1]) + (h[2] + h[3])) + ((h[4] + h[5]) + (h[6] + h[7]));
+    } else if (blo >= 0) {
         for (int j = 0; j < per; ++j) ssum += sc.hist[blo + ((j + tid) & (per - 1))];
+    }
     uint32_t tot;
     const uint32_t excl = block_scan(ssum, sc, &tot, sb);
     if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
         uint32_t cum = excl;
-        for (int bb = bhi - 1; bb >= blo; --bb) {
-            const uint32_t h = sc.hist[bb];
-            if (cum + h >= want) {
-                sc.res_bin = static_cast<uint32_t>(bb);
-                sc.res_above = cum;
-                break;
+        if (per == 8) {
+            bool found = false;
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                if (!found && cum + h[i] >= want) {
+                    sc.res_bin = static_cast<uint32_t>(blo + i);
+                    sc.res_above = cum;
+                    found = true;
+                }
+                cum += found ? 0u : h[i];
             }
-            cum += h;
+        } else {
+            for (int bb = bhi - 1; bb >= blo; --bb) {
+                const uint32_t hb = sc.hist[bb];
+                if (cum + hb >= want) {
+                    sc.res_bin = static_cast<uint32_t>(bb);
+                    sc.res_above = cum;
+                    break;
+                }
+                cum += hb;
+            }
         }
     }
     __syncthreads();
@@ -135,14 +164,134 @@ __device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uin
     *above = sc.res_above;
 }
 
+// The search for the K-th largest key over v = key - base: the bits of v
+// above `hi` are fixed to `prefix`, and `above` keys lie above them (all of
+// them kept).  Once done, the rule is: keep keys > thr_gt, and the first
+// `need` keys == thr_eq in candidate order.
+struct Cut {
+    uint32_t prefix = 0, above = 0, in_bin = 0;
+    int hi = 0;
+    bool done = false;
+    uint32_t thr_gt = 0, thr_eq = 0, need = 0;
+};
+
+// A. Histogram passes over a thread's M keys (those >= base whose bits above
+// hi match the prefix), until the rule is found or the threshold bin holds at
+// most kListMax keys.  The first pass's bins are zero on entry, ordered by a
+// CTA barrier.
+template <int M>
+__device__ __forceinline__ void passes(const uint32_t (&ks)[M], uint32_t base, uint32_t K, Cut &c, Scratch &sc,
+                                       int &sb)
+{
+    for (int pass = 0;; ++pass) {
+        if (c.hi == 0) {  // one key value left
+            c.thr_gt = c.thr_eq = base + c.prefix;
+            c.need = K - c.above;
+            c.done = true;
+            return;
+        }
+        const int d = c.hi < kBinBits ? c.hi : kBinBits, lo = c.hi - d, nb = 1 << d;
+        if (pass) {
+            __syncthreads();  // every thread has read the last pass's bins
+            zero_bins(sc, nb);
+            __syncthreads();
+        }
+        const uint32_t mask = c.hi >= 32 ? 0u : (0xFFFFFFFFu << c.hi);
+        const uint32_t pfx = c.hi >= 32 ? 0u : (c.prefix << c.hi);
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+            const uint32_t v = ks[j] - base;
+            if (ks[j] >= base && (v & mask) == pfx) atomicAdd(&sc.hist[(v >> lo) & (nb - 1)], 1u);
+        }
+        __syncthreads();
+        uint32_t bin, ab;
+        find_bin(nb, K - c.above, sc, &bin, &ab, sb);
+        c.above += ab;
+        const uint32_t in_bin = sc.hist[bin];
+        const uint32_t P = (c.prefix << d) | bin;
+        if (in_bin == K - c.above) {  // the bin is taken whole
+            c.thr_gt = base + (P << lo) - 1u;
+            c.done = true;
+            return;
+        }
+        if (lo == 0) {  // the bin is one key value
+            c.thr_gt = c.thr_eq = base + P;
+            c.need = K - c.above;
+            c.done = true;
+            return;
+        }
+        c.prefix = P;
+        c.hi = lo;
+        c.in_bin = in_bin;
+        if (in_bin <= kListMax) return;
+    }
+}
+
+// B. The threshold bin's keys ((key - base) >> hi == prefix, 1 <= hi < 32)
+// gathered into the list in candidate order; returns their number.
+template <int M, class Cand>
+__device__ __forceinline__ uint32_t gather(const uint32_t (&ks)[M], Cand cand, uint32_t base, const Cut &c,
+                                           Scratch &sc, int &sb)
+{
+    uint32_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < M; ++j) mine += (ks[j] >= base && ((ks[j] - base) >> c.hi) == c.prefix) ? 1u : 0u;
+    uint32_t m;
+    uint32_t off = block_scan(mine, sc, &m, sb);
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+        if (ks[j] >= base && ((ks[j] - base) >> c.hi) == c.prefix) {
+            sc.lk[off] = ks[j];
+            sc.lc[off] = cand(j);
+            ++off;
+        }
+    __syncthreads();
+    return m;
+}
+
+// Output: the kept candidates of a thread's M keys (key j is candidate
+// cand(j); a thread's keys are consecutive in candidate order, and threads in
+// order), positions from one scan of (kept, ties) counts.  Ends with a barrier.
+template <int M, class Cand>
+__device__ __forceinline__ void write_kept(const uint32_t (&ks)[M], Cand cand, const Cut &c, int32_t *obuf,
+                                           Scratch &sc, int &sb)
+{
+    uint32_t sel = 0, tie = 0;
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+        sel |= (ks[j] > c.thr_gt ? 1u : 0u) << j;
+        tie |= (c.need && ks[j] == c.thr_eq ? 1u : 0u) << j;
+    }
+    uint32_t tot2;
+    const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(sel)) << 16) | static_cast<uint32_t>(__popc(tie)), sc,
+                                   &tot2, sb);
+    const uint32_t a_before = ex >> 16, t_before = ex & 0xFFFFu;
+    if (c.need) {
+        // the first `need` ties in candidate order are kept
+        uint32_t take = c.need > t_before ? c.need - t_before : 0u;
+        uint32_t tb = tie;
+        while (take && tb) {
+            sel |= tb & (~tb + 1u);
+            tb &= tb - 1u;
+            --take;
+        }
+    }
+    uint32_t pos = a_before + min(t_before, c.need);
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+        if (sel & (1u << j)) obuf[pos++] = cand(j);
+    __syncthreads();
+}
+
 // The K largest of the keys of candidates [0, n), n <= kMaxKeys, read from
 // keys[key_slot(c)].  Writes the kept candidates' indices in ascending order
-// to obuf[0, kept) and returns kept = min(K, number of non-zero keys).  obuf
-// may be the key array itself (every key is in registers before the first
-// write).  Called by all kThreads threads, after a CTA barrier that follows
-// the keys' stores (and any earlier use of the scratch); ends with a CTA
-// barrier (obuf is then complete).
-__device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t K, int32_t *obuf, Scratch &sc)
+// to obuf[0, kept) and returns kept = min(K, number of non-zero keys).  keys
+// is kMaxKeys entries of shared memory that the selection may overwrite
+// (every key is in registers before the first write); obuf may be the key
+// array itself.  Called by all kThreads threads, after a CTA barrier that
+// follows the keys' stores (and any earlier use of the scratch); ends with a
+// CTA barrier (obuf is then complete).
+__device__ __forceinline__ int select_keys(uint32_t *keys, int n, uint32_t K, int32_t *obuf, Scratch &sc)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c0 = tid * kPerThread;
@@ -187,103 +336,80 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
     }
     zero_bins(sc, kBins);  // the first pass's bins, ordered before it by the barrier below
     __syncthreads();
-    kmin = 0xFFFFFFFFu;
-    kmax = 0;
-    gmin = 0xFFFFFFFFu;
-    uint32_t total = 0;
-    gcnt = 0;
-#pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
-        kmin = min(kmin, sc.wa[i]);
-        kmax = max(kmax, sc.wb[i]);
-        total += sc.wc[i];
-        gmin = min(gmin, sc.wd[i]);
-        gcnt += sc.we[i];
-    }
+    // lane i reads warp i's values (kWarps <= 32)
+    const bool wl = lane < kWarps;
+    kmin = __reduce_min_sync(0xFFFFFFFFu, wl ? sc.wa[lane] : 0xFFFFFFFFu);
+    kmax = __reduce_max_sync(0xFFFFFFFFu, wl ? sc.wb[lane] : 0u);
+    const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, wl ? sc.wc[lane] : 0u);
+    gmin = __reduce_min_sync(0xFFFFFFFFu, wl ? sc.wd[lane] : 0xFFFFFFFFu);
+    gcnt = __reduce_add_sync(0xFFFFFFFFu, wl ? sc.we[lane] : 0u);
     // Keys below base are never kept; every non-zero key is >= kmin >= 1, so
     // "key >= base" also excludes the empty candidates.
     const uint32_t base = gcnt >= K ? gmin : kmin;
+    auto own = [&](int j) { return c0 + j; };
 
-    // The rule: keep keys > thr_gt, and the first `need` keys == thr_eq.
-    uint32_t thr_gt = 0, thr_eq = 0, need = 0;
+    Cut c;
     int sb = 0;  // block_scan's buffer
+    bool listed = false;                                 // the keys >= base are in the big list
+    uint32_t e[kBigPer] = {};                            // this thread's entries of it
+    int32_t ec[kBigPer] = {};                            // and their candidates
+    auto from_list = [&](int j) { return ec[j]; };
     if (total > K) {
-        // v = key - base; the bits of v above `hi` are fixed to `prefix`, and
-        // `above` keys lie above them (all of them kept).
         const uint32_t range = kmax - base;
-        int hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
-        uint32_t prefix = 0, above = 0;
-        bool done = false;
-        int passes = 0;
-        // A. passes over all keys until the threshold bin holds <= kListMax keys
-        while (true) {
-            if (hi == 0) {  // one key value left
-                thr_gt = thr_eq = base + prefix;
-                need = K - above;
-                done = true;
-                break;
-            }
-            const int d = hi < kBinBits ? hi : kBinBits, lo = hi - d, nb = 1 << d;
-            if (passes++) {
-                __syncthreads();  // every thread has read the last pass's bins
-                zero_bins(sc, nb);
-                __syncthreads();
-            }
-            const uint32_t mask = hi >= 32 ? 0u : (0xFFFFFFFFu << hi);
-            const uint32_t pfx = hi >= 32 ? 0u : (prefix << hi);
+        c.hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
+        // The keys >= base, if few, move into the big list in candidate order
+        // (over the key array: every key is in registers), kBigPer entries a
+        // thread, and the passes run over those instead of over 32 keys a
+        // thread of which most lie below base.
+        uint32_t mine = 0;
 #pragma unroll
-            for (int j = 0; j < kPerThread; ++j) {
-                const uint32_t v = kk[j] - base;
-                if (kk[j] >= base && (v & mask) == pfx) atomicAdd(&sc.hist[(v >> lo) & (nb - 1)], 1u);
-            }
-            __syncthreads();
-            uint32_t bin, ab;
-            find_bin(nb, K - above, sc, &bin, &ab, sb);
-            above += ab;
-            const uint32_t in_bin = sc.hist[bin];
-            const uint32_t P = (prefix << d) | bin;
-            if (in_bin == K - above) {  // the bin is taken whole
-                thr_gt = base + (P << lo) - 1u;
-                done = true;
-                break;
-            }
-            if (lo == 0) {  // the bin is one key value
-                thr_gt = thr_eq = base + P;
-                need = K - above;
-                done = true;
-                break;
-            }
-            prefix = P;
-            hi = lo;
-            if (in_bin <= kListMax) break;
-        }
-        if (!done) {
-            // B. gather the bin's keys ((v >> hi) == prefix, 1 <= hi < 32) into
-            // the list, in candidate order
-            uint32_t mine = 0;
+        for (int j = 0; j < kPerThread; ++j) mine += kk[j] >= base ? 1u : 0u;
+        uint32_t nb_list;
+        uint32_t off = block_scan(mine, sc, &nb_list, sb);
+        listed = nb_list <= static_cast<uint32_t>(kBigList);
+        if (listed) {
+            uint32_t *bk = keys;
+            int32_t *bc = reinterpret_cast<int32_t *>(keys + kBigList);
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j)
-                mine += (kk[j] >= base && ((kk[j] - base) >> hi) == prefix) ? 1u : 0u;
-            uint32_t m;
-            uint32_t off = block_scan(mine, sc, &m, sb);
-#pragma unroll
-            for (int j = 0; j < kPerThread; ++j)
-                if (kk[j] >= base && ((kk[j] - base) >> hi) == prefix) {
-                    sc.lk[off] = kk[j];
-                    sc.lc[off] = c0 + j;
+                if (kk[j] >= base) {
+                    bk[off] = kk[j];
+                    bc[off] = c0 + j;
                     ++off;
                 }
             __syncthreads();
+            const int i0 = tid * kBigPer;
+#pragma unroll
+            for (int q = 0; q < kBigPer / 4; ++q) {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(bk + i0 + 4 * q);
+                const int4 cv = *reinterpret_cast<const int4 *>(bc + i0 + 4 * q);
+                const uint32_t kq[4] = {kv.x, kv.y, kv.z, kv.w};
+                const int32_t cq[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const bool has = static_cast<uint32_t>(i0 + 4 * q + r) < nb_list;
+                    e[4 * q + r] = has ? kq[r] : 0u;
+                    ec[4 * q + r] = has ? cq[r] : 0;
+                }
+            }
+            passes<kBigPer>(e, base, K, c, sc, sb);
+        } else {
+            passes<kPerThread>(kk, base, K, c, sc, sb);
+        }
+        if (!c.done) {
+            // B. gather the bin's keys into the list
+            uint32_t m = listed ? gather<kBigPer>(e, from_list, base, c, sc, sb)
+                                : gather<kPerThread>(kk, own, base, c, sc, sb);
             // C. passes over the list; thread t holds entries 2t and 2t + 1
-            uint32_t nd = K - above;  // keys still to keep, all in the list
+            uint32_t nd = K - c.above;  // keys still to keep, all in the list
             while (static_cast<int>(m) > kRankMax) {
-                if (hi == 0) {  // one key value left
-                    thr_gt = thr_eq = base + prefix;
-                    need = nd;
-                    done = true;
+                if (c.hi == 0) {  // one key value left
+                    c.thr_gt = c.thr_eq = base + c.prefix;
+                    c.need = nd;
+                    c.done = true;
                     break;
                 }
-                const int d = hi < kBinBits ? hi : kBinBits, lo = hi - d, nb = 1 << d;
+                const int d = c.hi < kBinBits ? c.hi : kBinBits, lo = c.hi - d, nb = 1 << d;
                 const int i0 = 2 * tid, i1 = 2 * tid + 1;
                 const bool h0 = i0 < static_cast<int>(m), h1 = i1 < static_cast<int>(m);
                 const uint32_t e0 = h0 ? sc.lk[i0] : 0u, e1 = h1 ? sc.lk[i1] : 0u;
@@ -298,17 +424,17 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                 find_bin(nb, nd, sc, &bin, &ab, sb);
                 nd -= ab;
                 const uint32_t in_bin = sc.hist[bin];
-                const uint32_t P = (prefix << d) | bin;
+                const uint32_t P = (c.prefix << d) | bin;
                 if (in_bin == nd) {
-                    thr_gt = base + (P << lo) - 1u;
-                    need = 0;
-                    done = true;
+                    c.thr_gt = base + (P << lo) - 1u;
+                    c.need = 0;
+                    c.done = true;
                     break;
                 }
                 if (lo == 0) {
-                    thr_gt = thr_eq = base + P;
-                    need = nd;
-                    done = true;
+                    c.thr_gt = c.thr_eq = base + P;
+                    c.need = nd;
+                    c.done = true;
                     break;
                 }
                 // keep the bin's entries, in order (each thread's entries were
@@ -325,10 +451,10 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                     sc.lc[o] = ec1;
                 }
                 __syncthreads();
-                prefix = P;
-                hi = lo;
+                c.prefix = P;
+                c.hi = lo;
             }
-            if (!done) {
+            if (!c.done) {
                 // D. rank the m <= 32 listed keys in one warp; the nd-th
                 // largest, V, sets the rule: keys > V, and the first
                 // nd - (listed keys > V) keys equal to V (every key equal to V
@@ -353,42 +479,18 @@ __device__ __forceinline__ int select_keys(const uint32_t *keys, int n, uint32_t
                     }
                 }
                 __syncthreads();
-                thr_gt = sc.thr_gt;
-                thr_eq = sc.thr_eq;
-                need = sc.need;
+                c.thr_gt = sc.thr_gt;
+                c.thr_eq = sc.thr_eq;
+                c.need = sc.need;
             }
         }
     }
 
-    // Output: this thread's kept candidates (bit j = candidate c0 + j), the
-    // positions from one scan of (kept, ties) counts.
-    uint32_t sel = 0, tie = 0;
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        sel |= (kk[j] > thr_gt ? 1u : 0u) << j;
-        tie |= (need && kk[j] == thr_eq ? 1u : 0u) << j;
-    }
-    uint32_t tot2;
-    const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(sel)) << 16) | static_cast<uint32_t>(__popc(tie)), sc,
-                                   &tot2, sb);
-    const uint32_t a_before = ex >> 16, t_before = ex & 0xFFFFu;
-    if (need) {
-        // the first `need` ties in candidate order are kept
-        uint32_t take = need > t_before ? need - t_before : 0u;
-        uint32_t tb = tie;
-        while (take && tb) {
-            sel |= tb & (~tb + 1u);
-            tb &= tb - 1u;
-            --take;
-        }
-    }
-    uint32_t pos = a_before + min(t_before, need);
-    while (sel) {
-        const int j = __ffs(static_cast<int>(sel)) - 1;
-        obuf[pos++] = c0 + j;
-        sel &= sel - 1u;
-    }
-    __syncthreads();
+    // Output: every kept key is >= base, so with the big list it alone holds them.
+    if (listed)
+        write_kept<kBigPer>(e, from_list, c, obuf, sc, sb);
+    else
+        write_kept<kPerThread>(kk, own, c, obuf, sc, sb);
     return static_cast<int>(total > K ? K : total);
 }
 
