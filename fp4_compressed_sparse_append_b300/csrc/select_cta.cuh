@@ -54,8 +54,8 @@ constexpr int kRankMax = 32;                     // list length ranked exactly b
 constexpr int kGroup = 8;                        // keys per group of the lower bound
 constexpr int kBigList = 4096;                   // keys >= the bound moved into one list, at most
 constexpr int kBigPer = kBigList / kThreads;     // its entries a thread
-static_assert(2 * kBigList <= kMaxKeys, "the big list's keys and candidates fit the key array");
-static_assert(kBigPer % 4 == 0, "a thread's list entries load as 16-byte pieces");
+static_assert(2 * kBigList <= kMaxKeys, "the big list's (key, candidate) pairs fit the key array");
+static_assert(kBigPer % 2 == 0, "a thread's list entries load as 16-byte pairs");
 constexpr int kWarps = kThreads / 32;
 static_assert(kWarps <= 32, "one lane per warp in the cross-warp reductions");
 static_assert(kListMax == 2 * kThreads, "list passes give each thread two entries");
@@ -368,29 +368,21 @@ __device__ __forceinline__ int select_keys(uint32_t *keys, int n, uint32_t K, in
         uint32_t off = block_scan(mine, sc, &nb_list, sb);
         listed = nb_list <= static_cast<uint32_t>(kBigList);
         if (listed) {
-            uint32_t *bk = keys;
-            int32_t *bc = reinterpret_cast<int32_t *>(keys + kBigList);
+            // entry i = (key, candidate) in one 8-byte store
+            uint2 *bl = reinterpret_cast<uint2 *>(keys);
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j)
-                if (kk[j] >= base) {
-                    bk[off] = kk[j];
-                    bc[off] = c0 + j;
-                    ++off;
-                }
+                if (kk[j] >= base) bl[off++] = make_uint2(kk[j], static_cast<uint32_t>(c0 + j));
             __syncthreads();
             const int i0 = tid * kBigPer;
 #pragma unroll
-            for (int q = 0; q < kBigPer / 4; ++q) {
-                const uint4 kv = *reinterpret_cast<const uint4 *>(bk + i0 + 4 * q);
-                const int4 cv = *reinterpret_cast<const int4 *>(bc + i0 + 4 * q);
-                const uint32_t kq[4] = {kv.x, kv.y, kv.z, kv.w};
-                const int32_t cq[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const bool has = static_cast<uint32_t>(i0 + 4 * q + r) < nb_list;
-                    e[4 * q + r] = has ? kq[r] : 0u;
-                    ec[4 * q + r] = has ? cq[r] : 0;
-                }
+            for (int q = 0; q < kBigPer / 2; ++q) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(bl + i0 + 2 * q);  // entries i0+2q, i0+2q+1
+                const bool h0 = static_cast<uint32_t>(i0 + 2 * q) < nb_list, h1 = static_cast<uint32_t>(i0 + 2 * q + 1) < nb_list;
+                e[2 * q] = h0 ? v.x : 0u;
+                ec[2 * q] = h0 ? static_cast<int32_t>(v.y) : 0;
+                e[2 * q + 1] = h1 ? v.z : 0u;
+                ec[2 * q + 1] = h1 ? static_cast<int32_t>(v.w) : 0;
             }
             passes<kBigPer>(e, base, K, c, sc, sb);
         } else {
