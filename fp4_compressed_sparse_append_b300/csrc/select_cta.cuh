@@ -283,6 +283,211 @@ __device__ __forceinline__ void write_kept(const uint32_t (&ks)[M], Cand cand, c
     __syncthreads();
 }
 
+// C and D on the m keys gathered from the threshold bin (the list): passes
+// over their next lower bits until at most kRankMax remain, then one warp
+// ranks those.  Sets the rule in c.
+__device__ __forceinline__ void list_rank(Cut &c, uint32_t m, uint32_t base, uint32_t K, Scratch &sc, int &sb)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // C. passes over the list; thread t holds entries 2t and 2t + 1
+    uint32_t nd = K - c.above;  // keys still to keep, all in the list
+    while (static_cast<int>(m) > kRankMax) {
+        if (c.hi == 0) {  // one key value left
+            c.thr_gt = c.thr_eq = base + c.prefix;
+            c.need = nd;
+            c.done = true;
+            break;
+        }
+        const int d = c.hi < kBinBits ? c.hi : kBinBits, lo = c.hi - d, nb = 1 << d;
+        const int i0 = 2 * tid, i1 = 2 * tid + 1;
+        const bool h0 = i0 < static_cast<int>(m), h1 = i1 < static_cast<int>(m);
+        const uint32_t e0 = h0 ? sc.lk[i0] : 0u, e1 = h1 ? sc.lk[i1] : 0u;
+        const int32_t ec0 = h0 ? sc.lc[i0] : 0, ec1 = h1 ? sc.lc[i1] : 0;
+        zero_bins(sc, nb);
+        __syncthreads();
+        const uint32_t b0 = ((e0 - base) >> lo) & (nb - 1), b1 = ((e1 - base) >> lo) & (nb - 1);
+        if (h0) atomicAdd(&sc.hist[b0], 1u);
+        if (h1) atomicAdd(&sc.hist[b1], 1u);
+        __syncthreads();
+        uint32_t bin, ab;
+        find_bin(nb, nd, sc, &bin, &ab, sb);
+        nd -= ab;
+        const uint32_t in_bin = sc.hist[bin];
+        const uint32_t P = (c.prefix << d) | bin;
+        if (in_bin == nd) {
+            c.thr_gt = base + (P << lo) - 1u;
+            c.need = 0;
+            c.done = true;
+            break;
+        }
+        if (lo == 0) {
+            c.thr_gt = c.thr_eq = base + P;
+            c.need = nd;
+            c.done = true;
+            break;
+        }
+        // keep the bin's entries, in order (each thread's entries were
+        // read before the scan's first barrier)
+        const bool k0 = h0 && b0 == bin, k1 = h1 && b1 == bin;
+        uint32_t o = block_scan((k0 ? 1u : 0u) + (k1 ? 1u : 0u), sc, &m, sb);
+        if (k0) {
+            sc.lk[o] = e0;
+            sc.lc[o] = ec0;
+            ++o;
+        }
+        if (k1) {
+            sc.lk[o] = e1;
+            sc.lc[o] = ec1;
+        }
+        __syncthreads();
+        c.prefix = P;
+        c.hi = lo;
+    }
+    if (!c.done) {
+        // D. rank the m <= 32 listed keys in one warp; the nd-th
+        // largest, V, sets the rule: keys > V, and the first
+        // nd - (listed keys > V) keys equal to V (every key equal to V
+        // is listed)
+        if (warp == 0) {
+            const bool has = lane < static_cast<int>(m);
+            const uint32_t key = has ? sc.lk[lane] : 0u;
+            const int32_t cand = has ? sc.lc[lane] : 0;
+            uint32_t r = 0;
+            for (int i = 0; i < static_cast<int>(m); ++i) {
+                const uint32_t o = __shfl_sync(0xFFFFFFFFu, key, i);
+                const int32_t oc = __shfl_sync(0xFFFFFFFFu, cand, i);
+                r += (o > key || (o == key && oc < cand)) ? 1u : 0u;
+            }
+            const unsigned at = __ballot_sync(0xFFFFFFFFu, has && r == nd - 1u);
+            const uint32_t V = __shfl_sync(0xFFFFFFFFu, key, __ffs(static_cast<int>(at)) - 1);
+            const uint32_t gt = __reduce_add_sync(0xFFFFFFFFu, (has && key > V) ? 1u : 0u);
+            if (lane == 0) {
+                sc.thr_gt = V;
+                sc.thr_eq = V;
+                sc.need = nd - gt;
+            }
+        }
+        __syncthreads();
+        c.thr_gt = sc.thr_gt;
+        c.thr_eq = sc.thr_eq;
+        c.need = sc.need;
+    }
+}
+
+// The selection over the keys left in shared memory (keys[key_slot(c)]),
+// in rolled loops: when more than kBigList keys reach the bound, or when every
+// key is kept.  Out of line, so that the common path's code stays short.
+// Called by all threads, after a CTA barrier; the first pass's bins are zero.
+static __device__ __noinline__ int select_keys_smem(const uint32_t *keys, int n, uint32_t K, uint32_t base, uint32_t kmax,
+                                             uint32_t total, int32_t *obuf, Scratch &sc, int sb)
+{
+    const int tid = threadIdx.x;
+    const int c0 = tid * kPerThread;
+    auto key = [&](int j) {
+        const int cand = c0 + j;
+        return cand < n ? keys[key_slot(cand)] : 0u;
+    };
+    Cut c;
+    if (total > K) {
+        const uint32_t range = kmax - base;
+        c.hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
+        // A. passes over all keys until the threshold bin holds <= kListMax
+        for (int pass = 0;; ++pass) {
+            if (c.hi == 0) {  // one key value left
+                c.thr_gt = c.thr_eq = base + c.prefix;
+                c.need = K - c.above;
+                c.done = true;
+                break;
+            }
+            const int d = c.hi < kBinBits ? c.hi : kBinBits, lo = c.hi - d, nb = 1 << d;
+            if (pass) {
+                __syncthreads();  // every thread has read the last pass's bins
+                zero_bins(sc, nb);
+                __syncthreads();
+            }
+            const uint32_t mask = c.hi >= 32 ? 0u : (0xFFFFFFFFu << c.hi);
+            const uint32_t pfx = c.hi >= 32 ? 0u : (c.prefix << c.hi);
+#pragma unroll 1
+            for (int j = 0; j < kPerThread; ++j) {
+                const uint32_t k = key(j), v = k - base;
+                if (k >= base && (v & mask) == pfx) atomicAdd(&sc.hist[(v >> lo) & (nb - 1)], 1u);
+            }
+            __syncthreads();
+            uint32_t bin, ab;
+            find_bin(nb, K - c.above, sc, &bin, &ab, sb);
+            c.above += ab;
+            const uint32_t in_bin = sc.hist[bin];
+            const uint32_t P = (c.prefix << d) | bin;
+            if (in_bin == K - c.above) {  // the bin is taken whole
+                c.thr_gt = base + (P << lo) - 1u;
+                c.done = true;
+                break;
+            }
+            if (lo == 0) {  // the bin is one key value
+                c.thr_gt = c.thr_eq = base + P;
+                c.need = K - c.above;
+                c.done = true;
+                break;
+            }
+            c.prefix = P;
+            c.hi = lo;
+            if (in_bin <= kListMax) break;
+        }
+        if (!c.done) {
+            // B. the bin's keys into the list, in candidate order
+            uint32_t mine = 0;
+#pragma unroll 1
+            for (int j = 0; j < kPerThread; ++j) {
+                const uint32_t k = key(j);
+                mine += (k >= base && ((k - base) >> c.hi) == c.prefix) ? 1u : 0u;
+            }
+            uint32_t m;
+            uint32_t off = block_scan(mine, sc, &m, sb);
+#pragma unroll 1
+            for (int j = 0; j < kPerThread; ++j) {
+                const uint32_t k = key(j);
+                if (k >= base && ((k - base) >> c.hi) == c.prefix) {
+                    sc.lk[off] = k;
+                    sc.lc[off] = c0 + j;
+                    ++off;
+                }
+            }
+            __syncthreads();
+            list_rank(c, m, base, K, sc, sb);
+        }
+    }
+    // Output (every key read before the scan's barrier, so obuf may be the
+    // key array)
+    uint32_t sel = 0, tie = 0;
+#pragma unroll 1
+    for (int j = 0; j < kPerThread; ++j) {
+        const uint32_t k = key(j);
+        sel |= (k > c.thr_gt ? 1u : 0u) << j;
+        tie |= (c.need && k == c.thr_eq ? 1u : 0u) << j;
+    }
+    uint32_t tot2;
+    const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(sel)) << 16) | static_cast<uint32_t>(__popc(tie)), sc,
+                                   &tot2, sb);
+    const uint32_t a_before = ex >> 16, t_before = ex & 0xFFFFu;
+    if (c.need) {
+        uint32_t take = c.need > t_before ? c.need - t_before : 0u;
+        uint32_t tb = tie;
+        while (take && tb) {
+            sel |= tb & (~tb + 1u);
+            tb &= tb - 1u;
+            --take;
+        }
+    }
+    uint32_t pos = a_before + min(t_before, c.need);
+    while (sel) {
+        const int j = __ffs(static_cast<int>(sel)) - 1;
+        obuf[pos++] = c0 + j;
+        sel &= sel - 1u;
+    }
+    __syncthreads();
+    return static_cast<int>(total > K ? K : total);
+}
+
 // The K largest of the keys of candidates [0, n), n <= kMaxKeys, read from
 // keys[key_slot(c)].  Writes the kept candidates' indices in ascending order
 // to obuf[0, kept) and returns kept = min(K, number of non-zero keys).  keys
@@ -346,17 +551,8 @@ __device__ __forceinline__ int select_keys(uint32_t *keys, int n, uint32_t K, in
     // Keys below base are never kept; every non-zero key is >= kmin >= 1, so
     // "key >= base" also excludes the empty candidates.
     const uint32_t base = gcnt >= K ? gmin : kmin;
-    auto own = [&](int j) { return c0 + j; };
-
-    Cut c;
     int sb = 0;  // block_scan's buffer
-    bool listed = false;                                 // the keys >= base are in the big list
-    uint32_t e[kBigPer] = {};                            // this thread's entries of it
-    int32_t ec[kBigPer] = {};                            // and their candidates
-    auto from_list = [&](int j) { return ec[j]; };
     if (total > K) {
-        const uint32_t range = kmax - base;
-        c.hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
         // The keys >= base, if few, move into the big list in candidate order
         // (over the key array: every key is in registers), kBigPer entries a
         // thread, and the passes run over those instead of over 32 keys a
@@ -366,14 +562,15 @@ __device__ __forceinline__ int select_keys(uint32_t *keys, int n, uint32_t K, in
         for (int j = 0; j < kPerThread; ++j) mine += kk[j] >= base ? 1u : 0u;
         uint32_t nb_list;
         uint32_t off = block_scan(mine, sc, &nb_list, sb);
-        listed = nb_list <= static_cast<uint32_t>(kBigList);
-        if (listed) {
+        if (nb_list <= static_cast<uint32_t>(kBigList)) {
             // entry i = (key, candidate) in one 8-byte store
             uint2 *bl = reinterpret_cast<uint2 *>(keys);
 #pragma unroll
             for (int j = 0; j < kPerThread; ++j)
                 if (kk[j] >= base) bl[off++] = make_uint2(kk[j], static_cast<uint32_t>(c0 + j));
             __syncthreads();
+            uint32_t e[kBigPer];   // this thread's entries of the list
+            int32_t ec[kBigPer];   // and their candidates
             const int i0 = tid * kBigPer;
 #pragma unroll
             for (int q = 0; q < kBigPer / 2; ++q) {
@@ -384,106 +581,18 @@ __device__ __forceinline__ int select_keys(uint32_t *keys, int n, uint32_t K, in
                 e[2 * q + 1] = h1 ? v.z : 0u;
                 ec[2 * q + 1] = h1 ? static_cast<int32_t>(v.w) : 0;
             }
+            auto from_list = [&](int j) { return ec[j]; };
+            Cut c;
+            const uint32_t range = kmax - base;
+            c.hi = range ? 32 - __clz(static_cast<int>(range)) : 0;
             passes<kBigPer>(e, base, K, c, sc, sb);
-        } else {
-            passes<kPerThread>(kk, base, K, c, sc, sb);
-        }
-        if (!c.done) {
-            // B. gather the bin's keys into the list
-            uint32_t m = listed ? gather<kBigPer>(e, from_list, base, c, sc, sb)
-                                : gather<kPerThread>(kk, own, base, c, sc, sb);
-            // C. passes over the list; thread t holds entries 2t and 2t + 1
-            uint32_t nd = K - c.above;  // keys still to keep, all in the list
-            while (static_cast<int>(m) > kRankMax) {
-                if (c.hi == 0) {  // one key value left
-                    c.thr_gt = c.thr_eq = base + c.prefix;
-                    c.need = nd;
-                    c.done = true;
-                    break;
-                }
-                const int d = c.hi < kBinBits ? c.hi : kBinBits, lo = c.hi - d, nb = 1 << d;
-                const int i0 = 2 * tid, i1 = 2 * tid + 1;
-                const bool h0 = i0 < static_cast<int>(m), h1 = i1 < static_cast<int>(m);
-                const uint32_t e0 = h0 ? sc.lk[i0] : 0u, e1 = h1 ? sc.lk[i1] : 0u;
-                const int32_t ec0 = h0 ? sc.lc[i0] : 0, ec1 = h1 ? sc.lc[i1] : 0;
-                zero_bins(sc, nb);
-                __syncthreads();
-                const uint32_t b0 = ((e0 - base) >> lo) & (nb - 1), b1 = ((e1 - base) >> lo) & (nb - 1);
-                if (h0) atomicAdd(&sc.hist[b0], 1u);
-                if (h1) atomicAdd(&sc.hist[b1], 1u);
-                __syncthreads();
-                uint32_t bin, ab;
-                find_bin(nb, nd, sc, &bin, &ab, sb);
-                nd -= ab;
-                const uint32_t in_bin = sc.hist[bin];
-                const uint32_t P = (c.prefix << d) | bin;
-                if (in_bin == nd) {
-                    c.thr_gt = base + (P << lo) - 1u;
-                    c.need = 0;
-                    c.done = true;
-                    break;
-                }
-                if (lo == 0) {
-                    c.thr_gt = c.thr_eq = base + P;
-                    c.need = nd;
-                    c.done = true;
-                    break;
-                }
-                // keep the bin's entries, in order (each thread's entries were
-                // read before the scan's first barrier)
-                const bool k0 = h0 && b0 == bin, k1 = h1 && b1 == bin;
-                uint32_t o = block_scan((k0 ? 1u : 0u) + (k1 ? 1u : 0u), sc, &m, sb);
-                if (k0) {
-                    sc.lk[o] = e0;
-                    sc.lc[o] = ec0;
-                    ++o;
-                }
-                if (k1) {
-                    sc.lk[o] = e1;
-                    sc.lc[o] = ec1;
-                }
-                __syncthreads();
-                c.prefix = P;
-                c.hi = lo;
-            }
-            if (!c.done) {
-                // D. rank the m <= 32 listed keys in one warp; the nd-th
-                // largest, V, sets the rule: keys > V, and the first
-                // nd - (listed keys > V) keys equal to V (every key equal to V
-                // is listed)
-                if (warp == 0) {
-                    const bool has = lane < static_cast<int>(m);
-                    const uint32_t key = has ? sc.lk[lane] : 0u;
-                    const int32_t cand = has ? sc.lc[lane] : 0;
-                    uint32_t r = 0;
-                    for (int i = 0; i < static_cast<int>(m); ++i) {
-                        const uint32_t o = __shfl_sync(0xFFFFFFFFu, key, i);
-                        const int32_t oc = __shfl_sync(0xFFFFFFFFu, cand, i);
-                        r += (o > key || (o == key && oc < cand)) ? 1u : 0u;
-                    }
-                    const unsigned at = __ballot_sync(0xFFFFFFFFu, has && r == nd - 1u);
-                    const uint32_t V = __shfl_sync(0xFFFFFFFFu, key, __ffs(static_cast<int>(at)) - 1);
-                    const uint32_t gt = __reduce_add_sync(0xFFFFFFFFu, (has && key > V) ? 1u : 0u);
-                    if (lane == 0) {
-                        sc.thr_gt = V;
-                        sc.thr_eq = V;
-                        sc.need = nd - gt;
-                    }
-                }
-                __syncthreads();
-                c.thr_gt = sc.thr_gt;
-                c.thr_eq = sc.thr_eq;
-                c.need = sc.need;
-            }
+            if (!c.done) list_rank(c, gather<kBigPer>(e, from_list, base, c, sc, sb), base, K, sc, sb);
+            // Output: every kept key is >= base, so the list alone holds them.
+            write_kept<kBigPer>(e, from_list, c, obuf, sc, sb);
+            return static_cast<int>(K);
         }
     }
-
-    // Output: every kept key is >= base, so with the big list it alone holds them.
-    if (listed)
-        write_kept<kBigPer>(e, from_list, c, obuf, sc, sb);
-    else
-        write_kept<kPerThread>(kk, own, c, obuf, sc, sb);
-    return static_cast<int>(total > K ? K : total);
+    return select_keys_smem(keys, n, K, base, kmax, total, obuf, sc, sb);
 }
 
 }  // namespace cta_select
