@@ -143,6 +143,10 @@ struct AttSmem {
     int abort;
 };
 
+// SWA: one split attends to the local window; CLUSTER: the splits of a query
+// form a cluster and merge on chip.  Each combination is its own kernel, so
+// the others' code is not in it.
+template <bool SWA, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_constant__ CUtensorMap qmap, AttArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     const int vunit = blockIdx.y, unit = vunit / a.G, split = blockIdx.x;
     const int b = unit / a.P;
     int len = 0;
-    const bool win = split == a.swa_split;
+    const bool win = SWA && split == a.swa_split;
     const int32_t *irow = a.idx + static_cast<int64_t>(unit) * a.K;
     const int mma_warp = kSoftWarps + kGatherWarps;
 
@@ -553,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             sm.l_fin[h] = l_run;
             sm.m_fin[h] = m_run;
         }
-        if (lane < 16 && active && !a.cluster) {
+        if (lane < 16 && active && !CLUSTER) {
             if (a.nsplit == 1) {
                 if (a.lse)
                     a.lse[static_cast<int64_t>(vunit) * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
@@ -576,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             const int q4 = warp & 3, grp = warp >> 2, ngrp = mma_warp / 4;
             const uint32_t loff = static_cast<uint32_t>(q4 * 32) << 16;
             const int nc16 = NH / 16, items = (D / 128) * nc16;
-            const bool final_out = a.nsplit == 1 && !a.cluster;
+            const bool final_out = a.nsplit == 1 && !CLUSTER;
             float *obuf = reinterpret_cast<float *>(v_s);
             float *obase = final_out ? a.out + static_cast<int64_t>(vunit) * H * D
                                      : a.part_o + (static_cast<int64_t>(vunit) * a.nsplit + split) * H * D;
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                     const int hh = c0 + k;
                     if (hh >= H) break;
                     float v = n_tiles > 0 ? __uint_as_float(r[k]) : 0.f;
-                    if (a.cluster) {
+                    if (CLUSTER) {
                         obuf[hh * D + d] = v;
                     } else {
                         if (final_out) {
@@ -607,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
 
     tc_fence_before();
     __syncthreads();
-    if (a.cluster) {
+    if (CLUSTER) {
         // Every split's O, m and l are in its shared memory after this barrier;
         // each CTA merges dims [d0, d1) of every head over the splits.
         namespace cg = cooperative_groups;
@@ -800,8 +804,9 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     const Plan p = plan(c, P, H, K, swa);
     const int Hg = H / p.G;  // heads per CTA
     const size_t smem = smem_bytes(c.D, (Hg + 15) / 16 * 16);
-    cudaError_t e =
-        cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    auto kernel = swa ? (p.cluster ? attend_kernel<true, true> : attend_kernel<true, false>)
+                      : (p.cluster ? attend_kernel<false, true> : attend_kernel<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (ws_bytes < attend_workspace_bytes(c, P, H, K, swa)) return cudaErrorInvalidValue;
     AttArgs a{};
@@ -839,7 +844,7 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     if (encode_tensor_map_2d_u8(&qm, q, static_cast<uint64_t>(c.D) * 2, static_cast<uint64_t>(units) * H, 128,
                                 a.NH, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    e = launch_kernel(attend_kernel, dim3(p.nsplit, units * p.G), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0,
+    e = launch_kernel(kernel, dim3(p.nsplit, units * p.G), dim3(kThreads), smem, st, p.cluster ? p.nsplit : 0,
                       qm, a);
     if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
     // The merge loads every split's value at once: 16 or 32 registers.

@@ -283,14 +283,20 @@ __device__ __forceinline__ void write_kept(const uint32_t (&ks)[M], Cand cand, c
     __syncthreads();
 }
 
-// C and D on the m keys gathered from the threshold bin (the list): passes
-// over their next lower bits until at most kRankMax remain, then one warp
-// ranks those.  Sets the rule in c.
-__device__ __forceinline__ void list_rank(Cut &c, uint32_t m, uint32_t base, uint32_t K, Scratch &sc, int &sb)
+// C. Passes over the list's next lower bits until at most kRankMax keys
+// remain (or the rule is found); thread t holds entries 2t and 2t + 1.  Out
+// of line: rare once the first pass spans [bound, maximum].
+struct ListState {
+    Cut c;
+    uint32_t m, nd;
+    int sb;
+};
+static __device__ __noinline__ ListState list_passes(ListState st, uint32_t base, Scratch &sc)
 {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // C. passes over the list; thread t holds entries 2t and 2t + 1
-    uint32_t nd = K - c.above;  // keys still to keep, all in the list
+    const int tid = threadIdx.x;
+    Cut &c = st.c;
+    uint32_t &m = st.m, &nd = st.nd;
+    int &sb = st.sb;
     while (static_cast<int>(m) > kRankMax) {
         if (c.hi == 0) {  // one key value left
             c.thr_gt = c.thr_eq = base + c.prefix;
@@ -342,6 +348,23 @@ __device__ __forceinline__ void list_rank(Cut &c, uint32_t m, uint32_t base, uin
         __syncthreads();
         c.prefix = P;
         c.hi = lo;
+    }
+    return st;
+}
+
+// C and D on the m keys gathered from the threshold bin (the list): passes
+// over their next lower bits until at most kRankMax remain, then one warp
+// ranks those.  Sets the rule in c.
+__device__ __forceinline__ void list_rank(Cut &c, uint32_t m, uint32_t base, uint32_t K, Scratch &sc, int &sb)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t nd = K - c.above;  // keys still to keep, all in the list
+    if (static_cast<int>(m) > kRankMax) {
+        const ListState st = list_passes(ListState{c, m, nd, sb}, base, sc);
+        c = st.c;
+        m = st.m;
+        nd = st.nd;
+        sb = st.sb;
     }
     if (!c.done) {
         // D. rank the m <= 32 listed keys in one warp; the nd-th
