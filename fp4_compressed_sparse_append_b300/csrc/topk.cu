@@ -386,45 +386,37 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelArgs a)
     uint32_t thr_gt = 0, thr_eq = 0, need = 0;
     const uint32_t total = find_bin(h0, kDigit0Bins, K, sh);
     if (total > K) {
-        const uint32_t d0 = sh.res_bin;
-        uint32_t above = sh.res_above;
-        if (h0[d0] == K - above) {
-            thr_gt = d0 ? (d0 << 20) - 1u : 0u;
-        } else {
-            __syncthreads();  // every thread has read h0 (the CTA's own histogram when alone)
-            zero_histogram(sh, kDigit1Bins);
+        // Digits of 12, 12 and 8 bits: after each, the key bits above `hi`
+        // are fixed to `prefix` and `above` keys lie above them.  One loop
+        // body serves the second and third digits (one copy of the code).
+        uint32_t prefix = sh.res_bin, above = sh.res_above;
+        const uint32_t *h = h0;
+        int hi = 20;
+        for (;;) {
+            const uint32_t in_bin = h[sh.res_bin];
+            if (in_bin == K - above) {  // the bin is taken whole
+                thr_gt = prefix ? (prefix << hi) - 1u : 0u;
+                break;
+            }
+            if (hi == 0) {  // prefix is one key value (>= 1: key 0 is never counted)
+                need = K - above;  // 1 <= need < in_bin
+                thr_gt = prefix;
+                thr_eq = prefix;
+                break;
+            }
+            const int d = hi > 8 ? 12 : 8, lo = hi - d, nb = 1 << d;
+            __syncthreads();  // every thread has read h (the CTA's own histogram when alone)
+            zero_histogram(sh, nb);
             __syncthreads();
             for (int i = tid; i < m; i += kSelThreads) {
                 const uint32_t k = cache[i];
-                if (k && (k >> 20) == d0) atomicAdd(&sh.hist_l[(k >> 8) & 0xFFFu], 1u);
+                if (k && (k >> hi) == prefix) atomicAdd(&sh.hist_l[(k >> lo) & static_cast<uint32_t>(nb - 1)], 1u);
             }
-            const uint32_t *h1 = reduce_histogram(sh, kDigit1Bins, C, rank);
-            find_bin(h1, kDigit1Bins, K - above, sh);
-            const uint32_t p24 = (d0 << 12) | sh.res_bin;
+            h = reduce_histogram(sh, nb, C, rank);
+            find_bin(h, nb, K - above, sh);
+            prefix = (prefix << d) | sh.res_bin;
             above += sh.res_above;
-            if (h1[sh.res_bin] == K - above) {
-                thr_gt = p24 ? (p24 << 8) - 1u : 0u;
-            } else {
-                __syncthreads();  // every thread has read h1 before the histogram is reused
-                zero_histogram(sh, kDigit2Bins);
-                __syncthreads();
-                for (int i = tid; i < m; i += kSelThreads) {
-                    const uint32_t k = cache[i];
-                    if (k && (k >> 8) == p24) atomicAdd(&sh.hist_l[k & 0xFFu], 1u);
-                }
-                const uint32_t *h2 = reduce_histogram(sh, kDigit2Bins, C, rank);
-                find_bin(h2, kDigit2Bins, K - above, sh);
-                const uint32_t t = (p24 << 8) | sh.res_bin;  // >= 1: key 0 is never counted
-                above += sh.res_above;
-                need = K - above;  // 1 <= need <= h2[res_bin]
-                if (need == h2[sh.res_bin]) {
-                    thr_gt = t - 1u;
-                    need = 0;
-                } else {
-                    thr_gt = t;
-                    thr_eq = t;
-                }
-            }
+            hi = lo;
         }
     }
 
