@@ -144,9 +144,11 @@ struct AttSmem {
 };
 
 // SWA: one split attends to the local window; CLUSTER: the splits of a query
-// form a cluster and merge on chip.  Each combination is its own kernel, so
-// the others' code is not in it.
-template <bool SWA, bool CLUSTER>
+// form a cluster and merge on chip; ONE: every split holds at most one tile
+// (no rescale of O, no next-tile gather).  Each combination is its own
+// kernel, so the others' code is not in it: a CTA runs its code once, and
+// code it carries but does not run still costs instruction fetches.
+template <bool SWA, bool CLUSTER, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_constant__ CUtensorMap qmap, AttArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
     }
     const int t_first = win ? 0 : split * a.tiles_per_split;
     const int t_last = win ? (w_hi - w_lo + kRows - 1) / kRows : min(a.tiles_total, t_first + a.tiles_per_split);
-    const int n_tiles = max(0, t_last - t_first);
+    const int n_tiles = ONE ? min(1, max(0, t_last - t_first)) : max(0, t_last - t_first);
 
     // Gather-warp state: the rows of tile i+1 are loaded while tile i is used;
     // thread (row gr, part gp) holds D/kParts channels of one FP4 row: nc
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                  mbar_wait(&sm.pempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            if (sm.flag[i & 1] == i + 1) {
+            if (!ONE && sm.flag[i & 1] == i + 1) {
                 // Rescale O^T: wait for O^T of tile i-1, then this warp's quarter of
                 // the lanes (dims) of every 128-dim block, all head columns.
                 if (!mbar_wait(&sm.pempty[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
@@ -804,8 +806,10 @@ cudaError_t launch_attend(const CacheView &c, int P, int H, const uint16_t *q, f
     const Plan p = plan(c, P, H, K, swa);
     const int Hg = H / p.G;  // heads per CTA
     const size_t smem = smem_bytes(c.D, (Hg + 15) / 16 * 16);
-    auto kernel = swa ? (p.cluster ? attend_kernel<true, true> : attend_kernel<true, false>)
-                      : (p.cluster ? attend_kernel<false, true> : attend_kernel<false, false>);
+    const bool one = !swa && p.tiles_per_split == 1;
+    auto kernel = swa ? (p.cluster ? attend_kernel<true, true, false> : attend_kernel<true, false, false>)
+                      : one ? (p.cluster ? attend_kernel<false, true, true> : attend_kernel<false, false, true>)
+                            : (p.cluster ? attend_kernel<false, true, false> : attend_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (ws_bytes < attend_workspace_bytes(c, P, H, K, swa)) return cudaErrorInvalidValue;
