@@ -486,14 +486,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 f = m_run == -INFINITY ? 0.f : fast_exp2(m_run - tmax);
                 m_run = tmax;
             }
-            if (lane < 16) sm.fac[i & 1][h] = f;
-            const bool mine = i > 0 && f != 1.f;
-            if (__any_sync(0xFFFFFFFFu, mine) && lane == 0) sm.flag[i & 1] = i + 1;
-            // Every softmax thread sees every head's factor and the flag; the P
-            // buffer of this tile is free once O^T of tile i-2 is done.
-            mbar_arrive(&sm.xbar);
-            ok = mbar_wait(&sm.xbar, i & 1, abort_flag) &&
-                 mbar_wait(&sm.pempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag);
+            if (!ONE) {
+                // Every softmax thread sees every head's factor and the flag
+                // (one tile: nothing is rescaled)
+                if (lane < 16) sm.fac[i & 1][h] = f;
+                const bool mine = i > 0 && f != 1.f;
+                if (__any_sync(0xFFFFFFFFu, mine) && lane == 0) sm.flag[i & 1] = i + 1;
+                mbar_arrive(&sm.xbar);
+                ok = mbar_wait(&sm.xbar, i & 1, abort_flag);
+            }
+            // the P buffer of this tile is free once O^T of tile i-2 is done
+            ok = ok && mbar_wait(&sm.pempty[i & 1], ((i >> 1) & 1) ^ 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             if (!ONE && sm.flag[i & 1] == i + 1) {
