@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
                 }
                 fence_async_smem();
                 mbar_arrive(&sm.vfull[i & 1]);
-                if (i + 1 < n_tiles) prefetch(t_first + i + 1);
+                if (!ONE && i + 1 < n_tiles) prefetch(t_first + i + 1);
                 continue;
             }
 #pragma unroll
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const __grid_consta
             }
             fence_async_smem();
             mbar_arrive(&sm.vfull[i & 1]);
-            if (i + 1 < n_tiles) prefetch(t_first + i + 1);
+            if (!ONE && i + 1 < n_tiles) prefetch(t_first + i + 1);
         }
     } else {
         // ------------------------------------------------------------ softmax warps

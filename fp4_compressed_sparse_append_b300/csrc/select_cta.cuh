@@ -110,53 +110,70 @@ __device__ __forceinline__ void zero_bins(Scratch &sc, int nb)
     }
 }
 
-// With sc.hist holding nb bins: the bin b holding the want-th largest key
-// (fewer than `want` keys in the bins above b, at least `want` in b and
-// above).  Thread t sums bins [nb - (t+1)*per, nb - t*per): with 4,096 bins,
-// its 8 bins in two 16-byte loads, kept in registers for the owner's search;
-// otherwise one by one, in an order rotated by t so that a warp's lanes hit
-// different banks.  Sets *bin and *above (the count in the bins above it),
-// the same in every thread.
-__device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uint32_t *bin, uint32_t *above, int &sb)
+// find_bin for fewer than 4,096 bins (later passes over short ranges): each
+// thread sums nb/kThreads bins (or one), read in an order rotated by the
+// thread so that a warp's lanes hit different banks.  Out of line: the first
+// pass of a selection uses 4,096 bins.
+static __device__ __noinline__ void find_bin_small(int nb, uint32_t want, Scratch &sc, int sb)
 {
     const int tid = threadIdx.x;
     const int per = nb >= kThreads ? nb / kThreads : 1;
     const int bhi = nb - tid * per, blo = bhi - per;
-    uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     uint32_t ssum = 0;
-    if (per == 8) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(&sc.hist[blo]);
-        const uint4 b = *reinterpret_cast<const uint4 *>(&sc.hist[blo + 4]);
-        h[0] = a.x, h[1] = a.y, h[2] = a.z, h[3] = a.w, h[4] = b.x, h[5] = b.y, h[6] = b.z, h[7] = b.w;
-        ssum = ((h[0] + h[1]) + (h[2] + h[3])) + ((h[4] + h[5]) + (h[6] + h[7]));
-    } else if (blo >= 0) {
+    if (blo >= 0)
         for (int j = 0; j < per; ++j) ssum += sc.hist[blo + ((j + tid) & (per - 1))];
-    }
     uint32_t tot;
     const uint32_t excl = block_scan(ssum, sc, &tot, sb);
     if (blo >= 0 && ssum && excl < want && excl + ssum >= want) {
         uint32_t cum = excl;
-        if (per == 8) {
-            bool found = false;
+        for (int bb = bhi - 1; bb >= blo; --bb) {
+            const uint32_t hb = sc.hist[bb];
+            if (cum + hb >= want) {
+                sc.res_bin = static_cast<uint32_t>(bb);
+                sc.res_above = cum;
+                break;
+            }
+            cum += hb;
+        }
+    }
+    __syncthreads();
+}
+
+// With sc.hist holding nb bins: the bin b holding the want-th largest key
+// (fewer than `want` keys in the bins above b, at least `want` in b and
+// above).  With 4,096 bins thread t sums bins [4096 - 8(t+1), 4096 - 8t) in
+// two 16-byte loads, kept in registers for the owner's search; fewer bins go
+// out of line.  Sets *bin and *above (the count in the bins above it), the
+// same in every thread.
+__device__ __forceinline__ void find_bin(int nb, uint32_t want, Scratch &sc, uint32_t *bin, uint32_t *above, int &sb)
+{
+    if (nb != kBins) {
+        find_bin_small(nb, want, sc, sb);
+        sb ^= 1;  // the one block scan inside
+        *bin = sc.res_bin;
+        *above = sc.res_above;
+        return;
+    }
+    const int tid = threadIdx.x;
+    const int blo = kBins - (tid + 1) * 8;
+    uint32_t h[8];
+    const uint4 a = *reinterpret_cast<const uint4 *>(&sc.hist[blo]);
+    const uint4 b = *reinterpret_cast<const uint4 *>(&sc.hist[blo + 4]);
+    h[0] = a.x, h[1] = a.y, h[2] = a.z, h[3] = a.w, h[4] = b.x, h[5] = b.y, h[6] = b.z, h[7] = b.w;
+    const uint32_t ssum = ((h[0] + h[1]) + (h[2] + h[3])) + ((h[4] + h[5]) + (h[6] + h[7]));
+    uint32_t tot;
+    const uint32_t excl = block_scan(ssum, sc, &tot, sb);
+    if (ssum && excl < want && excl + ssum >= want) {
+        uint32_t cum = excl;
+        bool found = false;
 #pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                if (!found && cum + h[i] >= want) {
-                    sc.res_bin = static_cast<uint32_t>(blo + i);
-                    sc.res_above = cum;
-                    found = true;
-                }
-                cum += found ? 0u : h[i];
+        for (int i = 7; i >= 0; --i) {
+            if (!found && cum + h[i] >= want) {
+                sc.res_bin = static_cast<uint32_t>(blo + i);
+                sc.res_above = cum;
+                found = true;
             }
-        } else {
-            for (int bb = bhi - 1; bb >= blo; --bb) {
-                const uint32_t hb = sc.hist[bb];
-                if (cum + hb >= want) {
-                    sc.res_bin = static_cast<uint32_t>(bb);
-                    sc.res_above = cum;
-                    break;
-                }
-                cum += hb;
-            }
+            cum += found ? 0u : h[i];
         }
     }
     __syncthreads();
