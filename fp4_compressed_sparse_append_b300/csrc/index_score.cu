@@ -363,6 +363,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) {
         // ------------------------------------------------------------- producer
         if (lane == 0 && j0 < j1) {
+            // A full scan reads every key once: its copies are the first lines
+            // the L2 gives up, so the scores and block maxima this kernel writes
+            // stay there for the top-K that reads them next.
+            const uint64_t stream = l2_evict_first_policy();
             JobIter it;
             jobs.seek(j0, it);
             int stage = 0;
@@ -392,9 +396,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                                           static_cast<uint32_t>(a.mt * kTileRows * (kMxCodeRow + kMxScaleRow)));
                     const int row0 = it.u * a.cap + it.job * a.mt * kTileRows;
                     for (int m = 0; m < a.mt; ++m) {
-                        tma_load_2d(dst + m * tile_bytes, &keys128, &full[stage], 0, row0 + m * kTileRows);
-                        tma_load_2d(ds + m * kTileRows * kMxScaleRow, &scl128, &full[stage], 0,
-                                    (row0 + m * kTileRows) / 4);
+                        tma_load_2d_hint(dst + m * tile_bytes, &keys128, &full[stage], 0, row0 + m * kTileRows, stream);
+                        tma_load_2d_hint(ds + m * kTileRows * kMxScaleRow, &scl128, &full[stage], 0,
+                                         (row0 + m * kTileRows) / 4, stream);
                     }
                 } else if (!a.pool_mode) {
                     // mt whole boxes; rows past the cache's end read as zeros
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
                     const int row0 = it.u * a.cap + it.job * a.mt * kTileRows;
                     for (int m = 0; m < a.mt; ++m)
-                        tma_load_2d(dst + m * tile_bytes, &keys128, &full[stage], 0, row0 + m * kTileRows);
+                        tma_load_2d_hint(dst + m * tile_bytes, &keys128, &full[stage], 0, row0 + m * kTileRows, stream);
                 } else {
                     const int b = it.u / a.P;
                     const int32_t *prow = a.pool + static_cast<int64_t>(it.u) * a.pool_blocks;
